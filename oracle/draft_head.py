@@ -1,0 +1,498 @@
+"""CPU oracle for the block-diffusion (DFlash-style) draft head propose forward.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports, calls or runs
+this module; only the test suite, the package's smoke check and the bench's
+CPU-baseline leg do. It shares no code with the CUDA library: it reads plain
+CPU tensors (bf16 weights, bf16 target stacks) and computes every step with
+torch CPU ops in float64, rounding to bf16 (or FP8 E4M3) exactly where the
+method stores a tensor in that format.
+
+Sources (API pages of the same head):
+  [P1] "Struct BlockDiffusionDraftHead" (spark_model::layers::dflash_head docs)
+  [P2] "BlockDiffusionDraftHead" (metrale_model_arch::dflash_head docs)
+  [P3] "Trait DraftProposer" (spark_model::speculative docs)
+
+Where the pages leave a step open, the reading taken is named inline as
+"reading: ..." and listed with the others in the design notes.
+
+Precision points (reading: a bf16 model runs bf16 GEMMs, so every GEMM
+operand is bf16 and every GEMM accumulates in wide precision):
+  * the residual stream x is kept wide (fp32 on the GPU, float64 here);
+  * GEMM inputs h, o, u, z, the ctx rows c, the block q/k/v and the cached
+    ctx K/V are rounded to bf16 (the cached K/V to E4M3 codes on the FP8 path);
+  * norms, RoPE, softmax, SiLU and the logit reductions are wide.
+
+Parity status: every function here is pinned by the CPU tests (closed forms,
+brute force on tiny inputs, invariants). Whole-model parity with a real trained
+DFlash drafter is unpinned: the pages print no values and no checkpoint exists.
+"""
+from __future__ import annotations
+
+import heapq
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+F64 = torch.float64
+E4M3_MAX = 448.0
+
+
+# ----------------------------------------------------------------- formats --
+def round_bf16(x: torch.Tensor) -> torch.Tensor:
+    """Round to bf16 (round to nearest even) and back to float64.
+
+    The value is first rounded to fp32, as a GPU register holds it, then to
+    bf16 by torch's conversion."""
+    return x.to(torch.float32).to(torch.bfloat16).to(F64)
+
+
+def e4m3_codes(x32: torch.Tensor) -> torch.Tensor:
+    """fp32 -> FP8 E4M3 value (as float64), round to nearest even, saturating
+    at +-448 (OCP 8-bit floating point, E4M3 'satfinite')."""
+    x32 = x32.to(torch.float32)
+    return x32.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).to(F64)
+
+
+# --------------------------------------------------------------- the math --
+def rms_norm(x: torch.Tensor, g: torch.Tensor, eps: float) -> torch.Tensor:
+    """RMSNorm over the last axis: g * x / sqrt(mean(x^2) + eps).
+
+    [P1] field ``rms_norm_eps`` (Qwen3 default 1e-6), ``hidden_norm``, ``norm``."""
+    x = x.to(F64)
+    return g.to(F64) * x / torch.sqrt((x * x).mean(dim=-1, keepdim=True) + eps)
+
+
+def rope(x: torch.Tensor, pos: torch.Tensor, inv_freq: torch.Tensor) -> torch.Tensor:
+    """Rotary embedding over the whole head ([P1] field ``rotary_dim``: full
+    rotation, rotary_dim = head_dim), angle pos * inv_freq[i] from the table
+    ([P1] field ``yarn_inv_freq``).
+
+    reading: rotate-half pairing (i, i + d/2), the Qwen/NeoX convention.
+    x: [..., rows, d]; pos: [rows] integer positions."""
+    d = x.shape[-1]
+    half = d // 2
+    ang = pos.to(F64)[:, None] * inv_freq.to(F64)[None, :]          # [rows, d/2]
+    c, s = torch.cos(ang), torch.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return torch.cat([x1 * c - x2 * s, x2 * c + x1 * s], dim=-1)
+
+
+def silu(a: torch.Tensor) -> torch.Tensor:
+    return a / (1.0 + torch.exp(-a))
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> torch.Tensor:
+    """softmax(q k^T / sqrt(d)) v for every query head, no mask.
+
+    q: [rows, nq, d]; k, v: [keys, nkv, d]. reading: query head j reads kv
+    head floor(j * nkv / nq) (contiguous GQA groups), scale 1/sqrt(d)."""
+    rows, nq, d = q.shape
+    nkv = k.shape[1]
+    out = torch.empty((rows, nq, d), dtype=F64)
+    for j in range(nq):
+        g = (j * nkv) // nq
+        s = q[:, j, :] @ k[:, g, :].T / math.sqrt(d)                 # [rows, keys]
+        s = s - s.max(dim=1, keepdim=True).values
+        p = torch.exp(s)
+        p = p / p.sum(dim=1, keepdim=True)
+        out[:, j, :] = p @ v[:, g, :]
+    return out
+
+
+def bitmask_allowed(bitmask_row: torch.Tensor, vocab: int) -> torch.Tensor:
+    """Bool [vocab] from ceil(vocab/32) int32 words: token t is allowed iff bit
+    (t & 31) of word (t >> 5) is set ([P3] ``propose`` argument
+    ``grammar_bitmask``: 'bit tok set => allowed'; reading: LSB-first)."""
+    words = bitmask_row.to(torch.int64) & 0xFFFFFFFF
+    t = torch.arange(vocab, dtype=torch.int64)
+    return ((words[t >> 5] >> (t & 31)) & 1).bool()
+
+
+def select_drafts(logits: torch.Tensor, allowed: torch.Tensor | None):
+    """Per-row argmax and top-1 softmax probability, then the chain.
+
+    [P1] field ``lm_head_shared`` (per-position argmax over the block's
+    logits), [P1]/[P3] ``last_confidence`` (min over drafts of the top-1
+    softmax probability). reading: ties go to the lowest token id; masked
+    tokens are excluded from the softmax; a row with no allowed token ends the
+    chain before it. Returns (drafts, n_out, conf, p1 per produced row)."""
+    drafts, p1s = [], []
+    for i in range(logits.shape[0]):
+        row = logits[i].to(F64)
+        if allowed is not None:
+            if not bool(allowed.any()):
+                break
+            row = torch.where(allowed, row, torch.full_like(row, -math.inf))
+        m = row.max()
+        idx = int(torch.nonzero(row == m)[0, 0])          # lowest id among maxima
+        p1 = 1.0 / float(torch.exp(row - m).sum())
+        drafts.append(idx)
+        p1s.append(p1)
+    conf = min(p1s) if p1s else 0.0
+    return drafts, len(drafts), conf, p1s
+
+
+# ------------------------------------------------------- page bookkeeping --
+class PagePool:
+    """Fixed pool of KV pages with ids 0..n-1; a take returns the lowest free
+    id (reading: the pages leave the allocation order open)."""
+
+    def __init__(self, n_pages: int):
+        self.free = list(range(n_pages))
+        heapq.heapify(self.free)
+        self.n_pages = n_pages
+
+    def take(self) -> int:
+        return heapq.heappop(self.free)
+
+    def give(self, page: int) -> None:
+        heapq.heappush(self.free, page)
+
+    def n_free(self) -> int:
+        return len(self.free)
+
+
+class OracleError(Exception):
+    def __init__(self, code: str, msg: str):
+        super().__init__(f"{code}: {msg}")
+        self.code = code
+
+
+@dataclass
+class SeqState:
+    cap: int                                   # ctx positions this state may hold
+    ctx_len: int = 0                           # target positions appended
+    pages: dict = field(default_factory=dict)  # logical page -> physical id
+    rows: dict = field(default_factory=dict)   # position -> (K [L,nkv,d], V [L,nkv,d])
+    pending: tuple | None = None               # (position, drafts returned)
+    expected_next: int | None = None
+
+
+# ------------------------------------------------------------------ model --
+class DraftHeadOracle:
+    """The draft head: construction, per-sequence state, prefill, propose,
+    propose_batch and after_verify.
+
+    cfg keys: num_layers hidden intermediate num_q_heads num_kv_heads head_dim
+    vocab gamma mask_token_id n_target_layers target_hidden rms_eps ctx_window
+    kv_block prefill_chunk max_batch max_seq_len kv_pool_blocks kv_dtype
+    (0 bf16, 1 fp8) lm_head_dtype (0 bf16, 1 fp8)."""
+
+    def __init__(self, cfg: dict, w: dict):
+        self.cfg = dict(cfg)
+        c = self.cfg
+        self.L, self.H = c["num_layers"], c["hidden"]
+        self.nq, self.nkv, self.d = c["num_q_heads"], c["num_kv_heads"], c["head_dim"]
+        self.kv = self.nkv * self.d
+        self.V, self.gamma = c["vocab"], c["gamma"]
+        self.eps, self.W, self.B = c["rms_eps"], c["ctx_window"], c["kv_block"]
+        if c.get("fc_in_features", c["n_target_layers"] * c["target_hidden"]) != \
+                c["n_target_layers"] * c["target_hidden"]:
+            # [P1] validate_against_target: a width mismatch is a hard error.
+            raise OracleError("EINVAL", "fc input width != n_target_layers*target_hidden")
+        f = lambda t: t.to(F64)
+        self.embed = w["embed"]                              # gathered per row
+        self.lm_head_bf16 = w["lm_head"]
+        self.fc = f(w["fc"])
+        self.hidden_norm, self.norm = f(w["hidden_norm"]), f(w["norm"])
+        self.inv_freq = w["inv_freq"].to(torch.float32)
+        self.layers = [{k: f(v) for k, v in lay.items()} for lay in w["layers"]]
+        # [P1]/[P2] field fused_kv_weight: rows [K0; V0; K1; V1; ...].
+        self.w_kv = torch.cat([torch.cat([lay["k"], lay["v"]], 0) for lay in self.layers], 0)
+        self.kv_fp8 = c.get("kv_dtype", 0) == 1
+        self.lm_fp8 = c.get("lm_head_dtype", 0) == 1
+        if self.kv_fp8:
+            self.kv_scale = w["kv_scale"].to(torch.float32)   # [L, nkv, 2]
+        if self.lm_fp8:
+            self.lm_codes = w["lm_head_fp8"]
+            self.lm_scale = w["lm_head_scale"].to(F64)
+        self._lm = None
+        self.pool = PagePool(self.n_pool_pages())
+        self.states: list[SeqState] = []
+
+    # -- sizes ----------------------------------------------------------------
+    def pages_per_seq(self) -> int:
+        c = self.cfg
+        span = min(self.W, c["max_seq_len"]) if self.W > 0 else 0
+        return 0 if span == 0 else span // self.B + 2
+
+    def n_pool_pages(self) -> int:
+        c = self.cfg
+        if c.get("kv_pool_blocks", 0) > 0:
+            return c["kv_pool_blocks"]
+        return max(1, c["max_batch"]) * self.pages_per_seq()
+
+    def lm_head(self) -> torch.Tensor:
+        """Float64 lm_head rows, built once: bf16 table, or the FP8 codes
+        (weight-only; the per-row scale is applied to the logits)."""
+        if self._lm is None:
+            src = self.lm_codes if self.lm_fp8 else self.lm_head_bf16
+            self._lm = src.to(F64)
+        return self._lm
+
+    # -- state ----------------------------------------------------------------
+    def alloc_state(self, budget_tokens: int | None = None) -> SeqState:
+        """[P3] alloc_state / alloc_state_for: a None budget means 'unknown,
+        use the ceiling' (max_seq_len)."""
+        cap = self.cfg["max_seq_len"]
+        if budget_tokens is not None:
+            if budget_tokens <= 0:
+                raise OracleError("EINVAL", "budget must be positive")
+            cap = min(cap, budget_tokens)
+        st = SeqState(cap=cap)
+        self.states.append(st)
+        return st
+
+    def free_state(self, st: SeqState) -> None:
+        """[P3] free_state: release every KV page the state holds."""
+        for b in sorted(st.pages):
+            self.pool.give(st.pages[b])
+        st.pages.clear()
+        st.rows.clear()
+        self.states.remove(st)
+
+    # -- ctx append: fc, hidden_norm, fused K/V, k_norm, RoPE, paged write ----
+    def _plan_append(self, st: SeqState, n: int):
+        """Which rows are stored and which pages retire / are taken.
+
+        reading: rows below new_len - ctx_window are neither computed nor
+        stored ([P1]/[P2] field ctx_window); pages entirely below the window
+        start retire; a page is taken when a row first lands in it."""
+        new_len = st.ctx_len + n
+        lo = max(st.ctx_len, new_len - self.W) if self.W > 0 else new_len
+        ws = max(0, new_len - self.W) if self.W > 0 else new_len
+        retire = sorted(b for b in st.pages if (b + 1) * self.B <= ws)
+        need = sorted({j // self.B for j in range(lo, new_len)} - set(st.pages))
+        return new_len, lo, retire, need
+
+    def _store_rows(self, st: SeqState, stack: torch.Tensor, positions: range) -> None:
+        """Compute and store the ctx K/V of the given positions.
+
+        [P1] field fc: c = fc(stack) maps the captured hidden stack into the
+        drafter; field hidden_norm: RMSNorm of the projected ctx;
+        field fused_kv_weight: one GEMM of c against [L*2*kv_dim, h] gives every
+        layer's ctx K and V; the keys then take the layer's k_norm and RoPE at
+        their position. reading: values are not normalised; the same c feeds
+        every layer (one fused GEMM needs one shared input)."""
+        if len(positions) == 0:
+            return
+        x = stack.to(F64)                                         # bf16 values
+        cvec = round_bf16(rms_norm(x @ self.fc.T, self.hidden_norm, self.eps))
+        kv = cvec @ self.w_kv.T                                   # [m, L*2*kv]
+        pos = torch.tensor(list(positions), dtype=torch.int64)
+        for l, lay in enumerate(self.layers):
+            base = l * 2 * self.kv
+            k = kv[:, base:base + self.kv].reshape(-1, self.nkv, self.d)
+            v = kv[:, base + self.kv:base + 2 * self.kv].reshape(-1, self.nkv, self.d)
+            k = rope(rms_norm(k, lay["k_norm"], self.eps).transpose(0, 1), pos,
+                     self.inv_freq).transpose(0, 1)
+            k_st, v_st = self._quant_kv(l, k), self._quant_kv(l, v, is_v=True)
+            for r, j in enumerate(positions):
+                if j not in st.rows:
+                    st.rows[j] = (torch.empty(self.L, self.nkv, self.d, dtype=F64),
+                                  torch.empty(self.L, self.nkv, self.d, dtype=F64))
+                st.rows[j][0][l] = k_st[r]
+                st.rows[j][1][l] = v_st[r]
+
+    def _quant_kv(self, l: int, t: torch.Tensor, is_v: bool = False) -> torch.Tensor:
+        """Cache storage format: bf16 ([P2] field kv_cache), or FP8 E4M3 codes
+        with a static per-(layer, kv head, K|V) scale ([P1] field kv_cache,
+        'paged FP8'): code = e4m3(x / s) taken in fp32, read back as code * s."""
+        if not self.kv_fp8:
+            return round_bf16(t)
+        s = self.kv_scale[l, :, 1 if is_v else 0]                  # [nkv] f32
+        codes = e4m3_codes(t.to(torch.float32) / s[None, :, None])
+        return codes * s.to(F64)[None, :, None]
+
+    def _commit_pages(self, st, retire, need):
+        for b in retire:
+            self.pool.give(st.pages.pop(b))
+        for b in need:
+            st.pages[b] = self.pool.take()
+
+    def _drop_retired_rows(self, st, ws):
+        for j in [j for j in st.rows if j < (ws // self.B) * self.B]:
+            del st.rows[j]
+
+    def prefill(self, st: SeqState, stack: torch.Tensor) -> None:
+        """Append n ctx rows (target hiddens of positions ctx_len..ctx_len+n-1).
+
+        reading: the stored rows are computed in chunks of prefill_chunk rows;
+        the chunking does not change the values."""
+        n = stack.shape[0]
+        if st not in self.states:
+            raise OracleError("EINVAL", "unknown state")
+        if st.pending is not None:
+            raise OracleError("ESTATE", "prefill before after_verify")
+        new_len, lo, retire, need = self._plan_append(st, n)
+        if new_len > st.cap:
+            raise OracleError("EINVAL", "ctx beyond state capacity")
+        if len(need) > self.pool.n_free() + len(retire):
+            raise OracleError("ENOMEM", "KV pool exhausted")
+        self._commit_pages(st, retire, need)
+        self._drop_retired_rows(st, max(0, new_len - self.W) if self.W > 0 else new_len)
+        ch = self.cfg.get("prefill_chunk", 512)
+        for a in range(lo, new_len, ch):
+            b = min(new_len, a + ch)
+            self._store_rows(st, stack[a - st.ctx_len:b - st.ctx_len], range(a, b))
+        st.ctx_len = new_len
+
+    # -- the block forward ----------------------------------------------------
+    def block_forward(self, st: SeqState, last_token: int, p: int, num_drafts: int,
+                      allowed: torch.Tensor | None, taps: dict | None = None):
+        """One non-causal block of gamma rows at positions p..p+gamma-1.
+
+        [P1] fields gamma/mask_token_id (block = the last verified token plus
+        gamma-1 mask rows), embed_tokens_shared (shared embed table), layers
+        (Qwen3-style layer stack), norm (final RMSNorm), lm_head_shared (argmax
+        over the block's logits). reading: rows 1..num_drafts give drafts
+        1..num_drafts; queries see the windowed ctx and every block key."""
+        g = self.gamma
+        toks = [last_token] + [self.cfg["mask_token_id"]] * (g - 1)
+        x = self.embed[torch.tensor(toks)].to(F64)                # [g, H]
+        pos = torch.arange(p, p + g, dtype=torch.int64)
+        ws = max(0, p - self.W) if self.W > 0 else p
+        ctx_pos = list(range(ws, p))
+        if taps is not None:
+            taps["x"] = [x.clone()]
+        for l, lay in enumerate(self.layers):
+            h = round_bf16(rms_norm(x, lay["in_norm"], self.eps))
+            q = (h @ lay["q"].T).reshape(g, self.nq, self.d)
+            k = (h @ lay["k"].T).reshape(g, self.nkv, self.d)
+            v = (h @ lay["v"].T).reshape(g, self.nkv, self.d)
+            q = rope(rms_norm(q, lay["q_norm"], self.eps).transpose(0, 1), pos,
+                     self.inv_freq).transpose(0, 1)
+            k = rope(rms_norm(k, lay["k_norm"], self.eps).transpose(0, 1), pos,
+                     self.inv_freq).transpose(0, 1)
+            q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)
+            if ctx_pos:
+                kc = torch.stack([st.rows[j][0][l] for j in ctx_pos])
+                vc = torch.stack([st.rows[j][1][l] for j in ctx_pos])
+                keys, vals = torch.cat([kc, k], 0), torch.cat([vc, v], 0)
+            else:
+                keys, vals = k, v
+            o = round_bf16(attention(q, keys, vals).reshape(g, self.nq * self.d))
+            x = x + o @ lay["o"].T
+            h2 = round_bf16(rms_norm(x, lay["post_norm"], self.eps))
+            u = round_bf16(silu(h2 @ lay["gate"].T) * (h2 @ lay["up"].T))
+            x = x + u @ lay["down"].T
+            if taps is not None:
+                taps["x"].append(x.clone())
+        z = round_bf16(rms_norm(x, self.norm, self.eps))
+        zr = z[1:1 + num_drafts]
+        logits = zr @ self.lm_head().T
+        if self.lm_fp8:
+            logits = logits * self.lm_scale[None, :]
+        if taps is not None:
+            taps["z"] = z
+            taps["logits"] = logits
+        return select_drafts(logits, allowed)
+
+    # -- trait calls ----------------------------------------------------------
+    def propose(self, st, last_token, position, new_rows, num_drafts, bitmask=None,
+                taps=None):
+        """[P3] propose: append the new ctx rows, run the block, return drafts.
+
+        reading: position == ctx_len + n_new (the new rows are the target
+        hiddens of positions ctx_len..position-1); after an after_verify(k) the
+        next position is p + k + 1."""
+        r = self.propose_batch([st], [last_token], [position], [new_rows], num_drafts,
+                               None if bitmask is None else bitmask[None, :], taps=taps,
+                               _single=True)
+        return r[0]
+
+    def _check(self, st, last_token, position, new_rows, num_drafts):
+        n_new = 0 if new_rows is None else new_rows.shape[0]
+        if st not in self.states:
+            raise OracleError("EINVAL", "unknown state")
+        if not (1 <= num_drafts <= self.gamma - 1):
+            raise OracleError("EINVAL", "num_drafts out of range")
+        if not (0 <= last_token < self.V):
+            raise OracleError("EINVAL", "token out of range")
+        if st.pending is not None:
+            raise OracleError("ESTATE", "propose before after_verify")
+        if position != st.ctx_len + n_new:
+            raise OracleError("EPOSITION", "position != ctx_len + n_new")
+        if st.expected_next is not None and position != st.expected_next:
+            raise OracleError("EPOSITION", "position != expected next")
+        if position > st.cap:
+            raise OracleError("EINVAL", "ctx beyond state capacity")
+        return n_new
+
+    def propose_batch(self, states, last_tokens, positions, new_rows, num_drafts,
+                      bitmask=None, taps=None, _single=False):
+        """[P1]/[P2]/[P3] propose_batch: per-sequence prep, then one forward for
+        every sequence (row i of every slice belongs to sequence i). Declines
+        (returns None) for fewer than 2 or more than max_batch sequences.
+
+        reading: all sequences retire first, then take pages, in sequence order;
+        a batch that cannot get its pages changes nothing."""
+        n = len(states)
+        if not _single and (n < 2 or n > self.cfg["max_batch"]):
+            return None
+        if len(set(map(id, states))) != n:
+            raise OracleError("EINVAL", "duplicate state")
+        n_news = [self._check(st, t, p, r, num_drafts)
+                  for st, t, p, r in zip(states, last_tokens, positions, new_rows)]
+        plans = [self._plan_append(st, nn) for st, nn in zip(states, n_news)]
+        need = sum(len(pl[3]) for pl in plans)
+        retire = sum(len(pl[2]) for pl in plans)
+        if need > self.pool.n_free() + retire:
+            raise OracleError("ENOMEM", "KV pool exhausted")
+        for st, pl in zip(states, plans):
+            for b in pl[2]:
+                self.pool.give(st.pages.pop(b))
+        for st, pl in zip(states, plans):
+            for b in pl[3]:
+                st.pages[b] = self.pool.take()
+        for st, rows, nn, pl in zip(states, new_rows, n_news, plans):
+            new_len, lo = pl[0], pl[1]
+            self._drop_retired_rows(st, max(0, new_len - self.W) if self.W > 0 else new_len)
+            if nn:
+                self._store_rows(st, rows[lo - st.ctx_len:], range(lo, new_len))
+            st.ctx_len = new_len
+        out = []
+        for i, (st, t, p) in enumerate(zip(states, last_tokens, positions)):
+            allowed = None if bitmask is None else bitmask_allowed(bitmask[i], self.V)
+            tp = None
+            if taps is not None:
+                tp = {}
+                taps.setdefault("seq", []).append(tp)
+            drafts, n_out, conf, _ = self.block_forward(st, t, p, num_drafts, allowed, tp)
+            st.pending = (p, n_out)
+            st.expected_next = None
+            out.append((drafts, n_out, conf))
+        return out
+
+    def after_verify(self, st: SeqState, num_accepted: int) -> None:
+        """[P3] after_verify: trim the state to the accepted count.
+
+        reading: the next propose sits at p + k + 1 and brings the k + 1 target
+        hiddens of positions p..p+k; pages below that propose's window retire
+        now."""
+        if st.pending is None:
+            raise OracleError("ESTATE", "after_verify without propose")
+        p, n_out = st.pending
+        if not (0 <= num_accepted <= n_out):
+            raise OracleError("EINVAL", "num_accepted out of range")
+        st.expected_next = p + num_accepted + 1
+        st.pending = None
+        ws = max(0, st.expected_next - self.W) if self.W > 0 else st.expected_next
+        for b in sorted(b for b in st.pages if (b + 1) * self.B <= ws):
+            self.pool.give(st.pages.pop(b))
+        self._drop_retired_rows(st, ws)
+
+    # -- views for parity checks ---------------------------------------------
+    def block_table(self, st: SeqState):
+        """(ctx_len, first live logical page, physical ids of the live pages)."""
+        if not st.pages:
+            return st.ctx_len, -1, []
+        lo, hi = min(st.pages), max(st.pages)
+        return st.ctx_len, lo, [st.pages.get(b, -1) for b in range(lo, hi + 1)]
+
+    def gather_kv(self, st: SeqState, layer: int, positions):
+        """Stored K, V of one layer at the given positions: [n, nkv, d] each."""
+        k = torch.stack([st.rows[j][0][layer] for j in positions])
+        v = torch.stack([st.rows[j][1][layer] for j in positions])
+        return k, v
