@@ -1,0 +1,342 @@
+"""Benchmark of the draft-head propose forward on GB300.
+
+A step is one dflash_propose of the whole hot path (ctx append of the new
+target row: fc, hidden_norm, fused K/V, k_norm, RoPE, paged write; the
+gamma-row block through all layers; final norm, lm_head, argmax, confidence),
+followed by the host-only after_verify. The default workload is the shipped
+geometry at batch 1: 8 layers, hidden 2048, 32/4 heads of 128, vocab 248320,
+gamma 16 (15 drafts), ctx 1024, one new row per step. Inputs are seeded
+synthetic tensors; weights are random N(0, 0.02) (no checkpoint exists here).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+
+N > 1 runs under torchrun: every rank runs its own replica (the single-
+sequence path does not shard); value = drafted tokens of all ranks / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from block_diffusion_speculative_forward_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "drafted tokens/s (gamma=16, batch 1)"
+UNIT = "tokens/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def head_cfg(geom, max_batch, max_seq_len, **kw):
+    c = dict(num_layers=geom.num_layers, hidden=geom.hidden, intermediate=geom.intermediate,
+             num_q_heads=geom.num_q_heads, num_kv_heads=geom.num_kv_heads,
+             head_dim=geom.head_dim, vocab=geom.vocab, gamma=geom.gamma,
+             mask_token_id=geom.mask_token_id, n_target_layers=geom.n_target_layers,
+             target_hidden=geom.target_hidden, rms_eps=geom.rms_eps,
+             ctx_window=geom.ctx_window, kv_block=geom.kv_block,
+             prefill_chunk=geom.prefill_chunk, max_batch=max_batch, max_seq_len=max_seq_len,
+             kv_pool_blocks=0, kv_dtype=0, lm_head_dtype=0)
+    c.update(kw)
+    return c
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads --
+def build_b1(geom, seed, ctx, n_steps_total):
+    """Head + one sequence prefilled with ctx-1 rows; device rows for every
+    step's new target row; pinned host copies of the same rows."""
+    from block_diffusion_speculative_forward_gb300 import binding as B
+    w = syn.make_weights(geom, seed)
+    wd = B.weights_to_device(w)
+    cfg = head_cfg(geom, 1, ctx + n_steps_total + 64)
+    head = B.DraftHead(cfg, wd)
+    st = head.alloc_state()
+    head.prefill(st, syn.make_stack(geom, ctx - 1, seed).cuda())
+    rows_host = syn.make_stack(geom, n_steps_total + 1, seed, idx=1).pin_memory()
+    rows_dev = rows_host.cuda()
+    torch.cuda.synchronize()
+    return w, wd, head, st, rows_dev, rows_host, cfg
+
+
+def lm_head_bytes(geom, n_rows):
+    """Algorithmic bytes of the lm_head stage: the vocab table once, the draft
+    rows' z in, (id, p1) per row out."""
+    return 2 * geom.vocab * geom.hidden + 2 * n_rows * geom.hidden + 8 * n_rows
+
+
+def step_bytes(geom, ctx, n_new):
+    wb = syn.weight_bytes(geom)
+    kv_row = geom.num_layers * 2 * geom.kv_dim * 2
+    return sum(wb.values()) + ctx * kv_row + n_new * geom.stack_width * 2
+
+
+def run_ours(args):
+    from block_diffusion_speculative_forward_gb300 import binding as B
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    geom, seed, ctx = syn.FULL, 1002, 1024
+    nd = geom.gamma - 1
+    K, W = args.steps, args.warmup
+    total = 2 * (K + W) + 2
+    w, wd, head, st, rows_dev, rows_host, cfg = build_b1(geom, seed, ctx, total)
+    lib = B.lib()
+    stream = torch.cuda.current_stream()
+    pos = ctx
+    used = 0
+
+    def step(row):
+        nonlocal pos
+        d, n, c = head.propose(st, 1000 + pos % 1000, pos, row, nd)
+        head.after_verify(st, 0)
+        pos += 1
+        return d
+
+    for _ in range(W):
+        step(rows_dev[used:used + 1])
+        used += 1
+    # device-timed region, inputs resident
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pb, pe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    import ctypes as C
+    lib.dflash_debug_set_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
+    lib.dflash_debug_launch_count.restype = C.c_int64
+    lib.dflash_debug_set_probe(head.ptr, C.c_void_p(pb.cuda_event), C.c_void_p(pe.cuda_event))
+    probe_ms = []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = lib.dflash_debug_launch_count()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(K):
+            step(rows_dev[used:used + 1])
+            used += 1
+            probe_ms.append(pb.elapsed_time(pe))
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    launches = lib.dflash_debug_launch_count() - launches0
+    lib.dflash_debug_set_probe(head.ptr, None, None)
+    t_ms = ev0.elapsed_time(ev1)
+    # end to end through the public call, host buffers: H2D of the step's new
+    # row from pinned memory inside the timed region; drafts come back to host.
+    for _ in range(2):
+        step(rows_host[used:used + 1])
+        used += 1
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step(rows_host[used:used + 1])
+        used += 1
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        tt = torch.tensor([t_ms, e2e_s], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms, e2e_s = float(tt[0]), float(tt[1])
+    hbm, tf, src = peaks()
+    lm_ms = statistics.mean(probe_ms)
+    lm_bytes = lm_head_bytes(geom, nd)
+    achieved = lm_bytes / (lm_ms * 1e-3) / 1e9
+    traffic = args.lm_traffic
+    out = {
+        "metric": METRIC, "value": world * K * nd / (t_ms * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": t_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; random-init weights of the shipped drafter geometry)",
+        "config": {"workload": "full_b1: L=8 H=2048 heads 32/4x128 I=6144 V=248320 gamma=16 "
+                               "ctx=1024 n_new=1 drafts=15",
+                   "batch": 1, "ctx": ctx, "gamma": geom.gamma, "num_drafts": nd,
+                   "l2": "no flush: every step streams 1.98 GB of weights, > 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": world * K * nd / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": geom.stack_width * 2,
+                "d2h_bytes_per_step": 4 * nd + 12},
+        "gpu_launches": int(launches),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "lm_head stage (GEMM over the vocab + argmax/confidence)",
+                     "peak_source": f"{src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": lm_bytes, "avg_ms": lm_ms},
+        "step_roofline": {"bytes_per_step": step_bytes(geom, ctx, 1),
+                          "achieved_gbs": step_bytes(geom, ctx, 1) / (t_ms / K * 1e-3) / 1e9,
+                          "frac_of_hbm": step_bytes(geom, ctx, 1) / (t_ms / K * 1e-3) / 1e9 / hbm},
+        "propose_us": 1e3 * t_ms / K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(w, cfg, geom, seed, ctx, args.cpu_steps)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    head.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(w, cfg, geom, seed, ctx, n_steps):
+    """The oracle, as it stands, on the host cores: prefill untimed, then a
+    bounded number of single-sequence proposes of the same workload."""
+    import oracle
+    ora = oracle.DraftHeadOracle(cfg, w)
+    st = ora.alloc_state()
+    ora.prefill(st, syn.make_stack(geom, ctx - 1, seed))
+    rows = syn.make_stack(geom, n_steps + 2, seed, idx=1)
+    ora.lm_head()
+    pos = ctx
+    ora.propose(st, 1, pos, rows[0:1], geom.gamma - 1)
+    ora.after_verify(st, 0)
+    pos += 1
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        ora.propose(st, 1000 + pos % 1000, pos, rows[1 + i:2 + i], geom.gamma - 1)
+        ora.after_verify(st, 0)
+        pos += 1
+    dt = time.perf_counter() - t0
+    return {"value": n_steps * (geom.gamma - 1) / dt, "unit": UNIT,
+            "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"{n_steps} single-sequence proposes of full_b1 after an untimed "
+                      f"{ctx - 1}-row prefill (torch CPU float64)",
+            "s_per_propose": dt / n_steps}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    geom, seed, ctx = syn.FULL, 1002, 1024
+    nd = geom.gamma - 1
+    w = syn.make_weights(geom, seed)
+    cfg = head_cfg(geom, 1, ctx + 4096)
+    import oracle
+    ora = oracle.DraftHeadOracle(cfg, w)
+    st = ora.alloc_state()
+    ora.prefill(st, syn.make_stack(geom, ctx - 1, seed))
+    ora.lm_head()
+    rows = syn.make_stack(geom, args.steps + args.warmup + 2, seed, idx=1)
+    pos, used = ctx, 0
+    for _ in range(args.warmup):
+        ora.propose(st, 1, pos, rows[used:used + 1], nd)
+        ora.after_verify(st, 0)
+        pos += 1
+        used += 1
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ora.propose(st, 1000 + pos % 1000, pos, rows[used:used + 1], nd)
+        ora.after_verify(st, 0)
+        pos += 1
+        used += 1
+    dt = time.perf_counter() - t0
+    v = args.steps * nd / dt
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)",
+           "config": {"workload": "full_b1: L=8 H=2048 heads 32/4x128 I=6144 V=248320 gamma=16 "
+                                  "ctx=1024 n_new=1 drafts=15", "batch": 1},
+           "cpu_baseline": {"value": v, "unit": UNIT, "cores": torch.get_num_threads(),
+                            "kind": "oracle",
+                            "sample": f"{args.steps} proposes after an untimed prefill"},
+           "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-steps", type=int, default=4)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--lm-traffic", type=float, default=None,
+                    help="ncu dram bytes per lm_head launch, when captured for this build")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        from block_diffusion_speculative_forward_gb300 import build
+        if int(os.environ.get("LOCAL_RANK", "0")) == 0:
+            build.build()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,624 @@
+// libdflash host side: the C ABI of include/dflash.h, the per-sequence state
+// machine and page pool, and the orchestration of the propose forward's
+// kernels on the caller's stream.
+//
+// Sources: [P1] "Struct BlockDiffusionDraftHead" (spark_model docs),
+// [P2] "BlockDiffusionDraftHead" (metrale docs), [P3] "Trait DraftProposer".
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "dflash.h"
+#include "internal.h"
+#include "forward.h"
+
+using dfl::bf16;
+
+namespace {
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CK(call)                                                                     \
+  do {                                                                               \
+    cudaError_t e_ = (call);                                                         \
+    if (e_ != cudaSuccess)                                                           \
+      return fail(DFLASH_ECUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_),     \
+                  __FILE__, __LINE__);                                               \
+  } while (0)
+}  // namespace
+
+// ------------------------------------------------------------- page pool --
+// Fixed pool of pages 0..n-1; a take returns the lowest free id.
+struct PagePool {
+  std::set<int32_t> free_ids;
+  int32_t total = 0;
+  void init(int32_t n) {
+    total = n;
+    free_ids.clear();
+    for (int32_t i = 0; i < n; ++i) free_ids.insert(free_ids.end(), i);
+  }
+  int32_t take() {
+    int32_t id = *free_ids.begin();
+    free_ids.erase(free_ids.begin());
+    return id;
+  }
+  void give(int32_t id) { free_ids.insert(id); }
+  int32_t n_free() const { return (int32_t)free_ids.size(); }
+};
+
+struct dflash_state {
+  dflash_handle *owner = nullptr;
+  int64_t cap = 0;                    // ctx positions the state may hold
+  int64_t ctx_len = 0;                // target positions appended
+  std::map<int64_t, int32_t> pages;   // logical page -> physical page
+  bool pending = false;               // a propose awaits after_verify
+  int64_t pend_pos = 0;
+  int32_t pend_nout = 0;
+  int64_t expected_next = -1;
+};
+
+struct dflash_handle {
+  dflash_config cfg{};
+  dfl::Geo g{};
+  bool compute = false;
+  dfl::Weights w{};
+  dfl::Buffers b{};
+  std::vector<void *> allocs;        // device allocations, freed at destroy
+  std::vector<void *> host_allocs;   // pinned host allocations
+  PagePool pool;
+  std::mutex mu;
+  std::set<dflash_state *> states;
+  int R_max = 0, D_max = 0, M_ctx = 0;
+  // per-call metadata staging
+  char *meta_host = nullptr, *meta_dev = nullptr;
+  size_t meta_cap = 0;
+  cudaEvent_t meta_ev = nullptr;
+  bool meta_ev_live = false;
+};
+
+// ------------------------------------------------------------ helpers --
+namespace {
+
+int64_t window_start(const dflash_handle *h, int64_t end) {
+  int64_t W = h->cfg.ctx_window;
+  return W > 0 ? std::max<int64_t>(0, end - W) : end;
+}
+
+struct AppendPlan {
+  dflash_state *st;
+  int64_t old_len, new_len, lo, ws;
+  std::vector<int64_t> retire, need;
+  const bf16 *src;  // the caller's rows for positions old_len..new_len-1
+};
+
+// Which rows a ctx append stores and which pages it retires and takes: rows
+// below new_len - ctx_window are skipped; pages wholly below the window
+// start retire; a page is taken when a row first lands in it.
+AppendPlan plan_append(const dflash_handle *h, dflash_state *st, int64_t n, const void *src) {
+  AppendPlan p;
+  p.st = st;
+  p.old_len = st->ctx_len;
+  p.new_len = st->ctx_len + n;
+  p.ws = window_start(h, p.new_len);
+  p.lo = h->cfg.ctx_window > 0 ? std::max(p.old_len, p.ws) : p.new_len;
+  p.src = (const bf16 *)src;
+  const int64_t B = h->cfg.kv_block;
+  for (auto &kv : st->pages)
+    if ((kv.first + 1) * B <= p.ws) p.retire.push_back(kv.first);
+  if (p.lo < p.new_len)
+    for (int64_t b = p.lo / B; b <= (p.new_len - 1) / B; ++b)
+      if (!st->pages.count(b)) p.need.push_back(b);
+  return p;
+}
+
+// All plans retire first, then take pages, in order; the caller has checked
+// that the pool can cover every take.
+void commit_plans(dflash_handle *h, std::vector<AppendPlan> &plans) {
+  for (auto &p : plans)
+    for (int64_t b : p.retire) {
+      h->pool.give(p.st->pages[b]);
+      p.st->pages.erase(b);
+    }
+  for (auto &p : plans)
+    for (int64_t b : p.need) p.st->pages[b] = h->pool.take();
+}
+
+bool pool_can_cover(const dflash_handle *h, const std::vector<AppendPlan> &plans) {
+  int64_t need = 0, retire = 0;
+  for (auto &p : plans) {
+    need += (int64_t)p.need.size();
+    retire += (int64_t)p.retire.size();
+  }
+  return need <= h->pool.n_free() + retire;
+}
+
+void retire_below(dflash_handle *h, dflash_state *st, int64_t ws) {
+  const int64_t B = h->cfg.kv_block;
+  for (auto it = st->pages.begin(); it != st->pages.end();) {
+    if ((it->first + 1) * B <= ws) {
+      h->pool.give(it->second);
+      it = st->pages.erase(it);
+    } else {
+      ++it;
+    }
+  }
+}
+
+template <class T>
+T *dev_alloc(dflash_handle *h, size_t count, cudaError_t *err) {
+  void *p = nullptr;
+  if (count == 0) return nullptr;
+  cudaError_t e = cudaMalloc(&p, count * sizeof(T));
+  if (e != cudaSuccess) {
+    *err = e;
+    return nullptr;
+  }
+  h->allocs.push_back(p);
+  return (T *)p;
+}
+
+void release(dflash_handle *h) {
+  for (auto *st : h->states) delete st;
+  h->states.clear();
+  if (h->meta_ev) cudaEventDestroy(h->meta_ev);
+  for (void *p : h->allocs) cudaFree(p);
+  for (void *p : h->host_allocs) cudaFreeHost(p);
+  h->allocs.clear();
+  h->host_allocs.clear();
+}
+
+int validate_config(const dflash_config *c) {
+  if (!c) return fail(DFLASH_EINVAL, "config is NULL");
+  if (c->num_layers < 1 || c->hidden < 64 || c->hidden % 64)
+    return fail(DFLASH_EINVAL, "num_layers >= 1 and hidden a multiple of 64 required");
+  if (c->intermediate < 64 || c->intermediate % 64)
+    return fail(DFLASH_EINVAL, "intermediate must be a positive multiple of 64");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(DFLASH_EINVAL, "head_dim must be 64 or 128");
+  if (c->num_q_heads < 1 || c->num_kv_heads < 1 || c->num_q_heads % c->num_kv_heads ||
+      c->num_kv_heads > 32)
+    return fail(DFLASH_EINVAL, "num_q_heads must be a multiple of num_kv_heads (<= 32)");
+  if (c->vocab < 2 || c->gamma < 2 || c->gamma > 64)
+    return fail(DFLASH_EINVAL, "vocab >= 2 and 2 <= gamma <= 64 required");
+  if (c->mask_token_id >= (uint32_t)c->vocab) return fail(DFLASH_EINVAL, "mask_token_id >= vocab");
+  if (c->n_target_layers < 1 || c->target_hidden < 1)
+    return fail(DFLASH_EINVAL, "n_target_layers and target_hidden must be positive");
+  if ((int64_t)c->fc_in_features != (int64_t)c->n_target_layers * c->target_hidden)
+    return fail(DFLASH_EINVAL,
+                "fc input width %d != n_target_layers*target_hidden %lld (validate_against_target)",
+                c->fc_in_features, (long long)c->n_target_layers * c->target_hidden);
+  if (c->fc_in_features % 64) return fail(DFLASH_EINVAL, "fc input width must be a multiple of 64");
+  if (!(c->rms_eps >= 0.f)) return fail(DFLASH_EINVAL, "rms_eps must be >= 0");
+  if (c->ctx_window < 0 || c->kv_block < 1 || c->kv_block > 256 || c->prefill_chunk < 1)
+    return fail(DFLASH_EINVAL, "ctx_window >= 0, 1 <= kv_block <= 256, prefill_chunk >= 1 required");
+  if (c->max_batch < 1 || c->max_seq_len < 1 || c->kv_pool_blocks < 0)
+    return fail(DFLASH_EINVAL, "max_batch, max_seq_len >= 1 and kv_pool_blocks >= 0 required");
+  if ((c->kv_dtype != 0 && c->kv_dtype != 1) || (c->lm_head_dtype != 0 && c->lm_head_dtype != 1))
+    return fail(DFLASH_EINVAL, "kv_dtype and lm_head_dtype must be 0 or 1");
+  return DFLASH_OK;
+}
+
+int32_t pool_pages_for(const dflash_config *c) {
+  if (c->kv_pool_blocks > 0) return c->kv_pool_blocks;
+  if (c->ctx_window == 0) return 0;
+  int64_t span = std::min<int64_t>(c->ctx_window, c->max_seq_len);
+  return (int32_t)(c->max_batch * (span / c->kv_block + 2));
+}
+
+// Stage the call's metadata (seq, rows, page ids) and copy it to the device
+// in one transfer. Waits first for the previous transfer out of the staging
+// buffer to finish.
+int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
+                const std::vector<dfl::RowMeta> &rows, const std::vector<int32_t> &page_ids,
+                cudaStream_t s, dfl::CallMeta *out) {
+  size_t off_seq = 0;
+  size_t off_rows = (seq.size() * sizeof(dfl::SeqMeta) + 15) & ~(size_t)15;
+  size_t off_pages = (off_rows + rows.size() * sizeof(dfl::RowMeta) + 15) & ~(size_t)15;
+  size_t total = off_pages + page_ids.size() * sizeof(int32_t) + 16;
+  if (h->meta_ev_live) {
+    CK(cudaEventSynchronize(h->meta_ev));
+    h->meta_ev_live = false;
+  }
+  if (total > h->meta_cap) {
+    CK(cudaStreamSynchronize(s));
+    size_t cap = std::max(total, h->meta_cap * 2);
+    void *hp = nullptr, *dp = nullptr;
+    CK(cudaMallocHost(&hp, cap));
+    cudaError_t e = cudaMalloc(&dp, cap);
+    if (e != cudaSuccess) {
+      cudaFreeHost(hp);
+      CK(e);
+    }
+    if (h->meta_host) {
+      cudaFreeHost(h->meta_host);
+      cudaFree(h->meta_dev);
+      h->host_allocs.erase(std::find(h->host_allocs.begin(), h->host_allocs.end(), h->meta_host));
+      h->allocs.erase(std::find(h->allocs.begin(), h->allocs.end(), h->meta_dev));
+    }
+    h->meta_host = (char *)hp;
+    h->meta_dev = (char *)dp;
+    h->host_allocs.push_back(hp);
+    h->allocs.push_back(dp);
+    h->meta_cap = cap;
+  }
+  if (!seq.empty()) memcpy(h->meta_host + off_seq, seq.data(), seq.size() * sizeof(dfl::SeqMeta));
+  if (!rows.empty())
+    memcpy(h->meta_host + off_rows, rows.data(), rows.size() * sizeof(dfl::RowMeta));
+  if (!page_ids.empty())
+    memcpy(h->meta_host + off_pages, page_ids.data(), page_ids.size() * sizeof(int32_t));
+  CK(cudaMemcpyAsync(h->meta_dev, h->meta_host, total, cudaMemcpyHostToDevice, s));
+  CK(cudaEventRecord(h->meta_ev, s));
+  h->meta_ev_live = true;
+  out->seq = (const dfl::SeqMeta *)(h->meta_dev + off_seq);
+  out->rows = (const dfl::RowMeta *)(h->meta_dev + off_rows);
+  out->page_ids = (const int32_t *)(h->meta_dev + off_pages);
+  out->n_seq = (int)seq.size();
+  out->n_rows = (int)rows.size();
+  return DFLASH_OK;
+}
+
+// Row metadata of every stored ctx row of the plans, in plan order.
+void rows_of(const dflash_handle *h, const std::vector<AppendPlan> &plans,
+             std::vector<dfl::RowMeta> *rows) {
+  const int64_t B = h->cfg.kv_block, S = h->g.S;
+  for (size_t i = 0; i < plans.size(); ++i) {
+    const AppendPlan &p = plans[i];
+    for (int64_t j = p.lo; j < p.new_len; ++j) {
+      dfl::RowMeta r;
+      r.pos = (int32_t)j;
+      auto it = p.st->pages.find(j / B);
+      r.page = it == p.st->pages.end() ? -1 : it->second;  // -1 trips the kernel's page check
+      r.slot = (int32_t)(j % B);
+      r.seq = (int32_t)i;
+      r.src = p.src + (j - p.old_len) * S;
+      rows->push_back(r);
+    }
+  }
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+}  // namespace
+
+// ================================================================ the ABI ==
+extern "C" {
+
+const char *dflash_last_error(void) { return g_err.c_str(); }
+
+int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_handle **out) {
+  if (!out) return fail(DFLASH_EINVAL, "out is NULL");
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  dflash_handle *h = new dflash_handle();
+  h->cfg = *cfg;
+  dfl::Geo &g = h->g;
+  g.L = cfg->num_layers;
+  g.H = cfg->hidden;
+  g.I = cfg->intermediate;
+  g.nq = cfg->num_q_heads;
+  g.nkv = cfg->num_kv_heads;
+  g.d = cfg->head_dim;
+  g.V = cfg->vocab;
+  g.gamma = cfg->gamma;
+  g.B = cfg->kv_block;
+  g.S = cfg->fc_in_features;
+  g.kv = g.nkv * g.d;
+  g.qkv_w = g.nq * g.d + 2 * g.kv;
+  g.kv_fp8 = cfg->kv_dtype;
+  g.eps = cfg->rms_eps;
+  g.pages = pool_pages_for(cfg);
+  h->pool.init(g.pages);
+  h->R_max = cfg->max_batch * g.gamma;
+  h->D_max = cfg->max_batch * (g.gamma - 1);
+  h->M_ctx = std::max(cfg->prefill_chunk, h->R_max);
+  h->compute = wts != nullptr;
+  if (!h->compute) {
+    *out = h;
+    return DFLASH_OK;
+  }
+  rc = dfl::build_device_side(h->cfg, h->g, wts, h->R_max, h->D_max, h->M_ctx, &h->w, &h->b,
+                              &h->allocs, &h->host_allocs);
+  if (rc == DFLASH_OK) {
+    cudaError_t e = cudaEventCreateWithFlags(&h->meta_ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) rc = fail(DFLASH_ECUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
+  } else {
+    g_err = dfl::last_build_error();
+  }
+  if (rc != DFLASH_OK) {
+    release(h);
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return DFLASH_OK;
+}
+
+void dflash_destroy(dflash_handle *h) {
+  if (!h) return;
+  if (h->compute) cudaDeviceSynchronize();
+  release(h);
+  delete h;
+}
+
+int dflash_propose_batch_max(const dflash_handle *h) { return h ? h->cfg.max_batch : DFLASH_EINVAL; }
+int dflash_block_gamma(const dflash_handle *h) { return h ? h->cfg.gamma : DFLASH_EINVAL; }
+
+int dflash_alloc_state(dflash_handle *h, int64_t budget_tokens, dflash_state **out) {
+  if (!h || !out) return fail(DFLASH_EINVAL, "NULL argument");
+  if (budget_tokens <= 0) return fail(DFLASH_EINVAL, "budget_tokens must be positive");
+  std::lock_guard<std::mutex> lk(h->mu);
+  dflash_state *st = new dflash_state();
+  st->owner = h;
+  st->cap = std::min<int64_t>(budget_tokens, h->cfg.max_seq_len);
+  h->states.insert(st);
+  *out = st;
+  return DFLASH_OK;
+}
+
+int dflash_free_state(dflash_handle *h, dflash_state *st) {
+  if (!h || !st) return fail(DFLASH_EINVAL, "NULL argument");
+  std::lock_guard<std::mutex> lk(h->mu);
+  if (!h->states.count(st)) return fail(DFLASH_EINVAL, "state does not belong to this handle");
+  for (auto &kv : st->pages) h->pool.give(kv.second);
+  h->states.erase(st);
+  delete st;
+  return DFLASH_OK;
+}
+
+int dflash_prefill(dflash_handle *h, dflash_state *st, const void *stack, int32_t n_rows,
+                   void *stream) {
+  if (!h || !st) return fail(DFLASH_EINVAL, "NULL argument");
+  cudaStream_t s = (cudaStream_t)stream;
+  std::lock_guard<std::mutex> lk(h->mu);
+  if (!h->states.count(st)) return fail(DFLASH_EINVAL, "state does not belong to this handle");
+  if (n_rows < 0) return fail(DFLASH_EINVAL, "n_rows < 0");
+  if (st->pending) return fail(DFLASH_ESTATE, "prefill while a propose awaits after_verify");
+  if (st->ctx_len + n_rows > st->cap) return fail(DFLASH_EINVAL, "ctx beyond the state's budget");
+  if (h->compute && n_rows > 0 && (!stack || !aligned16(stack)))
+    return fail(DFLASH_EINVAL, "stack must be a 16-byte aligned device pointer");
+  std::vector<AppendPlan> plans{plan_append(h, st, n_rows, stack)};
+  if (!pool_can_cover(h, plans)) return fail(DFLASH_ENOMEM, "KV pool exhausted");
+  commit_plans(h, plans);
+  st->ctx_len = plans[0].new_len;
+  if (!h->compute) return DFLASH_BOOKKEEPING_ONLY;
+  std::vector<dfl::RowMeta> rows;
+  rows_of(h, plans, &rows);
+  for (size_t a = 0; a < rows.size(); a += (size_t)h->cfg.prefill_chunk) {
+    size_t nb = std::min(rows.size() - a, (size_t)h->cfg.prefill_chunk);
+    std::vector<dfl::RowMeta> chunk(rows.begin() + a, rows.begin() + a + nb);
+    dfl::CallMeta cm;
+    int rc = upload_meta(h, {}, chunk, {}, s, &cm);
+    if (rc) return rc;
+    rc = dfl::ctx_append(h->g, h->w, h->b, cm.rows, cm.n_rows, h->M_ctx, s);
+    if (rc) return fail(rc, "%s", dfl::last_build_error());
+  }
+  return DFLASH_OK;
+}
+
+int dflash_propose_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
+                         const uint32_t *last_tokens, const int64_t *positions,
+                         const void *const *new_rows, const int32_t *n_new, int32_t num_drafts,
+                         const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
+                         void *stream);
+
+int dflash_propose(dflash_handle *h, dflash_state *st, uint32_t last_token, int64_t position,
+                   const void *new_rows, int32_t n_new, int32_t num_drafts, const int32_t *bitmask,
+                   uint32_t *drafts, int32_t *n_out, float *conf, void *stream) {
+  return dfl::propose_impl(h, 1, &st, &last_token, &position, &new_rows, &n_new, num_drafts,
+                           bitmask, drafts, n_out, conf, stream, true);
+}
+
+int dflash_propose_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
+                         const uint32_t *last_tokens, const int64_t *positions,
+                         const void *const *new_rows, const int32_t *n_new, int32_t num_drafts,
+                         const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
+                         void *stream) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  if (n < 2 || n > h->cfg.max_batch) return DFLASH_DECLINED;
+  return dfl::propose_impl(h, n, states, last_tokens, positions, new_rows, n_new, num_drafts,
+                           bitmask, drafts, n_out, conf, stream, false);
+}
+
+int dflash_after_verify(dflash_handle *h, dflash_state *st, int32_t num_accepted) {
+  if (!h || !st) return fail(DFLASH_EINVAL, "NULL argument");
+  std::lock_guard<std::mutex> lk(h->mu);
+  if (!h->states.count(st)) return fail(DFLASH_EINVAL, "state does not belong to this handle");
+  if (!st->pending) return fail(DFLASH_ESTATE, "after_verify without a propose");
+  if (num_accepted < 0 || num_accepted > st->pend_nout)
+    return fail(DFLASH_EINVAL, "num_accepted %d outside 0..%d", num_accepted, st->pend_nout);
+  st->expected_next = st->pend_pos + num_accepted + 1;
+  st->pending = false;
+  retire_below(h, st, window_start(h, st->expected_next));
+  return DFLASH_OK;
+}
+
+int dflash_debug_state(const dflash_state *st, int64_t *ctx_len, int32_t *first_block,
+                       int32_t *table, int32_t cap) {
+  if (!st) return fail(DFLASH_EINVAL, "NULL state");
+  if (ctx_len) *ctx_len = st->ctx_len;
+  if (st->pages.empty()) {
+    if (first_block) *first_block = -1;
+    return 0;
+  }
+  int64_t lo = st->pages.begin()->first, hi = st->pages.rbegin()->first;
+  if (first_block) *first_block = (int32_t)lo;
+  int32_t n = (int32_t)(hi - lo + 1);
+  for (int64_t b = lo; b <= hi && table && b - lo < cap; ++b) {
+    auto it = st->pages.find(b);
+    table[b - lo] = it == st->pages.end() ? -1 : it->second;
+  }
+  return n;
+}
+
+int dflash_debug_pool(const dflash_handle *h, int32_t *in_use, int32_t *total) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  if (in_use) *in_use = h->pool.total - h->pool.n_free();
+  if (total) *total = h->pool.total;
+  return DFLASH_OK;
+}
+
+int dflash_debug_gather_kv(dflash_handle *h, const dflash_state *st, int32_t layer, int64_t pos0,
+                           int32_t n, float *k_out, float *v_out, void *stream) {
+  if (!h || !st || !h->compute) return fail(DFLASH_EINVAL, "NULL argument or no device side");
+  if (layer < 0 || layer >= h->g.L || n < 0) return fail(DFLASH_EINVAL, "bad layer or count");
+  std::lock_guard<std::mutex> lk(h->mu);
+  std::vector<dfl::RowMeta> rows;
+  for (int64_t j = pos0; j < pos0 + n; ++j) {
+    auto it = st->pages.find(j / h->cfg.kv_block);
+    if (j < 0 || j >= st->ctx_len || it == st->pages.end())
+      return fail(DFLASH_EINVAL, "position %lld is not stored", (long long)j);
+    dfl::RowMeta r{};
+    r.pos = (int32_t)j;
+    r.page = it->second;
+    r.slot = (int32_t)(j % h->cfg.kv_block);
+    rows.push_back(r);
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  dfl::CallMeta cm;
+  int rc = upload_meta(h, {}, rows, {}, s, &cm);
+  if (rc) return rc;
+  CK(dfl::gather_kv_rows(h->g, h->w, h->b, cm.rows, n, layer, k_out, v_out, s));
+  return DFLASH_OK;
+}
+
+int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  h->b.probe_begin = (cudaEvent_t)ev_begin;
+  h->b.probe_end = (cudaEvent_t)ev_end;
+  return DFLASH_OK;
+}
+
+int64_t dflash_debug_launch_count(void) { return dfl::launch_count(); }
+
+int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  h->b.tap_x = x_taps;
+  h->b.tap_z = (bf16 *)z;
+  h->b.tap_logits = logits;
+  return DFLASH_OK;
+}
+
+}  // extern "C"
+
+// ====================================================== propose driver ==
+namespace dfl {
+
+int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
+                 const uint32_t *last_tokens, const int64_t *positions,
+                 const void *const *new_rows, const int32_t *n_new, int num_drafts,
+                 const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
+                 void *stream, bool single) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  if (!states || !last_tokens || !positions || !n_new || !drafts || !n_out)
+    return fail(DFLASH_EINVAL, "NULL argument");
+  cudaStream_t s = (cudaStream_t)stream;
+  std::lock_guard<std::mutex> lk(h->mu);
+  const dflash_config &c = h->cfg;
+  if (num_drafts < 1 || num_drafts > c.gamma - 1)
+    return fail(DFLASH_EINVAL, "num_drafts %d outside 1..%d", num_drafts, c.gamma - 1);
+  std::set<dflash_state *> seen;
+  for (int i = 0; i < n; ++i) {
+    dflash_state *st = states[i];
+    if (!st || !h->states.count(st)) return fail(DFLASH_EINVAL, "state %d unknown", i);
+    if (!seen.insert(st).second) return fail(DFLASH_EINVAL, "state %d repeated", i);
+    if (last_tokens[i] >= (uint32_t)c.vocab) return fail(DFLASH_EINVAL, "token %u >= vocab", last_tokens[i]);
+    if (st->pending) return fail(DFLASH_ESTATE, "sequence %d: propose before after_verify", i);
+    if (n_new[i] < 0) return fail(DFLASH_EINVAL, "n_new < 0");
+    if (positions[i] != st->ctx_len + n_new[i])
+      return fail(DFLASH_EPOSITION, "sequence %d: position %lld != ctx_len %lld + n_new %d", i,
+                  (long long)positions[i], (long long)st->ctx_len, n_new[i]);
+    if (st->expected_next >= 0 && positions[i] != st->expected_next)
+      return fail(DFLASH_EPOSITION, "sequence %d: position %lld != %lld set by after_verify", i,
+                  (long long)positions[i], (long long)st->expected_next);
+    if (positions[i] > st->cap) return fail(DFLASH_EINVAL, "sequence %d: beyond its budget", i);
+    if (h->compute && n_new[i] > 0 &&
+        (!new_rows || !new_rows[i] || !aligned16(new_rows[i])))
+      return fail(DFLASH_EINVAL, "sequence %d: new rows must be a 16-byte aligned device pointer", i);
+  }
+  std::vector<AppendPlan> plans;
+  for (int i = 0; i < n; ++i)
+    plans.push_back(plan_append(h, states[i], n_new[i], new_rows ? new_rows[i] : nullptr));
+  if (!pool_can_cover(h, plans)) return fail(DFLASH_ENOMEM, "KV pool exhausted");
+  commit_plans(h, plans);
+  for (auto &p : plans) p.st->ctx_len = p.new_len;
+  if (!h->compute) {
+    for (int i = 0; i < n; ++i) {
+      states[i]->pending = true;
+      states[i]->pend_pos = positions[i];
+      states[i]->pend_nout = num_drafts;
+      states[i]->expected_next = -1;
+      n_out[i] = num_drafts;
+      for (int t = 0; t < num_drafts; ++t) drafts[i * num_drafts + t] = 0;
+      if (conf) conf[i] = 0.f;
+    }
+    return DFLASH_BOOKKEEPING_ONLY;
+  }
+  // Metadata: sequences, stored ctx rows, live page ids of each window.
+  std::vector<SeqMeta> seq(n);
+  std::vector<RowMeta> rows;
+  std::vector<int32_t> page_ids;
+  rows_of(h, plans, &rows);
+  for (int i = 0; i < n; ++i) {
+    dflash_state *st = states[i];
+    SeqMeta &m = seq[i];
+    m.pos = (int32_t)positions[i];
+    m.ws = (int32_t)window_start(h, positions[i]);
+    m.token = (int32_t)last_tokens[i];
+    m.page_base = (int32_t)page_ids.size();
+    if (m.ws < m.pos)
+      for (int64_t b = m.ws / c.kv_block; b <= (m.pos - 1) / c.kv_block; ++b) {
+        auto it = st->pages.find(b);
+        if (it == st->pages.end())
+          return fail(DFLASH_ESTATE, "internal: window page %lld of sequence %d missing",
+                      (long long)b, i);
+        page_ids.push_back(it->second);
+      }
+  }
+  CallMeta cm;
+  int rc = upload_meta(h, seq, rows, page_ids, s, &cm);
+  if (rc) return rc;
+  rc = forward(h->g, c, h->w, h->b, cm, num_drafts, bitmask, h->M_ctx, s);
+  if (rc) return fail(rc, "%s", last_build_error());
+  // Results to the host: one transfer, one synchronisation.
+  size_t nd = (size_t)num_drafts;
+  CK(cudaMemcpyAsync(h->b.out_host, h->b.out_dev, h->b.out_bytes, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  const int32_t *status = (const int32_t *)h->b.out_host;
+  const uint32_t *dr = (const uint32_t *)(h->b.out_host + h->b.off_drafts);
+  const int32_t *no = (const int32_t *)(h->b.out_host + h->b.off_nout);
+  const float *cf = (const float *)(h->b.out_host + h->b.off_conf);
+  for (int i = 0; i < n; ++i) {
+    n_out[i] = no[i];
+    memcpy(drafts + i * nd, dr + i * nd, nd * sizeof(uint32_t));
+    if (conf) conf[i] = cf[i];
+    states[i]->pending = true;
+    states[i]->pend_pos = positions[i];
+    states[i]->pend_nout = no[i];
+    states[i]->expected_next = -1;
+  }
+  if (*status) {
+    int st_bits = *status;
+    CK(cudaMemsetAsync(h->b.status, 0, sizeof(int), s));
+    return fail(DFLASH_EDEVICE, "device bounds check tripped (status %d)", st_bits);
+  }
+  (void)single;
+  return DFLASH_OK;
+}
+
+}  // namespace dfl

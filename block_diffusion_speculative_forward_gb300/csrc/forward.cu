@@ -1,0 +1,262 @@
+// Device-side construction of a head and the kernel sequence of one propose.
+//
+// Sources: [P1] "Struct BlockDiffusionDraftHead" (spark_model docs),
+// [P2] "BlockDiffusionDraftHead" (metrale docs).
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "forward.h"
+
+namespace dfl {
+
+namespace {
+thread_local std::string g_build_err;
+
+int berr(int code, const char *what, cudaError_t e) {
+  char buf[384];
+  snprintf(buf, sizeof buf, "%s: %s", what, cudaGetErrorString(e));
+  g_build_err = buf;
+  return code;
+}
+
+#define BK(call)                                                  \
+  do {                                                            \
+    cudaError_t e_ = (call);                                      \
+    if (e_ != cudaSuccess) return berr(DFLASH_ECUDA, #call, e_);  \
+  } while (0)
+
+template <class T>
+int dalloc(std::vector<void *> *dev, T **p, size_t count) {
+  *p = nullptr;
+  if (count == 0) return DFLASH_OK;
+  void *q = nullptr;
+  cudaError_t e = cudaMalloc(&q, count * sizeof(T));
+  if (e != cudaSuccess) return berr(DFLASH_ENOMEM, "cudaMalloc", e);
+  dev->push_back(q);
+  *p = (T *)q;
+  return DFLASH_OK;
+}
+
+#define BA(ptr, count)                               \
+  do {                                               \
+    int r_ = dalloc(dev, &(ptr), (size_t)(count));   \
+    if (r_) return r_;                               \
+  } while (0)
+}  // namespace
+
+const char *last_build_error() { return g_build_err.c_str(); }
+
+namespace {
+std::atomic<int64_t> g_launches{0};
+}
+int64_t launch_count() { return g_launches.load(); }
+void count_launches(int n) { g_launches += n; }
+
+int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights *w, int R_max,
+                      int D_max, int M_ctx, Weights *W, Buffers *B, std::vector<void *> *dev,
+                      std::vector<void *> *host) {
+  if (!w->embed || !w->lm_head || !w->fc || !w->hidden_norm || !w->norm || !w->inv_freq ||
+      !w->layers) {
+    g_build_err = "a required weight pointer is NULL";
+    return DFLASH_EINVAL;
+  }
+  if (c.lm_head_dtype == 1 && (!w->lm_head_fp8 || !w->lm_head_scale)) {
+    g_build_err = "lm_head_dtype 1 needs lm_head_fp8 and lm_head_scale";
+    return DFLASH_EINVAL;
+  }
+  if (c.kv_dtype == 1 && !w->kv_scale) {
+    g_build_err = "kv_dtype 1 needs kv_scale";
+    return DFLASH_EINVAL;
+  }
+  W->embed = (const bf16 *)w->embed;
+  W->lm_head = (const bf16 *)w->lm_head;
+  W->lm_fp8 = (const uint8_t *)w->lm_head_fp8;
+  W->lm_scale = w->lm_head_scale;
+  W->lm_is_fp8 = c.lm_head_dtype == 1;
+  W->fc = (const bf16 *)w->fc;
+  W->hidden_norm = (const bf16 *)w->hidden_norm;
+  W->norm = (const bf16 *)w->norm;
+  W->inv_freq = w->inv_freq;
+  W->kv_scale = w->kv_scale;
+  const size_t H = g.H, kv = g.kv, I = g.I, qd = (size_t)g.nq * g.d;
+  // Stitched weights: fused ctx K/V [L*2*kv, H] ([P1]/[P2] field
+  // fused_kv_weight, rows [K0; V0; K1; V1; ...]) and, per layer, QKV
+  // [q; k; v] and gate-up [gate; up], each one GEMM operand.
+  BA(W->w_kv, (size_t)g.L * 2 * kv * H);
+  bf16 *w_qkv = nullptr, *w_gu = nullptr;
+  BA(w_qkv, (size_t)g.L * g.qkv_w * H);
+  BA(w_gu, (size_t)g.L * 2 * I * H);
+  std::vector<const bf16 *> knorm(g.L);
+  W->layers.resize(g.L);
+  for (int l = 0; l < g.L; ++l) {
+    const void *const *p = w->layers + (size_t)l * 11;
+    for (int t = 0; t < 11; ++t)
+      if (!p[t]) {
+        g_build_err = "a layer weight pointer is NULL";
+        return DFLASH_EINVAL;
+      }
+    LayerW &L = W->layers[l];
+    L.in_norm = (const bf16 *)p[0];
+    L.q_norm = (const bf16 *)p[4];
+    L.k_norm = (const bf16 *)p[5];
+    L.post_norm = (const bf16 *)p[7];
+    L.w_o = (const bf16 *)p[6];
+    L.w_down = (const bf16 *)p[10];
+    bf16 *qkv = w_qkv + (size_t)l * g.qkv_w * H;
+    BK(cudaMemcpy(qkv, p[1], qd * H * 2, cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy(qkv + qd * H, p[2], kv * H * 2, cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy(qkv + (qd + kv) * H, p[3], kv * H * 2, cudaMemcpyDeviceToDevice));
+    L.w_qkv = qkv;
+    bf16 *gu = w_gu + (size_t)l * 2 * I * H;
+    BK(cudaMemcpy(gu, p[8], I * H * 2, cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy(gu + I * H, p[9], I * H * 2, cudaMemcpyDeviceToDevice));
+    L.w_gu = gu;
+    bf16 *kvl = W->w_kv + (size_t)l * 2 * kv * H;
+    BK(cudaMemcpy(kvl, p[2], kv * H * 2, cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy(kvl + kv * H, p[3], kv * H * 2, cudaMemcpyDeviceToDevice));
+    knorm[l] = L.k_norm;
+  }
+  const bf16 **kn = nullptr;
+  BA(kn, (size_t)g.L);
+  BK(cudaMemcpy(kn, knorm.data(), sizeof(void *) * g.L, cudaMemcpyHostToDevice));
+  W->k_norm_dev = kn;
+  // RoPE table for every position a block row can reach.
+  const int max_pos = c.max_seq_len + g.gamma;
+  BA(W->cos_t, (size_t)max_pos * (g.d / 2));
+  BA(W->sin_t, (size_t)max_pos * (g.d / 2));
+  BK(rope_table(W->inv_freq, max_pos, g.d / 2, W->cos_t, W->sin_t, 0));
+  // KV pool.
+  const size_t elem = g.kv_fp8 ? 1 : 2;
+  const size_t pool_elems = (size_t)g.pages * g.L * 2 * g.nkv * g.B * g.d;
+  if (pool_elems) {
+    void *pool = nullptr;
+    cudaError_t e = cudaMalloc(&pool, pool_elems * elem);
+    if (e != cudaSuccess) return berr(DFLASH_ENOMEM, "KV pool cudaMalloc", e);
+    dev->push_back(pool);
+    W->pool = pool;
+    BK(cudaMemset(pool, 0, pool_elems * elem));
+  }
+  // Scratch.
+  BA(B->x, (size_t)R_max * H);
+  BA(B->h, (size_t)R_max * std::max(H, I));
+  BA(B->qkv, (size_t)R_max * g.qkv_w);
+  BA(B->q, (size_t)R_max * qd);
+  BA(B->kb, (size_t)R_max * kv);
+  BA(B->vb, (size_t)R_max * kv);
+  BA(B->o, (size_t)R_max * qd);
+  BA(B->gu, (size_t)R_max * 2 * I);
+  BA(B->u, (size_t)R_max * I);
+  BA(B->z, (size_t)D_max * H);
+  BA(B->logits, (size_t)D_max * g.V);
+  BA(B->row_id, (size_t)D_max);
+  BA(B->row_p1, (size_t)D_max);
+  BA(B->ctx_pack, (size_t)M_ctx * g.S);
+  BA(B->ctx_fc, (size_t)M_ctx * H);
+  BA(B->ctx_c, (size_t)M_ctx * H);
+  BA(B->ctx_kv, (size_t)M_ctx * g.L * 2 * kv);
+  BA(B->status, 4);
+  BK(cudaMemset(B->status, 0, 16));
+  const int nb = c.max_batch;
+  B->off_drafts = 16;
+  B->off_nout = (B->off_drafts + (size_t)D_max * 4 + 15) & ~(size_t)15;
+  B->off_conf = (B->off_nout + (size_t)nb * 4 + 15) & ~(size_t)15;
+  B->out_bytes = B->off_conf + (size_t)nb * 4;
+  BA(B->out_dev, B->out_bytes);
+  void *hp = nullptr;
+  BK(cudaMallocHost(&hp, B->out_bytes));
+  host->push_back(hp);
+  B->out_host = (char *)hp;
+  BK(cudaDeviceSynchronize());
+  return DFLASH_OK;
+}
+
+#define FK(call)                                                  \
+  do {                                                            \
+    cudaError_t e_ = (call);                                      \
+    if (e_ != cudaSuccess) return berr(DFLASH_ECUDA, #call, e_);  \
+  } while (0)
+
+// A kernel launch of this library: checked and counted.
+#define LK(call)          \
+  do {                    \
+    FK(call);             \
+    count_launches(1);    \
+  } while (0)
+
+int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *rows, int m,
+               int M_ctx, cudaStream_t s) {
+  const int kvw = g.L * 2 * g.kv;
+  for (int a = 0; a < m; a += M_ctx) {
+    const int mb = std::min(M_ctx, m - a);
+    const RowMeta *r = rows + a;
+    LK(pack_rows(r, mb, g.S, B.ctx_pack, s));
+    LK(gemm_simple(B.ctx_pack, g.S, W.fc, false, nullptr, B.ctx_fc, g.H, mb, g.H, g.S,
+                   EPI_STORE_F32, s));
+    LK(rmsnorm_rows(B.ctx_fc, mb, g.H, W.hidden_norm, g.eps, 0, 0, B.ctx_c, s));
+    LK(gemm_simple(B.ctx_c, g.H, W.w_kv, false, nullptr, B.ctx_kv, kvw, mb, kvw, g.H,
+                   EPI_STORE_F32, s));
+    LK(ctx_kv_write(B.ctx_kv, mb, r, g, W.k_norm_dev, W.cos_t, W.sin_t, W.pool, W.kv_scale,
+                    B.status, s));
+  }
+  return DFLASH_OK;
+}
+
+int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffers &B,
+            const CallMeta &cm, int nd, const int32_t *bitmask, int M_ctx, cudaStream_t s) {
+  if (cm.n_rows) {
+    int rc = ctx_append(g, W, B, cm.rows, cm.n_rows, M_ctx, s);
+    if (rc) return rc;
+  }
+  const int n = cm.n_seq, R = n * g.gamma, D = n * nd;
+  const int qd = g.nq * g.d;
+  const size_t xbytes = (size_t)R * g.H * sizeof(float);
+  LK(embed_block(W.embed, cm.seq, n, g, c.mask_token_id, B.x, B.status, s));
+  if (B.tap_x) FK(cudaMemcpyAsync(B.tap_x, B.x, xbytes, cudaMemcpyDeviceToDevice, s));
+  for (int l = 0; l < g.L; ++l) {
+    const LayerW &L = W.layers[l];
+    LK(rmsnorm_rows(B.x, R, g.H, L.in_norm, g.eps, 0, 0, B.h, s));
+    LK(gemm_simple(B.h, g.H, L.w_qkv, false, nullptr, B.qkv, g.qkv_w, R, g.qkv_w, g.H,
+                   EPI_STORE_F32, s));
+    LK(block_qkv_post(B.qkv, R, cm.seq, g, L.q_norm, L.k_norm, W.cos_t, W.sin_t, B.q, B.kb, B.vb,
+                      s));
+    LK(attention_simple(B.q, B.kb, B.vb, cm.seq, cm.page_ids, n, g, W.pool, l, W.kv_scale, B.o,
+                        B.status, s));
+    LK(gemm_simple(B.o, qd, L.w_o, false, nullptr, B.x, g.H, R, g.H, qd, EPI_ADD_F32, s));
+    LK(rmsnorm_rows(B.x, R, g.H, L.post_norm, g.eps, 0, 0, B.h, s));
+    LK(gemm_simple(B.h, g.H, L.w_gu, false, nullptr, B.gu, 2 * g.I, R, 2 * g.I, g.H,
+                   EPI_STORE_F32, s));
+    LK(swiglu(B.gu, R, g.I, B.u, s));
+    LK(gemm_simple(B.u, g.I, L.w_down, false, nullptr, B.x, g.H, R, g.H, g.I, EPI_ADD_F32, s));
+    if (B.tap_x)
+      FK(cudaMemcpyAsync(B.tap_x + (size_t)(l + 1) * R * g.H, B.x, xbytes,
+                         cudaMemcpyDeviceToDevice, s));
+  }
+  if (B.tap_z) LK(rmsnorm_rows(B.x, R, g.H, W.norm, g.eps, 0, 0, B.tap_z, s));
+  LK(rmsnorm_rows(B.x, D, g.H, W.norm, g.eps, nd, g.gamma, B.z, s));
+  if (B.probe_begin && B.probe_end) FK(cudaEventRecord(B.probe_begin, s));
+  if (W.lm_is_fp8)
+    LK(gemm_simple(B.z, g.H, W.lm_fp8, true, W.lm_scale, B.logits, g.V, D, g.V, g.H,
+                   EPI_STORE_F32, s));
+  else
+    LK(gemm_simple(B.z, g.H, W.lm_head, false, nullptr, B.logits, g.V, D, g.V, g.H,
+                   EPI_STORE_F32, s));
+  if (B.tap_logits)
+    FK(cudaMemcpyAsync(B.tap_logits, B.logits, (size_t)D * g.V * sizeof(float),
+                       cudaMemcpyDeviceToDevice, s));
+  LK(argmax_rows(B.logits, D, g.V, bitmask, nd, B.row_id, B.row_p1, s));
+  if (B.probe_begin && B.probe_end) FK(cudaEventRecord(B.probe_end, s));
+  LK(finalize(B.row_id, B.row_p1, n, nd, B.status, (uint32_t *)(B.out_dev + B.off_drafts),
+              (int32_t *)(B.out_dev + B.off_nout), (float *)(B.out_dev + B.off_conf),
+              (int32_t *)B.out_dev, s));
+  return DFLASH_OK;
+}
+
+cudaError_t gather_kv_rows(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *rows,
+                           int n, int layer, float *k_out, float *v_out, cudaStream_t s) {
+  (void)B;
+  return gather_kv(W.pool, g, layer, rows, n, W.kv_scale, k_out, v_out, s);
+}
+
+}  // namespace dfl

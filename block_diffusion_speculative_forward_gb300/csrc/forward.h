@@ -1,0 +1,85 @@
+// Device side of a head: weights as the kernels see them, scratch buffers,
+// and the kernel sequence of prefill and propose.
+#pragma once
+
+#include <vector>
+
+#include "dflash.h"
+#include "internal.h"
+
+struct dflash_handle;
+struct dflash_state;
+
+namespace dfl {
+
+struct Weights {
+  const bf16 *embed = nullptr, *lm_head = nullptr, *fc = nullptr, *hidden_norm = nullptr,
+             *norm = nullptr;
+  const uint8_t *lm_fp8 = nullptr;
+  const float *lm_scale = nullptr, *inv_freq = nullptr, *kv_scale = nullptr;
+  bool lm_is_fp8 = false;
+  std::vector<LayerW> layers;
+  const bf16 *const *k_norm_dev = nullptr;  // device array of L k_norm gains
+  bf16 *w_kv = nullptr;                     // [L*2*kv, H], rows [K0; V0; K1; V1; ...]
+  float *cos_t = nullptr, *sin_t = nullptr; // [max_seq_len + gamma][d/2]
+  void *pool = nullptr;                     // [pages][L][K|V][nkv][B][d]
+};
+
+struct Buffers {
+  float *x = nullptr;          // [R, H] residual
+  bf16 *h = nullptr;           // [R, H] normed GEMM input
+  float *qkv = nullptr;        // [R, qkv_w]
+  bf16 *q = nullptr, *kb = nullptr, *vb = nullptr, *o = nullptr;
+  float *gu = nullptr;         // [R, 2I]
+  bf16 *u = nullptr;           // [R, I]
+  bf16 *z = nullptr;           // [D, H] final-normed draft rows
+  float *logits = nullptr;     // [D, V]
+  int32_t *row_id = nullptr;
+  float *row_p1 = nullptr;
+  bf16 *ctx_pack = nullptr;    // [M, S]
+  float *ctx_fc = nullptr;     // [M, H]
+  bf16 *ctx_c = nullptr;       // [M, H]
+  float *ctx_kv = nullptr;     // [M, L*2*kv]
+  int *status = nullptr;
+  char *out_dev = nullptr, *out_host = nullptr;
+  size_t out_bytes = 0, off_drafts = 0, off_nout = 0, off_conf = 0;
+  float *tap_x = nullptr;
+  bf16 *tap_z = nullptr;
+  float *tap_logits = nullptr;
+  cudaEvent_t probe_begin = nullptr, probe_end = nullptr;  // around the lm_head stage
+};
+
+struct CallMeta {
+  const SeqMeta *seq = nullptr;
+  const RowMeta *rows = nullptr;
+  const int32_t *page_ids = nullptr;
+  int n_seq = 0, n_rows = 0;
+};
+
+int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights *w, int R_max,
+                      int D_max, int M_ctx, Weights *W, Buffers *B, std::vector<void *> *dev,
+                      std::vector<void *> *host);
+const char *last_build_error();
+
+// Kernels launched by this library since load (all handles).
+int64_t launch_count();
+void count_launches(int n);
+
+// Ctx rows: pack, fc GEMM, hidden_norm, fused K/V GEMM, k_norm + RoPE + paged write.
+int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *rows, int m,
+               int M_ctx, cudaStream_t s);
+
+// The whole propose forward for the call's sequences; results land in B.out_dev.
+int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffers &B,
+            const CallMeta &cm, int nd, const int32_t *bitmask, int M_ctx, cudaStream_t s);
+
+cudaError_t gather_kv_rows(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *rows,
+                           int n, int layer, float *k_out, float *v_out, cudaStream_t s);
+
+int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
+                 const uint32_t *last_tokens, const int64_t *positions,
+                 const void *const *new_rows, const int32_t *n_new, int num_drafts,
+                 const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
+                 void *stream, bool single);
+
+}  // namespace dfl

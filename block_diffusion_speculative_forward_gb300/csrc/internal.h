@@ -1,0 +1,113 @@
+// Internal declarations shared by libdflash's translation units: geometry,
+// per-call device metadata, and the kernel launchers. Nothing here is part of
+// the public ABI (include/dflash.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace dfl {
+
+using bf16 = __nv_bfloat16;
+
+// Geometry of one head, copied into kernels by value.
+struct Geo {
+  int L, H, I, nq, nkv, d, V, gamma, B, S;
+  int kv;        // nkv * d
+  int qkv_w;     // nq*d + 2*kv: width of the stitched QKV output
+  int pages;     // pages in the KV pool
+  int kv_fp8;    // cache dtype
+  float eps;
+};
+
+// One sequence of a propose call.
+struct SeqMeta {
+  int32_t pos;        // block position p (row 0 of the block)
+  int32_t ws;         // window start: ctx positions ws..pos-1 are attended
+  int32_t page_base;  // index in page_ids of logical page ws / B
+  int32_t token;      // last verified token
+};
+
+// One ctx row to compute and store.
+struct RowMeta {
+  int32_t pos;        // target position of the row
+  int32_t page;       // physical page that receives it
+  int32_t slot;       // pos % B
+  int32_t seq;        // sequence index within the call
+  const bf16 *src;    // the row in the caller's stack
+};
+
+// Per-layer weights as kernels see them.
+struct LayerW {
+  const bf16 *in_norm, *q_norm, *k_norm, *post_norm;
+  const bf16 *w_qkv;   // [qkv_w, H] stitched q;k;v
+  const bf16 *w_o;     // [H, nq*d]
+  const bf16 *w_gu;    // [2I, H] stitched gate;up
+  const bf16 *w_down;  // [H, I]
+};
+
+// Bits of the device status word.
+enum : int {
+  ST_TOKEN = 1,   // a token id >= vocab reached the embed gather
+  ST_PAGE = 2,    // a page id outside the pool reached a KV access
+};
+
+// Element offset of (page, layer, kind, kv head, slot, 0) in the KV pool,
+// laid out [page][L][K|V][nkv][B][d].
+__host__ __device__ inline int64_t kv_offset(const Geo &g, int64_t page, int l, int kind, int h,
+                                              int slot) {
+  return ((((page * g.L + l) * 2 + kind) * g.nkv + h) * (int64_t)g.B + slot) * g.d;
+}
+
+// ------------------------------------------------------------- launchers --
+enum GemmEpi { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_STORE_BF16 = 2 };
+
+// C[m, n] (op)= A[m, K] * W[n, K]^T. A bf16 with row stride lda; W bf16 or FP8
+// E4M3 (w_fp8) with optional per-row scale; K % 32 == 0.
+cudaError_t gemm_simple(const bf16 *A, int lda, const void *W, bool w_fp8, const float *wscale,
+                        void *C, int ldc, int m, int n, int K, GemmEpi epi, cudaStream_t s);
+
+// out[i] = bf16(g * x[r] / sqrt(mean(x[r]^2) + eps)); r = i when nd == 0,
+// else the i-th draft row: (i / nd) * gamma + 1 + i % nd.
+cudaError_t rmsnorm_rows(const float *x, int rows, int n, const bf16 *g, float eps, int nd,
+                         int gamma, bf16 *out, cudaStream_t s);
+
+cudaError_t embed_block(const bf16 *E, const SeqMeta *seq, int n_seq, const Geo &g,
+                        uint32_t mask_token, float *x, int *status, cudaStream_t s);
+
+cudaError_t pack_rows(const RowMeta *rows, int m, int S, bf16 *out, cudaStream_t s);
+
+cudaError_t ctx_kv_write(const float *kv, int m, const RowMeta *rows, const Geo &g,
+                         const bf16 *const *k_norm_dev, const float *cos_t, const float *sin_t,
+                         void *pool, const float *kv_scale, int *status, cudaStream_t s);
+
+cudaError_t block_qkv_post(const float *qkv, int R, const SeqMeta *seq, const Geo &g,
+                           const bf16 *q_norm, const bf16 *k_norm, const float *cos_t,
+                           const float *sin_t, bf16 *q, bf16 *kb, bf16 *vb, cudaStream_t s);
+
+cudaError_t attention_simple(const bf16 *q, const bf16 *kb, const bf16 *vb, const SeqMeta *seq,
+                             const int32_t *page_ids, int n_seq, const Geo &g, const void *pool,
+                             int layer, const float *kv_scale, bf16 *o, int *status,
+                             cudaStream_t s);
+
+cudaError_t swiglu(const float *gu, int R, int I, bf16 *u, cudaStream_t s);
+
+// Per draft row: (argmax id or -1 when nothing is allowed, top-1 probability).
+cudaError_t argmax_rows(const float *logits, int rows, int V, const int32_t *bitmask, int nd,
+                        int32_t *row_id, float *row_p1, cudaStream_t s);
+
+// Per sequence: drafts, n_out, conf (and the status word) into out.
+cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int nd,
+                     const int *status, uint32_t *drafts, int32_t *n_out, float *conf,
+                     int32_t *status_out, cudaStream_t s);
+
+cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float *cos_t, float *sin_t,
+                       cudaStream_t s);
+
+cudaError_t gather_kv(const void *pool, const Geo &g, int layer, const RowMeta *rows, int n,
+                      const float *kv_scale, float *k_out, float *v_out, cudaStream_t s);
+
+}  // namespace dfl

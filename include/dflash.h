@@ -1,0 +1,217 @@
+/*
+ * dflash.h — C ABI of libdflash: the propose forward of a block-diffusion
+ * (DFlash-style) speculative-decoding draft head on one sm_103a GPU.
+ *
+ * Sources (API pages of the head this library implements):
+ *   [P1] "Struct BlockDiffusionDraftHead"  (spark_model::layers::dflash_head)
+ *   [P2] "BlockDiffusionDraftHead"         (metrale_model_arch::dflash_head)
+ *   [P3] "Trait DraftProposer"             (spark_model::speculative)
+ *
+ * Conventions for every call:
+ *   - Every call returns a status (DFLASH_OK or a code below). On any error
+ *     the handle and every state are unchanged: a call checks all arguments
+ *     and the KV pool's capacity before it mutates anything.
+ *   - dflash_last_error() returns a message for the last failing call on the
+ *     calling thread.
+ *   - "dev" marks a device pointer, "host" a host pointer. Device work runs on
+ *     the caller's stream (a cudaStream_t passed as void*, NULL = the legacy
+ *     default stream).
+ *   - Ownership: the caller owns the weights, the input stacks and the
+ *     bitmasks, and keeps them alive for the handle's life (weights) or until
+ *     the call's stream work has finished (inputs). The library owns the
+ *     stitched K/V and QKV weights it builds, the paged KV pool, its scratch
+ *     and the states.
+ *   - One handle is driven by one host thread at a time; the KV pool inside a
+ *     handle is guarded by a lock (the Mutex around kv_cache in [P1]).
+ *
+ * Tensor layouts (row-major, bf16 unless noted; a "[out, in]" matrix is a
+ * linear layer's weight, y = x W^T):
+ *   embed, lm_head [vocab, hidden]      shared with the target ([P1] fields
+ *                                        embed_tokens_shared, lm_head_shared)
+ *   fc             [hidden, n_target_layers*target_hidden]   ([P1] field fc)
+ *   hidden_norm, norm [hidden]          RMSNorm gains ([P1] fields)
+ *   inv_freq       [head_dim/2] f32     RoPE table ([P1] field yarn_inv_freq)
+ *   per layer l, 11 pointers in this order:
+ *     in_norm [hidden], q [nq*d, hidden], k [nkv*d, hidden], v [nkv*d, hidden],
+ *     q_norm [d], k_norm [d], o [hidden, nq*d], post_norm [hidden],
+ *     gate [inter, hidden], up [inter, hidden], down [hidden, inter]
+ *   lm_head_fp8    [vocab, hidden] FP8 E4M3 codes, lm_head_scale [vocab] f32
+ *                  ([P1] field lm_head_shared_fp8; logit = scale_v * <z, codes_v>)
+ *   kv_scale       [num_layers][num_kv_heads][2] f32 (K, V) for the FP8 cache
+ *   target stack rows [rows, n_target_layers*target_hidden] bf16, the target's
+ *                  hiddens captured at target_layer_ids, shallow to deep
+ *                  ([P3] propose argument target_hidden_stack)
+ *   bitmask        [ceil(vocab/32)] int32 words per sequence; token t allowed
+ *                  iff bit (t & 31) of word (t >> 5) is set ([P3] propose
+ *                  argument grammar_bitmask)
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dflash_handle dflash_handle;
+typedef struct dflash_state dflash_state;
+
+enum {
+    DFLASH_OK = 0,
+    DFLASH_DECLINED = 1,          /* propose_batch declined: loop dflash_propose ([P3] propose_batch, Ok(None)) */
+    DFLASH_BOOKKEEPING_ONLY = 2,  /* handle built without weights: state updated, nothing computed */
+    DFLASH_EINVAL = -1,           /* bad argument or geometry */
+    DFLASH_ENOMEM = -2,           /* KV pool or device memory exhausted */
+    DFLASH_ESTATE = -3,           /* call out of order (propose twice, after_verify without propose) */
+    DFLASH_EPOSITION = -4,        /* position != ctx_len + n_new, or != the position after_verify set */
+    DFLASH_ECUDA = -5,            /* a CUDA call failed */
+    DFLASH_EDEVICE = -6           /* a kernel's own bounds check tripped (device status word) */
+};
+
+typedef struct {
+    int32_t num_layers, hidden, intermediate, num_q_heads, num_kv_heads, head_dim;
+    int32_t vocab;
+    int32_t gamma;               /* block rows per sequence ([P1] field gamma) */
+    uint32_t mask_token_id;      /* rows 1..gamma-1 of a block embed this id */
+    int32_t n_target_layers;     /* len(target_layer_ids) */
+    int32_t target_hidden;
+    int32_t fc_in_features;      /* the fc weight's input width; must equal n_target_layers*target_hidden
+                                    ([P1] validate_against_target: a mismatch is a hard error) */
+    float rms_eps;               /* 1e-6 ([P1] field rms_norm_eps) */
+    int32_t ctx_window;          /* most past positions attended; 0 = no ctx ([P1]/[P2] field ctx_window) */
+    int32_t kv_block;            /* positions per KV page */
+    int32_t prefill_chunk;       /* ctx rows per fused K/V GEMM pass in prefill */
+    int32_t max_batch;           /* widest propose_batch ([P1] propose_batch_max) */
+    int32_t max_seq_len;         /* per-state position ceiling ([P1] field max_seq_len) */
+    int32_t kv_pool_blocks;      /* pages in the pool; 0 = max_batch * (min(ctx_window, max_seq_len)/kv_block + 2) */
+    int32_t kv_dtype;            /* 0 = bf16 cache ([P2] kv_cache), 1 = FP8 E4M3 with kv_scale ([P1] kv_cache) */
+    int32_t lm_head_dtype;       /* 0 = bf16 lm_head, 1 = FP8 E4M3 codes + per-row scales */
+} dflash_config;
+
+typedef struct {
+    const void *embed, *lm_head;                       /* dev, borrowed */
+    const void *lm_head_fp8; const float *lm_head_scale;/* dev, used when lm_head_dtype == 1 */
+    const void *fc, *hidden_norm, *norm;               /* dev */
+    const float *inv_freq;                             /* dev [head_dim/2] */
+    const float *kv_scale;                             /* dev, used when kv_dtype == 1 */
+    const void *const *layers;                         /* HOST array of num_layers*11 dev pointers */
+} dflash_weights;
+
+/* Build a head ([P1] from_weights). Validates the geometry, stitches the fused
+ * ctx K/V weight [L*2*kv_dim, hidden] with rows [K0; V0; K1; V1; ...]
+ * ([P1]/[P2] field fused_kv_weight) and per-layer QKV / gate-up weights,
+ * builds the RoPE cos/sin table from inv_freq, and allocates the KV pool and
+ * the scratch. weights == NULL builds a bookkeeping-only handle (no device
+ * memory, no kernels) whose prefill/propose only run the page bookkeeping and
+ * return DFLASH_BOOKKEEPING_ONLY; it exists for host-side tests.
+ * Errors: EINVAL (geometry, fc width), ENOMEM, ECUDA. */
+DFLASH_API int dflash_create(const dflash_config *cfg, const dflash_weights *weights, dflash_handle **out);
+DFLASH_API void dflash_destroy(dflash_handle *h);   /* frees every state still alive, then the handle */
+
+/* [P1]/[P3] propose_batch_max: the widest batch one forward carries (max_batch). */
+DFLASH_API int dflash_propose_batch_max(const dflash_handle *h);
+/* [P1]/[P3] block_gamma: the trained block size gamma. */
+DFLASH_API int dflash_block_gamma(const dflash_handle *h);
+
+/* [P3] alloc_state / alloc_state_for. budget_tokens bounds the positions the
+ * state will hold (prompt + max new tokens); INT64_MAX means unknown and
+ * falls back to max_seq_len. Allocates no device memory (pages come from the
+ * shared pool as rows land). Errors: EINVAL. */
+DFLASH_API int dflash_alloc_state(dflash_handle *h, int64_t budget_tokens, dflash_state **out);
+/* [P3] free_state: returns every page the state holds to the pool and frees
+ * the state. Errors: EINVAL (unknown state). */
+DFLASH_API int dflash_free_state(dflash_handle *h, dflash_state *st);
+
+/* Append n_rows ctx rows (target stack rows of positions ctx_len ..
+ * ctx_len+n_rows-1): fc, hidden_norm, fused K/V GEMM, k_norm, RoPE and paged
+ * write ([P1] fields fc, hidden_norm, fused_kv_weight, kv_cache). Rows below
+ * ctx_len+n_rows-ctx_window are neither computed nor stored; the rest run in
+ * chunks of prefill_chunk rows. Asynchronous on the stream.
+ * stack: dev [n_rows, n_target_layers*target_hidden] bf16, rows 16-byte aligned.
+ * Errors: EINVAL, ESTATE (a propose awaits after_verify), ENOMEM (pool). */
+DFLASH_API int dflash_prefill(dflash_handle *h, dflash_state *st, const void *stack, int32_t n_rows,
+                   void *stream);
+
+/* [P3] propose: append the n_new target stack rows of positions
+ * ctx_len..position-1 (as dflash_prefill), then run the gamma-row block
+ * (last_token at `position`, mask_token_id at position+1..position+gamma-1)
+ * through the layers, the final norm and the lm_head, and return the argmax
+ * of block rows 1..num_drafts. position must equal ctx_len + n_new, and,
+ * after dflash_after_verify(k), the previous position + k + 1.
+ *   new_rows: dev [n_new, stack width] bf16 or NULL when n_new == 0
+ *   num_drafts: 1 .. gamma-1
+ *   bitmask: dev [ceil(vocab/32)] int32 or NULL (unconstrained)
+ *   drafts: host [num_drafts] u32; n_out: host, drafts produced (0 when the
+ *     bitmask allows no token); conf: host f32 or NULL — chain confidence, the
+ *     minimum over drafts of the top-1 softmax probability ([P1]/[P3]
+ *     last_confidence), 0 when n_out == 0.
+ * Synchronises the stream once (the drafts are returned on the host).
+ * Errors: EINVAL, ESTATE, EPOSITION, ENOMEM, ECUDA, EDEVICE. */
+DFLASH_API int dflash_propose(dflash_handle *h, dflash_state *st, uint32_t last_token, int64_t position,
+                   const void *new_rows, int32_t n_new, int32_t num_drafts,
+                   const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
+                   void *stream);
+
+/* [P1]/[P2]/[P3] propose_batch: the same as n dflash_propose calls, with one
+ * forward over n*gamma rows. Row i of every array belongs to sequence i.
+ * Returns DFLASH_DECLINED (nothing changed) for n < 2 or n > max_batch.
+ *   states: host [n]; last_tokens: host [n]; positions: host [n];
+ *   new_rows: host [n] array of dev pointers (NULL where n_new[i] == 0);
+ *   n_new: host [n]; bitmask: dev [n][ceil(vocab/32)] int32 or NULL;
+ *   drafts: host [n][num_drafts]; n_out: host [n]; conf: host [n] or NULL.
+ * Pages: all sequences retire first, then take pages, in sequence order.
+ * Errors: as dflash_propose; EINVAL also for a repeated state. */
+DFLASH_API int dflash_propose_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
+                         const uint32_t *last_tokens, const int64_t *positions,
+                         const void *const *new_rows, const int32_t *n_new, int32_t num_drafts,
+                         const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
+                         void *stream);
+
+/* [P3] after_verify: the target accepted num_accepted (0..n_out) drafts of
+ * the last propose. The next propose sits at position + num_accepted + 1 and
+ * brings the num_accepted + 1 target rows of positions position ..
+ * position + num_accepted. Pages below that propose's window return to the
+ * pool now. Host-only. Errors: EINVAL, ESTATE. */
+DFLASH_API int dflash_after_verify(dflash_handle *h, dflash_state *st, int32_t num_accepted);
+
+/* Message of the last failing call on this thread ("" if none). */
+DFLASH_API const char *dflash_last_error(void);
+
+/* ---- inspection, for tests ---------------------------------------------- */
+/* ctx_len, the first live logical page (-1 if none) and the physical ids of
+ * the live logical pages first..last (table, host, capacity cap). Returns the
+ * number of live pages, or a negative status. */
+DFLASH_API int dflash_debug_state(const dflash_state *st, int64_t *ctx_len, int32_t *first_block,
+                       int32_t *table, int32_t cap);
+/* Pages in use / in the pool. */
+DFLASH_API int dflash_debug_pool(const dflash_handle *h, int32_t *in_use, int32_t *total);
+/* Stored K and V of one layer at positions pos0..pos0+n-1 (all live),
+ * dequantised to f32: k_out, v_out dev [n, num_kv_heads, head_dim]. */
+DFLASH_API int dflash_debug_gather_kv(dflash_handle *h, const dflash_state *st, int32_t layer, int64_t pos0,
+                           int32_t n, float *k_out, float *v_out, void *stream);
+/* Taps filled by every later propose* (NULL disables each):
+ * x_taps dev f32 [num_layers+1][rows][hidden] (the residual entering each
+ * layer and leaving the last); z dev bf16 [rows][hidden] (final norm);
+ * logits dev f32 [n*num_drafts][vocab] (draft rows, sequence-major).
+ * rows = n*gamma of the call. The logits tap adds a separate GEMM. */
+/* Timing probe: when both events are non-NULL, every later propose* records
+ * ev_begin before and ev_end after its lm_head stage (the GEMM over the vocab
+ * and the per-row argmax/confidence reduction), on the call's stream. Events
+ * are the caller's cudaEvent_t. NULL, NULL disables it. */
+DFLASH_API int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end);
+/* Kernels this library has launched since it was loaded (all handles). */
+DFLASH_API int64_t dflash_debug_launch_count(void);
+DFLASH_API int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

@@ -1,0 +1,147 @@
+"""Shared helpers of the GPU parity tests: build the oracle and the library
+head from the same seeded CPU weights, and compare results with the
+tolerances of the parity gate:
+  * block tables, ctx_len, first page: bit-exact;
+  * residual taps, final z, gathered ctx K/V: max-abs 3e-2;
+  * logits: per row max|diff| / max|ref| <= 2e-2 (5e-2 on FP8 paths);
+  * draft ids: exact wherever the oracle's masked top-1 - top-2 gap > 1e-2;
+  * confidence: |diff| <= 1e-2."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from block_diffusion_speculative_forward_gb300 import binding as B
+from block_diffusion_speculative_forward_gb300 import synthetic as syn
+
+HIDDEN_TOL = 3e-2
+LOGIT_TOL = 2e-2
+LOGIT_TOL_FP8 = 5e-2
+GAP = 1e-2
+CONF_TOL = 1e-2
+
+
+def cfg_for(geom, **kw):
+    c = dict(num_layers=geom.num_layers, hidden=geom.hidden, intermediate=geom.intermediate,
+             num_q_heads=geom.num_q_heads, num_kv_heads=geom.num_kv_heads,
+             head_dim=geom.head_dim, vocab=geom.vocab, gamma=geom.gamma,
+             mask_token_id=geom.mask_token_id, n_target_layers=geom.n_target_layers,
+             target_hidden=geom.target_hidden, rms_eps=geom.rms_eps,
+             ctx_window=geom.ctx_window, kv_block=geom.kv_block,
+             prefill_chunk=geom.prefill_chunk, max_batch=4, max_seq_len=9216,
+             kv_pool_blocks=0, kv_dtype=0, lm_head_dtype=0)
+    c.update(kw)
+    return c
+
+
+class Pair:
+    """Oracle and library heads over the same weights."""
+
+    def __init__(self, geom, seed, cfg_kw=None, lm_fp8=False, kv_fp8=False, taps=True,
+                 max_rows=None):
+        self.geom = geom
+        self.cfg = cfg_for(geom, **(cfg_kw or {}),
+                           kv_dtype=int(kv_fp8), lm_head_dtype=int(lm_fp8))
+        self.w = syn.make_weights(geom, seed, lm_head_fp8=lm_fp8, kv_fp8=kv_fp8)
+        self.ora = oracle.DraftHeadOracle(self.cfg, self.w)
+        self.wd = B.weights_to_device(self.w)
+        self.lib = B.DraftHead(self.cfg, self.wd)
+        self.fp8 = lm_fp8 or kv_fp8
+        if taps:
+            rows = max_rows or self.cfg["max_batch"] * geom.gamma
+            self.tx = torch.zeros((geom.num_layers + 1, rows, geom.hidden), device="cuda")
+            self.tz = torch.zeros((rows, geom.hidden), dtype=torch.bfloat16, device="cuda")
+            self.tl = torch.zeros((rows, geom.vocab), device="cuda")
+            self.lib.set_taps(self.tx, self.tz, self.tl)
+
+
+def gaps(logits: torch.Tensor, allowed) -> torch.Tensor:
+    lg = logits.to(torch.float64)
+    if allowed is not None:
+        lg = torch.where(allowed[None, :], lg, torch.full_like(lg, -math.inf))
+    top = torch.topk(lg, 2, dim=1).values
+    return top[:, 0] - top[:, 1]
+
+
+def check_drafts(ref_drafts, got_drafts, ref_logits, allowed):
+    g = gaps(ref_logits, allowed)
+    n_checked = 0
+    for i, (a, b) in enumerate(zip(ref_drafts, got_drafts)):
+        if g[i] > GAP:
+            assert a == b, f"draft {i}: oracle {a} gpu {b} (gap {float(g[i]):.4f})"
+            n_checked += 1
+    return n_checked
+
+
+def check_logits(ref: torch.Tensor, got: torch.Tensor, tol: float):
+    ref = ref.to(torch.float64).cpu()
+    got = got.to(torch.float64).cpu()
+    for i in range(ref.shape[0]):
+        rel = float((ref[i] - got[i]).abs().max() / ref[i].abs().max())
+        assert rel <= tol, f"logit row {i}: rel err {rel:.3e} > {tol}"
+
+
+def check_abs(ref, got, tol, what):
+    ref = torch.as_tensor(ref).to(torch.float64).cpu()
+    got = torch.as_tensor(got).to(torch.float64).cpu()
+    err = float((ref - got).abs().max())
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol}"
+    return err
+
+
+def check_seq(pair: Pair, ref_tap: dict, ref_out, got_out, seq_idx: int, n_seq: int,
+              nd: int, allowed=None, hidden=True):
+    """Compare one sequence of a propose call: taps, logits, drafts, conf."""
+    g = pair.geom.gamma
+    torch.cuda.synchronize()
+    if hidden:
+        for l, xr in enumerate(ref_tap["x"]):
+            check_abs(xr, pair.tx[l, seq_idx * g:(seq_idx + 1) * g], HIDDEN_TOL, f"x tap {l}")
+        check_abs(ref_tap["z"], pair.tz[seq_idx * g:(seq_idx + 1) * g].float(), HIDDEN_TOL, "z")
+    got_logits = pair.tl[seq_idx * nd:(seq_idx + 1) * nd]
+    check_logits(ref_tap["logits"], got_logits, LOGIT_TOL_FP8 if pair.fp8 else LOGIT_TOL)
+    ref_d, ref_n, ref_c = ref_out
+    got_d, got_n, got_c = got_out
+    assert ref_n == got_n
+    n = check_drafts(ref_d[:ref_n], got_d[:got_n], ref_tap["logits"], allowed)
+    if got_c is not None:
+        assert abs(ref_c - got_c) <= CONF_TOL, (ref_c, got_c)
+    return n
+
+
+def check_kv(pair: Pair, so, sl, positions):
+    positions = list(positions)
+    if not positions:
+        return
+    for l in range(pair.geom.num_layers):
+        k, v = pair.lib.gather_kv(sl, l, positions[0], len(positions))
+        kr, vr = pair.ora.gather_kv(so, l, positions)
+        if pair.cfg["kv_dtype"] == 1:
+            check_fp8_kv(pair, l, kr, k, 0)
+            check_fp8_kv(pair, l, vr, v, 1)
+        else:
+            check_abs(kr, k, HIDDEN_TOL, f"ctx K layer {l}")
+            check_abs(vr, v, HIDDEN_TOL, f"ctx V layer {l}")
+
+
+def check_fp8_kv(pair, l, ref, got, kind):
+    """FP8 cache: codes equal, or one code apart where the oracle's unrounded
+    value sits near the rounding midpoint (the two sides' fp32 inputs differ
+    by GEMM summation order only)."""
+    s = pair.w["kv_scale"][l, :, kind].to(torch.float64)[None, :, None]
+    rc = (ref.to(torch.float64).cpu() / s)
+    gc = (got.to(torch.float64).cpu() / s)
+    diff = (rc - gc).abs()
+    bad = diff > 1e-9
+    frac = float(bad.double().mean())
+    # a code step is at most 1/8 of the code's magnitude (3 mantissa bits)
+    step_ok = (diff <= rc.abs().clamp(min=2 ** -6) * 0.125 + 1e-9)
+    assert bool(step_ok.all()), "FP8 KV codes more than one step apart"
+    assert frac <= 2e-3, f"FP8 KV: {frac:.2e} of codes differ"
+
+
+def assert_tables(pair, so, sl):
+    assert pair.lib.debug_state(sl) == pair.ora.block_table(so)

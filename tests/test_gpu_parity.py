@@ -1,0 +1,152 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, on the
+same seeded inputs. Small geometries are compared element by element; the full
+geometry is compared on sampled outputs (drafts, confidence, logits rows,
+residual taps, gathered ctx K/V), at the configuration the bench times."""
+from dataclasses import replace
+
+import pytest
+import torch
+
+from block_diffusion_speculative_forward_gb300 import synthetic as syn
+from tests.parity import (Pair, assert_tables, check_abs, check_kv, check_seq, HIDDEN_TOL)
+from tests.test_oracle_pins import MICRO
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from block_diffusion_speculative_forward_gb300 import build
+    build.build()
+
+
+def _prefill(pair, n_rows, seed, idx=0):
+    so, sl = pair.ora.alloc_state(), pair.lib.alloc_state()
+    stack = syn.make_stack(pair.geom, n_rows, seed, idx)
+    pair.ora.prefill(so, stack)
+    pair.lib.prefill(sl, stack.cuda())
+    return so, sl, stack
+
+
+def _propose(pair, so, sl, tok, pos, rows, nd, mask=None):
+    taps = {}
+    ref = pair.ora.propose(so, tok, pos, rows, nd, bitmask=mask, taps=taps)
+    got = pair.lib.propose(sl, tok, pos, None if rows is None else rows.cuda(), nd,
+                           bitmask=None if mask is None else mask.cuda())
+    return taps["seq"][0], ref, got
+
+
+def test_tiny_single_sequence():
+    """Tiny drafter: prefill 64 rows, propose at 64 with 3 drafts."""
+    pair = Pair(syn.TINY, 1001)
+    so, sl, _ = _prefill(pair, 64, 1001)
+    assert_tables(pair, so, sl)
+    check_kv(pair, so, sl, range(64))
+    tap, ref, got = _propose(pair, so, sl, 1234, 64, None, 3)
+    n = check_seq(pair, tap, ref, got, 0, 1, 3)
+    assert n >= 1
+    assert_tables(pair, so, sl)
+
+
+@pytest.mark.parametrize("window", [24, 0])
+def test_micro_window_rounds_and_trim(window):
+    """Window smaller than the context, pages of 8 rows, propose/after_verify
+    rounds with varying accept counts: drafts, taps, tables and KV each round."""
+    geom = replace(MICRO, ctx_window=window)
+    pair = Pair(geom, 31)
+    so, sl, _ = _prefill(pair, 45, 31)
+    assert_tables(pair, so, sl)
+    p, n_new = 45, 0
+    rows = syn.make_stack(geom, 200, 31, idx=1)
+    used = 0
+    for k in [0, 3, 1, 2, 0, 3, 3, 1]:
+        r = rows[used:used + n_new] if n_new else None
+        used += n_new
+        tap, ref, got = _propose(pair, so, sl, (7 * p) % geom.vocab, p, r, 3)
+        check_seq(pair, tap, ref, got, 0, 1, 3)
+        assert_tables(pair, so, sl)
+        pair.ora.after_verify(so, k)
+        pair.lib.after_verify(sl, k)
+        assert_tables(pair, so, sl)
+        p, n_new = p + k + 1, k + 1
+    ws = max(0, p - 1 - window) if window else p
+    check_kv(pair, so, sl, range(ws, p - n_new))
+
+
+def test_tiny_bitmask_cases():
+    pair = Pair(syn.TINY, 1011)
+    so, sl, _ = _prefill(pair, 40, 1011)
+    V = syn.TINY.vocab
+    words = (V + 31) // 32
+    mask = syn.make_bitmask(V, 1, 1011)[0]
+    tap, ref, got = _propose(pair, so, sl, 5, 40, None, 3, mask)
+    allowed = oracle.bitmask_allowed(mask, V)
+    check_seq(pair, tap, ref, got, 0, 1, 3, allowed=allowed)
+    for d in got[0]:
+        assert allowed[d]
+    # one allowed token: every draft is that token with confidence 1
+    one = torch.zeros(words, dtype=torch.int32)
+    one[77 >> 5] = 1 << (77 & 31)
+    pair.ora.after_verify(so, 0)
+    pair.lib.after_verify(sl, 0)
+    r = syn.make_stack(syn.TINY, 1, 1011, idx=5)
+    got = pair.lib.propose(sl, 9, 41, r.cuda(), 3, bitmask=one.cuda())
+    ref = pair.ora.propose(so, 9, 41, r, 3, bitmask=one)
+    assert got[0] == [77, 77, 77] and got[1] == 3 and abs(got[2] - 1.0) < 1e-6 and ref[0] == got[0]
+    # nothing allowed: no drafts, confidence 0
+    pair.ora.after_verify(so, 0)
+    pair.lib.after_verify(sl, 0)
+    r = syn.make_stack(syn.TINY, 1, 1011, idx=6)
+    zero = torch.zeros(words, dtype=torch.int32)
+    got = pair.lib.propose(sl, 9, 42, r.cuda(), 3, bitmask=zero.cuda())
+    ref = pair.ora.propose(so, 9, 42, r, 3, bitmask=zero)
+    assert got[1] == 0 and got[2] == 0.0 and ref[1] == 0
+
+
+def test_tiny_batch_ragged():
+    """propose_batch over 3 sequences with ragged ctx and new rows."""
+    pair = Pair(syn.TINY, 1021, cfg_kw=dict(max_batch=4))
+    ctx = [16, 61, 33]
+    so, sl = [], []
+    for i, c in enumerate(ctx):
+        a, b, _ = _prefill(pair, c, 1021, idx=i)
+        so.append(a)
+        sl.append(b)
+    n_new = [1, 3, 0]
+    rows = [syn.make_stack(syn.TINY, m, 1021, idx=10 + i) if m else None
+            for i, m in enumerate(n_new)]
+    pos = [c + m for c, m in zip(ctx, n_new)]
+    toks = [11, 4000, 4095]
+    masks = syn.make_bitmask(syn.TINY.vocab, 3, 1021)
+    taps = {}
+    ref = pair.ora.propose_batch(so, toks, pos, rows, 3, bitmask=masks, taps=taps)
+    got = pair.lib.propose_batch(sl, toks, pos, [None if r is None else r.cuda() for r in rows],
+                                 3, bitmask=masks.cuda())
+    for i in range(3):
+        allowed = oracle.bitmask_allowed(masks[i], syn.TINY.vocab)
+        check_seq(pair, taps["seq"][i], ref[i], got[i], i, 3, 3, allowed=allowed)
+        assert_tables(pair, so[i], sl[i])
+        check_kv(pair, so[i], sl[i], range(0, pos[i]))
+
+
+def test_tiny_fp8_kv_and_lm_head():
+    pair = Pair(syn.TINY, 1031, lm_fp8=True, kv_fp8=True)
+    so, sl, _ = _prefill(pair, 50, 1031)
+    check_kv(pair, so, sl, range(50))
+    tap, ref, got = _propose(pair, so, sl, 3, 50, None, 3)
+    check_seq(pair, tap, ref, got, 0, 1, 3)
+
+
+def test_full_geometry_single_sequence():
+    """Shipped geometry, 1 sequence: prefill 1023 rows, then propose at 1024
+    with one new row and 15 drafts (the timed single-sequence step)."""
+    geom = syn.FULL
+    pair = Pair(geom, 1002, cfg_kw=dict(max_batch=1))
+    so, sl, _ = _prefill(pair, 1023, 1002)
+    row = syn.make_stack(geom, 1, 1002, idx=1)
+    tap, ref, got = _propose(pair, so, sl, 424242, 1024, row, 15)
+    n = check_seq(pair, tap, ref, got, 0, 1, 15)
+    assert n >= 10, "too few drafts had a decisive logit gap to check"
+    assert_tables(pair, so, sl)
+    check_kv(pair, so, sl, [0, 1, 511, 1022, 1023][:1] + list(range(1019, 1024)))

@@ -18,9 +18,9 @@ GOLDEN = __import__("os").path.join(__import__("os").path.dirname(__file__), "go
 
 # A micro drafter: 2 layers so that the layer loop and the fused K/V row order
 # are exercised, GQA groups of 2, a window smaller than the context.
-MICRO = syn.Geometry(num_layers=2, hidden=64, intermediate=96, num_q_heads=4,
-                     num_kv_heads=2, head_dim=16, vocab=256, gamma=4, mask_token_id=255,
-                     n_target_layers=2, target_hidden=32, rope_theta=1e4,
+MICRO = syn.Geometry(num_layers=2, hidden=128, intermediate=128, num_q_heads=4,
+                     num_kv_heads=2, head_dim=64, vocab=256, gamma=4, mask_token_id=255,
+                     n_target_layers=2, target_hidden=64, rope_theta=1e4,
                      ctx_window=24, kv_block=8, prefill_chunk=10)
 
 
