@@ -174,6 +174,9 @@ def run_ours(args):
     # device-timed region, inputs resident
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pb, pe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pb.record(stream)   # creates the events so their handles exist
+    pe.record(stream)
+    torch.cuda.synchronize()
     import ctypes as C
     lib.dflash_debug_set_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
     lib.dflash_debug_launch_count.restype = C.c_int64

@@ -506,6 +506,46 @@ int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end) {
 
 int64_t dflash_debug_launch_count(void) { return dfl::launch_count(); }
 
+int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t m, int32_t n_w, int32_t k,
+                      int32_t grid_cap, void *stream) {
+  if (!w || !x || !y || m <= 0 || n_w <= 0 || k <= 0 || k % 64)
+    return fail(DFLASH_EINVAL, "bad GEMM arguments");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int bn = dfl::tc::pick_bn(m);
+  CUtensorMap mw, mx;
+  if (!dfl::tc::make_map_2d(&mw, w, false, n_w, k, 128) ||
+      !dfl::tc::make_map_2d(&mx, x, false, m, k, bn))
+    return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled failed");
+  dfl::GemmParams p{};
+  p.m_act = m;
+  p.n_w = n_w;
+  p.k = k;
+  p.epi = dfl::EPI_TC_STORE_F32;
+  p.out = y;
+  p.ldo = n_w;
+  p.grid_cap = grid_cap;
+  const int tiles = ((n_w + 127) / 128) * ((m + bn - 1) / bn);
+  void *ws = nullptr, *cnt = nullptr, *status = nullptr;
+  CK(cudaMalloc(&ws, dfl::tc::ws_floats(dfl::tc::num_sms()) * sizeof(float)));
+  CK(cudaMalloc(&cnt, sizeof(int) * (size_t)tiles + 16));
+  CK(cudaMalloc(&status, 16));
+  CK(cudaMemsetAsync(cnt, 0, sizeof(int) * (size_t)tiles + 16, s));
+  CK(cudaMemsetAsync(status, 0, 16, s));
+  p.ws = (float *)ws;
+  p.counters = (int *)cnt;
+  p.status = (int *)status;
+  cudaError_t e = dfl::tc::gemm(mw, mx, bn, p, s);
+  int st = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&st, status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  cudaFree(ws);
+  cudaFree(cnt);
+  cudaFree(status);
+  CK(e);
+  if (st) return fail(DFLASH_EDEVICE, "GEMM status %d", st);
+  return DFLASH_OK;
+}
+
 int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits) {
   if (!h) return fail(DFLASH_EINVAL, "NULL handle");
   h->b.tap_x = x_taps;

@@ -7,6 +7,8 @@
 #include <cstring>
 #include <string>
 
+#include <algorithm>
+
 #include "forward.h"
 
 namespace dfl {
@@ -122,6 +124,27 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(kn, (size_t)g.L);
   BK(cudaMemcpy(kn, knorm.data(), sizeof(void *) * g.L, cudaMemcpyHostToDevice));
   W->k_norm_dev = kn;
+  // TMA maps of every weight operand.
+  {
+    bool ok = tc::make_map_2d(&W->map_fc, W->fc, false, H, g.S, 128) &&
+              tc::make_map_2d(&W->map_wkv, W->w_kv, false, (int64_t)g.L * 2 * kv, H, 128) &&
+              tc::make_map_2d(&W->map_lm, W->lm_head, false, g.V, H, 128);
+    W->map_qkv.resize(g.L);
+    W->map_o.resize(g.L);
+    W->map_gu.resize(g.L);
+    W->map_down.resize(g.L);
+    for (int l = 0; l < g.L && ok; ++l) {
+      const LayerW &L = W->layers[l];
+      ok = tc::make_map_2d(&W->map_qkv[l], L.w_qkv, false, g.qkv_w, H, 128) &&
+           tc::make_map_2d(&W->map_o[l], L.w_o, false, H, qd, 128) &&
+           tc::make_map_2d(&W->map_gu[l], L.w_gu, false, 2 * I, H, 128) &&
+           tc::make_map_2d(&W->map_down[l], L.w_down, false, H, I, 128);
+    }
+    if (!ok) {
+      g_build_err = "cuTensorMapEncodeTiled failed for a weight operand";
+      return DFLASH_ECUDA;
+    }
+  }
   // RoPE table for every position a block row can reach.
   const int max_pos = c.max_seq_len + g.gamma;
   BA(W->cos_t, (size_t)max_pos * (g.d / 2));
@@ -149,7 +172,7 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->gu, (size_t)R_max * 2 * I);
   BA(B->u, (size_t)R_max * I);
   BA(B->z, (size_t)D_max * H);
-  BA(B->logits, (size_t)D_max * g.V);
+  BA(B->logits, c.lm_head_dtype == 1 ? (size_t)D_max * g.V : 0);
   BA(B->row_id, (size_t)D_max);
   BA(B->row_p1, (size_t)D_max);
   BA(B->ctx_pack, (size_t)M_ctx * g.S);
@@ -158,6 +181,30 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->ctx_kv, (size_t)M_ctx * g.L * 2 * kv);
   BA(B->status, 4);
   BK(cudaMemset(B->status, 0, 16));
+  // Stream-K workspace and counters; lm_head partials.
+  const int sms = tc::num_sms();
+  BA(B->ws, tc::ws_floats(sms));
+  const int vt = (g.V + 127) / 128;
+  B->n_counters = std::max(vt * ((D_max + 255) / 256 + 1),
+                           ((std::max({g.qkv_w, 2 * g.I, g.L * 2 * g.kv, g.H}) + 127) / 128) *
+                               ((std::max(R_max, M_ctx) + 15) / 16));
+  BA(B->counters, (size_t)B->n_counters);
+  BK(cudaMemset(B->counters, 0, sizeof(int) * (size_t)B->n_counters));
+  BA(B->lm_part, (size_t)D_max * vt);
+  // TMA maps of the activation operands, one per tile width.
+  {
+    struct A { int id; const void *p; int64_t rows, cols; } acts[ACT_COUNT] = {
+        {ACT_H, B->h, R_max, (int64_t)H}, {ACT_O, B->o, R_max, (int64_t)qd},
+        {ACT_U, B->u, R_max, (int64_t)I}, {ACT_Z, B->z, D_max, (int64_t)H},
+        {ACT_PACK, B->ctx_pack, M_ctx, (int64_t)g.S}, {ACT_C, B->ctx_c, M_ctx, (int64_t)H}};
+    const int bns[BN_COUNT] = {16, 32, 64, 128, 256};
+    for (auto &a : acts)
+      for (int j = 0; j < BN_COUNT; ++j)
+        if (!tc::make_map_2d(&B->act_map[a.id][j], a.p, false, a.rows, a.cols, bns[j])) {
+          g_build_err = "cuTensorMapEncodeTiled failed for an activation operand";
+          return DFLASH_ECUDA;
+        }
+  }
   const int nb = c.max_batch;
   B->off_drafts = 16;
   B->off_nout = (B->off_drafts + (size_t)D_max * 4 + 15) & ~(size_t)15;
@@ -185,6 +232,25 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     count_launches(1);    \
   } while (0)
 
+namespace {
+// One tensor-core GEMM: out[m_act, n_w] (epi)= act[m_act, k] * W[n_w, k]^T.
+cudaError_t tc_gemm(const Buffers &B, const CUtensorMap &map_w, ActBuf act, int m_act, int n_w,
+                    int k, int epi, void *out, int ldo, cudaStream_t s) {
+  GemmParams p{};
+  p.m_act = m_act;
+  p.n_w = n_w;
+  p.k = k;
+  p.epi = epi;
+  p.out = out;
+  p.ldo = ldo;
+  p.ws = B.ws;
+  p.counters = B.counters;
+  p.status = B.status;
+  const int bn = tc::pick_bn(m_act);
+  return tc::gemm(map_w, B.act_map[act][bn_index(bn)], bn, p, s);
+}
+}  // namespace
+
 int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *rows, int m,
                int M_ctx, cudaStream_t s) {
   const int kvw = g.L * 2 * g.kv;
@@ -192,11 +258,9 @@ int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *
     const int mb = std::min(M_ctx, m - a);
     const RowMeta *r = rows + a;
     LK(pack_rows(r, mb, g.S, B.ctx_pack, s));
-    LK(gemm_simple(B.ctx_pack, g.S, W.fc, false, nullptr, B.ctx_fc, g.H, mb, g.H, g.S,
-                   EPI_STORE_F32, s));
+    LK(tc_gemm(B, W.map_fc, ACT_PACK, mb, g.H, g.S, EPI_TC_STORE_F32, B.ctx_fc, g.H, s));
     LK(rmsnorm_rows(B.ctx_fc, mb, g.H, W.hidden_norm, g.eps, 0, 0, B.ctx_c, s));
-    LK(gemm_simple(B.ctx_c, g.H, W.w_kv, false, nullptr, B.ctx_kv, kvw, mb, kvw, g.H,
-                   EPI_STORE_F32, s));
+    LK(tc_gemm(B, W.map_wkv, ACT_C, mb, kvw, g.H, EPI_TC_STORE_F32, B.ctx_kv, kvw, s));
     LK(ctx_kv_write(B.ctx_kv, mb, r, g, W.k_norm_dev, W.cos_t, W.sin_t, W.pool, W.kv_scale,
                     B.status, s));
   }
@@ -217,18 +281,16 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   for (int l = 0; l < g.L; ++l) {
     const LayerW &L = W.layers[l];
     LK(rmsnorm_rows(B.x, R, g.H, L.in_norm, g.eps, 0, 0, B.h, s));
-    LK(gemm_simple(B.h, g.H, L.w_qkv, false, nullptr, B.qkv, g.qkv_w, R, g.qkv_w, g.H,
-                   EPI_STORE_F32, s));
+    LK(tc_gemm(B, W.map_qkv[l], ACT_H, R, g.qkv_w, g.H, EPI_TC_STORE_F32, B.qkv, g.qkv_w, s));
     LK(block_qkv_post(B.qkv, R, cm.seq, g, L.q_norm, L.k_norm, W.cos_t, W.sin_t, B.q, B.kb, B.vb,
                       s));
     LK(attention_simple(B.q, B.kb, B.vb, cm.seq, cm.page_ids, n, g, W.pool, l, W.kv_scale, B.o,
                         B.status, s));
-    LK(gemm_simple(B.o, qd, L.w_o, false, nullptr, B.x, g.H, R, g.H, qd, EPI_ADD_F32, s));
+    LK(tc_gemm(B, W.map_o[l], ACT_O, R, g.H, qd, EPI_TC_ADD_F32, B.x, g.H, s));
     LK(rmsnorm_rows(B.x, R, g.H, L.post_norm, g.eps, 0, 0, B.h, s));
-    LK(gemm_simple(B.h, g.H, L.w_gu, false, nullptr, B.gu, 2 * g.I, R, 2 * g.I, g.H,
-                   EPI_STORE_F32, s));
+    LK(tc_gemm(B, W.map_gu[l], ACT_H, R, 2 * g.I, g.H, EPI_TC_STORE_F32, B.gu, 2 * g.I, s));
     LK(swiglu(B.gu, R, g.I, B.u, s));
-    LK(gemm_simple(B.u, g.I, L.w_down, false, nullptr, B.x, g.H, R, g.H, g.I, EPI_ADD_F32, s));
+    LK(tc_gemm(B, W.map_down[l], ACT_U, R, g.H, g.I, EPI_TC_ADD_F32, B.x, g.H, s));
     if (B.tap_x)
       FK(cudaMemcpyAsync(B.tap_x + (size_t)(l + 1) * R * g.H, B.x, xbytes,
                          cudaMemcpyDeviceToDevice, s));
@@ -236,17 +298,36 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   if (B.tap_z) LK(rmsnorm_rows(B.x, R, g.H, W.norm, g.eps, 0, 0, B.tap_z, s));
   LK(rmsnorm_rows(B.x, D, g.H, W.norm, g.eps, nd, g.gamma, B.z, s));
   if (B.probe_begin && B.probe_end) FK(cudaEventRecord(B.probe_begin, s));
-  if (W.lm_is_fp8)
+  if (W.lm_is_fp8) {
     LK(gemm_simple(B.z, g.H, W.lm_fp8, true, W.lm_scale, B.logits, g.V, D, g.V, g.H,
                    EPI_STORE_F32, s));
-  else
-    LK(gemm_simple(B.z, g.H, W.lm_head, false, nullptr, B.logits, g.V, D, g.V, g.H,
-                   EPI_STORE_F32, s));
-  if (B.tap_logits)
-    FK(cudaMemcpyAsync(B.tap_logits, B.logits, (size_t)D * g.V * sizeof(float),
-                       cudaMemcpyDeviceToDevice, s));
-  LK(argmax_rows(B.logits, D, g.V, bitmask, nd, B.row_id, B.row_p1, s));
+    LK(argmax_rows(B.logits, D, g.V, bitmask, nd, B.row_id, B.row_p1, s));
+  } else {
+    // lm_head fused with the per-row reductions: no [rows, vocab] logits in HBM.
+    GemmParams p{};
+    p.m_act = D;
+    p.n_w = g.V;
+    p.k = g.H;
+    p.epi = EPI_TC_LMHEAD;
+    p.ws = B.ws;
+    p.counters = B.counters;
+    p.status = B.status;
+    p.bitmask = bitmask;
+    p.mask_words = (g.V + 31) / 32;
+    p.nd = nd;
+    p.lm_part = B.lm_part;
+    const int bn = tc::pick_bn(D);
+    LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
+    LK(lm_reduce(B.lm_part, D, (g.V + 127) / 128, B.row_id, B.row_p1, s));
+  }
   if (B.probe_begin && B.probe_end) FK(cudaEventRecord(B.probe_end, s));
+  if (B.tap_logits) {
+    if (W.lm_is_fp8)
+      FK(cudaMemcpyAsync(B.tap_logits, B.logits, (size_t)D * g.V * sizeof(float),
+                         cudaMemcpyDeviceToDevice, s));
+    else
+      LK(tc_gemm(B, W.map_lm, ACT_Z, D, g.V, g.H, EPI_TC_STORE_F32, B.tap_logits, g.V, s));
+  }
   LK(finalize(B.row_id, B.row_p1, n, nd, B.status, (uint32_t *)(B.out_dev + B.off_drafts),
               (int32_t *)(B.out_dev + B.off_nout), (float *)(B.out_dev + B.off_conf),
               (int32_t *)B.out_dev, s));

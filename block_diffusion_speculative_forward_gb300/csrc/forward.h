@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "dflash.h"
+#include "gemm_tc.h"
 #include "internal.h"
 
 struct dflash_handle;
@@ -23,7 +24,15 @@ struct Weights {
   bf16 *w_kv = nullptr;                     // [L*2*kv, H], rows [K0; V0; K1; V1; ...]
   float *cos_t = nullptr, *sin_t = nullptr; // [max_seq_len + gamma][d/2]
   void *pool = nullptr;                     // [pages][L][K|V][nkv][B][d]
+  // TMA maps of the weights (box: 128 weight rows x 64 K)
+  CUtensorMap map_fc, map_wkv, map_lm;
+  std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_down;
 };
+
+// Activation operands of the tensor-core GEMMs, one TMA map per tile width.
+enum ActBuf { ACT_H = 0, ACT_O, ACT_U, ACT_Z, ACT_PACK, ACT_C, ACT_COUNT };
+constexpr int BN_COUNT = 5;   // 16, 32, 64, 128, 256
+inline int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
 
 struct Buffers {
   float *x = nullptr;          // [R, H] residual
@@ -47,6 +56,11 @@ struct Buffers {
   bf16 *tap_z = nullptr;
   float *tap_logits = nullptr;
   cudaEvent_t probe_begin = nullptr, probe_end = nullptr;  // around the lm_head stage
+  CUtensorMap act_map[ACT_COUNT][BN_COUNT];
+  float *ws = nullptr;          // stream-K partials
+  int *counters = nullptr;      // stream-K tile arrival counters (zero between launches)
+  int n_counters = 0;
+  LmPartial *lm_part = nullptr; // [D_max][vocab tiles]
 };
 
 struct CallMeta {

@@ -1,0 +1,657 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA, for every dense contraction of the draft head:
+// fc, the fused ctx K/V projection, the per-layer QKV / o / gate-up / down
+// projections and the shared lm_head ([P1] fields fc, fused_kv_weight,
+// layers, lm_head_shared).
+//
+//   Y[a, f] = sum_k X[a, k] * W[f, k]      (X activations, W a linear weight)
+//
+// The weight is the MMA's A operand (128 weight rows per tile, M = 128) and
+// the activations are B (BN rows, N = BN), so a batch-1 step of 16 block rows
+// still runs full-width MMAs while every weight byte is read once ("swap AB").
+// Both operands are K-major, 64-element (128-byte) K slices in the 128-byte
+// swizzled layout TMA writes.
+//
+// One persistent CTA per SM walks a contiguous range of the (tile, k-block)
+// iteration space (stream-K), so every SM streams the same number of weight
+// bytes whatever the tile count. A tile whose k-range is split between CTAs is
+// finished by its last arriving contributor, which sums the contributors'
+// partials in a fixed order (deterministic) and runs the epilogue; nothing
+// spins on another CTA.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues MMAs from one thread, warps 2-5 (one per TMEM lane quarter) drain the
+// double-buffered accumulator and run the epilogue. Every mbarrier wait is
+// bounded; on timeout the CTA raises the status word, stops issuing work,
+// waits (bounded) for its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+#include "gemm_tc.h"
+
+namespace dfl {
+namespace tc {
+
+constexpr int BM = 128;                 // weight rows per tile
+constexpr int BK = 64;                  // K elements per stage (one 128-byte swizzle span)
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t TIMEOUT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+template <int BN>
+struct Cfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN <= 64) ? 8 : (BN <= 128 ? 6 : 4);
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 2048;
+};
+
+// ---------------------------------------------------------------- PTX --
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the barrier phase with the given parity. Returns false when the
+// CTA has aborted or the wait ran past TIMEOUT_NS (then it aborts the CTA).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > TIMEOUT_NS) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t bar, int x,
+                                            int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// 32 TMEM lanes (this warp's quarter) x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (the tcgen05 descriptor format:
+// start>>4 at bit 0, leading offset>>4 at 16, stride offset>>4 at 32,
+// version 1 at 46, layout 2 = 128B swizzle at 61).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor, kind::f16: f32 accumulate, bf16 A and B, both
+// K-major, N = BN, M = 128.
+template <int BN>
+__device__ __forceinline__ uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+// -------------------------------------------------------- stream-K map --
+struct Part {
+  int64_t total;  // tiles * kb
+  int G;          // CTAs
+  __device__ __forceinline__ int64_t begin(int c) const { return total * c / G; }
+  // The CTA whose range holds iteration i.
+  __device__ int owner(int64_t i) const {
+    int c = (int)((i * G) / total);
+    while (c + 1 < G && begin(c + 1) <= i) ++c;
+    while (c > 0 && begin(c) > i) --c;
+    return c;
+  }
+};
+
+// ----------------------------------------------------------- epilogues --
+struct Smem {
+  uint64_t full[8], empty[8], acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  uint32_t drain_issued, drain_parity;
+  int abort_flag;
+  int is_last;
+  float red_v[4][16];
+  int red_i[4][16];
+  float col_max[16];
+};
+
+// Applies the epilogue to 16 accumulator columns held by this thread
+// (feature row f of tile tm, activation rows a0..a0+15).
+template <int EPI>
+__device__ __forceinline__ void finish16(const GemmParams &p, Smem *sm, const float (&v)[16],
+                                         int f, int tm, int a0, int q, int lane) {
+  const bool f_ok = f < p.n_w;
+  if (EPI == EPI_TC_LMHEAD) {
+    // Per activation row: max / lowest argmax / sum exp over this tile's 128
+    // vocab rows, with the grammar bitmask (bit f of the sequence's mask).
+    float val[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int a = a0 + c;
+      bool ok = f_ok && a < p.m_act;
+      if (ok && p.bitmask) {
+        const uint32_t w = (uint32_t)p.bitmask[(int64_t)(a / p.nd) * p.mask_words + (f >> 5)];
+        ok = (w >> (f & 31)) & 1u;
+      }
+      float x = v[c];
+      if (p.wscale && f_ok) x *= p.wscale[f];
+      val[c] = ok ? x : -INFINITY;
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float m = val[c];
+      int id = val[c] == -INFINITY ? INT32_MAX : f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float om = __shfl_xor_sync(0xffffffffu, m, o);
+        int oi = __shfl_xor_sync(0xffffffffu, id, o);
+        if (om > m || (om == m && oi < id)) { m = om; id = oi; }
+      }
+      if (lane == 0) { sm->red_v[q][c] = m; sm->red_i[q][c] = id; }
+    }
+    epi_bar();
+    if (threadIdx.x - 64 < 16) {
+      const int c = threadIdx.x - 64;
+      float m = sm->red_v[0][c];
+      int id = sm->red_i[0][c];
+      for (int w = 1; w < 4; ++w) {
+        float om = sm->red_v[w][c];
+        int oi = sm->red_i[w][c];
+        if (om > m || (om == m && oi < id)) { m = om; id = oi; }
+      }
+      sm->col_max[c] = m;
+      sm->red_i[0][c] = id;   // keep the winner for the write below
+    }
+    epi_bar();
+    float s[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float m = sm->col_max[c];
+      float e = (m == -INFINITY || val[c] == -INFINITY) ? 0.f : __expf(val[c] - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+      s[c] = e;
+    }
+    epi_bar();   // red_v reuse below: everyone has read col_max/red_i
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sm->red_v[q][c] = s[c];
+    }
+    epi_bar();
+    if (threadIdx.x - 64 < 16) {
+      const int c = threadIdx.x - 64;
+      const int a = a0 + c;
+      if (a < p.m_act) {
+        LmPartial r;
+        r.max = sm->col_max[c];
+        r.id = sm->red_i[0][c];
+        r.sum = sm->red_v[0][c] + sm->red_v[1][c] + sm->red_v[2][c] + sm->red_v[3][c];
+        r.pad = 0;
+        p.lm_part[(int64_t)a * p.tiles_m + tm] = r;
+      }
+    }
+    epi_bar();
+    return;
+  }
+  if (!f_ok) return;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int a = a0 + c;
+    if (a >= p.m_act) break;
+    const int64_t off = (int64_t)a * p.ldo + f;
+    float x = v[c];
+    if (p.wscale) x *= p.wscale[f];
+    if (EPI == EPI_TC_STORE_F32) ((float *)p.out)[off] = x;
+    else if (EPI == EPI_TC_ADD_F32) ((float *)p.out)[off] += x;
+    else ((bf16 *)p.out)[off] = __float2bfloat16_rn(x);
+  }
+}
+
+// ---------------------------------------------------------------- kernel --
+template <int BN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+              GemmParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  Smem *sm = (Smem *)(gbase + C::STAGES * C::STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int kb = p.k / BK;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const Part part{(int64_t)tiles * kb, (int)gridDim.x};
+  const int64_t it_begin = part.begin(blockIdx.x), it_end = part.begin(blockIdx.x + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sm->acc_full[b]), 1);
+      mbar_init(smem_u32(&sm->acc_empty[b]), 4);
+    }
+    mbar_init(smem_u32(&sm->drain), 1);
+    sm->abort_flag = 0;
+    sm->drain_issued = 0;
+    sm->drain_parity = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_w) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_x) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sm->tmem_base)),
+                 "r"((uint32_t)C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int *abort_flag = &sm->abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ------
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, parity = 0;   // per stage: loads issued, phase they complete
+      for (int64_t it = it_begin; it < it_end && !*abort_flag;) {
+        const int t = (int)(it / kb);
+        const int k0 = (int)(it % kb);
+        const int k1 = (int)((int64_t)kb < (int64_t)k0 + (it_end - it) ? (int64_t)kb : (int64_t)k0 + (it_end - it));
+        const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+        for (int k = k0; k < k1; ++k) {
+          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) break;
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint32_t fb = smem_u32(&sm->full[stage]);
+          mbar_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(sa, &map_w, fb, k * BK, tm * BM, pol_w);
+          tma_load_2d(sa + A_BYTES, &map_x, fb, k * BK, tn * BN, pol_x);
+          issued |= 1u << stage;
+          parity = (parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        it += k1 - k0;
+      }
+      sm->drain_issued = issued;
+      sm->drain_parity = parity;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer --------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16<BN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int64_t it = it_begin; it < it_end && !*abort_flag;) {
+        const int k0 = (int)(it % kb);
+        const int k1 = (int)((int64_t)kb < (int64_t)k0 + (it_end - it) ? (int64_t)kb : (int64_t)k0 + (it_end - it));
+        if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), acc_phase ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        bool ok = true;
+        for (int k = k0; k < k1; ++k) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sw128_desc(sa + kk * 32);
+            const uint64_t bd = sw128_desc(sa + A_BYTES + kk * 32);
+            umma_bf16(d, ad, bd, idesc, (k > k0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&sm->empty[stage]));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&sm->acc_full[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        it += k1 - k0;
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue ----------
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int f_local = q * 32 + lane;       // weight row within the tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t it = it_begin; it < it_end;) {
+      const int t = (int)(it / kb);
+      const int k0 = (int)(it % kb);
+      const int k1 = (int)((int64_t)kb < (int64_t)k0 + (it_end - it) ? (int64_t)kb : (int64_t)k0 + (it_end - it));
+      const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+      const int f = tm * BM + f_local;
+      const bool whole = (k0 == 0 && k1 == kb);
+      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), acc_phase, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      // partial slot of this CTA for this tile: its first or its last segment
+      const int slot = 2 * blockIdx.x + (it == it_begin ? 0 : 1);
+      float *ws = p.ws + (int64_t)slot * BN * BM;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tbase + c0, v);
+        if (whole) {
+          finish16<EPI>(p, sm, v, f, tm, tn * BN + c0, q, lane);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) ws[(c0 + c) * BM + f_local] = v[c];
+        }
+      }
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(smem_u32(&sm->acc_empty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+      if (!whole) {
+        // stream-K fixup: the last contributor of the tile sums the partials
+        __threadfence();
+        epi_bar();
+        const int c_lo = part.owner((int64_t)t * kb);
+        const int c_hi = part.owner((int64_t)t * kb + kb - 1);
+        if (threadIdx.x == 64) {
+          const int old = atomicAdd(&p.counters[t], 1);
+          sm->is_last = (old == c_hi - c_lo);
+        }
+        epi_bar();
+        if (sm->is_last) {
+          __threadfence();
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = 0.f;
+            for (int cc = c_lo; cc <= c_hi; ++cc) {
+              const int sl = 2 * cc + ((cc == c_lo && part.begin(cc) < (int64_t)t * kb) ? 1 : 0);
+              const float *src = p.ws + (int64_t)sl * BN * BM;
+#pragma unroll
+              for (int c = 0; c < 16; ++c) v[c] += __ldcg(src + (c0 + c) * BM + f_local);
+            }
+            finish16<EPI>(p, sm, v, f, tm, tn * BN + c0, q, lane);
+          }
+          if (threadIdx.x == 64) p.counters[t] = 0;
+        }
+        epi_bar();
+      }
+      it += k1 - k0;
+    }
+  }
+
+  // ---------------------------------------------------------- teardown ----
+  __syncthreads();
+  if (*abort_flag) {
+    // Let this CTA's own copies and MMAs land before its shared memory and
+    // TMEM go away; each wait is bounded (100 ms).
+    if (threadIdx.x == 0) {
+      atomicOr(p.status, ST_TIMEOUT);
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (!((sm->drain_issued >> s) & 1u)) continue;
+        const uint32_t par = (sm->drain_parity >> s) & 1u;
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(smem_u32(&sm->full[s]), par) && global_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+    if (threadIdx.x == 32) {
+      umma_commit(smem_u32(&sm->drain));
+      const uint64_t t0 = global_ns();
+      while (!mbar_test(smem_u32(&sm->drain), 0) && global_ns() - t0 < 100000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"((uint32_t)C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ============================================================ host side ==
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+int g_num_sms = 0;
+
+void init_driver() {
+  cudaDriverEntryPointQueryResult q;
+  void *fn = nullptr;
+  if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+template <int BN, int EPI>
+cudaError_t set_smem_attr() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, EPI>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_bn(const CUtensorMap &mw, const CUtensorMap &mx, const GemmParams &p, int grid,
+                      cudaStream_t s) {
+  cudaError_t e = set_smem_attr<BN, EPI>();
+  if (e != cudaSuccess) return e;
+  k_gemm_tc<BN, EPI><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(mw, mx, p);
+  return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_epi(int bn, const CUtensorMap &mw, const CUtensorMap &mx, const GemmParams &p,
+                       int grid, cudaStream_t s) {
+  switch (bn) {
+    case 16: return launch_bn<16, EPI>(mw, mx, p, grid, s);
+    case 32: return launch_bn<32, EPI>(mw, mx, p, grid, s);
+    case 64: return launch_bn<64, EPI>(mw, mx, p, grid, s);
+    case 128: return launch_bn<128, EPI>(mw, mx, p, grid, s);
+    case 256: return launch_bn<256, EPI>(mw, mx, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+}  // namespace
+
+int num_sms() {
+  std::call_once(g_once, init_driver);
+  return g_num_sms;
+}
+
+bool make_map_2d(CUtensorMap *map, const void *base, bool fp8, int64_t rows, int64_t cols,
+                 int box_rows) {
+  std::call_once(g_once, init_driver);
+  if (!g_encode) return false;
+  const int esz = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int pick_bn(int m_act) {
+  if (m_act <= 16) return 16;
+  if (m_act <= 32) return 32;
+  if (m_act <= 64) return 64;
+  if (m_act <= 128) return 128;
+  return 256;
+}
+
+cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, GemmParams p,
+                 cudaStream_t s) {
+  if (p.m_act <= 0 || p.n_w <= 0) return cudaSuccess;
+  if (p.k % BK) return cudaErrorInvalidValue;
+  p.tiles_m = (p.n_w + BM - 1) / BM;
+  p.tiles_n = (p.m_act + bn - 1) / bn;
+  const int64_t total = (int64_t)p.tiles_m * p.tiles_n * (p.k / BK);
+  int grid = num_sms();
+  if (p.grid_cap > 0 && p.grid_cap < grid) grid = p.grid_cap;
+  if (total < grid) grid = (int)total;
+  if (grid < 1) grid = 1;
+  switch (p.epi) {
+    case EPI_TC_STORE_F32: return launch_epi<EPI_TC_STORE_F32>(bn, map_w, map_x, p, grid, s);
+    case EPI_TC_ADD_F32: return launch_epi<EPI_TC_ADD_F32>(bn, map_w, map_x, p, grid, s);
+    case EPI_TC_STORE_BF16: return launch_epi<EPI_TC_STORE_BF16>(bn, map_w, map_x, p, grid, s);
+    case EPI_TC_LMHEAD: return launch_epi<EPI_TC_LMHEAD>(bn, map_w, map_x, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tc
+
+// ------------------------------------------------------- lm_head merge --
+// Merges the (max, lowest argmax, sum exp) partials of one draft row over all
+// vocab tiles: draft id (or -1 when no token is allowed) and the top-1
+// softmax probability 1 / sum_v exp(l_v - max).
+__device__ __forceinline__ void lm_merge(float &m, int &id, float &s, float m2, int id2,
+                                         float s2) {
+  const float M = fmaxf(m, m2);
+  const int I = (m > m2 || (m == m2 && id < id2)) ? id : id2;
+  const float a = (m == -INFINITY) ? 0.f : s * __expf(m - M);
+  const float b = (m2 == -INFINITY) ? 0.f : s2 * __expf(m2 - M);
+  m = M;
+  id = I;
+  s = a + b;
+}
+
+__global__ void k_lm_reduce(const LmPartial *__restrict__ part, int tiles,
+                            int32_t *__restrict__ row_id, float *__restrict__ row_p1) {
+  __shared__ float sm_m[32], sm_s[32];
+  __shared__ int sm_i[32];
+  const int r = blockIdx.x;
+  const LmPartial *pr = part + (int64_t)r * tiles;
+  float m = -INFINITY, s = 0.f;
+  int id = INT32_MAX;
+  for (int t = threadIdx.x; t < tiles; t += blockDim.x) {
+    const LmPartial q = pr[t];
+    lm_merge(m, id, s, q.max, q.id, q.sum);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, id, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lm_merge(m, id, s, m2, i2, s2);
+  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) { sm_m[w] = m; sm_i[w] = id; sm_s[w] = s; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) lm_merge(m, id, s, sm_m[i], sm_i[i], sm_s[i]);
+    const bool none = (m == -INFINITY);
+    row_id[r] = none ? -1 : id;
+    row_p1[r] = none ? 0.f : 1.f / s;
+  }
+}
+
+cudaError_t lm_reduce(const LmPartial *part, int rows, int tiles, int32_t *row_id, float *row_p1,
+                      cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  k_lm_reduce<<<rows, 256, 0, s>>>(part, tiles, row_id, row_p1);
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

@@ -53,6 +53,7 @@ struct LayerW {
 enum : int {
   ST_TOKEN = 1,   // a token id >= vocab reached the embed gather
   ST_PAGE = 2,    // a page id outside the pool reached a KV access
+  ST_TIMEOUT = 4, // a bounded wait inside a kernel ran out; that kernel's output is invalid
 };
 
 // Element offset of (page, layer, kind, kv head, slot, 0) in the KV pool,

@@ -209,6 +209,12 @@ DFLASH_API int dflash_debug_gather_kv(dflash_handle *h, const dflash_state *st, 
 DFLASH_API int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end);
 /* Kernels this library has launched since it was loaded (all handles). */
 DFLASH_API int64_t dflash_debug_launch_count(void);
+/* One tensor-core GEMM in isolation, for kernel tests: y[m, n_w] = x[m, k] *
+ * w[n_w, k]^T (bf16 in, f32 out, k % 64 == 0), all dev pointers 16-byte
+ * aligned. grid_cap > 0 caps the persistent grid (to force split k-ranges).
+ * Synchronises the stream; allocates its own workspace. */
+DFLASH_API int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t m, int32_t n_w,
+                                 int32_t k, int32_t grid_cap, void *stream);
 DFLASH_API int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits);
 
 #ifdef __cplusplus

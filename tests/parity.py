@@ -98,8 +98,10 @@ def check_seq(pair: Pair, ref_tap: dict, ref_out, got_out, seq_idx: int, n_seq: 
     g = pair.geom.gamma
     torch.cuda.synchronize()
     if hidden:
+        R, H, L = n_seq * g, pair.geom.hidden, pair.geom.num_layers
+        tx = pair.tx.reshape(-1)[:(L + 1) * R * H].reshape(L + 1, R, H)
         for l, xr in enumerate(ref_tap["x"]):
-            check_abs(xr, pair.tx[l, seq_idx * g:(seq_idx + 1) * g], HIDDEN_TOL, f"x tap {l}")
+            check_abs(xr, tx[l, seq_idx * g:(seq_idx + 1) * g], HIDDEN_TOL, f"x tap {l}")
         check_abs(ref_tap["z"], pair.tz[seq_idx * g:(seq_idx + 1) * g].float(), HIDDEN_TOL, "z")
     got_logits = pair.tl[seq_idx * nd:(seq_idx + 1) * nd]
     check_logits(ref_tap["logits"], got_logits, LOGIT_TOL_FP8 if pair.fp8 else LOGIT_TOL)
@@ -135,10 +137,10 @@ def check_fp8_kv(pair, l, ref, got, kind):
     rc = (ref.to(torch.float64).cpu() / s)
     gc = (got.to(torch.float64).cpu() / s)
     diff = (rc - gc).abs()
-    bad = diff > 1e-9
+    bad = diff > 1e-5 * rc.abs().clamp(min=1.0)     # beyond the fp32 dequant rounding
     frac = float(bad.double().mean())
     # a code step is at most 1/8 of the code's magnitude (3 mantissa bits)
-    step_ok = (diff <= rc.abs().clamp(min=2 ** -6) * 0.125 + 1e-9)
+    step_ok = (diff <= rc.abs().clamp(min=2 ** -6) * 0.125 * (1 + 1e-5))
     assert bool(step_ok.all()), "FP8 KV codes more than one step apart"
     assert frac <= 2e-3, f"FP8 KV: {frac:.2e} of codes differ"
 
