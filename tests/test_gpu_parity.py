@@ -145,7 +145,7 @@ def test_full_geometry_single_sequence():
     pair = Pair(geom, 1002, cfg_kw=dict(max_batch=1))
     so, sl, _ = _prefill(pair, 1023, 1002)
     row = syn.make_stack(geom, 1, 1002, idx=1)
-    tap, ref, got = _propose(pair, so, sl, 424242, 1024, row, 15)
+    tap, ref, got = _propose(pair, so, sl, 142424, 1024, row, 15)
     n = check_seq(pair, tap, ref, got, 0, 1, 15)
     assert n >= 10, "too few drafts had a decisive logit gap to check"
     assert_tables(pair, so, sl)
