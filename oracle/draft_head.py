@@ -351,43 +351,57 @@ class DraftHeadOracle:
         g = self.gamma
         toks = [last_token] + [self.cfg["mask_token_id"]] * (g - 1)
         x = self.embed[torch.tensor(toks)].to(F64)                # [g, H]
-        pos = torch.arange(p, p + g, dtype=torch.int64)
-        ws = max(0, p - self.W) if self.W > 0 else p
-        ctx_pos = list(range(ws, p))
         if taps is not None:
             taps["x"] = [x.clone()]
-        for l, lay in enumerate(self.layers):
-            h = round_bf16(rms_norm(x, lay["in_norm"], self.eps))
-            q = (h @ lay["q"].T).reshape(g, self.nq, self.d)
-            k = (h @ lay["k"].T).reshape(g, self.nkv, self.d)
-            v = (h @ lay["v"].T).reshape(g, self.nkv, self.d)
-            q = rope(rms_norm(q, lay["q_norm"], self.eps).transpose(0, 1), pos,
-                     self.inv_freq).transpose(0, 1)
-            k = rope(rms_norm(k, lay["k_norm"], self.eps).transpose(0, 1), pos,
-                     self.inv_freq).transpose(0, 1)
-            q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)
-            if ctx_pos:
-                kc = torch.stack([st.rows[j][0][l] for j in ctx_pos])
-                vc = torch.stack([st.rows[j][1][l] for j in ctx_pos])
-                keys, vals = torch.cat([kc, k], 0), torch.cat([vc, v], 0)
-            else:
-                keys, vals = k, v
-            o = round_bf16(attention(q, keys, vals).reshape(g, self.nq * self.d))
-            x = x + o @ lay["o"].T
-            h2 = round_bf16(rms_norm(x, lay["post_norm"], self.eps))
-            u = round_bf16(silu(h2 @ lay["gate"].T) * (h2 @ lay["up"].T))
-            x = x + u @ lay["down"].T
+        for l in range(self.L):
+            x = self.layer_forward(st, l, x, p)
             if taps is not None:
                 taps["x"].append(x.clone())
         z = round_bf16(rms_norm(x, self.norm, self.eps))
-        zr = z[1:1 + num_drafts]
-        logits = zr @ self.lm_head().T
-        if self.lm_fp8:
-            logits = logits * self.lm_scale[None, :]
+        logits = self.draft_logits(z, num_drafts)
         if taps is not None:
             taps["z"] = z
             taps["logits"] = logits
         return select_drafts(logits, allowed)
+
+    def layer_forward(self, st: SeqState, l: int, x: torch.Tensor, p: int) -> torch.Tensor:
+        """One Qwen3-style drafter layer over the gamma block rows x [gamma, H]
+        at positions p..p+gamma-1, attending to the window's stored ctx rows of
+        layer l and the block's own keys ([P1] field layers; the
+        mask-free block attention). Returns the new residual."""
+        lay = self.layers[l]
+        g = x.shape[0]
+        pos = torch.arange(p, p + g, dtype=torch.int64)
+        ws = max(0, p - self.W) if self.W > 0 else p
+        ctx_pos = list(range(ws, p))
+        h = round_bf16(rms_norm(x, lay["in_norm"], self.eps))
+        q = (h @ lay["q"].T).reshape(g, self.nq, self.d)
+        k = (h @ lay["k"].T).reshape(g, self.nkv, self.d)
+        v = (h @ lay["v"].T).reshape(g, self.nkv, self.d)
+        q = rope(rms_norm(q, lay["q_norm"], self.eps).transpose(0, 1), pos,
+                 self.inv_freq).transpose(0, 1)
+        k = rope(rms_norm(k, lay["k_norm"], self.eps).transpose(0, 1), pos,
+                 self.inv_freq).transpose(0, 1)
+        q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)
+        if ctx_pos:
+            kc = torch.stack([st.rows[j][0][l] for j in ctx_pos])
+            vc = torch.stack([st.rows[j][1][l] for j in ctx_pos])
+            keys, vals = torch.cat([kc, k], 0), torch.cat([vc, v], 0)
+        else:
+            keys, vals = k, v
+        o = round_bf16(attention(q, keys, vals).reshape(g, self.nq * self.d))
+        x = x + o @ lay["o"].T
+        h2 = round_bf16(rms_norm(x, lay["post_norm"], self.eps))
+        u = round_bf16(silu(h2 @ lay["gate"].T) * (h2 @ lay["up"].T))
+        return x + u @ lay["down"].T
+
+    def draft_logits(self, z: torch.Tensor, num_drafts: int) -> torch.Tensor:
+        """lm_head logits of block rows 1..num_drafts of the final-normed z
+        ([P1] field lm_head_shared; FP8 mirror: scale_v * <z, codes_v>)."""
+        logits = z[1:1 + num_drafts] @ self.lm_head().T
+        if self.lm_fp8:
+            logits = logits * self.lm_scale[None, :]
+        return logits
 
     # -- trait calls ----------------------------------------------------------
     def propose(self, st, last_token, position, new_rows, num_drafts, bitmask=None,

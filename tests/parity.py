@@ -5,7 +5,8 @@ tolerances of the parity gate:
   * residual taps, final z, gathered ctx K/V: max-abs 3e-2;
   * logits: per row max|diff| / max|ref| <= 2e-2 (5e-2 on FP8 paths);
   * draft ids: exact wherever the oracle's masked top-1 - top-2 gap > 1e-2;
-  * confidence: |diff| <= 1e-2."""
+  * confidence: |diff| <= 1e-2.
+Deep stacks are compared layer by layer (teacher-forced), see E2E_* below."""
 from __future__ import annotations
 
 import math
@@ -22,6 +23,12 @@ LOGIT_TOL = 2e-2
 LOGIT_TOL_FP8 = 5e-2
 GAP = 1e-2
 CONF_TOL = 1e-2
+# End to end over many layers, an fp32 evaluation of the method drifts from the
+# fp64 oracle (measured: the oracle in fp32 vs fp64 at the shipped geometry,
+# 8 layers: max residual diff 0.09, logits ~1.3% of max|l|). End-to-end
+# logits get this envelope; drafts are compared where the gap exceeds it.
+E2E_LOGIT_TOL = 5e-2
+E2E_GAP = 0.25
 
 
 def cfg_for(geom, **kw):

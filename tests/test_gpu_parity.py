@@ -8,7 +8,9 @@ import pytest
 import torch
 
 from block_diffusion_speculative_forward_gb300 import synthetic as syn
-from tests.parity import (Pair, assert_tables, check_abs, check_kv, check_seq, HIDDEN_TOL)
+from tests.parity import (CONF_TOL, E2E_GAP, E2E_LOGIT_TOL, HIDDEN_TOL, LOGIT_TOL, Pair,
+                          assert_tables, check_abs, check_drafts, check_kv, check_logits,
+                          check_seq, gaps)
 from tests.test_oracle_pins import MICRO
 import oracle
 
@@ -140,13 +142,44 @@ def test_tiny_fp8_kv_and_lm_head():
 
 def test_full_geometry_single_sequence():
     """Shipped geometry, 1 sequence: prefill 1023 rows, then propose at 1024
-    with one new row and 15 drafts (the timed single-sequence step)."""
+    with one new row and 15 drafts (the timed single-sequence step).
+
+    Hidden states are compared layer by layer: each oracle layer is fed the
+    GPU's residual entering it. End to end, the residual drifts from the fp64
+    oracle by ~1% after 8 layers for ANY fp32 evaluation of the method (the
+    oracle itself run in fp32 drifts as much: summation-order differences are
+    amplified through the bf16 rounding points), so end-to-end logits get the
+    envelope tolerance and drafts are compared where the gap is decisive."""
     geom = syn.FULL
     pair = Pair(geom, 1002, cfg_kw=dict(max_batch=1))
     so, sl, _ = _prefill(pair, 1023, 1002)
+    check_kv(pair, so, sl, [0] + list(range(1016, 1023)))
     row = syn.make_stack(geom, 1, 1002, idx=1)
     tap, ref, got = _propose(pair, so, sl, 142424, 1024, row, 15)
-    n = check_seq(pair, tap, ref, got, 0, 1, 15)
+    torch.cuda.synchronize()
+    g, H, L = geom.gamma, geom.hidden, geom.num_layers
+    tx = pair.tx.reshape(-1)[:(L + 1) * g * H].reshape(L + 1, g, H).double().cpu()
+    check_abs(tap["x"][0], tx[0], 0.0, "embed")
+    for l in range(L):
+        ref_l = pair.ora.layer_forward(so, l, tx[l], 1024)
+        check_abs(ref_l, tx[l + 1], HIDDEN_TOL, f"layer {l} (teacher-forced)")
+    z_ref = oracle.round_bf16(oracle.rms_norm(tx[L], pair.ora.norm, geom.rms_eps))
+    z_got = pair.tz[:g].double().cpu()
+    check_abs(z_ref, z_got, HIDDEN_TOL, "final norm (teacher-forced)")
+    lg_ref = pair.ora.draft_logits(z_got, 15)
+    lg_got = pair.tl[:15]
+    check_logits(lg_ref, lg_got, LOGIT_TOL)
+    d_ref, n_ref, c_ref, _ = oracle.select_drafts(lg_ref, None)
+    assert got[1] == n_ref == 15
+    n = check_drafts(d_ref, got[0], lg_ref, None)
     assert n >= 10, "too few drafts had a decisive logit gap to check"
+    assert abs(got[2] - c_ref) <= CONF_TOL
+    # end to end against the fp64 oracle, within the fp32 envelope
+    check_logits(tap["logits"], lg_got, E2E_LOGIT_TOL)
+    g_e2e = gaps(tap["logits"], None)
+    for i in range(15):
+        if g_e2e[i] > E2E_GAP:
+            assert ref[0][i] == got[0][i], (i, ref[0][i], got[0][i])
+    assert abs(ref[2] - got[2]) <= CONF_TOL
     assert_tables(pair, so, sl)
-    check_kv(pair, so, sl, [0, 1, 511, 1022, 1023][:1] + list(range(1019, 1024)))
+    check_kv(pair, so, sl, list(range(1019, 1024)))
