@@ -122,9 +122,19 @@ def check_seq(pair: Pair, ref_tap: dict, ref_out, got_out, seq_idx: int, n_seq: 
 
 
 def check_kv(pair: Pair, so, sl, positions):
-    positions = list(positions)
-    if not positions:
-        return
+    """Gathered ctx K/V of every layer at the given positions (any order);
+    the library gathers contiguous runs."""
+    positions = sorted(positions)
+    runs, start = [], 0
+    for i in range(1, len(positions) + 1):
+        if i == len(positions) or positions[i] != positions[i - 1] + 1:
+            runs.append(positions[start:i])
+            start = i
+    for run in runs:
+        _check_kv_run(pair, so, sl, run)
+
+
+def _check_kv_run(pair: Pair, so, sl, positions):
     for l in range(pair.geom.num_layers):
         k, v = pair.lib.gather_kv(sl, l, positions[0], len(positions))
         kr, vr = pair.ora.gather_kv(so, l, positions)
