@@ -215,6 +215,23 @@ DFLASH_API int64_t dflash_debug_launch_count(void);
  * Synchronises the stream; allocates its own workspace. */
 DFLASH_API int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t m, int32_t n_w,
                                  int32_t k, int32_t grid_cap, void *stream);
+/* The tensor-core GEMM y[m, n_w] = x[m, k] * w[n_w, k]^T (bf16 in, f32 out),
+ * for callers that may not allocate device memory while they run, e.g. an
+ * engine that has already handed the whole GPU to its own arena, or a
+ * latency-critical loop that cannot afford the device-wide synchronisation
+ * of cudaMalloc/cudaFree. It allocates nothing: its scratch (stream-K
+ * partials, tile counters, a status word; 2.6 MB) is a fixed array inside
+ * the library that every GPU loading the library holds until exit. The API
+ * pages have no counterpart of this call.
+ * Limits: 1 <= m <= 16, k % 64 == 0, n_w <= 524288 (4096 tiles of 128 rows);
+ * w and x 16-byte aligned dev pointers, y a dev pointer. Larger sizes return
+ * DFLASH_EINVAL. The first call on each device looks up the array's device
+ * address with that device current; make that first call before any stream
+ * capture. All calls share the array, so calls that overlap on the GPU race:
+ * order them. Synchronises the stream; returns DFLASH_OK, DFLASH_EINVAL,
+ * DFLASH_ECUDA or DFLASH_EDEVICE (dflash_last_error is not updated). */
+DFLASH_API int dflash_gemm_noalloc(const void *w, const void *x, float *y, int32_t m, int32_t n_w,
+                                   int32_t k, void *stream);
 DFLASH_API int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits);
 
 #ifdef __cplusplus
