@@ -1,0 +1,384 @@
+// Block attention of the draft head: for each sequence and kv head, the
+// gamma block rows of every query head in the GQA group attend, without a
+// mask, to the ctx window (paged K/V, bf16 or FP8 with per-head scales) and to
+// the block's own gamma keys ([P1] fields kv_cache, ctx_window, layers;
+// [P2] field propose_graphs: attention runs between the layer halves).
+//
+// Split-KV: the host cuts every (sequence, kv head) key range into chunks;
+// each CTA takes one chunk and holds the whole group's gamma x (nq/nkv) query
+// vectors (<= 128) as one Q tile. QK^T and PV run on tensor cores
+// (mma.sync m16n8k16, bf16 in, f32 accumulate) with an online softmax in
+// registers; K/V tiles of 32 keys stream through a double-buffered cp.async
+// ring. A pair cut into several chunks writes unnormalised partials
+// (acc, row max, row sum) that k_attn_merge combines; a pair of one chunk
+// writes its output directly.
+#include "attention.h"
+
+#include <cmath>
+
+namespace dfl {
+
+namespace {
+
+constexpr int QT = 128;     // query vectors per CTA (rows of the Q tile)
+constexpr int KT = 32;      // keys per K/V tile
+constexpr int THREADS = 128;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+  const int n = valid ? 16 : 0;   // zero-fill when invalid
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float fp8_to_float(uint8_t c) {
+  __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(hr));
+}
+
+template <int D>
+struct Smem {
+  static constexpr int LD = D + 8;   // padded row (bf16): conflict-free ldmatrix
+  bf16 q[QT * LD];
+  bf16 k[2][KT * LD];
+  bf16 v[2][KT * LD];
+};
+
+// Loads keys [kt, kt+KT) of the item (key index space: [0, n_ctx) ctx rows at
+// positions ws.., then the gamma block rows) into one K/V stage. Keys past
+// k1 are zero-filled (and masked by the caller).
+template <int D, bool FP8>
+__device__ __forceinline__ void load_kv_tile(const AttnArgs &a, const AttnItem &it,
+                                             const SeqMeta &sm, Smem<D> *sh, int stage, int kt,
+                                             int *status) {
+  constexpr int LD = Smem<D>::LD;
+  constexpr int CH = D / 8;   // 16-byte chunks per row (bf16)
+  const Geo &g = a.g;
+  const int n_ctx = sm.pos - sm.ws;
+  for (int idx = threadIdx.x; idx < KT * CH; idx += THREADS) {
+    const int r = idx / CH, c = idx % CH;
+    const int kk = kt + r;
+    const bool valid = kk < it.k1;
+    bf16 *dk = sh->k[stage] + r * LD + c * 8;
+    bf16 *dv = sh->v[stage] + r * LD + c * 8;
+    if (!valid) {
+      // padding key past k1: zeros (masked out of the softmax by the caller)
+      *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+    } else if (kk < n_ctx) {
+      // ctx key: position ws + kk, through the window's page list
+      const int pos = sm.ws + kk;
+      int page = a.page_ids[sm.page_base + (pos / g.B - sm.ws / g.B)];
+      const int slot = pos % g.B;
+      if (page < 0 || page >= g.pages) {
+        atomicOr(status, ST_PAGE);
+        page = 0;
+      }
+      const int64_t ko = kv_offset(g, page, a.layer, 0, it.g, slot) + c * 8;
+      const int64_t vo = kv_offset(g, page, a.layer, 1, it.g, slot) + c * 8;
+      if (FP8) {
+        const uint2 kr = *reinterpret_cast<const uint2 *>((const uint8_t *)a.pool + ko);
+        const uint2 vr = *reinterpret_cast<const uint2 *>((const uint8_t *)a.pool + vo);
+        const uint8_t *kb = reinterpret_cast<const uint8_t *>(&kr);
+        const uint8_t *vb = reinterpret_cast<const uint8_t *>(&vr);
+        uint32_t ko4[4], vo4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ko4[e] = pack_bf16(fp8_to_float(kb[2 * e]), fp8_to_float(kb[2 * e + 1]));
+          vo4[e] = pack_bf16(fp8_to_float(vb[2 * e]), fp8_to_float(vb[2 * e + 1]));
+        }
+        *reinterpret_cast<uint4 *>(dk) = make_uint4(ko4[0], ko4[1], ko4[2], ko4[3]);
+        *reinterpret_cast<uint4 *>(dv) = make_uint4(vo4[0], vo4[1], vo4[2], vo4[3]);
+      } else {
+        cp_async16(smem_u32(dk), (const bf16 *)a.pool + ko, true);
+        cp_async16(smem_u32(dv), (const bf16 *)a.pool + vo, true);
+      }
+    } else {
+      // block key: row (s*gamma + kk - n_ctx) of the block's own K/V
+      const int64_t off = (int64_t)(it.s * g.gamma + kk - n_ctx) * g.kv + it.g * D + c * 8;
+      if (FP8) {
+        *reinterpret_cast<uint4 *>(dk) = *reinterpret_cast<const uint4 *>(a.kb + off);
+        *reinterpret_cast<uint4 *>(dv) = *reinterpret_cast<const uint4 *>(a.vb + off);
+      } else {
+        cp_async16(smem_u32(dk), a.kb + off, true);
+        cp_async16(smem_u32(dv), a.vb + off, true);
+      }
+    }
+  }
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
+  constexpr int LD = Smem<D>::LD;
+  constexpr int NT = D / 8;          // n8 tiles across the head dim (output)
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem<D> *sh = reinterpret_cast<Smem<D> *>(smem_raw);
+  const AttnItem it = a.items[blockIdx.x];
+  const SeqMeta sm = a.seq[it.s];
+  const Geo &g = a.g;
+  const int grp = g.nq / g.nkv;
+  const int n_q = g.gamma * grp;
+  const int n_ctx = sm.pos - sm.ws;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+
+  // Q tile: query vector qv = i * grp + hh is row i of the block, head g*grp+hh.
+  for (int idx = threadIdx.x; idx < QT * (D / 8); idx += THREADS) {
+    const int r = idx / (D / 8), c = idx % (D / 8);
+    bf16 *dst = sh->q + r * LD + c * 8;
+    const bool valid = r < n_q;
+    const int64_t off = valid ? ((int64_t)(it.s * g.gamma + r / grp) * g.nq + it.g * grp + r % grp) * D + c * 8 : 0;
+    cp_async16(smem_u32(dst), a.q + off, valid);
+  }
+  const bool is_ctx = it.k0 < n_ctx;
+  float sk = 1.f, sv = 1.f;
+  if (FP8 && is_ctx) {
+    sk = a.kv_scale[(a.layer * g.nkv + it.g) * 2 + 0];
+    sv = a.kv_scale[(a.layer * g.nkv + it.g) * 2 + 1];
+  }
+  const float qk_scale = a.scale * sk;
+  const int n_tiles = (it.k1 - it.k0 + KT - 1) / KT;
+  load_kv_tile<D, FP8>(a, it, sm, sh, 0, it.k0, a.status);
+  cp_commit();
+
+  float acc[2][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+  float row_m[2][2], row_l[2][2];   // [m-tile][row gid / gid+8]
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    row_m[mt][0] = row_m[mt][1] = -INFINITY;
+    row_l[mt][0] = row_l[mt][1] = 0.f;
+  }
+  const int qrow0 = warp * 32;   // this warp's 32 query rows
+
+  for (int t = 0; t < n_tiles; ++t) {
+    const int stage = t & 1;
+    if (t + 1 < n_tiles) {
+      load_kv_tile<D, FP8>(a, it, sm, sh, stage ^ 1, it.k0 + (t + 1) * KT, a.status);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    const int kt = it.k0 + t * KT;
+    // S = Q K^T for this warp's 32 rows x 32 keys
+    float s[2][4][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[mt][j][e] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < D; k0 += 16) {
+      uint32_t af[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int row = qrow0 + mt * 16 + (lane & 15);
+        const int col = k0 + (lane >> 4) * 8;
+        ldsm_x4(smem_u32(sh->q + row * LD + col), af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
+      }
+#pragma unroll
+      for (int jp = 0; jp < 2; ++jp) {   // pairs of n8 key tiles
+        uint32_t b0, b1, b2, b3;
+        const int key = jp * 16 + (lane >> 4) * 8 + (lane & 7);
+        const int col = k0 + ((lane >> 3) & 1) * 8;
+        ldsm_x4(smem_u32(sh->k[stage] + key * LD + col), b0, b1, b2, b3);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          mma16816(s[mt][2 * jp], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
+          mma16816(s[mt][2 * jp + 1], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b2, b3);
+        }
+      }
+    }
+    // online softmax over the tile's keys (masking keys >= k1)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {   // row gid (h=0) or gid+8 (h=1)
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = kt + j * 8 + 2 * tig + e;
+            float v = s[mt][j][2 * h + e] * qk_scale;
+            v = key < it.k1 ? v : -INFINITY;
+            s[mt][j][2 * h + e] = v;
+            mx = fmaxf(mx, v);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(row_m[mt][h], mx);
+        const float corr = (row_m[mt][h] == -INFINITY) ? 0.f : __expf(row_m[mt][h] - m_new);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float v = s[mt][j][2 * h + e];
+            const float p = (v == -INFINITY) ? 0.f : __expf(v - m_new);
+            s[mt][j][2 * h + e] = p;
+            sum += p;
+          }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        row_l[mt][h] = row_l[mt][h] * corr + sum;
+        row_m[mt][h] = m_new;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          acc[mt][nt][2 * h] *= corr;
+          acc[mt][nt][2 * h + 1] *= corr;
+        }
+      }
+    }
+    // O += P V  (P from the S registers, values scaled by sv for FP8 ctx)
+#pragma unroll
+    for (int kc = 0; kc < 2; ++kc) {   // 16-key slices of the tile
+      uint32_t pa[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        pa[mt][0] = pack_bf16(s[mt][2 * kc][0] * sv, s[mt][2 * kc][1] * sv);
+        pa[mt][1] = pack_bf16(s[mt][2 * kc][2] * sv, s[mt][2 * kc][3] * sv);
+        pa[mt][2] = pack_bf16(s[mt][2 * kc + 1][0] * sv, s[mt][2 * kc + 1][1] * sv);
+        pa[mt][3] = pack_bf16(s[mt][2 * kc + 1][2] * sv, s[mt][2 * kc + 1][3] * sv);
+      }
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {   // pairs of n8 dim tiles
+        uint32_t b0, b1, b2, b3;
+        const int key = kc * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int col = np * 16 + (lane >> 4) * 8;
+        ldsm_x4_t(smem_u32(sh->v[stage] + key * LD + col), b0, b1, b2, b3);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          mma16816(acc[mt][2 * np], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b0, b1);
+          mma16816(acc[mt][2 * np + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b2, b3);
+        }
+      }
+    }
+    __syncthreads();   // the stage is reloaded two tiles later
+  }
+
+  // epilogue: direct output, or partials for the merge
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int qv = qrow0 + mt * 16 + gid + 8 * h;
+      if (qv >= n_q) continue;
+      if (it.slot < 0) {
+        const float inv = 1.f / row_l[mt][h];
+        bf16 *orow = a.o + ((int64_t)(it.s * g.gamma + qv / grp) * g.nq + it.g * grp + qv % grp) * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          *reinterpret_cast<__nv_bfloat162 *>(orow + nt * 8 + 2 * tig) =
+              __floats2bfloat162_rn(acc[mt][nt][2 * h] * inv, acc[mt][nt][2 * h + 1] * inv);
+      } else {
+        float *ws = a.ws + (int64_t)it.slot * a.slot_floats;
+        float *arow = ws + (int64_t)qv * D;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          *reinterpret_cast<float2 *>(arow + nt * 8 + 2 * tig) =
+              make_float2(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+        if (tig == 0) {
+          ws[(int64_t)n_q * D + qv] = row_m[mt][h];
+          ws[(int64_t)n_q * D + n_q + qv] = row_l[mt][h];
+        }
+      }
+    }
+  }
+}
+
+// One block per (pair, query vector), D threads: combine the pair's chunks.
+template <int D>
+__global__ void __launch_bounds__(D) k_attn_merge(AttnArgs a) {
+  const AttnPair pr = a.pairs[blockIdx.x];
+  const int qv = blockIdx.y;
+  const Geo &g = a.g;
+  const int grp = g.nq / g.nkv;
+  const int n_q = g.gamma * grp;
+  if (qv >= n_q) return;
+  float M = -INFINITY;
+  for (int c = 0; c < pr.nc; ++c) {
+    const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
+    M = fmaxf(M, __ldcg(ws + (int64_t)n_q * D + qv));
+  }
+  float l = 0.f, o = 0.f;
+  for (int c = 0; c < pr.nc; ++c) {
+    const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
+    const float m = __ldcg(ws + (int64_t)n_q * D + qv);
+    const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
+    l += w * __ldcg(ws + (int64_t)n_q * D + n_q + qv);
+    o += w * __ldcg(ws + (int64_t)qv * D + threadIdx.x);
+  }
+  bf16 *orow = a.o + ((int64_t)(pr.s * g.gamma + qv / grp) * g.nq + pr.g * grp + qv % grp) * D;
+  orow[threadIdx.x] = __float2bfloat16_rn(o / l);
+}
+
+template <int D, bool FP8>
+cudaError_t launch(const AttnArgs &a, cudaStream_t s) {
+  const int smem = (int)sizeof(Smem<D>);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_split<D, FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k_attn_split<D, FP8><<<a.n_items, THREADS, smem, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_pairs == 0) return e;
+  const int grp = a.g.nq / a.g.nkv;
+  k_attn_merge<D><<<dim3(a.n_pairs, a.g.gamma * grp), D, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_query_rows(const Geo &g) { return g.gamma * (g.nq / g.nkv); }
+
+cudaError_t attention_split(const AttnArgs &a, cudaStream_t s) {
+  if (a.n_items <= 0) return cudaSuccess;
+  if (attn_query_rows(a.g) > QT) return cudaErrorInvalidValue;
+  if (a.g.d == 128) return a.g.kv_fp8 ? launch<128, true>(a, s) : launch<128, false>(a, s);
+  if (a.g.d == 64) return a.g.kv_fp8 ? launch<64, true>(a, s) : launch<64, false>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dfl

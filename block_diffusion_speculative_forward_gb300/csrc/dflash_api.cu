@@ -225,11 +225,15 @@ int32_t pool_pages_for(const dflash_config *c) {
 // buffer to finish.
 int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
                 const std::vector<dfl::RowMeta> &rows, const std::vector<int32_t> &page_ids,
-                cudaStream_t s, dfl::CallMeta *out) {
+                cudaStream_t s, dfl::CallMeta *out,
+                const std::vector<dfl::AttnItem> &items = {},
+                const std::vector<dfl::AttnPair> &pairs = {}) {
   size_t off_seq = 0;
   size_t off_rows = (seq.size() * sizeof(dfl::SeqMeta) + 15) & ~(size_t)15;
   size_t off_pages = (off_rows + rows.size() * sizeof(dfl::RowMeta) + 15) & ~(size_t)15;
-  size_t total = off_pages + page_ids.size() * sizeof(int32_t) + 16;
+  size_t off_items = (off_pages + page_ids.size() * sizeof(int32_t) + 15) & ~(size_t)15;
+  size_t off_pairs = (off_items + items.size() * sizeof(dfl::AttnItem) + 15) & ~(size_t)15;
+  size_t total = off_pairs + pairs.size() * sizeof(dfl::AttnPair) + 16;
   if (h->meta_ev_live) {
     CK(cudaEventSynchronize(h->meta_ev));
     h->meta_ev_live = false;
@@ -261,14 +265,22 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
     memcpy(h->meta_host + off_rows, rows.data(), rows.size() * sizeof(dfl::RowMeta));
   if (!page_ids.empty())
     memcpy(h->meta_host + off_pages, page_ids.data(), page_ids.size() * sizeof(int32_t));
+  if (!items.empty())
+    memcpy(h->meta_host + off_items, items.data(), items.size() * sizeof(dfl::AttnItem));
+  if (!pairs.empty())
+    memcpy(h->meta_host + off_pairs, pairs.data(), pairs.size() * sizeof(dfl::AttnPair));
   CK(cudaMemcpyAsync(h->meta_dev, h->meta_host, total, cudaMemcpyHostToDevice, s));
   CK(cudaEventRecord(h->meta_ev, s));
   h->meta_ev_live = true;
   out->seq = (const dfl::SeqMeta *)(h->meta_dev + off_seq);
   out->rows = (const dfl::RowMeta *)(h->meta_dev + off_rows);
   out->page_ids = (const int32_t *)(h->meta_dev + off_pages);
+  out->items = (const dfl::AttnItem *)(h->meta_dev + off_items);
+  out->pairs = (const dfl::AttnPair *)(h->meta_dev + off_pairs);
   out->n_seq = (int)seq.size();
   out->n_rows = (int)rows.size();
+  out->n_items = (int)items.size();
+  out->n_pairs = (int)pairs.size();
   return DFLASH_OK;
 }
 
@@ -630,8 +642,11 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
         page_ids.push_back(it->second);
       }
   }
+  std::vector<AttnItem> items;
+  std::vector<AttnPair> pairs;
+  build_attn_work(h->g, seq, h->b.attn_slots, &items, &pairs);
   CallMeta cm;
-  int rc = upload_meta(h, seq, rows, page_ids, s, &cm);
+  int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs);
   if (rc) return rc;
   rc = forward(h->g, c, h->w, h->b, cm, num_drafts, bitmask, h->M_ctx, s);
   if (rc) return fail(rc, "%s", last_build_error());

@@ -8,6 +8,7 @@
 #include <string>
 
 #include <algorithm>
+#include <cmath>
 
 #include "forward.h"
 
@@ -191,6 +192,18 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->counters, (size_t)B->n_counters);
   BK(cudaMemset(B->counters, 0, sizeof(int) * (size_t)B->n_counters));
   BA(B->lm_part, (size_t)D_max * vt);
+  // Split-KV attention partials: at most two ctx chunks per (sequence, kv
+  // head) beyond 3 x SMs, plus one block-key item each.
+  {
+    const int n_q = attn_query_rows(g);
+    if (n_q > 128) {
+      g_build_err = "gamma * (num_q_heads / num_kv_heads) must be <= 128";
+      return DFLASH_EINVAL;
+    }
+    B->attn_slot_floats = (int64_t)n_q * g.d + 2 * n_q;
+    B->attn_slots = 3 * sms + 3 * c.max_batch * g.nkv + 64;
+    BA(B->attn_ws, (size_t)B->attn_slots * B->attn_slot_floats);
+  }
   // TMA maps of the activation operands, one per tile width.
   {
     struct A { int id; const void *p; int64_t rows, cols; } acts[ACT_COUNT] = {
@@ -284,8 +297,29 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     LK(tc_gemm(B, W.map_qkv[l], ACT_H, R, g.qkv_w, g.H, EPI_TC_STORE_F32, B.qkv, g.qkv_w, s));
     LK(block_qkv_post(B.qkv, R, cm.seq, g, L.q_norm, L.k_norm, W.cos_t, W.sin_t, B.q, B.kb, B.vb,
                       s));
-    LK(attention_simple(B.q, B.kb, B.vb, cm.seq, cm.page_ids, n, g, W.pool, l, W.kv_scale, B.o,
-                        B.status, s));
+    {
+      AttnArgs a{};
+      a.g = g;
+      a.q = B.q;
+      a.kb = B.kb;
+      a.vb = B.vb;
+      a.o = B.o;
+      a.seq = cm.seq;
+      a.page_ids = cm.page_ids;
+      a.pool = W.pool;
+      a.kv_scale = W.kv_scale;
+      a.layer = l;
+      a.scale = (float)(1.0 / std::sqrt((double)g.d));
+      a.items = cm.items;
+      a.n_items = cm.n_items;
+      a.pairs = cm.pairs;
+      a.n_pairs = cm.n_pairs;
+      a.ws = B.attn_ws;
+      a.slot_floats = B.attn_slot_floats;
+      a.status = B.status;
+      LK(attention_split(a, s));
+      if (cm.n_pairs) count_launches(1);
+    }
     LK(tc_gemm(B, W.map_o[l], ACT_O, R, g.H, qd, EPI_TC_ADD_F32, B.x, g.H, s));
     LK(rmsnorm_rows(B.x, R, g.H, L.post_norm, g.eps, 0, 0, B.h, s));
     LK(tc_gemm(B, W.map_gu[l], ACT_H, R, 2 * g.I, g.H, EPI_TC_STORE_F32, B.gu, 2 * g.I, s));
@@ -338,6 +372,43 @@ cudaError_t gather_kv_rows(const Geo &g, const Weights &W, const Buffers &B, con
                            int n, int layer, float *k_out, float *v_out, cudaStream_t s) {
   (void)B;
   return gather_kv(W.pool, g, layer, rows, n, W.kv_scale, k_out, v_out, s);
+}
+
+}  // namespace dfl
+
+namespace dfl {
+
+void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
+                     std::vector<AttnItem> *items, std::vector<AttnPair> *pairs) {
+  int64_t total = 0;
+  for (const SeqMeta &m : seq) total += (int64_t)(m.pos - m.ws) * g.nkv;
+  const int sms = tc::num_sms();
+  // Chunk so that the ctx items fill about two waves of the SMs.
+  int64_t chunk = (total + 2 * sms - 1) / (2 * sms);
+  chunk = std::max<int64_t>(32, (chunk + 31) / 32 * 32);
+  for (;;) {
+    items->clear();
+    pairs->clear();
+    int slots = 0;
+    for (int s = 0; s < (int)seq.size(); ++s) {
+      const int n_ctx = seq[s].pos - seq[s].ws;
+      const int nc = (int)((n_ctx + chunk - 1) / chunk);
+      for (int h = 0; h < g.nkv; ++h) {
+        if (nc == 0) {
+          items->push_back({s, h, 0, g.gamma, -1});
+          continue;
+        }
+        pairs->push_back({s, h, slots, nc + 1});
+        for (int c = 0; c < nc; ++c) {
+          const int k0 = (int)(c * chunk), k1 = (int)std::min<int64_t>(n_ctx, (c + 1) * chunk);
+          items->push_back({s, h, k0, k1, slots++});
+        }
+        items->push_back({s, h, n_ctx, n_ctx + g.gamma, slots++});
+      }
+    }
+    if (slots <= slot_cap) return;
+    chunk *= 2;
+  }
 }
 
 }  // namespace dfl

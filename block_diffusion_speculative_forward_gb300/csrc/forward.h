@@ -4,6 +4,7 @@
 
 #include <vector>
 
+#include "attention.h"
 #include "dflash.h"
 #include "gemm_tc.h"
 #include "internal.h"
@@ -61,13 +62,23 @@ struct Buffers {
   int *counters = nullptr;      // stream-K tile arrival counters (zero between launches)
   int n_counters = 0;
   LmPartial *lm_part = nullptr; // [D_max][vocab tiles]
+  float *attn_ws = nullptr;     // split-KV attention partial slots
+  int attn_slots = 0;           // slot capacity
+  int64_t attn_slot_floats = 0; // n_q*d + 2*n_q per slot
 };
+
+// Cuts every (sequence, kv head) key range of the call into split-KV items
+// (ctx chunks plus one block-key item) within the workspace's slot capacity.
+void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
+                     std::vector<AttnItem> *items, std::vector<AttnPair> *pairs);
 
 struct CallMeta {
   const SeqMeta *seq = nullptr;
   const RowMeta *rows = nullptr;
   const int32_t *page_ids = nullptr;
-  int n_seq = 0, n_rows = 0;
+  const AttnItem *items = nullptr;
+  const AttnPair *pairs = nullptr;
+  int n_seq = 0, n_rows = 0, n_items = 0, n_pairs = 0;
 };
 
 int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights *w, int R_max,
