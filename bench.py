@@ -319,6 +319,38 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_kernel_case(args):
+    """One tensor-core GEMM at the lm_head shape (15 draft rows x 248320 vocab
+    rows x 2048), 1.02 GB of bf16 weights, timed alone with CUDA events: the
+    small case used for detailed profiles of the weight-streaming kernel."""
+    import ctypes as C
+    from block_diffusion_speculative_forward_gb300 import binding as B
+    L = B.lib()
+    L.dflash_gemm_noalloc.argtypes = [C.c_void_p] * 3 + [C.c_int32] * 3 + [C.c_void_p]
+    m, n, k = 15, syn.FULL.vocab, syn.FULL.hidden
+    g = torch.Generator(device="cuda").manual_seed(5)
+    w = (torch.randn(n, k, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    x = torch.randn(m, k, device="cuda", generator=g).to(torch.bfloat16)
+    y = torch.empty(m, n, device="cuda")
+    s = torch.cuda.current_stream()
+    times = []
+    for i in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        rc = L.dflash_gemm_noalloc(w.data_ptr(), x.data_ptr(), y.data_ptr(), m, n, k, s.cuda_stream)
+        e1.record(s)
+        torch.cuda.synchronize()
+        assert rc == 0, rc
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    nbytes = 2 * n * k + 2 * m * k + 4 * m * n
+    hbm, _, src = peaks()
+    print(json.dumps({"kernel": "tcgen05 GEMM, lm_head shape", "m": m, "n": n, "k": k,
+                      "median_ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                      "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm, "peak_source": src}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -327,12 +359,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-steps", type=int, default=4)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--kernel", default=None, choices=["lm_head"],
+                    help="time one kernel alone instead of the propose step")
     ap.add_argument("--lm-traffic", type=float, default=None,
                     help="ncu dram bytes per lm_head launch, when captured for this build")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.kernel:
+        from block_diffusion_speculative_forward_gb300 import build
+        build.build()
+        run_kernel_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         from block_diffusion_speculative_forward_gb300 import build
