@@ -74,6 +74,7 @@ def lib() -> C.CDLL:
             "dflash_debug_pool": (C.c_int, [vp, C.POINTER(i32), C.POINTER(i32)]),
             "dflash_debug_gather_kv": (C.c_int, [vp, vp, i32, i64, i32, vp, vp, vp]),
             "dflash_debug_set_taps": (C.c_int, [vp, vp, vp, vp]),
+            "dflash_debug_set_graphs": (C.c_int, [vp, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -251,6 +252,10 @@ class DraftHead:
                                             v.data_ptr(), _stream()))
         torch.cuda.current_stream().synchronize()
         return k, v
+
+    def set_graphs(self, enable: bool):
+        """Replay captured CUDA graphs (default) or launch kernels one by one."""
+        _check(lib().dflash_debug_set_graphs(self.ptr, 1 if enable else 0))
 
     def set_taps(self, x_taps=None, z=None, logits=None):
         self._taps = (x_taps, z, logits)

@@ -139,6 +139,9 @@ __device__ __forceinline__ void load_kv_tile(const AttnArgs &a, const AttnItem &
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
+  if ((int)blockIdx.x >= a.counts[0]) return;   // grid sized for the capacity
+  pdl_trigger();
+  pdl_wait();
   constexpr int LD = Smem<D>::LD;
   constexpr int NT = D / 8;          // n8 tiles across the head dim (output)
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -325,30 +328,63 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
   }
 }
 
-// One block per (pair, query vector), D threads: combine the pair's chunks.
+// One warp per (pair, query vector), 4 per block: combine the pair's chunks.
+// m and l of every chunk are read lane-parallel; the partial rows are read as
+// vectors, independent across chunks.
 template <int D>
-__global__ void __launch_bounds__(D) k_attn_merge(AttnArgs a) {
+__global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
+  if ((int)blockIdx.x >= a.counts[1]) return;   // grid sized for the capacity
+  pdl_trigger();
+  pdl_wait();
+  constexpr int VPL = D / 32;   // floats per lane
   const AttnPair pr = a.pairs[blockIdx.x];
-  const int qv = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qv = blockIdx.y * 4 + warp;
   const Geo &g = a.g;
   const int grp = g.nq / g.nkv;
   const int n_q = g.gamma * grp;
   if (qv >= n_q) return;
+  const int64_t off_m = (int64_t)n_q * D + qv, off_l = (int64_t)n_q * D + n_q + qv;
   float M = -INFINITY;
-  for (int c = 0; c < pr.nc; ++c) {
+  for (int c = lane; c < pr.nc; c += 32)
+    M = fmaxf(M, __ldcg(a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats + off_m));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float l = 0.f;
+  for (int c = lane; c < pr.nc; c += 32) {
     const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
-    M = fmaxf(M, __ldcg(ws + (int64_t)n_q * D + qv));
+    const float m = __ldcg(ws + off_m);
+    l += (m == -INFINITY) ? 0.f : __expf(m - M) * __ldcg(ws + off_l);
   }
-  float l = 0.f, o = 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  float acc[VPL];
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
   for (int c = 0; c < pr.nc; ++c) {
     const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
-    const float m = __ldcg(ws + (int64_t)n_q * D + qv);
+    const float m = __ldcg(ws + off_m);
     const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
-    l += w * __ldcg(ws + (int64_t)n_q * D + n_q + qv);
-    o += w * __ldcg(ws + (int64_t)qv * D + threadIdx.x);
+    const float *row = ws + (int64_t)qv * D + lane * VPL;
+    if (VPL == 4) {
+      const float4 r = __ldcg(reinterpret_cast<const float4 *>(row));
+      acc[0] += w * r.x;
+      acc[1] += w * r.y;
+      acc[2] += w * r.z;
+      acc[3] += w * r.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) acc[e] += w * __ldcg(row + e);
+    }
   }
-  bf16 *orow = a.o + ((int64_t)(pr.s * g.gamma + qv / grp) * g.nq + pr.g * grp + qv % grp) * D;
-  orow[threadIdx.x] = __float2bfloat16_rn(o / l);
+  const float inv = 1.f / l;
+  bf16 *orow = a.o + ((int64_t)(pr.s * g.gamma + qv / grp) * g.nq + pr.g * grp + qv % grp) * D +
+               lane * VPL;
+#pragma unroll
+  for (int e = 0; e < VPL; e += 2)
+    *reinterpret_cast<__nv_bfloat162 *>(orow + e) =
+        __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
 }
 
 template <int D, bool FP8>
@@ -361,11 +397,11 @@ cudaError_t launch(const AttnArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_attn_split<D, FP8><<<a.n_items, THREADS, smem, s>>>(a);
+  launch_pdl(k_attn_split<D, FP8>, dim3(a.n_items), dim3(THREADS), smem, s, a);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.n_pairs == 0) return e;
+  if (e != cudaSuccess || a.n_pairs == 0) return e;   // capacity 0: no ctx window at all
   const int grp = a.g.nq / a.g.nkv;
-  k_attn_merge<D><<<dim3(a.n_pairs, a.g.gamma * grp), D, 0, s>>>(a);
+  launch_pdl(k_attn_merge<D>, dim3(a.n_pairs, (a.g.gamma * grp + 3) / 4), dim3(128), 0, s, a);
   return cudaGetLastError();
 }
 

@@ -30,9 +30,10 @@ struct AttnArgs {
   int layer;
   float scale;                // 1/sqrt(d)
   const AttnItem *items;
-  int n_items;
+  int n_items;                // grid size: at least the call's item count
   const AttnPair *pairs;
-  int n_pairs;
+  int n_pairs;                // grid size: at least the call's pair count
+  const int *counts;          // device: [0] items, [1] pairs of this call
   float *ws;                  // partial slots
   int64_t slot_floats;        // n_q*d + 2*n_q
   int *status;

@@ -1,0 +1,151 @@
+// Consumers of the projections: each reads a GEMM's output through a
+// Partials view (dense, or the k-segment partials summed in a fixed order)
+// and applies the step that follows that projection in the layer:
+//   residual add + RMSNorm   (o_proj, down_proj, fc -> hidden_norm, final norm)
+//   per-head q/k RMSNorm + RoPE   (after the stitched QKV projection)
+//   SwiGLU                    (after the interleaved gate/up projection)
+// Sources: [P1] "Struct BlockDiffusionDraftHead" fields hidden_norm, norm,
+// layers, rms_norm_eps, rotary_dim, yarn_inv_freq.
+#include "consumers.h"
+
+namespace dfl {
+
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One block of 1024 threads per row: x[a] (+)= y[a]; out = bf16(g * x / rms(x)).
+__global__ void __launch_bounds__(1024) k_add_norm(AddNormArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sh[32];
+  __shared__ TileRange tr[32];
+  const int a = blockIdx.x;
+  const int n = p.n;
+  constexpr int MAXE = 4;    // up to 4096 features per row
+  if (p.has_y && p.y.ws && threadIdx.x < (n + 127) / 128)
+    tr[threadIdx.x] = part_range(p.y, part_tile(p.y, a, threadIdx.x * 128));
+  __syncthreads();
+  float xv[MAXE];
+  float ss = 0.f;
+#pragma unroll
+  for (int t = 0; t < MAXE; ++t) {
+    const int f = threadIdx.x + t * 1024;
+    if (f < n) {
+      float v = p.x ? p.x[(int64_t)a * n + f] : 0.f;
+      if (p.has_y) v += p.y.ws ? part_sum(p.y, tr[f >> 7], a, f) : part_value(p.y, a, f);
+      xv[t] = v;
+      ss += v * v;
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 32; ++w) tot += sh[w];
+  const float inv = rsqrtf(tot / (float)n + p.eps);
+  // draft-row index of this row, or -1
+  int drow = -1;
+  if (p.z) {
+    const int i = a % p.gamma;
+    if (i >= 1 && i <= p.nd) drow = (a / p.gamma) * p.nd + (i - 1);
+  }
+#pragma unroll
+  for (int t = 0; t < MAXE; ++t) {
+    const int f = threadIdx.x + t * 1024;
+    if (f < n) {
+      const float v = xv[t];
+      if (p.x && p.has_y) p.x[(int64_t)a * n + f] = v;
+      if (p.x_tap) p.x_tap[(int64_t)a * n + f] = v;
+      const bf16 h = __float2bfloat16_rn(__bfloat162float(p.g[f]) * (v * inv));
+      if (p.out) p.out[(int64_t)a * n + f] = h;
+      if (p.z_tap) p.z_tap[(int64_t)a * n + f] = h;
+      if (drow >= 0) p.z[(int64_t)drow * n + f] = h;
+    }
+  }
+}
+
+// Warp per (row, head): q and k heads take RMSNorm with their gain and RoPE at
+// the row's position; v is rounded to bf16.
+template <int NP>
+__global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  const Geo &g = p.g;
+  const int r = blockIdx.x;
+  const int head = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int d = g.d, half = d / 2;
+  const int pos = p.seq[r / g.gamma].pos + r % g.gamma;
+  if (head < g.nq + g.nkv) {
+    const bool is_q = head < g.nq;
+    const int base = is_q ? head * d : g.nq * d + (head - g.nq) * d;
+    float v[2 * NP];
+    float ss = 0.f;
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+      v[2 * t] = part_value(p.y, r, base + lane + 32 * t);
+      v[2 * t + 1] = part_value(p.y, r, base + lane + 32 * t + half);
+      ss += v[2 * t] * v[2 * t] + v[2 * t + 1] * v[2 * t + 1];
+    }
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / (float)d + g.eps);
+    const bf16 *gain = is_q ? p.q_norm : p.k_norm;
+    bf16 *dst = is_q ? p.q + (int64_t)r * g.nq * d + head * d
+                     : p.kb + (int64_t)r * g.kv + (head - g.nq) * d;
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+      const int i = lane + 32 * t;
+      const float x1 = __bfloat162float(gain[i]) * (v[2 * t] * inv);
+      const float x2 = __bfloat162float(gain[i + half]) * (v[2 * t + 1] * inv);
+      const float c = p.cos_t[(int64_t)pos * half + i], sn = p.sin_t[(int64_t)pos * half + i];
+      dst[i] = __float2bfloat16_rn(x1 * c - x2 * sn);
+      dst[i + half] = __float2bfloat16_rn(x2 * c + x1 * sn);
+    }
+  }
+  if (blockIdx.y == 0) {
+    const int vbase = g.nq * d + g.kv;
+    for (int e = threadIdx.x; e < g.kv; e += blockDim.x)
+      p.vb[(int64_t)r * g.kv + e] = __float2bfloat16_rn(part_value(p.y, r, vbase + e));
+  }
+}
+
+// u[a, f] = silu(gate) * up with gate/up rows interleaved in blocks of 64.
+__global__ void __launch_bounds__(256) k_swiglu_part(SwigluArgs p) {
+  pdl_trigger();
+  pdl_wait();
+  const int a = blockIdx.x;
+  for (int f = blockIdx.y * 256 + threadIdx.x; f < p.I; f += gridDim.y * 256) {
+    const int gr = (f >> 6) * 128 + (f & 63);
+    const float gt = part_value(p.y, a, gr), up = part_value(p.y, a, gr + 64);
+    p.u[(int64_t)a * p.I + f] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
+  }
+}
+
+}  // namespace
+
+cudaError_t add_norm(const AddNormArgs &p, int rows, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (p.n > 4 * 1024) return cudaErrorInvalidValue;
+  return launch_pdl(k_add_norm, dim3(rows), dim3(1024), 0, s, p);
+}
+
+cudaError_t qkv_post(const QkvPostArgs &p, int R, cudaStream_t s) {
+  dim3 grid(R, (p.g.nq + p.g.nkv + 7) / 8);
+  if (p.g.d == 128) return launch_pdl(k_qkv_post<2>, grid, dim3(256), 0, s, p);
+  if (p.g.d == 64) return launch_pdl(k_qkv_post<1>, grid, dim3(256), 0, s, p);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t swiglu_part(const SwigluArgs &p, int R, cudaStream_t s) {
+  const int per = (p.I + 255) / 256;
+  const int gy = per < 8 ? per : 8;
+  return launch_pdl(k_swiglu_part, dim3(R, gy), dim3(256), 0, s, p);
+}
+
+}  // namespace dfl

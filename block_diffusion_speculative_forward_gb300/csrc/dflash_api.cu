@@ -90,6 +90,13 @@ struct dflash_handle {
   size_t meta_cap = 0;
   cudaEvent_t meta_ev = nullptr;
   bool meta_ev_live = false;
+  // fixed sections of the metadata buffer (rows follow them)
+  int cap_seq = 0, cap_pages = 0, cap_items = 0, cap_pairs = 0;
+  size_t off_seq = 0, off_pages = 0, off_items = 0, off_pairs = 0, off_rows = 0;
+  // captured propose graphs, keyed by the call's launch shape
+  bool use_graphs = true;
+  cudaStream_t cap_stream = nullptr;
+  std::map<std::vector<uintptr_t>, std::pair<cudaGraphExec_t, int64_t>> graphs;
 };
 
 // ------------------------------------------------------------ helpers --
@@ -173,7 +180,14 @@ T *dev_alloc(dflash_handle *h, size_t count, cudaError_t *err) {
   return (T *)p;
 }
 
+void drop_graphs(dflash_handle *h) {
+  for (auto &kv : h->graphs) cudaGraphExecDestroy(kv.second.first);
+  h->graphs.clear();
+}
+
 void release(dflash_handle *h) {
+  drop_graphs(h);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   for (auto *st : h->states) delete st;
   h->states.clear();
   if (h->meta_ev) cudaEventDestroy(h->meta_ev);
@@ -185,14 +199,16 @@ void release(dflash_handle *h) {
 
 int validate_config(const dflash_config *c) {
   if (!c) return fail(DFLASH_EINVAL, "config is NULL");
-  if (c->num_layers < 1 || c->hidden < 64 || c->hidden % 64)
-    return fail(DFLASH_EINVAL, "num_layers >= 1 and hidden a multiple of 64 required");
+  if (c->num_layers < 1 || c->hidden < 64 || c->hidden % 64 || c->hidden > 4096)
+    return fail(DFLASH_EINVAL, "num_layers >= 1 and hidden a multiple of 64, at most 4096");
   if (c->intermediate < 64 || c->intermediate % 64)
     return fail(DFLASH_EINVAL, "intermediate must be a positive multiple of 64");
   if (c->head_dim != 64 && c->head_dim != 128) return fail(DFLASH_EINVAL, "head_dim must be 64 or 128");
   if (c->num_q_heads < 1 || c->num_kv_heads < 1 || c->num_q_heads % c->num_kv_heads ||
       c->num_kv_heads > 32)
     return fail(DFLASH_EINVAL, "num_q_heads must be a multiple of num_kv_heads (<= 32)");
+  if ((c->num_q_heads * c->head_dim) % 128 || (c->num_kv_heads * c->head_dim) % 128)
+    return fail(DFLASH_EINVAL, "num_q_heads*head_dim and num_kv_heads*head_dim must be multiples of 128");
   if (c->vocab < 2 || c->gamma < 2 || c->gamma > 64)
     return fail(DFLASH_EINVAL, "vocab >= 2 and 2 <= gamma <= 64 required");
   if (c->mask_token_id >= (uint32_t)c->vocab) return fail(DFLASH_EINVAL, "mask_token_id >= vocab");
@@ -223,17 +239,20 @@ int32_t pool_pages_for(const dflash_config *c) {
 // Stage the call's metadata (seq, rows, page ids) and copy it to the device
 // in one transfer. Waits first for the previous transfer out of the staging
 // buffer to finish.
+// Stage the call's metadata and copy it to the device in one transfer. The
+// sections sit at offsets fixed per handle ([counts][seq][page ids][items]
+// [pairs][rows...]), so kernels captured in a graph keep valid pointers
+// across calls. Waits first for the previous transfer out of the staging
+// buffer to finish.
 int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
                 const std::vector<dfl::RowMeta> &rows, const std::vector<int32_t> &page_ids,
                 cudaStream_t s, dfl::CallMeta *out,
                 const std::vector<dfl::AttnItem> &items = {},
                 const std::vector<dfl::AttnPair> &pairs = {}) {
-  size_t off_seq = 0;
-  size_t off_rows = (seq.size() * sizeof(dfl::SeqMeta) + 15) & ~(size_t)15;
-  size_t off_pages = (off_rows + rows.size() * sizeof(dfl::RowMeta) + 15) & ~(size_t)15;
-  size_t off_items = (off_pages + page_ids.size() * sizeof(int32_t) + 15) & ~(size_t)15;
-  size_t off_pairs = (off_items + items.size() * sizeof(dfl::AttnItem) + 15) & ~(size_t)15;
-  size_t total = off_pairs + pairs.size() * sizeof(dfl::AttnPair) + 16;
+  if ((int)seq.size() > h->cap_seq || (int)page_ids.size() > h->cap_pages ||
+      (int)items.size() > h->cap_items || (int)pairs.size() > h->cap_pairs)
+    return fail(DFLASH_EINVAL, "internal: call metadata beyond the handle's capacity");
+  size_t total = h->off_rows + rows.size() * sizeof(dfl::RowMeta) + 16;
   if (h->meta_ev_live) {
     CK(cudaEventSynchronize(h->meta_ev));
     h->meta_ev_live = false;
@@ -259,28 +278,35 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
     h->host_allocs.push_back(hp);
     h->allocs.push_back(dp);
     h->meta_cap = cap;
+    drop_graphs(h);   // captured kernels point into the old buffer
   }
-  if (!seq.empty()) memcpy(h->meta_host + off_seq, seq.data(), seq.size() * sizeof(dfl::SeqMeta));
-  if (!rows.empty())
-    memcpy(h->meta_host + off_rows, rows.data(), rows.size() * sizeof(dfl::RowMeta));
+  int32_t *counts = (int32_t *)h->meta_host;
+  counts[0] = (int32_t)items.size();
+  counts[1] = (int32_t)pairs.size();
+  if (!seq.empty()) memcpy(h->meta_host + h->off_seq, seq.data(), seq.size() * sizeof(dfl::SeqMeta));
   if (!page_ids.empty())
-    memcpy(h->meta_host + off_pages, page_ids.data(), page_ids.size() * sizeof(int32_t));
+    memcpy(h->meta_host + h->off_pages, page_ids.data(), page_ids.size() * sizeof(int32_t));
   if (!items.empty())
-    memcpy(h->meta_host + off_items, items.data(), items.size() * sizeof(dfl::AttnItem));
+    memcpy(h->meta_host + h->off_items, items.data(), items.size() * sizeof(dfl::AttnItem));
   if (!pairs.empty())
-    memcpy(h->meta_host + off_pairs, pairs.data(), pairs.size() * sizeof(dfl::AttnPair));
+    memcpy(h->meta_host + h->off_pairs, pairs.data(), pairs.size() * sizeof(dfl::AttnPair));
+  if (!rows.empty())
+    memcpy(h->meta_host + h->off_rows, rows.data(), rows.size() * sizeof(dfl::RowMeta));
   CK(cudaMemcpyAsync(h->meta_dev, h->meta_host, total, cudaMemcpyHostToDevice, s));
   CK(cudaEventRecord(h->meta_ev, s));
   h->meta_ev_live = true;
-  out->seq = (const dfl::SeqMeta *)(h->meta_dev + off_seq);
-  out->rows = (const dfl::RowMeta *)(h->meta_dev + off_rows);
-  out->page_ids = (const int32_t *)(h->meta_dev + off_pages);
-  out->items = (const dfl::AttnItem *)(h->meta_dev + off_items);
-  out->pairs = (const dfl::AttnPair *)(h->meta_dev + off_pairs);
+  out->counts = (const int *)h->meta_dev;
+  out->seq = (const dfl::SeqMeta *)(h->meta_dev + h->off_seq);
+  out->rows = (const dfl::RowMeta *)(h->meta_dev + h->off_rows);
+  out->page_ids = (const int32_t *)(h->meta_dev + h->off_pages);
+  out->items = (const dfl::AttnItem *)(h->meta_dev + h->off_items);
+  out->pairs = (const dfl::AttnPair *)(h->meta_dev + h->off_pairs);
   out->n_seq = (int)seq.size();
   out->n_rows = (int)rows.size();
   out->n_items = (int)items.size();
   out->n_pairs = (int)pairs.size();
+  out->cap_items = h->cap_items;
+  out->cap_pairs = h->cap_pairs;
   return DFLASH_OK;
 }
 
@@ -340,6 +366,17 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_ha
   h->D_max = cfg->max_batch * (g.gamma - 1);
   h->M_ctx = std::max(cfg->prefill_chunk, h->R_max);
   h->compute = wts != nullptr;
+  {
+    // fixed metadata sections: sequences, window page ids, attention work
+    const int64_t span = cfg->ctx_window > 0 ? std::min<int64_t>(cfg->ctx_window, cfg->max_seq_len) : 0;
+    h->cap_seq = cfg->max_batch;
+    h->cap_pages = (int)(cfg->max_batch * (span / cfg->kv_block + 2));
+    h->cap_pairs = cfg->max_batch * g.nkv;
+    auto al = [](size_t x) { return (x + 15) & ~(size_t)15; };
+    h->off_seq = 16;
+    h->off_pages = al(h->off_seq + sizeof(dfl::SeqMeta) * h->cap_seq);
+    h->off_items = al(h->off_pages + sizeof(int32_t) * h->cap_pages);
+  }
   if (!h->compute) {
     *out = h;
     return DFLASH_OK;
@@ -348,6 +385,7 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_ha
                               &h->allocs, &h->host_allocs);
   if (rc == DFLASH_OK) {
     cudaError_t e = cudaEventCreateWithFlags(&h->meta_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) rc = fail(DFLASH_ECUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
   } else {
     g_err = dfl::last_build_error();
@@ -357,6 +395,9 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_ha
     delete h;
     return rc;
   }
+  h->cap_items = h->b.attn_slots + h->cap_pairs;
+  h->off_pairs = (h->off_items + sizeof(dfl::AttnItem) * h->cap_items + 15) & ~(size_t)15;
+  h->off_rows = (h->off_pairs + sizeof(dfl::AttnPair) * h->cap_pairs + 15) & ~(size_t)15;
   *out = h;
   return DFLASH_OK;
 }
@@ -509,6 +550,13 @@ int dflash_debug_gather_kv(dflash_handle *h, const dflash_state *st, int32_t lay
   return DFLASH_OK;
 }
 
+int dflash_debug_set_graphs(dflash_handle *h, int32_t enable) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  h->use_graphs = enable != 0;
+  if (!h->use_graphs) drop_graphs(h);
+  return DFLASH_OK;
+}
+
 int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end) {
   if (!h) return fail(DFLASH_EINVAL, "NULL handle");
   h->b.probe_begin = (cudaEvent_t)ev_begin;
@@ -570,6 +618,48 @@ int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logit
 
 // ====================================================== propose driver ==
 namespace dfl {
+
+// Runs the forward of a call: replays the graph captured for the call's launch
+// shape (capturing it on first use), or launches the kernels directly when
+// graphs are off or the capture fails.
+int run_forward(dflash_handle *h, const CallMeta &cm, int nd, const int32_t *bitmask,
+                cudaStream_t s) {
+  if (h->use_graphs) {
+    const std::vector<uintptr_t> key = {
+        (uintptr_t)cm.n_seq, (uintptr_t)cm.n_rows, (uintptr_t)nd, (uintptr_t)bitmask,
+        (uintptr_t)h->b.tap_x, (uintptr_t)h->b.tap_z, (uintptr_t)h->b.tap_logits,
+        (uintptr_t)h->b.probe_begin, (uintptr_t)h->b.probe_end};
+    auto it = h->graphs.find(key);
+    if (it == h->graphs.end()) {
+      const int64_t l0 = launch_count();
+      cudaGraph_t graph = nullptr;
+      cudaGraphExec_t exec = nullptr;
+      bool ok = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed) == cudaSuccess;
+      int rc = ok ? forward(h->g, h->cfg, h->w, h->b, cm, nd, bitmask, h->M_ctx, h->cap_stream)
+                  : DFLASH_ECUDA;
+      if (ok) ok = cudaStreamEndCapture(h->cap_stream, &graph) == cudaSuccess && rc == DFLASH_OK;
+      if (ok) ok = cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+      if (graph) cudaGraphDestroy(graph);
+      const int64_t launches = launch_count() - l0;
+      count_launches((int)-launches);   // counted when the graph runs
+      cudaGetLastError();
+      if (ok) {
+        if (h->graphs.size() >= 64) drop_graphs(h);
+        it = h->graphs.emplace(key, std::make_pair(exec, launches)).first;
+      } else {
+        h->use_graphs = false;   // capture is not available here: launch directly from now on
+      }
+    }
+    if (it != h->graphs.end()) {
+      CK(cudaGraphLaunch(it->second.first, s));
+      count_launches((int)it->second.second);
+      return DFLASH_OK;
+    }
+  }
+  const int rc = forward(h->g, h->cfg, h->w, h->b, cm, nd, bitmask, h->M_ctx, s);
+  if (rc) return fail(rc, "%s", last_build_error());
+  return DFLASH_OK;
+}
 
 int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
                  const uint32_t *last_tokens, const int64_t *positions,
@@ -648,8 +738,8 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   CallMeta cm;
   int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs);
   if (rc) return rc;
-  rc = forward(h->g, c, h->w, h->b, cm, num_drafts, bitmask, h->M_ctx, s);
-  if (rc) return fail(rc, "%s", last_build_error());
+  rc = run_forward(h, cm, num_drafts, bitmask, s);
+  if (rc) return rc;
   // Results to the host: one transfer, one synchronisation.
   size_t nd = (size_t)num_drafts;
   CK(cudaMemcpyAsync(h->b.out_host, h->b.out_dev, h->b.out_bytes, cudaMemcpyDeviceToHost, s));

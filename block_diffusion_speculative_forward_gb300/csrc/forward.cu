@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include "consumers.h"
 #include "forward.h"
 
 namespace dfl {
@@ -112,9 +113,13 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     BK(cudaMemcpy(qkv + qd * H, p[2], kv * H * 2, cudaMemcpyDeviceToDevice));
     BK(cudaMemcpy(qkv + (qd + kv) * H, p[3], kv * H * 2, cudaMemcpyDeviceToDevice));
     L.w_qkv = qkv;
+    // gate/up interleaved by blocks of 64 rows: [gate 0..63; up 0..63; gate
+    // 64..127; up 64..127; ...], so one 128-row tile holds matching features.
     bf16 *gu = w_gu + (size_t)l * 2 * I * H;
-    BK(cudaMemcpy(gu, p[8], I * H * 2, cudaMemcpyDeviceToDevice));
-    BK(cudaMemcpy(gu + I * H, p[9], I * H * 2, cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy2D(gu, 128 * H * 2, p[8], 64 * H * 2, 64 * H * 2, I / 64,
+                    cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy2D(gu + 64 * H, 128 * H * 2, p[9], 64 * H * 2, 64 * H * 2, I / 64,
+                    cudaMemcpyDeviceToDevice));
     L.w_gu = gu;
     bf16 *kvl = W->w_kv + (size_t)l * 2 * kv * H;
     BK(cudaMemcpy(kvl, p[2], kv * H * 2, cudaMemcpyDeviceToDevice));
@@ -165,12 +170,10 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   // Scratch.
   BA(B->x, (size_t)R_max * H);
   BA(B->h, (size_t)R_max * std::max(H, I));
-  BA(B->qkv, (size_t)R_max * g.qkv_w);
   BA(B->q, (size_t)R_max * qd);
   BA(B->kb, (size_t)R_max * kv);
   BA(B->vb, (size_t)R_max * kv);
   BA(B->o, (size_t)R_max * qd);
-  BA(B->gu, (size_t)R_max * 2 * I);
   BA(B->u, (size_t)R_max * I);
   BA(B->z, (size_t)D_max * H);
   BA(B->logits, c.lm_head_dtype == 1 ? (size_t)D_max * g.V : 0);
@@ -264,6 +267,38 @@ cudaError_t tc_gemm(const Buffers &B, const CUtensorMap &map_w, ActBuf act, int 
 }
 }  // namespace
 
+namespace {
+
+// A projection whose consumer reads it through a Partials view: split-K
+// partials when the shape allows (no inter-CTA fixup in the GEMM), otherwise
+// a dense f32 store into `dense` [m_act, n_w].
+int project(const Buffers &B, const CUtensorMap &map_w, ActBuf act, int m_act, int n_w, int k,
+            float *dense, Partials *view, cudaStream_t s) {
+  GemmParams p{};
+  p.m_act = m_act;
+  p.n_w = n_w;
+  p.k = k;
+  p.ws = B.ws;
+  p.counters = B.counters;
+  p.status = B.status;
+  const int bn = tc::pick_bn(m_act);
+  if (tc::partial_ok(m_act, n_w, k)) {
+    p.epi = EPI_TC_PARTIAL;
+    LK(tc::gemm(map_w, B.act_map[act][bn_index(bn)], bn, p, s, view));
+  } else {
+    p.epi = EPI_TC_STORE_F32;
+    p.out = dense;
+    p.ldo = n_w;
+    LK(tc::gemm(map_w, B.act_map[act][bn_index(bn)], bn, p, s));
+    *view = Partials{};
+    view->dense = dense;
+    view->ld = n_w;
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace
+
 int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *rows, int m,
                int M_ctx, cudaStream_t s) {
   const int kvw = g.L * 2 * g.kv;
@@ -271,11 +306,22 @@ int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *
     const int mb = std::min(M_ctx, m - a);
     const RowMeta *r = rows + a;
     LK(pack_rows(r, mb, g.S, B.ctx_pack, s));
-    LK(tc_gemm(B, W.map_fc, ACT_PACK, mb, g.H, g.S, EPI_TC_STORE_F32, B.ctx_fc, g.H, s));
-    LK(rmsnorm_rows(B.ctx_fc, mb, g.H, W.hidden_norm, g.eps, 0, 0, B.ctx_c, s));
-    LK(tc_gemm(B, W.map_wkv, ACT_C, mb, kvw, g.H, EPI_TC_STORE_F32, B.ctx_kv, kvw, s));
-    LK(ctx_kv_write(B.ctx_kv, mb, r, g, W.k_norm_dev, W.cos_t, W.sin_t, W.pool, W.kv_scale,
-                    B.status, s));
+    Partials fcv, kvv;
+    int rc = project(B, W.map_fc, ACT_PACK, mb, g.H, g.S, B.ctx_fc, &fcv, s);
+    if (rc) return rc;
+    AddNormArgs an{};
+    an.x = nullptr;
+    an.has_y = true;
+    an.y = fcv;
+    an.g = W.hidden_norm;
+    an.eps = g.eps;
+    an.n = g.H;
+    an.out = B.ctx_c;
+    LK(add_norm(an, mb, s));
+    rc = project(B, W.map_wkv, ACT_C, mb, kvw, g.H, B.ctx_kv, &kvv, s);
+    if (rc) return rc;
+    LK(ctx_kv_write(kvv, mb, r, g, W.k_norm_dev, W.cos_t, W.sin_t, W.pool, W.kv_scale, B.status,
+                    s));
   }
   return DFLASH_OK;
 }
@@ -288,15 +334,68 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   }
   const int n = cm.n_seq, R = n * g.gamma, D = n * nd;
   const int qd = g.nq * g.d;
-  const size_t xbytes = (size_t)R * g.H * sizeof(float);
+  const int bnR = tc::pick_bn(R);
   LK(embed_block(W.embed, cm.seq, n, g, c.mask_token_id, B.x, B.status, s));
-  if (B.tap_x) FK(cudaMemcpyAsync(B.tap_x, B.x, xbytes, cudaMemcpyDeviceToDevice, s));
+  // The residual update of each o/down projection is applied by the RMSNorm
+  // that follows it (pending), or by the GEMM itself when the partial mode
+  // does not fit the shape.
+  Partials pending{};
+  bool has_pending = false;
   for (int l = 0; l < g.L; ++l) {
     const LayerW &L = W.layers[l];
-    LK(rmsnorm_rows(B.x, R, g.H, L.in_norm, g.eps, 0, 0, B.h, s));
-    LK(tc_gemm(B, W.map_qkv[l], ACT_H, R, g.qkv_w, g.H, EPI_TC_STORE_F32, B.qkv, g.qkv_w, s));
-    LK(block_qkv_post(B.qkv, R, cm.seq, g, L.q_norm, L.k_norm, W.cos_t, W.sin_t, B.q, B.kb, B.vb,
-                      s));
+    {
+      AddNormArgs an{};
+      an.x = B.x;
+      an.has_y = has_pending;
+      an.y = pending;
+      an.g = L.in_norm;
+      an.eps = g.eps;
+      an.n = g.H;
+      an.out = B.h;
+      an.x_tap = B.tap_x ? B.tap_x + (size_t)l * R * g.H : nullptr;
+      LK(add_norm(an, R, s));
+    }
+    const bool part = tc::partial_ok(R, g.qkv_w, g.H);
+    if (part) {
+      // QKV partials, then per-head q/k RMSNorm + RoPE
+      QkvPostArgs qp{};
+      qp.g = g;
+      int rc = project(B, W.map_qkv[l], ACT_H, R, g.qkv_w, g.H, nullptr, &qp.y, s);
+      if (rc) return rc;
+      qp.seq = cm.seq;
+      qp.q_norm = L.q_norm;
+      qp.k_norm = L.k_norm;
+      qp.cos_t = W.cos_t;
+      qp.sin_t = W.sin_t;
+      qp.q = B.q;
+      qp.kb = B.kb;
+      qp.vb = B.vb;
+      LK(qkv_post(qp, R, s));
+    } else {
+      // QKV with per-head q/k RMSNorm + RoPE fused in the epilogue
+      GemmParams p{};
+      p.m_act = R;
+      p.n_w = g.qkv_w;
+      p.k = g.H;
+      p.epi = EPI_TC_QKV;
+      p.ws = B.ws;
+      p.counters = B.counters;
+      p.status = B.status;
+      p.seq = cm.seq;
+      p.gamma = g.gamma;
+      p.head_dim = g.d;
+      p.q_rows = qd;
+      p.k_rows = g.kv;
+      p.q_norm = L.q_norm;
+      p.k_norm = L.k_norm;
+      p.cos_t = W.cos_t;
+      p.sin_t = W.sin_t;
+      p.eps = g.eps;
+      p.q_out = B.q;
+      p.k_out = B.kb;
+      p.v_out = B.vb;
+      LK(tc::gemm(W.map_qkv[l], B.act_map[ACT_H][bn_index(bnR)], bnR, p, s));
+    }
     {
       AttnArgs a{};
       a.g = g;
@@ -311,27 +410,81 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       a.layer = l;
       a.scale = (float)(1.0 / std::sqrt((double)g.d));
       a.items = cm.items;
-      a.n_items = cm.n_items;
+      a.n_items = cm.cap_items;
       a.pairs = cm.pairs;
-      a.n_pairs = cm.n_pairs;
+      a.n_pairs = cm.cap_pairs;
+      a.counts = cm.counts;
       a.ws = B.attn_ws;
       a.slot_floats = B.attn_slot_floats;
       a.status = B.status;
       LK(attention_split(a, s));
-      if (cm.n_pairs) count_launches(1);
+      if (cm.cap_pairs) count_launches(1);
     }
-    LK(tc_gemm(B, W.map_o[l], ACT_O, R, g.H, qd, EPI_TC_ADD_F32, B.x, g.H, s));
-    LK(rmsnorm_rows(B.x, R, g.H, L.post_norm, g.eps, 0, 0, B.h, s));
-    LK(tc_gemm(B, W.map_gu[l], ACT_H, R, 2 * g.I, g.H, EPI_TC_STORE_F32, B.gu, 2 * g.I, s));
-    LK(swiglu(B.gu, R, g.I, B.u, s));
-    LK(tc_gemm(B, W.map_down[l], ACT_U, R, g.H, g.I, EPI_TC_ADD_F32, B.x, g.H, s));
-    if (B.tap_x)
-      FK(cudaMemcpyAsync(B.tap_x + (size_t)(l + 1) * R * g.H, B.x, xbytes,
-                         cudaMemcpyDeviceToDevice, s));
+    // o_proj: residual added by the post-attention norm (or by the GEMM)
+    has_pending = tc::partial_ok(R, g.H, qd);
+    if (has_pending) {
+      int rc = project(B, W.map_o[l], ACT_O, R, g.H, qd, nullptr, &pending, s);
+      if (rc) return rc;
+    } else {
+      LK(tc_gemm(B, W.map_o[l], ACT_O, R, g.H, qd, EPI_TC_ADD_F32, B.x, g.H, s));
+    }
+    {
+      AddNormArgs an{};
+      an.x = B.x;
+      an.has_y = has_pending;
+      an.y = pending;
+      an.g = L.post_norm;
+      an.eps = g.eps;
+      an.n = g.H;
+      an.out = B.h;
+      LK(add_norm(an, R, s));
+    }
+    if (tc::partial_ok(R, 2 * g.I, g.H)) {
+      SwigluArgs sp{};
+      int rc = project(B, W.map_gu[l], ACT_H, R, 2 * g.I, g.H, nullptr, &sp.y, s);
+      if (rc) return rc;
+      sp.I = g.I;
+      sp.u = B.u;
+      LK(swiglu_part(sp, R, s));
+    } else {
+      // gate/up with SwiGLU fused in the epilogue
+      GemmParams p{};
+      p.m_act = R;
+      p.n_w = 2 * g.I;
+      p.k = g.H;
+      p.epi = EPI_TC_SWIGLU;
+      p.ws = B.ws;
+      p.counters = B.counters;
+      p.status = B.status;
+      p.u_out = B.u;
+      LK(tc::gemm(W.map_gu[l], B.act_map[ACT_H][bn_index(bnR)], bnR, p, s));
+    }
+    has_pending = tc::partial_ok(R, g.H, g.I);
+    if (has_pending) {
+      int rc = project(B, W.map_down[l], ACT_U, R, g.H, g.I, nullptr, &pending, s);
+      if (rc) return rc;
+    } else {
+      LK(tc_gemm(B, W.map_down[l], ACT_U, R, g.H, g.I, EPI_TC_ADD_F32, B.x, g.H, s));
+    }
   }
-  if (B.tap_z) LK(rmsnorm_rows(B.x, R, g.H, W.norm, g.eps, 0, 0, B.tap_z, s));
-  LK(rmsnorm_rows(B.x, D, g.H, W.norm, g.eps, nd, g.gamma, B.z, s));
-  if (B.probe_begin && B.probe_end) FK(cudaEventRecord(B.probe_begin, s));
+  {
+    // last residual update, the final norm of the draft rows (and the taps)
+    AddNormArgs an{};
+    an.x = B.x;
+    an.has_y = has_pending;
+    an.y = pending;
+    an.g = W.norm;
+    an.eps = g.eps;
+    an.n = g.H;
+    an.out = nullptr;
+    an.x_tap = B.tap_x ? B.tap_x + (size_t)g.L * R * g.H : nullptr;
+    an.z_tap = B.tap_z;
+    an.z = B.z;
+    an.nd = nd;
+    an.gamma = g.gamma;
+    LK(add_norm(an, R, s));
+  }
+  if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));
   if (W.lm_is_fp8) {
     LK(gemm_simple(B.z, g.H, W.lm_fp8, true, W.lm_scale, B.logits, g.V, D, g.V, g.H,
                    EPI_STORE_F32, s));
@@ -354,7 +507,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
     LK(lm_reduce(B.lm_part, D, (g.V + 127) / 128, B.row_id, B.row_p1, s));
   }
-  if (B.probe_begin && B.probe_end) FK(cudaEventRecord(B.probe_end, s));
+  if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_end, s, cudaEventRecordExternal));
   if (B.tap_logits) {
     if (W.lm_is_fp8)
       FK(cudaMemcpyAsync(B.tap_logits, B.logits, (size_t)D * g.V * sizeof(float),
@@ -383,9 +536,10 @@ void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap
   int64_t total = 0;
   for (const SeqMeta &m : seq) total += (int64_t)(m.pos - m.ws) * g.nkv;
   const int sms = tc::num_sms();
-  // Chunk so that the ctx items fill about two waves of the SMs.
-  int64_t chunk = (total + 2 * sms - 1) / (2 * sms);
-  chunk = std::max<int64_t>(32, (chunk + 31) / 32 * 32);
+  // About half an SM wave of ctx items, at least 64 keys each: fewer chunks
+  // keep the partial merge cheap.
+  int64_t chunk = (total + sms / 2 - 1) / (sms / 2);
+  chunk = std::max<int64_t>(64, (chunk + 31) / 32 * 32);
   for (;;) {
     items->clear();
     pairs->clear();

@@ -38,9 +38,7 @@ inline int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 
 struct Buffers {
   float *x = nullptr;          // [R, H] residual
   bf16 *h = nullptr;           // [R, H] normed GEMM input
-  float *qkv = nullptr;        // [R, qkv_w]
   bf16 *q = nullptr, *kb = nullptr, *vb = nullptr, *o = nullptr;
-  float *gu = nullptr;         // [R, 2I]
   bf16 *u = nullptr;           // [R, I]
   bf16 *z = nullptr;           // [D, H] final-normed draft rows
   float *logits = nullptr;     // [D, V]
@@ -78,7 +76,9 @@ struct CallMeta {
   const int32_t *page_ids = nullptr;
   const AttnItem *items = nullptr;
   const AttnPair *pairs = nullptr;
+  const int *counts = nullptr;   // device: items, pairs
   int n_seq = 0, n_rows = 0, n_items = 0, n_pairs = 0;
+  int cap_items = 0, cap_pairs = 0;
 };
 
 int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights *w, int R_max,

@@ -27,6 +27,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
 #include <cstdio>
 #include <mutex>
 
@@ -42,13 +43,20 @@ constexpr int A_BYTES = BM * BK * 2;    // 16 KB
 constexpr int NUM_THREADS = 192;
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
-template <int BN>
+template <int BN, int EPI>
 struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN <= 64) ? 8 : (BN <= 128 ? 6 : 4);
+  // Partial mode (the short batch-1 layer GEMMs): 5 stages and no exchange
+  // buffer, ~95 KB, so two GEMM CTAs fit on an SM and the next GEMM streams
+  // its first weight tiles while this one drains. Other modes: 8 x 16 KB of
+  // weight tiles in flight at the 16-row tile (the lm_head stream needs it).
+  static constexpr bool kPartial = (EPI == EPI_TC_PARTIAL);
+  static constexpr int STAGES = (kPartial && BN == 16) ? 5 : (BN <= 64) ? 8 : (BN <= 128 ? 6 : 4);
+  static_assert(STAGES <= 8, "the barrier arrays in Smem hold 8 stages");
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 2048;
+  static constexpr int EXTRA = kPartial ? 1536 : 10240;   // Smem (without / with xch)
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA;
 };
 
 // ---------------------------------------------------------------- PTX --
@@ -195,7 +203,10 @@ struct Smem {
   float red_v[4][16];
   int red_i[4][16];
   float col_max[16];
+  float xch[16][128];   // per-column exchange between the tile's rows (fused epilogues only)
 };
+// Partial mode reserves shared memory only up to xch, which it never touches.
+static_assert(offsetof(Smem, xch) <= 1536, "Smem head must fit the partial-mode reservation");
 
 // Applies the epilogue to 16 accumulator columns held by this thread
 // (feature row f of tile tm, activation rows a0..a0+15).
@@ -275,6 +286,88 @@ __device__ __forceinline__ void finish16(const GemmParams &p, Smem *sm, const fl
     epi_bar();
     return;
   }
+  if (EPI == EPI_TC_QKV) {
+    // Per-head RMSNorm (gain q_norm / k_norm) then RoPE over the full head for
+    // q and k rows; v rows are stored as they are. A 128-row tile lies in one
+    // region and holds 128 / head_dim whole heads.
+    const int fl = q * 32 + lane;
+    const int d = p.head_dim;
+    const int tile0 = tm * BM;
+    if (tile0 >= p.q_rows + p.k_rows) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int a = a0 + c;
+        if (a < p.m_act)
+          p.v_out[(int64_t)a * p.k_rows + (f - p.q_rows - p.k_rows)] = __float2bfloat16_rn(v[c]);
+      }
+      return;
+    }
+    const bool is_q = tile0 < p.q_rows;
+    const bf16 *gain = is_q ? p.q_norm : p.k_norm;
+    const int i = fl % d;
+    float ss[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float x2 = v[c] * v[c];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x2 += __shfl_xor_sync(0xffffffffu, x2, o);
+      ss[c] = x2;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sm->red_v[q][c] = ss[c];
+    }
+    epi_bar();
+    const float gi = __bfloat162float(gain[i]);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float tot;
+      if (d == 128) tot = sm->red_v[0][c] + sm->red_v[1][c] + sm->red_v[2][c] + sm->red_v[3][c];
+      else tot = sm->red_v[q & 2][c] + sm->red_v[(q & 2) + 1][c];   // d == 64: warps {0,1} / {2,3}
+      const float y = gi * (v[c] * rsqrtf(tot / (float)d + p.eps));
+      sm->xch[c][fl] = y;
+    }
+    epi_bar();
+    const int half = d / 2;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int a = a0 + c;
+      const float y = sm->xch[c][fl];
+      const float other = sm->xch[c][fl ^ half];
+      if (a < p.m_act) {
+        const int pos = p.seq[a / p.gamma].pos + a % p.gamma;
+        const float cs = p.cos_t[(int64_t)pos * half + (i % half)];
+        const float sn = p.sin_t[(int64_t)pos * half + (i % half)];
+        const float o = (i < half) ? (y * cs - other * sn) : (y * cs + other * sn);
+        if (is_q) p.q_out[(int64_t)a * p.q_rows + f] = __float2bfloat16_rn(o);
+        else p.k_out[(int64_t)a * p.k_rows + (f - p.q_rows)] = __float2bfloat16_rn(o);
+      }
+    }
+    epi_bar();
+    return;
+  }
+  if (EPI == EPI_TC_SWIGLU) {
+    // Tile tm holds gate rows of features 64*tm..64*tm+63 in its first 64
+    // rows and the matching up rows in the next 64.
+    const int fl = q * 32 + lane;
+    if (fl >= 64) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sm->xch[c][fl - 64] = v[c];
+    }
+    epi_bar();
+    if (fl < 64) {
+      const int ldu = p.n_w / 2;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int a = a0 + c;
+        if (a >= p.m_act) break;
+        const float gt = v[c], up = sm->xch[c][fl];
+        p.u_out[(int64_t)a * ldu + tm * 64 + fl] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
+      }
+    }
+    epi_bar();
+    return;
+  }
   if (!f_ok) return;
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
@@ -294,7 +387,7 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
               GemmParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -323,6 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  if (threadIdx.x == 0) pdl_trigger();
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_w) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_x) : "memory");
@@ -344,32 +438,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------ TMA producer ------
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
       uint32_t issued = 0, parity = 0;   // per stage: loads issued, phase they complete
-      for (int64_t it = it_begin; it < it_end && !*abort_flag;) {
-        const int t = (int)(it / kb);
-        const int k0 = (int)(it % kb);
-        const int k1 = (int)((int64_t)kb < (int64_t)k0 + (it_end - it) ? (int64_t)kb : (int64_t)k0 + (it_end - it));
-        const int tm = t % p.tiles_m, tn = t / p.tiles_m;
-        for (int k = k0; k < k1; ++k) {
-          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) break;
-          const uint32_t sa = base + stage * C::STAGE_BYTES;
-          const uint32_t fb = smem_u32(&sm->full[stage]);
+      const int64_t n_it = it_end - it_begin;
+      // Weights do not depend on the previous kernel: fill the first stages
+      // with weight tiles before waiting for it, then add the activations.
+      const int n_pre = (int)(n_it < C::STAGES ? n_it : C::STAGES);
+      int t0 = (int)(it_begin / kb), k0 = (int)(it_begin % kb);   // (tile, k-block) of it_begin
+      {
+        int t = t0, k = k0;
+        for (int j = 0; j < n_pre; ++j) {
+          const uint32_t fb = smem_u32(&sm->full[j]);
           mbar_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(sa, &map_w, fb, k * BK, tm * BM, pol_w);
-          tma_load_2d(sa + A_BYTES, &map_x, fb, k * BK, tn * BN, pol_x);
-          issued |= 1u << stage;
-          parity = (parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+          tma_load_2d(base + j * C::STAGE_BYTES, &map_w, fb, k * BK, (t % p.tiles_m) * BM, pol_w);
+          issued |= 1u << j;
+          if (++k == kb) { k = 0; ++t; }
         }
-        it += k1 - k0;
+      }
+      pdl_wait();
+      int t = t0, k = k0;
+      for (int j = 0; j < n_pre; ++j) {
+        tma_load_2d(base + j * C::STAGE_BYTES + A_BYTES, &map_x, smem_u32(&sm->full[j]), k * BK,
+                    (t / p.tiles_m) * BN, pol_x);
+        if (++k == kb) { k = 0; ++t; }
+      }
+      int stage = n_pre % C::STAGES;
+      uint32_t phase = (n_pre == C::STAGES) ? 1u : 0u;
+      for (int64_t j = n_pre; j < n_it && !*abort_flag; ++j) {
+        if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) break;
+        const uint32_t sa = base + stage * C::STAGE_BYTES;
+        const uint32_t fb = smem_u32(&sm->full[stage]);
+        mbar_expect_tx(fb, C::STAGE_BYTES);
+        tma_load_2d(sa, &map_w, fb, k * BK, (t % p.tiles_m) * BM, pol_w);
+        tma_load_2d(sa + A_BYTES, &map_x, fb, k * BK, (t / p.tiles_m) * BN, pol_x);
+        issued |= 1u << stage;
+        parity = (parity & ~(1u << stage)) | (phase << stage);
+        if (++k == kb) { k = 0; ++t; }
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       }
       sm->drain_issued = issued;
       sm->drain_parity = parity;
+    } else {
+      pdl_wait();
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer --------
+    pdl_wait();
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<BN>();
       int stage = 0;
@@ -405,6 +518,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------ epilogue ----------
+    pdl_wait();
     const int q = warp & 3;                  // TMEM lane quarter of this warp
     const int f_local = q * 32 + lane;       // weight row within the tile
     int acc = 0;
@@ -425,18 +539,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
         tmem_ld16(tbase + c0, v);
-        if (whole) {
+        if (EPI == EPI_TC_PARTIAL) {
+          // [BN rows][128 features]: coalesced for this store and for the
+          // consumer, which reads along features
+#pragma unroll
+          for (int c = 0; c < 16; ++c) ws[(int64_t)(c0 + c) * BM + f_local] = v[c];
+        } else if (whole) {
           finish16<EPI>(p, sm, v, f, tm, tn * BN + c0, q, lane);
         } else {
+          // thread-major partial: this thread's BN columns are contiguous
+          float4 *dst = reinterpret_cast<float4 *>(ws + (int64_t)f_local * BN + c0);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) ws[(c0 + c) * BM + f_local] = v[c];
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         }
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(smem_u32(&sm->acc_empty[acc]));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
-      if (!whole) {
+      if (!whole && EPI != EPI_TC_PARTIAL) {
         // stream-K fixup: the last contributor of the tile sums the partials
         __threadfence();
         epi_bar();
@@ -453,11 +575,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float v[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] = 0.f;
-            for (int cc = c_lo; cc <= c_hi; ++cc) {
-              const int sl = 2 * cc + ((cc == c_lo && part.begin(cc) < (int64_t)t * kb) ? 1 : 0);
-              const float *src = p.ws + (int64_t)sl * BN * BM;
+            // contributors in ascending order, four partial reads in flight
+            for (int cc0 = c_lo; cc0 <= c_hi; cc0 += 4) {
+              float4 r[4][4];
 #pragma unroll
-              for (int c = 0; c < 16; ++c) v[c] += __ldcg(src + (c0 + c) * BM + f_local);
+              for (int u = 0; u < 4; ++u) {
+                const int cc = cc0 + u;
+                if (cc <= c_hi) {
+                  const int sl =
+                      2 * cc + ((cc == c_lo && part.begin(cc) < (int64_t)t * kb) ? 1 : 0);
+                  const float4 *src = reinterpret_cast<const float4 *>(
+                      p.ws + (int64_t)sl * BN * BM + (int64_t)f_local * BN + c0);
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) r[u][c] = __ldcg(src + c);
+                } else {
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) r[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  v[4 * c] += r[u][c].x;
+                  v[4 * c + 1] += r[u][c].y;
+                  v[4 * c + 2] += r[u][c].z;
+                  v[4 * c + 3] += r[u][c].w;
+                }
             }
             finish16<EPI>(p, sm, v, f, tm, tn * BN + c0, q, lane);
           }
@@ -523,7 +667,8 @@ cudaError_t set_smem_attr() {
   static bool done = false;
   if (done) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, EPI>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<BN, EPI>::SMEM);
   if (e == cudaSuccess) done = true;
   return e;
 }
@@ -533,7 +678,8 @@ cudaError_t launch_bn(const CUtensorMap &mw, const CUtensorMap &mx, const GemmPa
                       cudaStream_t s) {
   cudaError_t e = set_smem_attr<BN, EPI>();
   if (e != cudaSuccess) return e;
-  k_gemm_tc<BN, EPI><<<grid, NUM_THREADS, Cfg<BN>::SMEM, s>>>(mw, mx, p);
+  e = launch_pdl(k_gemm_tc<BN, EPI>, dim3(grid), dim3(NUM_THREADS), Cfg<BN, EPI>::SMEM, s, mw, mx, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -580,8 +726,16 @@ int pick_bn(int m_act) {
   return 256;
 }
 
+bool partial_ok(int m_act, int n_w, int k) {
+  const int bn = pick_bn(m_act);
+  const int64_t total = (int64_t)((n_w + BM - 1) / BM) * ((m_act + bn - 1) / bn) * (k / BK);
+  int grid = num_sms();
+  if (total < grid) grid = (int)total;
+  return grid > 0 && (total + grid - 1) / grid <= k / BK && total * grid < (1ll << 31);
+}
+
 cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, GemmParams p,
-                 cudaStream_t s) {
+                 cudaStream_t s, Partials *view) {
   if (p.m_act <= 0 || p.n_w <= 0) return cudaSuccess;
   if (p.k % BK) return cudaErrorInvalidValue;
   p.tiles_m = (p.n_w + BM - 1) / BM;
@@ -591,11 +745,25 @@ cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, Gem
   if (p.grid_cap > 0 && p.grid_cap < grid) grid = p.grid_cap;
   if (total < grid) grid = (int)total;
   if (grid < 1) grid = 1;
+  if (p.epi == EPI_TC_PARTIAL) {
+    if ((total + grid - 1) / grid > p.k / BK || !view) return cudaErrorInvalidValue;
+    view->ws = p.ws;
+    view->dense = nullptr;
+    view->ld = 0;
+    view->tiles_m = p.tiles_m;
+    view->kb = p.k / BK;
+    view->G = grid;
+    view->bn = bn;
+    view->total = (int)total;
+  }
   switch (p.epi) {
     case EPI_TC_STORE_F32: return launch_epi<EPI_TC_STORE_F32>(bn, map_w, map_x, p, grid, s);
     case EPI_TC_ADD_F32: return launch_epi<EPI_TC_ADD_F32>(bn, map_w, map_x, p, grid, s);
     case EPI_TC_STORE_BF16: return launch_epi<EPI_TC_STORE_BF16>(bn, map_w, map_x, p, grid, s);
     case EPI_TC_LMHEAD: return launch_epi<EPI_TC_LMHEAD>(bn, map_w, map_x, p, grid, s);
+    case EPI_TC_QKV: return launch_epi<EPI_TC_QKV>(bn, map_w, map_x, p, grid, s);
+    case EPI_TC_SWIGLU: return launch_epi<EPI_TC_SWIGLU>(bn, map_w, map_x, p, grid, s);
+    case EPI_TC_PARTIAL: return launch_epi<EPI_TC_PARTIAL>(bn, map_w, map_x, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -621,6 +789,8 @@ __global__ void k_lm_reduce(const LmPartial *__restrict__ part, int tiles,
                             int32_t *__restrict__ row_id, float *__restrict__ row_p1) {
   __shared__ float sm_m[32], sm_s[32];
   __shared__ int sm_i[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const LmPartial *pr = part + (int64_t)r * tiles;
   float m = -INFINITY, s = 0.f;
@@ -650,7 +820,8 @@ __global__ void k_lm_reduce(const LmPartial *__restrict__ part, int tiles,
 cudaError_t lm_reduce(const LmPartial *part, int rows, int tiles, int32_t *row_id, float *row_p1,
                       cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  k_lm_reduce<<<rows, 256, 0, s>>>(part, tiles, row_id, row_p1);
+  cudaError_t e = launch_pdl(k_lm_reduce, dim3(rows), dim3(256), 0, s, part, tiles, row_id, row_p1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

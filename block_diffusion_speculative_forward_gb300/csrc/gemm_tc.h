@@ -12,7 +12,67 @@ enum TcEpi {
   EPI_TC_ADD_F32 = 1,     // out[a, f] += y        (residual stream)
   EPI_TC_STORE_BF16 = 2,  // out[a, f] = bf16(y)
   EPI_TC_LMHEAD = 3,      // per (row, 128-row vocab tile): max, lowest argmax, sum exp
+  EPI_TC_QKV = 4,         // stitched q;k;v rows: per-head RMSNorm + RoPE for q and k, bf16 out
+  EPI_TC_SWIGLU = 5,      // gate/up rows interleaved by 64: u = silu(gate) * up, bf16 out
+  EPI_TC_PARTIAL = 6,     // every k-segment writes its f32 partial; the consumer sums them
 };
+
+// The output of a GEMM as its consumer reads it: either a dense f32 matrix,
+// or the k-segment partials of an EPI_TC_PARTIAL launch. Element (a, f) of a
+// partial view is the sum, in ascending CTA order, of the partials of the
+// CTAs whose k-ranges cover tile (f / 128, a / bn): the same value a fused
+// epilogue would see, without any inter-CTA synchronisation in the GEMM.
+struct Partials {
+  const float *ws = nullptr;     // partial slots, or NULL for a dense matrix
+  const float *dense = nullptr;  // [rows, ld]
+  int ld = 0;
+  int tiles_m = 0, kb = 0, G = 0, bn = 0, total = 0;
+};
+
+__device__ __forceinline__ int part_begin(int total, int G, int c) {
+  return (int)(((unsigned)total * (unsigned)c) / (unsigned)G);
+}
+__device__ __forceinline__ int part_owner(int total, int G, int i) {
+  int c = (int)(((unsigned)i * (unsigned)G) / (unsigned)total);
+  while (c + 1 < G && part_begin(total, G, c + 1) <= i) ++c;
+  while (c > 0 && part_begin(total, G, c) > i) --c;
+  return c;
+}
+
+// Contributors of one tile: CTAs c_lo..c_hi; c_lo's segment of the tile is
+// its second one when lo_second.
+struct TileRange {
+  int c_lo, c_hi, lo_second;
+};
+__device__ __forceinline__ TileRange part_range(const Partials &P, int t) {
+  const int i0 = t * P.kb;
+  TileRange r;
+  r.c_lo = part_owner(P.total, P.G, i0);
+  r.c_hi = part_owner(P.total, P.G, i0 + P.kb - 1);
+  r.lo_second = part_begin(P.total, P.G, r.c_lo) < i0 ? 1 : 0;
+  return r;
+}
+// Partial slots are laid out [slot][bn rows][128 features].
+__device__ __forceinline__ float part_sum(const Partials &P, const TileRange &r, int a, int f) {
+  const float *base = P.ws + (a % P.bn) * 128 + (f & 127);
+  const long long stride = (long long)P.bn * 128;
+  float s = __ldcg(base + (2 * r.c_lo + r.lo_second) * stride);
+  for (int c = r.c_lo + 1; c <= r.c_hi; c += 4) {   // four loads in flight, added in order
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = (c + u <= r.c_hi) ? __ldcg(base + 2 * (c + u) * stride) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) s += v[u];
+  }
+  return s;
+}
+__device__ __forceinline__ int part_tile(const Partials &P, int a, int f) {
+  return (a / P.bn) * P.tiles_m + (f >> 7);
+}
+__device__ __forceinline__ float part_value(const Partials &P, int a, int f) {
+  if (!P.ws) return P.dense[(long long)a * P.ld + f];
+  return part_sum(P, part_range(P, part_tile(P, a, f)), a, f);
+}
 
 // One (row, vocab tile) partial of the lm_head reduction.
 struct LmPartial {
@@ -40,6 +100,17 @@ struct GemmParams {
   int nd;             // draft rows per sequence (row a belongs to sequence a / nd)
   LmPartial *lm_part; // [m_act][tiles_m]
   int *status;
+  // QKV epilogue: rows [0, q_rows) are q heads, [q_rows, q_rows + k_rows) k
+  // heads, the rest v; row a of the activations is block row a % gamma of
+  // sequence a / gamma, at position seq[a / gamma].pos + a % gamma.
+  const SeqMeta *seq;
+  int gamma, head_dim, q_rows, k_rows;
+  const bf16 *q_norm, *k_norm;
+  const float *cos_t, *sin_t;
+  float eps;
+  bf16 *q_out, *k_out, *v_out;   // [m_act, q_rows], [m_act, k_rows], [m_act, k_rows]
+  // SwiGLU epilogue: u[m_act, n_w / 2]
+  bf16 *u_out;
   // filled by the launcher
   int tiles_m, tiles_n;
 };
@@ -50,8 +121,12 @@ int pick_bn(int m_act);
 // 2-D row-major map [rows, cols], box = 128 bytes of a row x box_rows rows, 128B swizzle.
 bool make_map_2d(CUtensorMap *map, const void *base, bool fp8, int64_t rows, int64_t cols,
                  int box_rows);
+// Launches the GEMM. For EPI_TC_PARTIAL, *view receives the partials' layout.
 cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, GemmParams p,
-                 cudaStream_t s);
+                 cudaStream_t s, Partials *view = nullptr);
+// Whether EPI_TC_PARTIAL can serve this shape: every CTA's k-range must span
+// at most two tiles (two partial slots per CTA).
+bool partial_ok(int m_act, int n_w, int k);
 // Bytes of stream-K partial workspace for the widest tile and a full grid.
 inline size_t ws_floats(int grid) { return (size_t)2 * grid * 256 * 128; }
 }  // namespace tc

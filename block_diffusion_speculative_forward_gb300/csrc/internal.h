@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 namespace dfl {
 
@@ -63,6 +64,34 @@ __host__ __device__ inline int64_t kv_offset(const Geo &g, int64_t page, int l, 
   return ((((page * g.L + l) * 2 + kind) * g.nkv + h) * (int64_t)g.B + slot) * g.d;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Every kernel of the forward is launched with programmatic stream
+// serialisation: it may start while its predecessor drains, lets its own
+// successor launch at once (pdl_trigger), and touches data produced upstream
+// only after pdl_wait, which returns once the predecessor grid has completed
+// and its writes are visible. Every kernel executes pdl_wait, so completion
+// is transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------- launchers --
 enum GemmEpi { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_STORE_BF16 = 2 };
 
@@ -81,20 +110,10 @@ cudaError_t embed_block(const bf16 *E, const SeqMeta *seq, int n_seq, const Geo 
 
 cudaError_t pack_rows(const RowMeta *rows, int m, int S, bf16 *out, cudaStream_t s);
 
-cudaError_t ctx_kv_write(const float *kv, int m, const RowMeta *rows, const Geo &g,
+struct Partials;
+cudaError_t ctx_kv_write(const Partials &kv, int m, const RowMeta *rows, const Geo &g,
                          const bf16 *const *k_norm_dev, const float *cos_t, const float *sin_t,
                          void *pool, const float *kv_scale, int *status, cudaStream_t s);
-
-cudaError_t block_qkv_post(const float *qkv, int R, const SeqMeta *seq, const Geo &g,
-                           const bf16 *q_norm, const bf16 *k_norm, const float *cos_t,
-                           const float *sin_t, bf16 *q, bf16 *kb, bf16 *vb, cudaStream_t s);
-
-cudaError_t attention_simple(const bf16 *q, const bf16 *kb, const bf16 *vb, const SeqMeta *seq,
-                             const int32_t *page_ids, int n_seq, const Geo &g, const void *pool,
-                             int layer, const float *kv_scale, bf16 *o, int *status,
-                             cudaStream_t s);
-
-cudaError_t swiglu(const float *gu, int R, int I, bf16 *u, cudaStream_t s);
 
 // Per draft row: (argmax id or -1 when nothing is allowed, top-1 probability).
 cudaError_t argmax_rows(const float *logits, int rows, int V, const int32_t *bitmask, int nd,

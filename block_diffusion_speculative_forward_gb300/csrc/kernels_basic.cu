@@ -6,6 +6,7 @@
 //   [P1] "Struct BlockDiffusionDraftHead" (spark_model docs)
 //   [P2] "BlockDiffusionDraftHead" (metrale docs)
 //   [P3] "Trait DraftProposer" (spark_model docs)
+#include "gemm_tc.h"
 #include "internal.h"
 
 #include <cfloat>
@@ -48,6 +49,8 @@ __global__ void __launch_bounds__(256) k_gemm_simple(const bf16 *__restrict__ A,
                                                      const void *__restrict__ W,
                                                      const float *__restrict__ wscale, void *C,
                                                      int ldc, int m, int n, int K) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float As[32][65];
   __shared__ float Ws[32][65];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -108,9 +111,9 @@ cudaError_t gemm_simple(const bf16 *A, int lda, const void *W, bool w_fp8, const
 #define DFL_GEMM_CASE(E)                                                                       \
   if (epi == E) {                                                                              \
     if (w_fp8)                                                                                 \
-      k_gemm_simple<E, true><<<grid, 256, 0, s>>>(A, lda, W, wscale, C, ldc, m, n, K);         \
+      launch_pdl(k_gemm_simple<E, true>, dim3(grid), dim3(256), 0, s, A, lda, W, wscale, C, ldc, m, n, K);         \
     else                                                                                       \
-      k_gemm_simple<E, false><<<grid, 256, 0, s>>>(A, lda, W, wscale, C, ldc, m, n, K);        \
+      launch_pdl(k_gemm_simple<E, false>, dim3(grid), dim3(256), 0, s, A, lda, W, wscale, C, ldc, m, n, K);        \
   }
   DFL_GEMM_CASE(EPI_STORE_F32)
   DFL_GEMM_CASE(EPI_ADD_F32)
@@ -123,6 +126,8 @@ cudaError_t gemm_simple(const bf16 *A, int lda, const void *W, bool w_fp8, const
 // [P1] fields rms_norm_eps, hidden_norm, norm; the Qwen3 layer norms.
 __global__ void k_rmsnorm_rows(const float *__restrict__ x, int n, const bf16 *__restrict__ g,
                                float eps, int nd, int gamma, bf16 *__restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sh[32];
   int i = blockIdx.x;
   int r = nd > 0 ? (i / nd) * gamma + 1 + (i % nd) : i;
@@ -138,7 +143,7 @@ __global__ void k_rmsnorm_rows(const float *__restrict__ x, int n, const bf16 *_
 cudaError_t rmsnorm_rows(const float *x, int rows, int n, const bf16 *g, float eps, int nd,
                          int gamma, bf16 *out, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  k_rmsnorm_rows<<<rows, 256, 0, s>>>(x, n, g, eps, nd, gamma, out);
+  launch_pdl(k_rmsnorm_rows, dim3(rows), dim3(256), 0, s, x, n, g, eps, nd, gamma, out);
   return cudaGetLastError();
 }
 
@@ -148,6 +153,8 @@ cudaError_t rmsnorm_rows(const float *x, int rows, int n, const bf16 *g, float e
 __global__ void k_embed_block(const bf16 *__restrict__ E, const SeqMeta *__restrict__ seq,
                               int gamma, int H, int V, uint32_t mask_token, float *__restrict__ x,
                               int *status) {
+  pdl_trigger();
+  pdl_wait();
   int r = blockIdx.x;
   int i = r % gamma;
   uint32_t tok = i == 0 ? (uint32_t)seq[r / gamma].token : mask_token;
@@ -161,7 +168,7 @@ __global__ void k_embed_block(const bf16 *__restrict__ E, const SeqMeta *__restr
 
 cudaError_t embed_block(const bf16 *E, const SeqMeta *seq, int n_seq, const Geo &g,
                         uint32_t mask_token, float *x, int *status, cudaStream_t s) {
-  k_embed_block<<<n_seq * g.gamma, 256, 0, s>>>(E, seq, g.gamma, g.H, g.V, mask_token, x, status);
+  launch_pdl(k_embed_block, dim3(n_seq * g.gamma), dim3(256), 0, s, E, seq, g.gamma, g.H, g.V, mask_token, x, status);
   return cudaGetLastError();
 }
 
@@ -169,6 +176,8 @@ cudaError_t embed_block(const bf16 *E, const SeqMeta *seq, int n_seq, const Geo 
 // Gathers the ctx rows to compute from the callers' stacks into one
 // contiguous [m, S] buffer (16-byte vectors; S*2 is a multiple of 16).
 __global__ void k_pack_rows(const RowMeta *__restrict__ rows, int S, bf16 *__restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   int r = blockIdx.x;
   const uint4 *src = (const uint4 *)rows[r].src;
   uint4 *dst = (uint4 *)(out + (int64_t)r * S);
@@ -178,7 +187,7 @@ __global__ void k_pack_rows(const RowMeta *__restrict__ rows, int S, bf16 *__res
 
 cudaError_t pack_rows(const RowMeta *rows, int m, int S, bf16 *out, cudaStream_t s) {
   if (m <= 0) return cudaSuccess;
-  k_pack_rows<<<m, 256, 0, s>>>(rows, S, out);
+  launch_pdl(k_pack_rows, dim3(m), dim3(256), 0, s, rows, S, out);
   return cudaGetLastError();
 }
 
@@ -213,10 +222,12 @@ __device__ __forceinline__ void norm_rope_warp(float (&v)[2 * NP], const bf16 *g
 // K/V GEMM output [L*2*kv] (per layer K then V) becomes, per layer and kv
 // head, k = RoPE(k_norm(k), pos) and v, written to (page, slot) of the pool.
 template <int NP>
-__global__ void k_ctx_kv_write(const float *__restrict__ kv, const RowMeta *__restrict__ rows,
+__global__ void k_ctx_kv_write(const Partials kv, const RowMeta *__restrict__ rows,
                                Geo g, const bf16 *const *__restrict__ k_norm,
                                const float *__restrict__ cos_t, const float *__restrict__ sin_t,
                                void *pool, const float *__restrict__ kv_scale, int *status) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, l = blockIdx.y;
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = g.d, half = d / 2;
@@ -225,13 +236,12 @@ __global__ void k_ctx_kv_write(const float *__restrict__ kv, const RowMeta *__re
     if (threadIdx.x == 0) atomicOr(status, ST_PAGE);
     return;
   }
-  const float *kr = kv + (int64_t)r * (g.L * 2 * g.kv) + (int64_t)l * 2 * g.kv + h * d;
-  const float *vr = kr + g.kv;
+  const int kcol = l * 2 * g.kv + h * d, vcol = kcol + g.kv;
   float v[2 * NP];
 #pragma unroll
   for (int t = 0; t < NP; ++t) {
-    v[2 * t] = kr[lane + 32 * t];
-    v[2 * t + 1] = kr[lane + 32 * t + half];
+    v[2 * t] = part_value(kv, r, kcol + lane + 32 * t);
+    v[2 * t + 1] = part_value(kv, r, kcol + lane + 32 * t + half);
   }
   norm_rope_warp<NP>(v, k_norm[l], g.eps, d, cos_t + (int64_t)rm.pos * half,
                      sin_t + (int64_t)rm.pos * half);
@@ -246,7 +256,7 @@ __global__ void k_ctx_kv_write(const float *__restrict__ kv, const RowMeta *__re
       P[ko + i] = float_to_fp8(v[2 * t] / sk);
       P[ko + i + half] = float_to_fp8(v[2 * t + 1] / sk);
     }
-    for (int e = lane; e < d; e += 32) P[vo + e] = float_to_fp8(vr[e] / sv);
+    for (int e = lane; e < d; e += 32) P[vo + e] = float_to_fp8(part_value(kv, r, vcol + e) / sv);
   } else {
     bf16 *P = (bf16 *)pool;
 #pragma unroll
@@ -255,194 +265,23 @@ __global__ void k_ctx_kv_write(const float *__restrict__ kv, const RowMeta *__re
       P[ko + i] = __float2bfloat16_rn(v[2 * t]);
       P[ko + i + half] = __float2bfloat16_rn(v[2 * t + 1]);
     }
-    for (int e = lane; e < d; e += 32) P[vo + e] = __float2bfloat16_rn(vr[e]);
+    for (int e = lane; e < d; e += 32) P[vo + e] = __float2bfloat16_rn(part_value(kv, r, vcol + e));
   }
 }
 
-cudaError_t ctx_kv_write(const float *kv, int m, const RowMeta *rows, const Geo &g,
+cudaError_t ctx_kv_write(const Partials &kv, int m, const RowMeta *rows, const Geo &g,
                          const bf16 *const *k_norm_dev, const float *cos_t, const float *sin_t,
                          void *pool, const float *kv_scale, int *status, cudaStream_t s) {
   if (m <= 0) return cudaSuccess;
   dim3 grid(m, g.L);
   if (g.d == 128)
-    k_ctx_kv_write<2><<<grid, 32 * g.nkv, 0, s>>>(kv, rows, g, k_norm_dev, cos_t, sin_t, pool,
+    launch_pdl(k_ctx_kv_write<2>, dim3(grid), dim3(32 * g.nkv), 0, s, kv, rows, g, k_norm_dev, cos_t, sin_t, pool,
                                                   kv_scale, status);
   else if (g.d == 64)
-    k_ctx_kv_write<1><<<grid, 32 * g.nkv, 0, s>>>(kv, rows, g, k_norm_dev, cos_t, sin_t, pool,
+    launch_pdl(k_ctx_kv_write<1>, dim3(grid), dim3(32 * g.nkv), 0, s, kv, rows, g, k_norm_dev, cos_t, sin_t, pool,
                                                   kv_scale, status);
   else
     return cudaErrorInvalidValue;
-  return cudaGetLastError();
-}
-
-// ----------------------------------------- block q/k norm + RoPE, v copy --
-// The Qwen3 per-head q/k RMSNorm, then RoPE at the row's position p + i.
-template <int NP>
-__global__ void k_block_qkv_post(const float *__restrict__ qkv, const SeqMeta *__restrict__ seq,
-                                 Geo g, const bf16 *__restrict__ q_norm,
-                                 const bf16 *__restrict__ k_norm, const float *__restrict__ cos_t,
-                                 const float *__restrict__ sin_t, bf16 *__restrict__ q,
-                                 bf16 *__restrict__ kb, bf16 *__restrict__ vb) {
-  const int r = blockIdx.x;
-  const int head = blockIdx.y * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int d = g.d, half = d / 2;
-  const int pos = seq[r / g.gamma].pos + r % g.gamma;
-  const float *row = qkv + (int64_t)r * g.qkv_w;
-  if (head < g.nq + g.nkv) {
-    const bool is_q = head < g.nq;
-    const float *src = is_q ? row + head * d : row + g.nq * d + (head - g.nq) * d;
-    float v[2 * NP];
-#pragma unroll
-    for (int t = 0; t < NP; ++t) {
-      v[2 * t] = src[lane + 32 * t];
-      v[2 * t + 1] = src[lane + 32 * t + half];
-    }
-    norm_rope_warp<NP>(v, is_q ? q_norm : k_norm, g.eps, d, cos_t + (int64_t)pos * half,
-                       sin_t + (int64_t)pos * half);
-    bf16 *dst = is_q ? q + (int64_t)r * g.nq * d + head * d
-                     : kb + (int64_t)r * g.kv + (head - g.nq) * d;
-#pragma unroll
-    for (int t = 0; t < NP; ++t) {
-      dst[lane + 32 * t] = __float2bfloat16_rn(v[2 * t]);
-      dst[lane + 32 * t + half] = __float2bfloat16_rn(v[2 * t + 1]);
-    }
-  }
-  if (blockIdx.y == 0) {
-    const float *vsrc = row + g.nq * d + g.kv;
-    for (int e = threadIdx.x; e < g.kv; e += blockDim.x)
-      vb[(int64_t)r * g.kv + e] = __float2bfloat16_rn(vsrc[e]);
-  }
-}
-
-cudaError_t block_qkv_post(const float *qkv, int R, const SeqMeta *seq, const Geo &g,
-                           const bf16 *q_norm, const bf16 *k_norm, const float *cos_t,
-                           const float *sin_t, bf16 *q, bf16 *kb, bf16 *vb, cudaStream_t s) {
-  dim3 grid(R, (g.nq + g.nkv + 7) / 8);
-  if (g.d == 128)
-    k_block_qkv_post<2><<<grid, 256, 0, s>>>(qkv, seq, g, q_norm, k_norm, cos_t, sin_t, q, kb, vb);
-  else if (g.d == 64)
-    k_block_qkv_post<1><<<grid, 256, 0, s>>>(qkv, seq, g, q_norm, k_norm, cos_t, sin_t, q, kb, vb);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
-}
-
-// -------------------------------------------------- block attention --
-// One warp per (block row, q head): online softmax over the window's ctx keys
-// (paged) and the gamma block keys, no mask inside the block. q head j reads
-// kv head j * nkv / nq. Lane owns d/32 contiguous elements.
-template <int EPL>
-__global__ void k_attention_simple(const bf16 *__restrict__ q, const bf16 *__restrict__ kb,
-                                   const bf16 *__restrict__ vb, const SeqMeta *__restrict__ seq,
-                                   const int32_t *__restrict__ page_ids, Geo g,
-                                   const void *__restrict__ pool, int layer,
-                                   const float *__restrict__ kv_scale, float scale,
-                                   bf16 *__restrict__ o, int *status) {
-  const int r = blockIdx.x, j = blockIdx.y, lane = threadIdx.x;
-  const int s_idx = r / g.gamma;
-  const SeqMeta sm = seq[s_idx];
-  const int kvh = (j * g.nkv) / g.nq;
-  const int e0 = lane * EPL;
-  float qv[EPL], acc[EPL];
-  const bf16 *qr = q + (int64_t)r * g.nq * g.d + j * g.d + e0;
-#pragma unroll
-  for (int t = 0; t < EPL; ++t) {
-    qv[t] = __bfloat162float(qr[t]) * scale;
-    acc[t] = 0.f;
-  }
-  float mx = -INFINITY, den = 0.f;
-  float sk = 1.f, sv = 1.f;
-  if (g.kv_fp8) {
-    sk = kv_scale[(layer * g.nkv + kvh) * 2 + 0];
-    sv = kv_scale[(layer * g.nkv + kvh) * 2 + 1];
-  }
-  const int b0 = sm.ws / g.B;
-  for (int pos = sm.ws; pos < sm.pos; ++pos) {
-    int page = page_ids[sm.page_base + (pos / g.B - b0)];
-    if (page < 0 || page >= g.pages) {
-      if (lane == 0) atomicOr(status, ST_PAGE);
-      break;
-    }
-    int64_t ko = kv_offset(g, page, layer, 0, kvh, pos % g.B) + e0;
-    int64_t vo = kv_offset(g, page, layer, 1, kvh, pos % g.B) + e0;
-    float kx[EPL], vx[EPL];
-    if (g.kv_fp8) {
-      const uint8_t *P = (const uint8_t *)pool;
-#pragma unroll
-      for (int t = 0; t < EPL; ++t) {
-        kx[t] = fp8_to_float(P[ko + t]) * sk;
-        vx[t] = fp8_to_float(P[vo + t]) * sv;
-      }
-    } else {
-      const bf16 *P = (const bf16 *)pool;
-#pragma unroll
-      for (int t = 0; t < EPL; ++t) {
-        kx[t] = __bfloat162float(P[ko + t]);
-        vx[t] = __bfloat162float(P[vo + t]);
-      }
-    }
-    float dot = 0.f;
-#pragma unroll
-    for (int t = 0; t < EPL; ++t) dot = fmaf(qv[t], kx[t], dot);
-    dot = warp_sum(dot);
-    float mn = fmaxf(mx, dot);
-    float corr = __expf(mx - mn), p = __expf(dot - mn);
-    den = den * corr + p;
-#pragma unroll
-    for (int t = 0; t < EPL; ++t) acc[t] = acc[t] * corr + p * vx[t];
-    mx = mn;
-  }
-  for (int t2 = 0; t2 < g.gamma; ++t2) {
-    const int br = s_idx * g.gamma + t2;
-    const bf16 *kr = kb + (int64_t)br * g.kv + kvh * g.d + e0;
-    const bf16 *vr = vb + (int64_t)br * g.kv + kvh * g.d + e0;
-    float dot = 0.f;
-#pragma unroll
-    for (int t = 0; t < EPL; ++t) dot = fmaf(qv[t], __bfloat162float(kr[t]), dot);
-    dot = warp_sum(dot);
-    float mn = fmaxf(mx, dot);
-    float corr = __expf(mx - mn), p = __expf(dot - mn);
-    den = den * corr + p;
-#pragma unroll
-    for (int t = 0; t < EPL; ++t) acc[t] = acc[t] * corr + p * __bfloat162float(vr[t]);
-    mx = mn;
-  }
-  bf16 *orow = o + (int64_t)r * g.nq * g.d + j * g.d + e0;
-  float inv = 1.f / den;
-#pragma unroll
-  for (int t = 0; t < EPL; ++t) orow[t] = __float2bfloat16_rn(acc[t] * inv);
-}
-
-cudaError_t attention_simple(const bf16 *q, const bf16 *kb, const bf16 *vb, const SeqMeta *seq,
-                             const int32_t *page_ids, int n_seq, const Geo &g, const void *pool,
-                             int layer, const float *kv_scale, bf16 *o, int *status,
-                             cudaStream_t s) {
-  dim3 grid(n_seq * g.gamma, g.nq);
-  float scale = (float)(1.0 / std::sqrt((double)g.d));
-  if (g.d == 128)
-    k_attention_simple<4><<<grid, 32, 0, s>>>(q, kb, vb, seq, page_ids, g, pool, layer, kv_scale,
-                                              scale, o, status);
-  else if (g.d == 64)
-    k_attention_simple<2><<<grid, 32, 0, s>>>(q, kb, vb, seq, page_ids, g, pool, layer, kv_scale,
-                                              scale, o, status);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
-}
-
-// ------------------------------------------------------------------ SwiGLU --
-__global__ void k_swiglu(const float *__restrict__ gu, int I, bf16 *__restrict__ u) {
-  const int r = blockIdx.x;
-  const float *gr = gu + (int64_t)r * 2 * I;
-  for (int e = threadIdx.x; e < I; e += blockDim.x) {
-    float a = gr[e], b = gr[I + e];
-    u[(int64_t)r * I + e] = __float2bfloat16_rn(a / (1.f + __expf(-a)) * b);
-  }
-}
-
-cudaError_t swiglu(const float *gu, int R, int I, bf16 *u, cudaStream_t s) {
-  k_swiglu<<<R, 256, 0, s>>>(gu, I, u);
   return cudaGetLastError();
 }
 
@@ -453,6 +292,8 @@ cudaError_t swiglu(const float *gu, int R, int I, bf16 *u, cudaStream_t s) {
 __global__ void k_argmax_rows(const float *__restrict__ logits, int V,
                               const int32_t *__restrict__ bitmask, int nd,
                               int32_t *__restrict__ row_id, float *__restrict__ row_p1) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float smx[32];
   __shared__ int sid[32];
   __shared__ float ssum[32];
@@ -503,7 +344,7 @@ __global__ void k_argmax_rows(const float *__restrict__ logits, int V,
 
 cudaError_t argmax_rows(const float *logits, int rows, int V, const int32_t *bitmask, int nd,
                         int32_t *row_id, float *row_p1, cudaStream_t s) {
-  k_argmax_rows<<<rows, 1024, 0, s>>>(logits, V, bitmask, nd, row_id, row_p1);
+  launch_pdl(k_argmax_rows, dim3(rows), dim3(1024), 0, s, logits, V, bitmask, nd, row_id, row_p1);
   return cudaGetLastError();
 }
 
@@ -512,6 +353,8 @@ cudaError_t argmax_rows(const float *logits, int rows, int V, const int32_t *bit
 __global__ void k_finalize(const int32_t *__restrict__ row_id, const float *__restrict__ row_p1,
                            int n_seq, int nd, const int *status, uint32_t *drafts, int32_t *n_out,
                            float *conf, int32_t *status_out) {
+  pdl_trigger();
+  pdl_wait();
   int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s == 0) *status_out = *status;
   if (s >= n_seq) return;
@@ -532,7 +375,7 @@ __global__ void k_finalize(const int32_t *__restrict__ row_id, const float *__re
 cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int nd,
                      const int *status, uint32_t *drafts, int32_t *n_out, float *conf,
                      int32_t *status_out, cudaStream_t s) {
-  k_finalize<<<(n_seq + 127) / 128, 128, 0, s>>>(row_id, row_p1, n_seq, nd, status, drafts, n_out,
+  launch_pdl(k_finalize, dim3((n_seq + 127) / 128), dim3(128), 0, s, row_id, row_p1, n_seq, nd, status, drafts, n_out,
                                                   conf, status_out);
   return cudaGetLastError();
 }
@@ -542,6 +385,8 @@ cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int 
 // evaluated in double and stored f32 ([P1] field yarn_inv_freq).
 __global__ void k_rope_table(const float *__restrict__ inv_freq, int max_pos, int half,
                              float *__restrict__ cos_t, float *__restrict__ sin_t) {
+  pdl_trigger();
+  pdl_wait();
   int64_t n = (int64_t)max_pos * half;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n;
        t += (int64_t)gridDim.x * blockDim.x) {
@@ -556,7 +401,7 @@ __global__ void k_rope_table(const float *__restrict__ inv_freq, int max_pos, in
 
 cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float *cos_t, float *sin_t,
                        cudaStream_t s) {
-  k_rope_table<<<1024, 256, 0, s>>>(inv_freq, max_pos, half, cos_t, sin_t);
+  launch_pdl(k_rope_table, dim3(1024), dim3(256), 0, s, inv_freq, max_pos, half, cos_t, sin_t);
   return cudaGetLastError();
 }
 
@@ -564,6 +409,8 @@ cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float *cos_
 __global__ void k_gather_kv(const void *__restrict__ pool, Geo g, int layer,
                             const RowMeta *__restrict__ rows, const float *__restrict__ kv_scale,
                             float *k_out, float *v_out) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int page = rows[r].page, slot = rows[r].slot;
   for (int e = threadIdx.x; e < g.kv; e += blockDim.x) {
@@ -586,7 +433,7 @@ __global__ void k_gather_kv(const void *__restrict__ pool, Geo g, int layer,
 cudaError_t gather_kv(const void *pool, const Geo &g, int layer, const RowMeta *rows, int n,
                       const float *kv_scale, float *k_out, float *v_out, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  k_gather_kv<<<n, 256, 0, s>>>(pool, g, layer, rows, kv_scale, k_out, v_out);
+  launch_pdl(k_gather_kv, dim3(n), dim3(256), 0, s, pool, g, layer, rows, kv_scale, k_out, v_out);
   return cudaGetLastError();
 }
 

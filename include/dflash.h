@@ -207,6 +207,10 @@ DFLASH_API int dflash_debug_gather_kv(dflash_handle *h, const dflash_state *st, 
  * and the per-row argmax/confidence reduction), on the call's stream. Events
  * are the caller's cudaEvent_t. NULL, NULL disables it. */
 DFLASH_API int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end);
+/* Propose calls replay a CUDA graph captured per launch shape (sequences,
+ * new ctx rows, drafts, bitmask and tap/probe pointers); enable = 0 launches
+ * the kernels one by one instead (same results). On by default. */
+DFLASH_API int dflash_debug_set_graphs(dflash_handle *h, int32_t enable);
 /* Kernels this library has launched since it was loaded (all handles). */
 DFLASH_API int64_t dflash_debug_launch_count(void);
 /* One tensor-core GEMM in isolation, for kernel tests: y[m, n_w] = x[m, k] *

@@ -132,6 +132,30 @@ def test_tiny_batch_ragged():
         check_kv(pair, so[i], sl[i], range(0, pos[i]))
 
 
+def test_graph_replay_matches_direct_launches():
+    """Captured-graph replay and kernel-by-kernel launches give bit-identical
+    drafts, confidence and logits over several rounds (new rows each round)."""
+    outs = []
+    for graphs in (True, False):
+        pair = Pair(syn.TINY, 1041)
+        pair.lib.set_graphs(graphs)
+        so, sl, _ = _prefill(pair, 37, 1041)
+        rows = syn.make_stack(syn.TINY, 12, 1041, idx=3)
+        res, p, n_new, used = [], 37, 0, 0
+        for k in [1, 0, 2, 1]:
+            r = rows[used:used + n_new] if n_new else None
+            used += n_new
+            got = pair.lib.propose(sl, 100 + p, p, None if r is None else r.cuda(), 3)
+            torch.cuda.synchronize()
+            res.append((got, pair.tl[:3].clone().cpu()))
+            pair.lib.after_verify(sl, k)
+            p, n_new = p + k + 1, k + 1
+        outs.append(res)
+    for (ga, la), (gb, lb) in zip(*outs):
+        assert ga == gb
+        assert torch.equal(la, lb)
+
+
 def test_tiny_fp8_kv_and_lm_head():
     pair = Pair(syn.TINY, 1031, lm_fp8=True, kv_fp8=True)
     so, sl, _ = _prefill(pair, 50, 1031)
