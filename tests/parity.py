@@ -146,20 +146,37 @@ def _check_kv_run(pair: Pair, so, sl, positions):
             check_abs(vr, v, HIDDEN_TOL, f"ctx V layer {l}")
 
 
-def check_fp8_kv(pair, l, ref, got, kind):
-    """FP8 cache: codes equal, or one code apart where the oracle's unrounded
-    value sits near the rounding midpoint (the two sides' fp32 inputs differ
-    by GEMM summation order only)."""
+def e4m3_step(x: torch.Tensor) -> torch.Tensor:
+    """Spacing of E4M3 codes just below |x| and at |x| (3 mantissa bits,
+    subnormal spacing 2^-9 below 2^-6): the larger of the two."""
+    a = x.abs().clamp(min=2.0 ** -6)
+    e = torch.floor(torch.log2(a))
+    at = torch.pow(2.0, e - 3)
+    below = torch.where(a == torch.pow(2.0, e), torch.pow(2.0, e - 4), at)
+    return torch.maximum(torch.maximum(at, below), torch.full_like(at, 2.0 ** -9))
+
+
+def check_fp8_kv(pair, l, ref, got, kind, max_frac=5e-3):
+    """FP8 cache: each dequantised value within the FP8-path tolerance
+    (max-abs 5e-2), or its code exactly one E4M3 step from the oracle's (a
+    rounding decision on either side of a midpoint: the two sides' fp32
+    inputs differ by summation order and by bf16 flips of the ctx rows, about
+    1e-4 absolute). Measured at the shipped geometry: ~1e-3 of the codes
+    differ."""
     s = pair.w["kv_scale"][l, :, kind].to(torch.float64)[None, :, None]
-    rc = (ref.to(torch.float64).cpu() / s)
-    gc = (got.to(torch.float64).cpu() / s)
+    ref = ref.to(torch.float64).cpu()
+    got = got.to(torch.float64).cpu()
+    rc, gc = ref / s, got / s
     diff = (rc - gc).abs()
     bad = diff > 1e-5 * rc.abs().clamp(min=1.0)     # beyond the fp32 dequant rounding
     frac = float(bad.double().mean())
-    # a code step is at most 1/8 of the code's magnitude (3 mantissa bits)
-    step_ok = (diff <= rc.abs().clamp(min=2 ** -6) * 0.125 * (1 + 1e-5))
-    assert bool(step_ok.all()), "FP8 KV codes more than one step apart"
-    assert frac <= 2e-3, f"FP8 KV: {frac:.2e} of codes differ"
+    step = torch.maximum(e4m3_step(rc), e4m3_step(gc))
+    far = (diff > step * (1 + 1e-5)) & ((ref - got).abs() > LOGIT_TOL_FP8)
+    if bool(far.any()):
+        i = tuple(torch.nonzero(far)[0].tolist())
+        raise AssertionError(f"FP8 KV layer {l} kind {kind}: codes {float(rc[i])} vs "
+                             f"{float(gc[i])} differ by more than one step and 5e-2 at {i}")
+    assert frac <= max_frac, f"FP8 KV: {frac:.2e} of codes differ"
 
 
 def assert_tables(pair, so, sl):
