@@ -245,13 +245,111 @@ def run_ours(args):
         "propose_us": 1e3 * t_ms / K,
         "clocks": clk.summary(),
     }
+    head.close()
+    del wd
+    torch.cuda.empty_cache()
+    if not args.no_batch:
+        # the metric's batch-32 leg: 32 sequences, gamma 16, ragged ctx, bitmask
+        out["batch32"] = run_batched(syn.FULL, 1004, 32, 256, 4096, 15, False, True,
+                                     max(3, K // 2), W)
+        out["batch32"]["workload"] = ("full_b32: propose_batch of 32 sequences, ctx U[256,4096], "
+                                      "new rows U[1,16], 50% bitmask, confidence on")
+        torch.cuda.empty_cache()
+    if args.workload == "fp8_b128":
+        out["fp8_b128"] = run_batched(syn.FULL_G8, 1005, 128, 512, 4096, 7, True, False,
+                                      max(3, K // 2), W)
+        torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(w, cfg, geom, seed, ctx, args.cpu_steps)
     if rank == 0:
         print(json.dumps(out), flush=True)
-    head.close()
     if dist:
         dist.destroy_process_group()
+
+
+def batched_work(geom, ctx_list, n_new_list, nd, kv_elem):
+    """Algorithmic FLOPs and HBM bytes of one propose_batch step."""
+    H, I, L, S = geom.hidden, geom.intermediate, geom.num_layers, geom.stack_width
+    n = len(ctx_list)
+    R, D, m = n * geom.gamma, n * nd, sum(n_new_list)
+    layer_w = geom.q_dim * H + 2 * geom.kv_dim * H + H * geom.q_dim + 3 * I * H
+    flops = 2 * R * layer_w * L + 2 * D * geom.vocab * H + 2 * m * (H * S + L * 2 * geom.kv_dim * H)
+    keys = sum(c + geom.gamma for c in ctx_list)
+    flops += 4 * geom.gamma * geom.q_dim * keys * L
+    wb = syn.weight_bytes(geom)
+    lm_bytes = geom.vocab * H * (1 if kv_elem == 1 else 2)
+    byts = wb["layers"] + wb["fc"] + lm_bytes + sum(ctx_list) * L * 2 * geom.kv_dim * kv_elem
+    return flops, byts
+
+
+def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
+    """propose_batch over n sequences with ragged ctx; each step brings the
+    target rows of the drafts the previous verify accepted (1..gamma rows)."""
+    from block_diffusion_speculative_forward_gb300 import binding as B
+    steps = K + W + 2
+    w = syn.make_weights(geom, seed, lm_head_fp8=fp8, kv_fp8=fp8)
+    wd = B.weights_to_device(w)
+    del w
+    cfg = head_cfg(geom, n, ctx_hi + geom.gamma * (steps + 2), kv_dtype=int(fp8),
+                   lm_head_dtype=int(fp8))
+    head = B.DraftHead(cfg, wd)
+    ctx = syn.uniform_ints(ctx_lo, ctx_hi, n, seed, 1)
+    states, tails = [], []
+    for i in range(n):
+        g = torch.Generator(device="cuda").manual_seed(seed * 1000 + i)
+        stack = torch.randn((ctx[i] + geom.gamma * steps, geom.stack_width), device="cuda",
+                            generator=g).to(torch.bfloat16)
+        st = head.alloc_state()
+        head.prefill(st, stack[:ctx[i]])
+        torch.cuda.synchronize()
+        tails.append(stack[ctx[i]:].clone())
+        states.append(st)
+        del stack
+    mask = syn.make_bitmask(geom.vocab, n, seed).cuda() if use_mask else None
+    pos, used = list(ctx), [0] * n
+    n_new = syn.uniform_ints(1, geom.gamma, n, seed, 2)
+    work = []
+
+    def step(t):
+        nonlocal pos, n_new
+        rows = [tails[i][used[i]:used[i] + n_new[i]] for i in range(n)]
+        for i in range(n):
+            used[i] += n_new[i]
+        newpos = [p + m for p, m in zip(pos, n_new)]
+        toks = syn.uniform_ints(0, geom.vocab - 1, n, seed, 900 + t)
+        work.append(batched_work(geom, [p - m for p, m in zip(newpos, n_new)], n_new, nd,
+                                 1 if fp8 else 2))
+        head.propose_batch(states, toks, newpos, rows, nd, bitmask=mask)
+        ks = syn.uniform_ints(0, nd, n, seed, 1900 + t)
+        for i in range(n):
+            head.after_verify(states[i], ks[i])
+        pos = newpos
+        n_new = [k + 1 for k in ks]
+
+    for t in range(W):
+        step(t)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    work.clear()
+    torch.cuda.synchronize()
+    e0.record(s)
+    for t in range(W, W + K):
+        step(t)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    flops = sum(f for f, _ in work) / K
+    byts = sum(b for _, b in work) / K
+    hbm, tf, src = peaks()
+    head.close()
+    return {"value": n * nd / (ms * 1e-3), "unit": UNIT, "propose_us": 1e3 * ms,
+            "batch": n, "gamma": geom.gamma, "num_drafts": nd, "steps": K, "warmup": W,
+            "ctx": f"U[{ctx_lo},{ctx_hi}]", "bitmask": use_mask, "fp8_kv_and_lm_head": fp8,
+            "flops_per_step": flops, "bytes_per_step": byts,
+            "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": tf,
+                         "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / tf,
+                         "peak_source": f"{src} bf16_tflops (burst)",
+                         "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm}}
 
 
 def cpu_baseline(w, cfg, geom, seed, ctx, n_steps):
@@ -324,10 +422,38 @@ def run_reference(args):
 def run_kernel_case(args):
     """One tensor-core GEMM at the lm_head shape (15 draft rows x 248320 vocab
     rows x 2048), 1.02 GB of bf16 weights, timed alone with CUDA events: the
-    small case used for detailed profiles of the weight-streaming kernel."""
+    small case used for detailed profiles of the weight-streaming kernel.
+    lm_head_b32: the many-row lm_head kernel at 480 draft rows (32 sequences
+    x 15 drafts)."""
     import ctypes as C
     from block_diffusion_speculative_forward_gb300 import binding as B
     L = B.lib()
+    if args.kernel == "lm_head_b32":
+        L.dflash_debug_lmhead.argtypes = [C.c_void_p] * 3 + [C.c_int32] * 3 + [C.c_void_p]
+        m, n, k = 480, syn.FULL.vocab, syn.FULL.hidden
+        g = torch.Generator(device="cuda").manual_seed(6)
+        w = (torch.randn(n, k, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        x = torch.randn(m, k, device="cuda", generator=g).to(torch.bfloat16)
+        part = torch.empty(m * ((n + 255) // 256) * 4, dtype=torch.int32, device="cuda")
+        s = torch.cuda.current_stream()
+        times = []
+        for i in range(args.warmup + args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            rc = L.dflash_debug_lmhead(w.data_ptr(), x.data_ptr(), part.data_ptr(), m, n, k,
+                                       s.cuda_stream)
+            e1.record(s)
+            torch.cuda.synchronize()
+            assert rc == 0, rc
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        _, tf, src = peaks()
+        fl = 2.0 * m * n * k
+        print(json.dumps({"kernel": "lm_head, 480 draft rows", "median_ms": ms,
+                          "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+                          "frac_bf16": fl / (ms * 1e-3) / 1e12 / tf, "peak_source": src}))
+        return
     L.dflash_gemm_noalloc.argtypes = [C.c_void_p] * 3 + [C.c_int32] * 3 + [C.c_void_p]
     m, n, k = 15, syn.FULL.vocab, syn.FULL.hidden
     g = torch.Generator(device="cuda").manual_seed(5)
@@ -361,7 +487,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-steps", type=int, default=4)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--kernel", default=None, choices=["lm_head"],
+    ap.add_argument("--no-batch", action="store_true", help="skip the batch-32 leg")
+    ap.add_argument("--batch-only", action="store_true",
+                    help="only the batch-32 leg (for profiling it alone)")
+    ap.add_argument("--workload", default="full_b1", choices=["full_b1", "fp8_b128"],
+                    help="fp8_b128 adds the 128-sequence FP8 configuration")
+    ap.add_argument("--kernel", default=None, choices=["lm_head", "lm_head_b32"],
                     help="time one kernel alone instead of the propose step")
     ap.add_argument("--lm-traffic", type=float, default=None,
                     help="ncu dram bytes per lm_head launch, when captured for this build")
@@ -372,6 +503,11 @@ def main():
         from block_diffusion_speculative_forward_gb300 import build
         build.build()
         run_kernel_case(args)
+    elif args.batch_only:
+        from block_diffusion_speculative_forward_gb300 import build
+        build.build()
+        r = run_batched(syn.FULL, 1004, 32, 256, 4096, 15, False, True, args.steps, args.warmup)
+        print(json.dumps({"batch32": r}), flush=True)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -606,6 +606,36 @@ int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t m, int32_t
   return DFLASH_OK;
 }
 
+int dflash_debug_lmhead(const void *w, const void *x, void *partials, int32_t m, int32_t n_w,
+                        int32_t k, void *stream) {
+  if (!w || !x || !partials || m <= 0 || n_w <= 0 || k <= 0 || k % 64)
+    return fail(DFLASH_EINVAL, "bad lm_head arguments");
+  cudaStream_t s = (cudaStream_t)stream;
+  CUtensorMap mx, mw;
+  if (!dfl::tc::make_map_2d(&mx, x, false, m, k, 128) ||
+      !dfl::tc::make_map_2d(&mw, w, false, n_w, k, 256))
+    return fail(DFLASH_ECUDA, "cuTensorMapEncodeTiled failed");
+  void *status = nullptr;
+  CK(cudaMalloc(&status, 16));
+  CK(cudaMemsetAsync(status, 0, 16, s));
+  dfl::LmArgs p{};
+  p.m_act = m;
+  p.n_w = n_w;
+  p.k = k;
+  p.nd = m;
+  p.mask_words = (n_w + 31) / 32;
+  p.out = (dfl::LmPartial *)partials;
+  p.status = (int *)status;
+  cudaError_t e = dfl::tc::lmhead(mx, mw, p, s);
+  int st = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&st, status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  cudaFree(status);
+  CK(e);
+  if (st) return fail(DFLASH_EDEVICE, "lm_head status %d", st);
+  return DFLASH_OK;
+}
+
 int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits) {
   if (!h) return fail(DFLASH_EINVAL, "NULL handle");
   h->b.tap_x = x_taps;

@@ -130,11 +130,23 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(kn, (size_t)g.L);
   BK(cudaMemcpy(kn, knorm.data(), sizeof(void *) * g.L, cudaMemcpyHostToDevice));
   W->k_norm_dev = kn;
+  // FP8 lm_head ([P1] field lm_head_shared_fp8): the E4M3 codes are widened
+  // once to bf16 (exact: every E4M3 value is a bf16 value) for the
+  // tensor-core GEMM; the per-row scale is applied to the logits in its
+  // epilogue, so the logits are s_v * <z, codes_v>.
+  const void *lm_operand = W->lm_head;
+  if (W->lm_is_fp8) {
+    bf16 *wide = nullptr;
+    BA(wide, (size_t)g.V * H);
+    BK(widen_fp8(W->lm_fp8, (int64_t)g.V * H, wide, 0));
+    lm_operand = wide;
+  }
   // TMA maps of every weight operand.
   {
     bool ok = tc::make_map_2d(&W->map_fc, W->fc, false, H, g.S, 128) &&
               tc::make_map_2d(&W->map_wkv, W->w_kv, false, (int64_t)g.L * 2 * kv, H, 128) &&
-              tc::make_map_2d(&W->map_lm, W->lm_head, false, g.V, H, 128);
+              tc::make_map_2d(&W->map_lm, lm_operand, false, g.V, H, 128) &&
+              tc::make_map_2d(&W->map_lm256, lm_operand, false, g.V, H, 256);
     W->map_qkv.resize(g.L);
     W->map_o.resize(g.L);
     W->map_gu.resize(g.L);
@@ -176,7 +188,6 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->o, (size_t)R_max * qd);
   BA(B->u, (size_t)R_max * I);
   BA(B->z, (size_t)D_max * H);
-  BA(B->logits, c.lm_head_dtype == 1 ? (size_t)D_max * g.V : 0);
   BA(B->row_id, (size_t)D_max);
   BA(B->row_p1, (size_t)D_max);
   BA(B->ctx_pack, (size_t)M_ctx * g.S);
@@ -485,17 +496,15 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     LK(add_norm(an, R, s));
   }
   if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));
-  if (W.lm_is_fp8) {
-    LK(gemm_simple(B.z, g.H, W.lm_fp8, true, W.lm_scale, B.logits, g.V, D, g.V, g.H,
-                   EPI_STORE_F32, s));
-    LK(argmax_rows(B.logits, D, g.V, bitmask, nd, B.row_id, B.row_p1, s));
-  } else {
-    // lm_head fused with the per-row reductions: no [rows, vocab] logits in HBM.
+  if (D <= 64) {
+    // Few draft rows: the vocab rows are the MMA's M (the weight stream
+    // bounds the kernel), fused per-row reductions over 128-row vocab tiles.
     GemmParams p{};
     p.m_act = D;
     p.n_w = g.V;
     p.k = g.H;
     p.epi = EPI_TC_LMHEAD;
+    p.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
     p.ws = B.ws;
     p.counters = B.counters;
     p.status = B.status;
@@ -506,14 +515,37 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     const int bn = tc::pick_bn(D);
     LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
     LK(lm_reduce(B.lm_part, D, (g.V + 127) / 128, B.row_id, B.row_p1, s));
+  } else {
+    // Many draft rows: draft rows are the MMA's M, so each epilogue thread
+    // reduces its own row over 256-row vocab tiles.
+    LmArgs p{};
+    p.m_act = D;
+    p.n_w = g.V;
+    p.k = g.H;
+    p.bitmask = bitmask;
+    p.mask_words = (g.V + 31) / 32;
+    p.nd = nd;
+    p.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+    p.out = B.lm_part;
+    p.status = B.status;
+    LK(tc::lmhead(B.act_map[ACT_Z][bn_index(128)], W.map_lm256, p, s));
+    LK(lm_reduce(B.lm_part, D, tc::lmhead_vocab_tiles(g.V), B.row_id, B.row_p1, s));
   }
   if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_end, s, cudaEventRecordExternal));
   if (B.tap_logits) {
-    if (W.lm_is_fp8)
-      FK(cudaMemcpyAsync(B.tap_logits, B.logits, (size_t)D * g.V * sizeof(float),
-                         cudaMemcpyDeviceToDevice, s));
-    else
-      LK(tc_gemm(B, W.map_lm, ACT_Z, D, g.V, g.H, EPI_TC_STORE_F32, B.tap_logits, g.V, s));
+    GemmParams p{};
+    p.m_act = D;
+    p.n_w = g.V;
+    p.k = g.H;
+    p.epi = EPI_TC_STORE_F32;
+    p.out = B.tap_logits;
+    p.ldo = g.V;
+    p.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+    p.ws = B.ws;
+    p.counters = B.counters;
+    p.status = B.status;
+    const int bn = tc::pick_bn(D);
+    LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
   }
   LK(finalize(B.row_id, B.row_p1, n, nd, B.status, (uint32_t *)(B.out_dev + B.off_drafts),
               (int32_t *)(B.out_dev + B.off_nout), (float *)(B.out_dev + B.off_conf),
@@ -536,9 +568,9 @@ void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap
   int64_t total = 0;
   for (const SeqMeta &m : seq) total += (int64_t)(m.pos - m.ws) * g.nkv;
   const int sms = tc::num_sms();
-  // About half an SM wave of ctx items, at least 64 keys each: fewer chunks
-  // keep the partial merge cheap.
-  int64_t chunk = (total + sms / 2 - 1) / (sms / 2);
+  // About three SM waves of ctx items (three attention CTAs fit on an SM),
+  // at least 64 keys each so the partial merge stays cheap.
+  int64_t chunk = (total + 3 * sms - 1) / (3 * sms);
   chunk = std::max<int64_t>(64, (chunk + 31) / 32 * 32);
   for (;;) {
     items->clear();

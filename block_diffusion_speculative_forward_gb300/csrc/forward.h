@@ -26,7 +26,7 @@ struct Weights {
   float *cos_t = nullptr, *sin_t = nullptr; // [max_seq_len + gamma][d/2]
   void *pool = nullptr;                     // [pages][L][K|V][nkv][B][d]
   // TMA maps of the weights (box: 128 weight rows x 64 K)
-  CUtensorMap map_fc, map_wkv, map_lm;
+  CUtensorMap map_fc, map_wkv, map_lm, map_lm256;
   std::vector<CUtensorMap> map_qkv, map_o, map_gu, map_down;
 };
 
@@ -41,7 +41,6 @@ struct Buffers {
   bf16 *q = nullptr, *kb = nullptr, *vb = nullptr, *o = nullptr;
   bf16 *u = nullptr;           // [R, I]
   bf16 *z = nullptr;           // [D, H] final-normed draft rows
-  float *logits = nullptr;     // [D, V]
   int32_t *row_id = nullptr;
   float *row_p1 = nullptr;
   bf16 *ctx_pack = nullptr;    // [M, S]

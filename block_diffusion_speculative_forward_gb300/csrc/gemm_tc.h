@@ -115,8 +115,25 @@ struct GemmParams {
   int tiles_m, tiles_n;
 };
 
+// The fused lm_head + row reductions (lmhead_tc.cu).
+struct LmArgs {
+  int m_act;               // draft rows
+  int n_w;                 // vocab
+  int k;                   // hidden, multiple of 64
+  const int32_t *bitmask;  // [n_seq][mask_words] or NULL
+  int mask_words;
+  int nd;                  // draft rows per sequence
+  const float *wscale;     // per vocab row scale (FP8 head) or NULL
+  LmPartial *out;          // [m_act][vocab tiles of 256]
+  int *status;
+};
+
 namespace tc {
 int num_sms();
+// map_x: draft rows, box 128 rows; map_w: vocab rows, box 256 rows.
+cudaError_t lmhead(const CUtensorMap &map_x, const CUtensorMap &map_w, const LmArgs &p,
+                   cudaStream_t s);
+int lmhead_vocab_tiles(int vocab);
 int pick_bn(int m_act);
 // 2-D row-major map [rows, cols], box = 128 bytes of a row x box_rows rows, 128B swizzle.
 bool make_map_2d(CUtensorMap *map, const void *base, bool fp8, int64_t rows, int64_t cols,

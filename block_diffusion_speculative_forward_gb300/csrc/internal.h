@@ -93,13 +93,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // ------------------------------------------------------------- launchers --
-enum GemmEpi { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_STORE_BF16 = 2 };
-
-// C[m, n] (op)= A[m, K] * W[n, K]^T. A bf16 with row stride lda; W bf16 or FP8
-// E4M3 (w_fp8) with optional per-row scale; K % 32 == 0.
-cudaError_t gemm_simple(const bf16 *A, int lda, const void *W, bool w_fp8, const float *wscale,
-                        void *C, int ldc, int m, int n, int K, GemmEpi epi, cudaStream_t s);
-
 // out[i] = bf16(g * x[r] / sqrt(mean(x[r]^2) + eps)); r = i when nd == 0,
 // else the i-th draft row: (i / nd) * gamma + 1 + i % nd.
 cudaError_t rmsnorm_rows(const float *x, int rows, int n, const bf16 *g, float eps, int nd,
@@ -115,14 +108,12 @@ cudaError_t ctx_kv_write(const Partials &kv, int m, const RowMeta *rows, const G
                          const bf16 *const *k_norm_dev, const float *cos_t, const float *sin_t,
                          void *pool, const float *kv_scale, int *status, cudaStream_t s);
 
-// Per draft row: (argmax id or -1 when nothing is allowed, top-1 probability).
-cudaError_t argmax_rows(const float *logits, int rows, int V, const int32_t *bitmask, int nd,
-                        int32_t *row_id, float *row_p1, cudaStream_t s);
-
 // Per sequence: drafts, n_out, conf (and the status word) into out.
 cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int nd,
                      const int *status, uint32_t *drafts, int32_t *n_out, float *conf,
                      int32_t *status_out, cudaStream_t s);
+
+cudaError_t widen_fp8(const uint8_t *src, int64_t n, bf16 *dst, cudaStream_t s);
 
 cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float *cos_t, float *sin_t,
                        cudaStream_t s);

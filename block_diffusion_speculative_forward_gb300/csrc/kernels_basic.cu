@@ -42,86 +42,6 @@ __device__ float block_sum(float v, float *sh) {
   return t;
 }
 
-// ------------------------------------------------------------ plain GEMM --
-// 64x64 output tile, K step 32, 256 threads with a 4x4 micro tile each.
-template <int EPI, bool FP8>
-__global__ void __launch_bounds__(256) k_gemm_simple(const bf16 *__restrict__ A, int lda,
-                                                     const void *__restrict__ W,
-                                                     const float *__restrict__ wscale, void *C,
-                                                     int ldc, int m, int n, int K) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float As[32][65];
-  __shared__ float Ws[32][65];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += 32) {
-    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-      int r = i >> 5, kk = i & 31;
-      int gr = m0 + r, gc = n0 + r;
-      As[kk][r] = gr < m ? __bfloat162float(A[(int64_t)gr * lda + k0 + kk]) : 0.f;
-      float wv = 0.f;
-      if (gc < n) {
-        if (FP8)
-          wv = fp8_to_float(((const uint8_t *)W)[(int64_t)gc * K + k0 + kk]);
-        else
-          wv = __bfloat162float(((const bf16 *)W)[(int64_t)gc * K + k0 + kk]);
-      }
-      Ws[kk][r] = wv;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < 32; ++kk) {
-      float a[4], w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = Ws[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int r = m0 + ty * 4 + i;
-    if (r >= m) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      int c = n0 + tx * 4 + j;
-      if (c >= n) continue;
-      float v = acc[i][j];
-      if (wscale) v *= wscale[c];
-      int64_t off = (int64_t)r * ldc + c;
-      if (EPI == EPI_STORE_F32) ((float *)C)[off] = v;
-      else if (EPI == EPI_ADD_F32) ((float *)C)[off] += v;
-      else ((bf16 *)C)[off] = __float2bfloat16_rn(v);
-    }
-  }
-}
-
-cudaError_t gemm_simple(const bf16 *A, int lda, const void *W, bool w_fp8, const float *wscale,
-                        void *C, int ldc, int m, int n, int K, GemmEpi epi, cudaStream_t s) {
-  if (m <= 0 || n <= 0) return cudaSuccess;
-  if (K % 32) return cudaErrorInvalidValue;
-  dim3 grid((n + 63) / 64, (m + 63) / 64);
-#define DFL_GEMM_CASE(E)                                                                       \
-  if (epi == E) {                                                                              \
-    if (w_fp8)                                                                                 \
-      launch_pdl(k_gemm_simple<E, true>, dim3(grid), dim3(256), 0, s, A, lda, W, wscale, C, ldc, m, n, K);         \
-    else                                                                                       \
-      launch_pdl(k_gemm_simple<E, false>, dim3(grid), dim3(256), 0, s, A, lda, W, wscale, C, ldc, m, n, K);        \
-  }
-  DFL_GEMM_CASE(EPI_STORE_F32)
-  DFL_GEMM_CASE(EPI_ADD_F32)
-  DFL_GEMM_CASE(EPI_STORE_BF16)
-#undef DFL_GEMM_CASE
-  return cudaGetLastError();
-}
-
 // --------------------------------------------------------------- RMSNorm --
 // [P1] fields rms_norm_eps, hidden_norm, norm; the Qwen3 layer norms.
 __global__ void k_rmsnorm_rows(const float *__restrict__ x, int n, const bf16 *__restrict__ g,
@@ -285,69 +205,6 @@ cudaError_t ctx_kv_write(const Partials &kv, int m, const RowMeta *rows, const G
   return cudaGetLastError();
 }
 
-// ------------------------------------------------- argmax + confidence --
-// [P1] field lm_head_shared (per-position argmax), [P3] grammar_bitmask
-// (bit tok set => allowed), last_confidence (top-1 softmax probability).
-// Ties go to the lowest token id.
-__global__ void k_argmax_rows(const float *__restrict__ logits, int V,
-                              const int32_t *__restrict__ bitmask, int nd,
-                              int32_t *__restrict__ row_id, float *__restrict__ row_p1) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float smx[32];
-  __shared__ int sid[32];
-  __shared__ float ssum[32];
-  const int r = blockIdx.x;
-  const int words = (V + 31) / 32;
-  const int32_t *bm = bitmask ? bitmask + (int64_t)(r / nd) * words : nullptr;
-  const float *lr = logits + (int64_t)r * V;
-  float best = -INFINITY;
-  int bid = INT32_MAX;
-  for (int t = threadIdx.x; t < V; t += blockDim.x) {
-    if (bm && !((((uint32_t)bm[t >> 5]) >> (t & 31)) & 1u)) continue;
-    float v = lr[t];
-    if (v > best || (v == best && t < bid)) { best = v; bid = t; }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, best, off);
-    int oi = __shfl_xor_sync(0xffffffffu, bid, off);
-    if (ov > best || (ov == best && oi < bid)) { best = ov; bid = oi; }
-  }
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  if (lane == 0) { smx[w] = best; sid[w] = bid; }
-  __syncthreads();
-  best = smx[0];
-  bid = sid[0];
-  for (int i = 1; i < nw; ++i)
-    if (smx[i] > best || (smx[i] == best && sid[i] < bid)) { best = smx[i]; bid = sid[i]; }
-  if (bid == INT32_MAX) {
-    if (threadIdx.x == 0) { row_id[r] = -1; row_p1[r] = 0.f; }
-    return;
-  }
-  float sum = 0.f;
-  for (int t = threadIdx.x; t < V; t += blockDim.x) {
-    if (bm && !((((uint32_t)bm[t >> 5]) >> (t & 31)) & 1u)) continue;
-    sum += __expf(lr[t] - best);
-  }
-  sum = warp_sum(sum);
-  __syncthreads();
-  if (lane == 0) ssum[w] = sum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int i = 0; i < nw; ++i) tot += ssum[i];
-    row_id[r] = bid;
-    row_p1[r] = 1.f / tot;
-  }
-}
-
-cudaError_t argmax_rows(const float *logits, int rows, int V, const int32_t *bitmask, int nd,
-                        int32_t *row_id, float *row_p1, cudaStream_t s) {
-  launch_pdl(k_argmax_rows, dim3(rows), dim3(1024), 0, s, logits, V, bitmask, nd, row_id, row_p1);
-  return cudaGetLastError();
-}
-
 // Chain: drafts stop before the first row with nothing allowed; conf is the
 // minimum top-1 probability over the produced drafts (0 when none).
 __global__ void k_finalize(const int32_t *__restrict__ row_id, const float *__restrict__ row_p1,
@@ -377,6 +234,21 @@ cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int 
                      int32_t *status_out, cudaStream_t s) {
   launch_pdl(k_finalize, dim3((n_seq + 127) / 128), dim3(128), 0, s, row_id, row_p1, n_seq, nd, status, drafts, n_out,
                                                   conf, status_out);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- FP8 widening --
+// E4M3 codes to bf16, exactly (E4M3 values are a subset of bf16 values).
+__global__ void k_widen_fp8(const uint8_t *__restrict__ src, int64_t n, bf16 *__restrict__ dst) {
+  pdl_trigger();
+  pdl_wait();
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(fp8_to_float(src[i]));
+}
+
+cudaError_t widen_fp8(const uint8_t *src, int64_t n, bf16 *dst, cudaStream_t s) {
+  launch_pdl(k_widen_fp8, dim3(4096), dim3(256), 0, s, src, n, dst);
   return cudaGetLastError();
 }
 

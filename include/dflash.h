@@ -236,6 +236,13 @@ DFLASH_API int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t
  * DFLASH_ECUDA or DFLASH_EDEVICE (dflash_last_error is not updated). */
 DFLASH_API int dflash_gemm_noalloc(const void *w, const void *x, float *y, int32_t m, int32_t n_w,
                                    int32_t k, void *stream);
+/* The many-row lm_head kernel in isolation, for kernel tests: for each of the
+ * m rows of x [m, k] and each 256-row tile of w [n_w, k] (bf16), the tile's
+ * max logit, lowest argmax and sum exp(logit - max), no mask, written to
+ * partials dev [m][ceil(n_w/256)] of 16-byte (f32 max, i32 id, f32 sum, pad)
+ * records. Synchronises the stream. */
+DFLASH_API int dflash_debug_lmhead(const void *w, const void *x, void *partials, int32_t m,
+                                   int32_t n_w, int32_t k, void *stream);
 DFLASH_API int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits);
 
 #ifdef __cplusplus
