@@ -399,15 +399,23 @@ cudaError_t launch(const AttnArgs &a, cudaStream_t s) {
   }
   launch_pdl(k_attn_split<D, FP8>, dim3(a.n_items), dim3(THREADS), smem, s, a);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.n_pairs == 0) return e;   // capacity 0: no ctx window at all
-  const int grp = a.g.nq / a.g.nkv;
-  launch_pdl(k_attn_merge<D>, dim3(a.n_pairs, (a.g.gamma * grp + 3) / 4), dim3(128), 0, s, a);
-  return cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return attention_merge(a, s);
 }
 
 }  // namespace
 
 int attn_query_rows(const Geo &g) { return g.gamma * (g.nq / g.nkv); }
+
+cudaError_t attention_merge(const AttnArgs &a, cudaStream_t s) {
+  if (a.n_pairs == 0) return cudaSuccess;   // capacity 0: no ctx window at all
+  const int grp = a.g.nq / a.g.nkv;
+  const dim3 grid(a.n_pairs, (a.g.gamma * grp + 3) / 4);
+  if (a.g.d == 128) launch_pdl(k_attn_merge<128>, grid, dim3(128), 0, s, a);
+  else if (a.g.d == 64) launch_pdl(k_attn_merge<64>, grid, dim3(128), 0, s, a);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t attention_split(const AttnArgs &a, cudaStream_t s) {
   if (a.n_items <= 0) return cudaSuccess;

@@ -1,0 +1,520 @@
+// Block attention on the 5th-generation tensor cores (bf16 KV cache, head dim
+// 128): for each sequence and kv head, the gamma block rows of every query
+// head in the GQA group attend, without a mask, to the ctx window and to the
+// block's own gamma keys ([P1] fields kv_cache, ctx_window, layers).
+//
+// Work: the same split-KV items as the mma.sync kernel (attention.cu), run by
+// one persistent CTA per SM over a host-balanced list of items. Per item the
+// group's gamma x (nq / nkv) <= 128 query vectors are the M = 128 operand;
+// keys stream in tiles of 64 (four 16-key pages) through a 3-stage TMA ring
+// straight from the paged pool. Per tile:
+//   S   = Q K^T   tcgen05, M 128 x N 64 x K 128, into TMEM (double buffered)
+//   P   = exp(S * scale - m)  by four softmax warps, one thread per query
+//         vector, written to shared memory as bf16 (double buffered)
+//   O_t = P V     tcgen05, M 128 x N 128 x K 64 with V as an MN-major operand,
+//         into TMEM (double buffered); the softmax thread folds O_t into its
+//         register accumulator with the running-max correction.
+// Keys outside the item (ragged page edges) are masked to -inf; 16-key groups
+// holding no key of the item are neither loaded nor multiplied. An item
+// writes its normalised output, or (acc, max, sum) partials for the merge.
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
+// warps 2-5 softmax. Every wait is bounded.
+#include <cuda.h>
+
+#include "attention.h"
+#include "gemm_tc.h"
+#include "tc_ptx.h"
+
+namespace dfl {
+
+namespace {
+
+using namespace tc;
+
+constexpr int AQ = 128;                      // query vectors per tile (MMA M)
+constexpr int AD = 128;                      // head dim
+constexpr int AK = 64;                       // keys per tile
+constexpr int KV_STAGES = 3;
+constexpr int Q_BYTES = AQ * AD * 2;         // 32 KB: two 64-column halves
+constexpr int Q_HALF = Q_BYTES / 2;
+constexpr int P_BYTES = AQ * AK * 2;         // 16 KB
+constexpr int KT_BYTES = AK * AD * 2;        // 16 KB: two 64-column halves
+constexpr int KT_HALF = KT_BYTES / 2;
+constexpr int STAGE_BYTES = 2 * KT_BYTES;    // K tile then V tile
+constexpr int GROUP_BYTES = 16 * 128;        // one 16-key page half: 16 rows x 128 B
+constexpr int OFF_P = 2 * Q_BYTES;
+constexpr int OFF_KV = OFF_P + 2 * P_BYTES;
+constexpr int TILE_BYTES = OFF_KV + KV_STAGES * STAGE_BYTES;   // 192 KB
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_S = 0;               // two 64-column S buffers
+constexpr uint32_t TMEM_O = 128;             // two 128-column O buffers
+
+struct Bars {
+  uint64_t q_full[2], q_empty[2], kv_full[KV_STAGES], kv_empty[KV_STAGES];
+  uint64_t s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2], drain;
+  uint32_t tmem_base;
+  uint32_t q_issued, q_parity, kv_issued, kv_parity;
+  int abort_flag;
+};
+constexpr int SMEM = 1024 + TILE_BYTES + (int)sizeof(Bars);
+
+// Key range of an item in the tile's coordinates: ctx items count positions
+// (tile j starts at p0 + 64 j, p0 the item's first position rounded down to a
+// page), the block item counts its keys from 0.
+struct ItemGeo {
+  int lo, hi, p0, ntiles;
+  bool block;
+};
+
+__device__ __forceinline__ ItemGeo item_geo(const AttnItem &it, const SeqMeta &sm, int gamma) {
+  ItemGeo r;
+  const int n_ctx = sm.pos - sm.ws;
+  r.block = it.k0 >= n_ctx;
+  if (r.block) {
+    r.lo = 0;
+    r.hi = gamma;
+    r.p0 = 0;
+  } else {
+    r.lo = sm.ws + it.k0;
+    r.hi = sm.ws + it.k1;
+    r.p0 = r.lo & ~15;
+  }
+  r.ntiles = (r.hi - r.p0 + AK - 1) / AK;
+  return r;
+}
+
+// Bit q: the tile's keys 16q..16q+15 include a key of the item.
+__device__ __forceinline__ uint32_t group_mask(const ItemGeo &ig, int j) {
+  const int base = ig.p0 + j * AK;
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < AK / 16; ++q)
+    if (base + 16 * q < ig.hi) m |= 1u << q;
+  return m;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint32_t bar, int x,
+                                            int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Descriptor of an MN-major operand in the 128-byte swizzle: rows of 64
+// consecutive N elements (128 B), 8 K-rows per 1024-byte atom; lbo = bytes
+// between 64-wide N blocks, sbo = bytes between 8-row K groups.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_pool,
+              const __grid_constant__ CUtensorMap map_kb, const __grid_constant__ CUtensorMap map_vb,
+              AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  Bars *bar = (Bars *)(smem_raw + (base - raw) + TILE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Geo &g = a.g;
+  const int grp = g.nq / g.nkv;
+  const int n_q = g.gamma * grp;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar->q_full[b]), 1);
+      mbar_init(smem_u32(&bar->q_empty[b]), 1);
+      mbar_init(smem_u32(&bar->s_full[b]), 1);
+      mbar_init(smem_u32(&bar->s_empty[b]), 4);
+      mbar_init(smem_u32(&bar->p_full[b]), 4);
+      mbar_init(smem_u32(&bar->o_full[b]), 1);
+      mbar_init(smem_u32(&bar->o_empty[b]), 4);
+    }
+    for (int s = 0; s < KV_STAGES; ++s) {
+      mbar_init(smem_u32(&bar->kv_full[s]), 1);
+      mbar_init(smem_u32(&bar->kv_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar->drain), 1);
+    bar->abort_flag = 0;
+    bar->q_issued = bar->q_parity = bar->kv_issued = bar->kv_parity = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_q) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_pool) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_kb) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_vb) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&bar->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_trigger();
+  pdl_wait();
+  const uint32_t tmem = bar->tmem_base;
+  volatile int *abort_flag = &bar->abort_flag;
+  const int c_begin = a.cta_off[blockIdx.x], c_end = a.cta_off[blockIdx.x + 1];
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ------
+    if (lane == 0) {
+      const uint64_t pol_kv = policy_evict_first();
+      const uint64_t pol_q = policy_evict_normal();
+      uint32_t q_issued = 0, q_par = 0, kv_issued = 0, kv_par = 0;
+      int stage = 0;
+      uint32_t kv_phase = 0;
+      int qi = 0;
+      for (int c = c_begin; c < c_end && !*abort_flag; ++c, ++qi) {
+        const AttnItem it = a.items[c];
+        const SeqMeta sm = a.seq[it.s];
+        const ItemGeo ig = item_geo(it, sm, g.gamma);
+        const int qb = qi & 1;
+        const uint32_t qph = (qi >> 1) & 1;
+        if (!mbar_wait(smem_u32(&bar->q_empty[qb]), qph ^ 1, abort_flag)) break;
+        const uint32_t qf = smem_u32(&bar->q_full[qb]);
+        mbar_expect_tx(qf, 2 * 64 * n_q * 2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(base + qb * Q_BYTES + h * Q_HALF, &map_q, qf, h * 64, it.g * grp,
+                      it.s * g.gamma, pol_q);
+        q_issued |= 1u << qb;
+        q_par = (q_par & ~(1u << qb)) | (qph << qb);
+        bool ok = true;
+        for (int j = 0; j < ig.ntiles; ++j) {
+          if (!mbar_wait(smem_u32(&bar->kv_empty[stage]), kv_phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t gm = group_mask(ig, j);
+          const uint32_t sb = base + OFF_KV + stage * STAGE_BYTES;
+          const uint32_t fb = smem_u32(&bar->kv_full[stage]);
+          mbar_expect_tx(fb, __popc(gm) * 4 * GROUP_BYTES);
+#pragma unroll
+          for (int q = 0; q < AK / 16; ++q) {
+            if (!((gm >> q) & 1u)) continue;
+            if (!ig.block) {
+              const int pos = ig.p0 + j * AK + 16 * q;
+              int page = a.page_ids[sm.page_base + pos / 16 - sm.ws / 16];
+              if (page < 0 || page >= g.pages) {
+                atomicOr(a.status, ST_PAGE);
+                page = 0;
+              }
+              const int row_k = (((page * g.L + a.layer) * 2) * g.nkv + it.g) * 16;
+              const int row_v = row_k + g.nkv * 16;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                tma_load_2d(sb + h * KT_HALF + q * GROUP_BYTES, &map_pool, fb, h * 64, row_k,
+                            pol_kv);
+                tma_load_2d(sb + KT_BYTES + h * KT_HALF + q * GROUP_BYTES, &map_pool, fb, h * 64,
+                            row_v, pol_kv);
+              }
+            } else {
+              const int row = it.s * g.gamma + j * AK + 16 * q;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                tma_load_2d(sb + h * KT_HALF + q * GROUP_BYTES, &map_kb, fb, it.g * AD + h * 64,
+                            row, pol_q);
+                tma_load_2d(sb + KT_BYTES + h * KT_HALF + q * GROUP_BYTES, &map_vb, fb,
+                            it.g * AD + h * 64, row, pol_q);
+              }
+            }
+          }
+          kv_issued |= 1u << stage;
+          kv_par = (kv_par & ~(1u << stage)) | (kv_phase << stage);
+          if (++stage == KV_STAGES) {
+            stage = 0;
+            kv_phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      bar->q_issued = q_issued;
+      bar->q_parity = q_par;
+      bar->kv_issued = kv_issued;
+      bar->kv_parity = kv_par;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer --------
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_mn<AQ, AK>();
+      const uint32_t idesc_o = idesc_bf16_mn<AQ, AD>() | (1u << 16);   // B (V) MN-major
+      int stage = 0;
+      uint32_t kv_phase = 0;
+      int T = 0, qi = 0;
+      bool have_prev = false;
+      int prev_T = 0, prev_stage = 0;
+      uint32_t prev_gm = 0;
+      bool ok = true;
+      // O_T = P_T V_T for the tile issued before
+      auto issue_pv = [&](int t, int st, uint32_t gm) -> bool {
+        const int pb = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (!mbar_wait(smem_u32(&bar->p_full[pb]), ph, abort_flag)) return false;
+        if (!mbar_wait(smem_u32(&bar->o_empty[pb]), ph ^ 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + TMEM_O + pb * AD;
+        const uint32_t pa = base + OFF_P + pb * P_BYTES;
+        const uint32_t vb = base + OFF_KV + st * STAGE_BYTES + KT_BYTES;
+        uint32_t acc = 0;
+#pragma unroll
+        for (int kq = 0; kq < AK / 16; ++kq) {
+          if (!((gm >> kq) & 1u)) continue;
+          umma_bf16(d, sw128_desc(pa + kq * 32), sw128_desc_mn(vb + kq * 16 * 128, KT_HALF, 1024),
+                    idesc_o, acc);
+          acc = 1;
+        }
+        umma_commit(smem_u32(&bar->o_full[pb]));
+        umma_commit(smem_u32(&bar->kv_empty[st]));
+        return true;
+      };
+      for (int c = c_begin; c < c_end && ok && !*abort_flag; ++c, ++qi) {
+        const AttnItem it = a.items[c];
+        const ItemGeo ig = item_geo(it, a.seq[it.s], g.gamma);
+        const int qb = qi & 1;
+        if (!mbar_wait(smem_u32(&bar->q_full[qb]), (qi >> 1) & 1, abort_flag)) break;
+        const uint32_t qa = base + qb * Q_BYTES;
+        for (int j = 0; j < ig.ntiles; ++j, ++T) {
+          if (!mbar_wait(smem_u32(&bar->kv_full[stage]), kv_phase, abort_flag)) { ok = false; break; }
+          const int sbuf = T & 1;
+          if (!mbar_wait(smem_u32(&bar->s_empty[sbuf]), ((T >> 1) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + TMEM_S + sbuf * AK;
+          const uint32_t kb = base + OFF_KV + stage * STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < AD / 16; ++kk) {
+            const int h = kk >> 2, off = (kk & 3) * 32;
+            umma_bf16(d, sw128_desc(qa + h * Q_HALF + off), sw128_desc(kb + h * KT_HALF + off),
+                      idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&bar->s_full[sbuf]));
+          if (j == ig.ntiles - 1) umma_commit(smem_u32(&bar->q_empty[qb]));
+          if (have_prev && !issue_pv(prev_T, prev_stage, prev_gm)) { ok = false; break; }
+          have_prev = true;
+          prev_T = T;
+          prev_stage = stage;
+          prev_gm = group_mask(ig, j);
+          if (++stage == KV_STAGES) {
+            stage = 0;
+            kv_phase ^= 1;
+          }
+        }
+      }
+      if (ok && have_prev && !*abort_flag) issue_pv(prev_T, prev_stage, prev_gm);
+    }
+  } else {
+    // ------------------------------------------------ softmax -----------
+    const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
+    const int r = q4 * 32 + lane;            // query vector of this thread
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    int T = 0;
+    bool ok = true;
+    for (int c = c_begin; c < c_end && ok; ++c) {
+      const AttnItem it = a.items[c];
+      const ItemGeo ig = item_geo(it, a.seq[it.s], g.gamma);
+      float o[AD];
+#pragma unroll
+      for (int e = 0; e < AD; ++e) o[e] = 0.f;
+      float m = -INFINITY, l = 0.f, pend_corr = 0.f;
+      // folds O of tile t into o (o was relative to the previous max)
+      auto fold_o = [&](int t, float corr) -> bool {
+        const int ob = t & 1;
+        if (!mbar_wait(smem_u32(&bar->o_full[ob]), (t >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[64];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            tmem_ld16_nowait(tmem + lane_off + TMEM_O + ob * AD + hh * 64 + 16 * i, v + 16 * i);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 64; ++e) o[hh * 64 + e] = fmaf(o[hh * 64 + e], corr, v[e]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar->o_empty[ob]));
+        return true;
+      };
+      for (int j = 0; j < ig.ntiles; ++j, ++T) {
+        const int sbuf = T & 1;
+        if (!mbar_wait(smem_u32(&bar->s_full[sbuf]), (T >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float x[AK];
+#pragma unroll
+        for (int i = 0; i < AK / 16; ++i)
+          tmem_ld16_nowait(tmem + lane_off + TMEM_S + sbuf * AK + 16 * i, x + 16 * i);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar->s_empty[sbuf]));
+        const int kbase = ig.p0 + j * AK;
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < AK; ++cc) {
+          const int key = kbase + cc;
+          const float v = (key >= ig.lo && key < ig.hi) ? x[cc] * a.scale : -INFINITY;
+          x[cc] = v;
+          tmax = fmaxf(tmax, v);
+        }
+        const float m_new = fmaxf(m, tmax);
+        const float mm = (m_new == -INFINITY) ? 0.f : m_new;
+        const float corr = __expf(m - mm);   // 0 while m is -inf
+        float s0 = 0.f, s1 = 0.f;
+        // P row (bf16) in the 128B-swizzled K-major layout: 16-byte chunk ch
+        // of row r sits at chunk position ch ^ (r % 8)
+        const uint32_t prow = base + OFF_P + sbuf * P_BYTES + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < AK / 8; ++ch) {
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) p[e] = __expf(x[ch * 8 + e] - mm);
+          s0 += (p[0] + p[1]) + (p[2] + p[3]);
+          s1 += (p[4] + p[5]) + (p[6] + p[7]);
+          const uint32_t w0 = pack_bf16(p[0], p[1]), w1 = pack_bf16(p[2], p[3]);
+          const uint32_t w2 = pack_bf16(p[4], p[5]), w3 = pack_bf16(p[6], p[7]);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           prow + ((uint32_t)(ch ^ (r & 7)) << 4)),
+                       "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                       : "memory");
+        }
+        l = l * corr + (s0 + s1);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar->p_full[sbuf]));
+        if (j > 0 && !fold_o(T - 1, pend_corr)) { ok = false; break; }
+        pend_corr = corr;
+        m = m_new;
+      }
+      if (!ok || !fold_o(T - 1, pend_corr)) {
+        ok = false;
+        break;
+      }
+      if (r < n_q) {
+        if (it.slot < 0) {
+          const float inv = 1.f / l;
+          bf16 *orow = a.o + ((int64_t)(it.s * g.gamma + r / grp) * g.nq + it.g * grp + r % grp) * AD;
+#pragma unroll
+          for (int e = 0; e < AD; e += 8) {
+            uint4 w;
+            w.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
+            w.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
+            w.z = pack_bf16(o[e + 4] * inv, o[e + 5] * inv);
+            w.w = pack_bf16(o[e + 6] * inv, o[e + 7] * inv);
+            *reinterpret_cast<uint4 *>(orow + e) = w;
+          }
+        } else {
+          float *ws = a.ws + (int64_t)it.slot * a.slot_floats;
+          float *arow = ws + (int64_t)r * AD;
+#pragma unroll
+          for (int e = 0; e < AD; e += 4)
+            *reinterpret_cast<float4 *>(arow + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          ws[(int64_t)n_q * AD + r] = m;
+          ws[(int64_t)n_q * AD + n_q + r] = l;
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------- teardown ----
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      atomicOr(a.status, ST_TIMEOUT);
+      // wait (bounded) for every load this CTA issued to land
+      for (int b = 0; b < 2; ++b) {
+        if (!((bar->q_issued >> b) & 1u)) continue;
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(smem_u32(&bar->q_full[b]), (bar->q_parity >> b) & 1u) &&
+               global_ns() - t0 < 100000000ull) {
+        }
+      }
+      for (int s = 0; s < KV_STAGES; ++s) {
+        if (!((bar->kv_issued >> s) & 1u)) continue;
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(smem_u32(&bar->kv_full[s]), (bar->kv_parity >> s) & 1u) &&
+               global_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+    if (threadIdx.x == 32) {
+      umma_commit(smem_u32(&bar->drain));
+      const uint64_t t0 = global_ns();
+      while (!mbar_test(smem_u32(&bar->drain), 0) && global_ns() - t0 < 100000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+bool attention_tc_supported(const Geo &g) {
+  return !g.kv_fp8 && g.d == AD && attn_query_rows(g) <= AQ && g.B == 16 &&
+         (int64_t)g.pages * g.L * 2 * g.nkv * g.B < (1ll << 31);
+}
+
+bool attention_tc_maps(const Geo &g, int R_max, const void *q, const void *pool, const void *kb,
+                       const void *vb, AttnMaps *m) {
+  m->ok = false;
+  if (!attention_tc_supported(g)) return true;
+  const int grp = g.nq / g.nkv;
+  const int64_t qdims[3] = {g.d, g.nq, R_max};
+  const int64_t qstr[2] = {(int64_t)g.d * 2, (int64_t)g.nq * g.d * 2};
+  const int qbox[3] = {64, grp, g.gamma};
+  if (!tc::make_map_3d(&m->q, q, qdims, qstr, qbox)) return false;
+  const int64_t pool_rows = (int64_t)g.pages * g.L * 2 * g.nkv * g.B;
+  if (!tc::make_map_2d(&m->pool, pool, false, pool_rows, g.d, 16) ||
+      !tc::make_map_2d(&m->kb, kb, false, R_max, g.kv, 16) ||
+      !tc::make_map_2d(&m->vb, vb, false, R_max, g.kv, 16))
+    return false;
+  m->ok = true;
+  return true;
+}
+
+cudaError_t attention_tc(const AttnArgs &a, const AttnMaps &m, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  launch_pdl(k_attn_tc, dim3(a.grid_tc), dim3(THREADS), SMEM, s, m.q, m.pool, m.kb, m.vb, a);
+  return cudaGetLastError();
+}
+
+int attention_tc_tiles(const Geo &g, const SeqMeta &sm, const AttnItem &it) {
+  const int n_ctx = sm.pos - sm.ws;
+  if (it.k0 >= n_ctx) return (g.gamma + AK - 1) / AK;
+  const int lo = sm.ws + it.k0, hi = sm.ws + it.k1;
+  return (hi - (lo & ~15) + AK - 1) / AK;
+}
+
+}  // namespace dfl

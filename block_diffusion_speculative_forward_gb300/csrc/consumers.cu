@@ -115,14 +115,13 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
   }
 }
 
-// u[a, f] = silu(gate) * up with gate/up rows interleaved in blocks of 64.
+// u[a, f] = silu(gate) * up with gate/up rows alternating (2f gate, 2f+1 up).
 __global__ void __launch_bounds__(256) k_swiglu_part(SwigluArgs p) {
   pdl_trigger();
   pdl_wait();
   const int a = blockIdx.x;
   for (int f = blockIdx.y * 256 + threadIdx.x; f < p.I; f += gridDim.y * 256) {
-    const int gr = (f >> 6) * 128 + (f & 63);
-    const float gt = part_value(p.y, a, gr), up = part_value(p.y, a, gr + 64);
+    const float gt = part_value(p.y, a, 2 * f), up = part_value(p.y, a, 2 * f + 1);
     p.u[(int64_t)a * p.I + f] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
   }
 }

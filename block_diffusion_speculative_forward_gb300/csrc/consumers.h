@@ -30,7 +30,7 @@ struct QkvPostArgs {
 };
 
 struct SwigluArgs {
-  Partials y;           // [R, 2I], gate/up interleaved by 64 rows
+  Partials y;           // [R, 2I], gate/up rows alternating
   int I;
   bf16 *u;              // [R, I]
 };

@@ -92,7 +92,8 @@ struct dflash_handle {
   bool meta_ev_live = false;
   // fixed sections of the metadata buffer (rows follow them)
   int cap_seq = 0, cap_pages = 0, cap_items = 0, cap_pairs = 0;
-  size_t off_seq = 0, off_pages = 0, off_items = 0, off_pairs = 0, off_rows = 0;
+  size_t off_seq = 0, off_pages = 0, off_items = 0, off_pairs = 0, off_sched = 0, off_rows = 0;
+  int cap_sched = 0;
   // captured propose graphs, keyed by the call's launch shape
   bool use_graphs = true;
   cudaStream_t cap_stream = nullptr;
@@ -248,9 +249,11 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
                 const std::vector<dfl::RowMeta> &rows, const std::vector<int32_t> &page_ids,
                 cudaStream_t s, dfl::CallMeta *out,
                 const std::vector<dfl::AttnItem> &items = {},
-                const std::vector<dfl::AttnPair> &pairs = {}) {
+                const std::vector<dfl::AttnPair> &pairs = {},
+                const std::vector<int32_t> &cta_off = {}) {
   if ((int)seq.size() > h->cap_seq || (int)page_ids.size() > h->cap_pages ||
-      (int)items.size() > h->cap_items || (int)pairs.size() > h->cap_pairs)
+      (int)items.size() > h->cap_items || (int)pairs.size() > h->cap_pairs ||
+      (int)cta_off.size() > h->cap_sched)
     return fail(DFLASH_EINVAL, "internal: call metadata beyond the handle's capacity");
   size_t total = h->off_rows + rows.size() * sizeof(dfl::RowMeta) + 16;
   if (h->meta_ev_live) {
@@ -290,6 +293,8 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
     memcpy(h->meta_host + h->off_items, items.data(), items.size() * sizeof(dfl::AttnItem));
   if (!pairs.empty())
     memcpy(h->meta_host + h->off_pairs, pairs.data(), pairs.size() * sizeof(dfl::AttnPair));
+  if (!cta_off.empty())
+    memcpy(h->meta_host + h->off_sched, cta_off.data(), cta_off.size() * sizeof(int32_t));
   if (!rows.empty())
     memcpy(h->meta_host + h->off_rows, rows.data(), rows.size() * sizeof(dfl::RowMeta));
   CK(cudaMemcpyAsync(h->meta_dev, h->meta_host, total, cudaMemcpyHostToDevice, s));
@@ -301,6 +306,7 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
   out->page_ids = (const int32_t *)(h->meta_dev + h->off_pages);
   out->items = (const dfl::AttnItem *)(h->meta_dev + h->off_items);
   out->pairs = (const dfl::AttnPair *)(h->meta_dev + h->off_pairs);
+  out->cta_off = (const int32_t *)(h->meta_dev + h->off_sched);
   out->n_seq = (int)seq.size();
   out->n_rows = (int)rows.size();
   out->n_items = (int)items.size();
@@ -397,7 +403,9 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_ha
   }
   h->cap_items = h->b.attn_slots + h->cap_pairs;
   h->off_pairs = (h->off_items + sizeof(dfl::AttnItem) * h->cap_items + 15) & ~(size_t)15;
-  h->off_rows = (h->off_pairs + sizeof(dfl::AttnPair) * h->cap_pairs + 15) & ~(size_t)15;
+  h->cap_sched = h->b.attn_grid_tc + 1;
+  h->off_sched = (h->off_pairs + sizeof(dfl::AttnPair) * h->cap_pairs + 15) & ~(size_t)15;
+  h->off_rows = (h->off_sched + sizeof(int32_t) * h->cap_sched + 15) & ~(size_t)15;
   *out = h;
   return DFLASH_OK;
 }
@@ -764,9 +772,10 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   }
   std::vector<AttnItem> items;
   std::vector<AttnPair> pairs;
-  build_attn_work(h->g, seq, h->b.attn_slots, &items, &pairs);
+  std::vector<int32_t> cta_off;
+  build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs, &cta_off);
   CallMeta cm;
-  int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs);
+  int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off);
   if (rc) return rc;
   rc = run_forward(h, cm, num_drafts, bitmask, s);
   if (rc) return rc;

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <queue>
 #include <string>
 
 #include <algorithm>
@@ -113,13 +114,11 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     BK(cudaMemcpy(qkv + qd * H, p[2], kv * H * 2, cudaMemcpyDeviceToDevice));
     BK(cudaMemcpy(qkv + (qd + kv) * H, p[3], kv * H * 2, cudaMemcpyDeviceToDevice));
     L.w_qkv = qkv;
-    // gate/up interleaved by blocks of 64 rows: [gate 0..63; up 0..63; gate
-    // 64..127; up 64..127; ...], so one 128-row tile holds matching features.
+    // gate/up rows alternate: row 2j = gate j, row 2j+1 = up j, so the two
+    // inputs of SwiGLU feature j sit in adjacent accumulator lanes.
     bf16 *gu = w_gu + (size_t)l * 2 * I * H;
-    BK(cudaMemcpy2D(gu, 128 * H * 2, p[8], 64 * H * 2, 64 * H * 2, I / 64,
-                    cudaMemcpyDeviceToDevice));
-    BK(cudaMemcpy2D(gu + 64 * H, 128 * H * 2, p[9], 64 * H * 2, 64 * H * 2, I / 64,
-                    cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy2D(gu, 2 * H * 2, p[8], H * 2, H * 2, I, cudaMemcpyDeviceToDevice));
+    BK(cudaMemcpy2D(gu + H, 2 * H * 2, p[9], H * 2, H * 2, I, cudaMemcpyDeviceToDevice));
     L.w_gu = gu;
     bf16 *kvl = W->w_kv + (size_t)l * 2 * kv * H;
     BK(cudaMemcpy(kvl, p[2], kv * H * 2, cudaMemcpyDeviceToDevice));
@@ -186,6 +185,7 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->kb, (size_t)R_max * kv);
   BA(B->vb, (size_t)R_max * kv);
   BA(B->o, (size_t)R_max * qd);
+  BA(B->qkv_dense, (size_t)R_max * g.qkv_w);
   BA(B->u, (size_t)R_max * I);
   BA(B->z, (size_t)D_max * H);
   BA(B->row_id, (size_t)D_max);
@@ -217,6 +217,15 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     B->attn_slot_floats = (int64_t)n_q * g.d + 2 * n_q;
     B->attn_slots = 3 * sms + 3 * c.max_batch * g.nkv + 64;
     BA(B->attn_ws, (size_t)B->attn_slots * B->attn_slot_floats);
+    // The tensor-core kernel reads whole 16-row blocks of the block K/V
+    // rows (masked past gamma): keep never-written rows finite.
+    BK(cudaMemset(B->kb, 0, sizeof(bf16) * (size_t)R_max * kv));
+    BK(cudaMemset(B->vb, 0, sizeof(bf16) * (size_t)R_max * kv));
+    if (!attention_tc_maps(g, R_max, B->q, W->pool, B->kb, B->vb, &B->attn_maps)) {
+      g_build_err = "cuTensorMapEncodeTiled failed for an attention operand";
+      return DFLASH_ECUDA;
+    }
+    B->attn_grid_tc = B->attn_maps.ok ? sms : 0;
   }
   // TMA maps of the activation operands, one per tile width.
   {
@@ -346,6 +355,12 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   const int n = cm.n_seq, R = n * g.gamma, D = n * nd;
   const int qd = g.nq * g.d;
   const int bnR = tc::pick_bn(R);
+  // Many rows: the fused QKV and gate/up GEMMs run whole tiles per CTA
+  // (data-parallel, epilogue in the GEMM); few rows: split-K partials read by
+  // the consumer kernels, so every SM streams weights.
+  const bool dp = R > 64;
+  const int bn_qkv = dp ? tc::pick_bn_dp(R, g.qkv_w, g.H) : bnR;
+  const int bn_gu = dp ? tc::pick_bn_dp(R, 2 * g.I, g.H) : bnR;
   LK(embed_block(W.embed, cm.seq, n, g, c.mask_token_id, B.x, B.status, s));
   // The residual update of each o/down projection is applied by the RMSNorm
   // that follows it (pending), or by the GEMM itself when the partial mode
@@ -366,8 +381,35 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       an.x_tap = B.tap_x ? B.tap_x + (size_t)l * R * g.H : nullptr;
       LK(add_norm(an, R, s));
     }
-    const bool part = tc::partial_ok(R, g.qkv_w, g.H);
-    if (part) {
+    const bool part = !dp && tc::partial_ok(R, g.qkv_w, g.H);
+    if (dp) {
+      // whole-tile QKV into a dense f32 buffer, then per-head q/k RMSNorm + RoPE
+      GemmParams p{};
+      p.m_act = R;
+      p.n_w = g.qkv_w;
+      p.k = g.H;
+      p.epi = EPI_TC_STORE_F32;
+      p.out = B.qkv_dense;
+      p.ldo = g.qkv_w;
+      p.ws = B.ws;
+      p.counters = B.counters;
+      p.status = B.status;
+      p.dp = 1;
+      LK(tc::gemm(W.map_qkv[l], B.act_map[ACT_H][bn_index(bn_qkv)], bn_qkv, p, s));
+      QkvPostArgs qp{};
+      qp.g = g;
+      qp.y.dense = B.qkv_dense;
+      qp.y.ld = g.qkv_w;
+      qp.seq = cm.seq;
+      qp.q_norm = L.q_norm;
+      qp.k_norm = L.k_norm;
+      qp.cos_t = W.cos_t;
+      qp.sin_t = W.sin_t;
+      qp.q = B.q;
+      qp.kb = B.kb;
+      qp.vb = B.vb;
+      LK(qkv_post(qp, R, s));
+    } else if (part) {
       // QKV partials, then per-head q/k RMSNorm + RoPE
       QkvPostArgs qp{};
       qp.g = g;
@@ -428,7 +470,14 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       a.ws = B.attn_ws;
       a.slot_floats = B.attn_slot_floats;
       a.status = B.status;
-      LK(attention_split(a, s));
+      a.cta_off = cm.cta_off;
+      a.grid_tc = B.attn_grid_tc;
+      if (B.attn_maps.ok) {
+        LK(attention_tc(a, B.attn_maps, s));
+        LK(attention_merge(a, s));
+      } else {
+        LK(attention_split(a, s));
+      }
       if (cm.cap_pairs) count_launches(1);
     }
     // o_proj: residual added by the post-attention norm (or by the GEMM)
@@ -450,7 +499,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       an.out = B.h;
       LK(add_norm(an, R, s));
     }
-    if (tc::partial_ok(R, 2 * g.I, g.H)) {
+    if (!dp && tc::partial_ok(R, 2 * g.I, g.H)) {
       SwigluArgs sp{};
       int rc = project(B, W.map_gu[l], ACT_H, R, 2 * g.I, g.H, nullptr, &sp.y, s);
       if (rc) return rc;
@@ -468,7 +517,8 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       p.counters = B.counters;
       p.status = B.status;
       p.u_out = B.u;
-      LK(tc::gemm(W.map_gu[l], B.act_map[ACT_H][bn_index(bnR)], bnR, p, s));
+      p.dp = dp;
+      LK(tc::gemm(W.map_gu[l], B.act_map[ACT_H][bn_index(bn_gu)], bn_gu, p, s));
     }
     has_pending = tc::partial_ok(R, g.H, g.I);
     if (has_pending) {
@@ -563,22 +613,25 @@ cudaError_t gather_kv_rows(const Geo &g, const Weights &W, const Buffers &B, con
 
 namespace dfl {
 
-void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
-                     std::vector<AttnItem> *items, std::vector<AttnPair> *pairs) {
+void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
+                     std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
+                     std::vector<int32_t> *cta_off) {
   int64_t total = 0;
   for (const SeqMeta &m : seq) total += (int64_t)(m.pos - m.ws) * g.nkv;
   const int sms = tc::num_sms();
-  // About three SM waves of ctx items (three attention CTAs fit on an SM),
-  // at least 64 keys each so the partial merge stays cheap.
+  // About three SM waves of ctx items, at least 64 keys each so the partial
+  // merge stays cheap. Chunk boundaries fall on positions that are multiples
+  // of 64, so every tile but a window's first starts on a page.
   int64_t chunk = (total + 3 * sms - 1) / (3 * sms);
-  chunk = std::max<int64_t>(64, (chunk + 31) / 32 * 32);
+  chunk = std::max<int64_t>(64, (chunk + 63) / 64 * 64);
   for (;;) {
     items->clear();
     pairs->clear();
     int slots = 0;
     for (int s = 0; s < (int)seq.size(); ++s) {
       const int n_ctx = seq[s].pos - seq[s].ws;
-      const int nc = (int)((n_ctx + chunk - 1) / chunk);
+      const int off = (int)(seq[s].ws % 64);
+      const int nc = n_ctx > 0 ? (int)((n_ctx + off + chunk - 1) / chunk) : 0;
       for (int h = 0; h < g.nkv; ++h) {
         if (nc == 0) {
           items->push_back({s, h, 0, g.gamma, -1});
@@ -586,15 +639,45 @@ void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap
         }
         pairs->push_back({s, h, slots, nc + 1});
         for (int c = 0; c < nc; ++c) {
-          const int k0 = (int)(c * chunk), k1 = (int)std::min<int64_t>(n_ctx, (c + 1) * chunk);
+          const int k0 = (int)std::max<int64_t>(0, c * chunk - off);
+          const int k1 = (int)std::min<int64_t>(n_ctx, (c + 1) * chunk - off);
           items->push_back({s, h, k0, k1, slots++});
         }
         items->push_back({s, h, n_ctx, n_ctx + g.gamma, slots++});
       }
     }
-    if (slots <= slot_cap) return;
+    if (slots <= slot_cap) break;
     chunk *= 2;
   }
+  cta_off->clear();
+  if (grid_tc <= 0) return;
+  // Longest-first onto the least-loaded CTA (cost: key tiles + one for the
+  // item's setup and output), then the items regrouped CTA by CTA.
+  const int n = (int)items->size();
+  std::vector<int> cost(n), order(n);
+  for (int i = 0; i < n; ++i) {
+    cost[i] = attention_tc_tiles(g, seq[(*items)[i].s], (*items)[i]) + 1;
+    order[i] = i;
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+  using Load = std::pair<int64_t, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int b = 0; b < grid_tc; ++b) heap.push({0, b});
+  std::vector<std::vector<int>> per(grid_tc);
+  for (int i : order) {
+    Load t = heap.top();
+    heap.pop();
+    per[t.second].push_back(i);
+    heap.push({t.first + cost[i], t.second});
+  }
+  std::vector<AttnItem> regrouped;
+  regrouped.reserve(n);
+  cta_off->push_back(0);
+  for (int b = 0; b < grid_tc; ++b) {
+    for (int i : per[b]) regrouped.push_back((*items)[i]);
+    cta_off->push_back((int32_t)regrouped.size());
+  }
+  items->swap(regrouped);
 }
 
 }  // namespace dfl

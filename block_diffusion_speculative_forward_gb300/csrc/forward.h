@@ -40,6 +40,7 @@ struct Buffers {
   bf16 *h = nullptr;           // [R, H] normed GEMM input
   bf16 *q = nullptr, *kb = nullptr, *vb = nullptr, *o = nullptr;
   bf16 *u = nullptr;           // [R, I]
+  float *qkv_dense = nullptr;  // [R, qkv_w] f32 QKV of a many-row call
   bf16 *z = nullptr;           // [D, H] final-normed draft rows
   int32_t *row_id = nullptr;
   float *row_p1 = nullptr;
@@ -60,14 +61,19 @@ struct Buffers {
   int n_counters = 0;
   LmPartial *lm_part = nullptr; // [D_max][vocab tiles]
   float *attn_ws = nullptr;     // split-KV attention partial slots
+  AttnMaps attn_maps;           // tensor-core attention operands (ok = false: mma.sync kernel)
+  int attn_grid_tc = 0;         // persistent CTAs of the tensor-core attention
   int attn_slots = 0;           // slot capacity
   int64_t attn_slot_floats = 0; // n_q*d + 2*n_q per slot
 };
 
 // Cuts every (sequence, kv head) key range of the call into split-KV items
 // (ctx chunks plus one block-key item) within the workspace's slot capacity.
-void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
-                     std::vector<AttnItem> *items, std::vector<AttnPair> *pairs);
+// With grid_tc > 0 the items are also balanced over grid_tc persistent CTAs
+// of the tensor-core kernel: CTA b runs items [cta_off[b], cta_off[b + 1]).
+void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
+                     std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
+                     std::vector<int32_t> *cta_off);
 
 struct CallMeta {
   const SeqMeta *seq = nullptr;
@@ -75,6 +81,7 @@ struct CallMeta {
   const int32_t *page_ids = nullptr;
   const AttnItem *items = nullptr;
   const AttnPair *pairs = nullptr;
+  const int32_t *cta_off = nullptr;   // tensor-core attention schedule (grid_tc + 1)
   const int *counts = nullptr;   // device: items, pairs
   int n_seq = 0, n_rows = 0, n_items = 0, n_pairs = 0;
   int cap_items = 0, cap_pairs = 0;

@@ -227,38 +227,52 @@ __device__ __forceinline__ void finish16(const GemmParams &p, Smem *sm, const fl
     return;
   }
   if (EPI == EPI_TC_SWIGLU) {
-    // Tile tm holds gate rows of features 64*tm..64*tm+63 in its first 64
-    // rows and the matching up rows in the next 64.
-    const int fl = q * 32 + lane;
-    if (fl >= 64) {
+    // Weight rows alternate gate / up of one feature (row 2j gate j, 2j+1 up
+    // j): the pair sits in lanes (2i, 2i+1) of a warp. The 16 columns run
+    // phase by phase (all shuffles, all exponentials, then the stores) so the
+    // dependent chains overlap. silu(g) = g / (1 + e^-g), the exponent
+    // clamped at 80 so the fast divide stays in range (silu(g) < 1e-33 there).
+    const int ldu = p.n_w / 2;
+    float up[16], y[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) sm->xch[c][fl - 64] = v[c];
-    }
-    epi_bar();
-    if (fl < 64) {
-      const int ldu = p.n_w / 2;
+    for (int c = 0; c < 16; ++c) up[c] = __shfl_xor_sync(0xffffffffu, v[c], 1);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int a = a0 + c;
-        if (a >= p.m_act) break;
-        const float gt = v[c], up = sm->xch[c][fl];
-        p.u_out[(int64_t)a * ldu + tm * 64 + fl] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
+    for (int c = 0; c < 16; ++c)
+      y[c] = __fdividef(v[c], 1.f + __expf(fminf(-v[c], 80.f))) * up[c];
+    if (!(lane & 1) && f_ok) {
+      bf16 *dst = p.u_out + (int64_t)a0 * ldu + (f >> 1);
+      if (a0 + 16 <= p.m_act) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[(int64_t)c * ldu] = __float2bfloat16_rn(y[c]);
+      } else {
+        const int n = p.m_act - a0;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c < n) dst[(int64_t)c * ldu] = __float2bfloat16_rn(y[c]);
       }
     }
-    epi_bar();
     return;
   }
   if (!f_ok) return;
+  const float sc = p.wscale ? p.wscale[f] : 1.f;
+  const int nrows = p.m_act - a0 < 16 ? p.m_act - a0 : 16;
+  if (EPI == EPI_TC_ADD_F32) {
+    // all loads first, then the stores
+    float *o = (float *)p.out + (int64_t)a0 * p.ldo + f;
+    float r[16];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    const int a = a0 + c;
-    if (a >= p.m_act) break;
-    const int64_t off = (int64_t)a * p.ldo + f;
-    float x = v[c];
-    if (p.wscale) x *= p.wscale[f];
-    if (EPI == EPI_TC_STORE_F32) ((float *)p.out)[off] = x;
-    else if (EPI == EPI_TC_ADD_F32) ((float *)p.out)[off] += x;
-    else ((bf16 *)p.out)[off] = __float2bfloat16_rn(x);
+    for (int c = 0; c < 16; ++c) r[c] = c < nrows ? o[(int64_t)c * p.ldo] : 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      if (c < nrows) o[(int64_t)c * p.ldo] = r[c] + v[c] * sc;
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      if (c >= nrows) break;
+      const int64_t off = (int64_t)(a0 + c) * p.ldo + f;
+      if (EPI == EPI_TC_STORE_F32) ((float *)p.out)[off] = v[c] * sc;
+      else ((bf16 *)p.out)[off] = __float2bfloat16_rn(v[c] * sc);
+    }
   }
 }
 
@@ -278,7 +292,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int kb = p.k / BK;
   const int tiles = p.tiles_m * p.tiles_n;
   const Part part{(int64_t)tiles * kb, (int)gridDim.x};
-  const int64_t it_begin = part.begin(blockIdx.x), it_end = part.begin(blockIdx.x + 1);
+  // Iteration range of this CTA. Stream-K: a contiguous range of (tile,
+  // k-block) iterations, tile = it / kb. Data-parallel: whole tiles
+  // blockIdx.x, blockIdx.x + G, ...; iteration it is k-block it % kb of the
+  // CTA's (it / kb)-th tile.
+  const bool dp = p.dp != 0;
+  const int n_dp = dp ? (tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const int64_t it_begin = dp ? 0 : part.begin(blockIdx.x);
+  const int64_t it_end = dp ? (int64_t)n_dp * kb : part.begin(blockIdx.x + 1);
+  const int t_step = dp ? (int)gridDim.x : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -323,7 +345,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Weights do not depend on the previous kernel: fill the first stages
       // with weight tiles before waiting for it, then add the activations.
       const int n_pre = (int)(n_it < C::STAGES ? n_it : C::STAGES);
-      int t0 = (int)(it_begin / kb), k0 = (int)(it_begin % kb);   // (tile, k-block) of it_begin
+      // (tile, k-block) of it_begin
+      int t0 = dp ? (int)blockIdx.x : (int)(it_begin / kb), k0 = (int)(it_begin % kb);
       {
         int t = t0, k = k0;
         for (int j = 0; j < n_pre; ++j) {
@@ -331,7 +354,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_expect_tx(fb, C::STAGE_BYTES);
           tma_load_2d(base + j * C::STAGE_BYTES, &map_w, fb, k * BK, (t % p.tiles_m) * BM, pol_w);
           issued |= 1u << j;
-          if (++k == kb) { k = 0; ++t; }
+          if (++k == kb) { k = 0; t += t_step; }
         }
       }
       pdl_wait();
@@ -339,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < n_pre; ++j) {
         tma_load_2d(base + j * C::STAGE_BYTES + A_BYTES, &map_x, smem_u32(&sm->full[j]), k * BK,
                     (t / p.tiles_m) * BN, pol_x);
-        if (++k == kb) { k = 0; ++t; }
+        if (++k == kb) { k = 0; t += t_step; }
       }
       int stage = n_pre % C::STAGES;
       uint32_t phase = (n_pre == C::STAGES) ? 1u : 0u;
@@ -352,7 +375,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(sa + A_BYTES, &map_x, fb, k * BK, (t / p.tiles_m) * BN, pol_x);
         issued |= 1u << stage;
         parity = (parity & ~(1u << stage)) | (phase << stage);
-        if (++k == kb) { k = 0; ++t; }
+        if (++k == kb) { k = 0; t += t_step; }
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       }
       sm->drain_issued = issued;
@@ -404,7 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t it = it_begin; it < it_end;) {
-      const int t = (int)(it / kb);
+      const int t = dp ? (int)blockIdx.x + (int)(it / kb) * (int)gridDim.x : (int)(it / kb);
       const int k0 = (int)(it % kb);
       const int k1 = (int)((int64_t)kb < (int64_t)k0 + (it_end - it) ? (int64_t)kb : (int64_t)k0 + (it_end - it));
       const int tm = t % p.tiles_m, tn = t / p.tiles_m;
@@ -416,22 +439,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // partial slot of this CTA for this tile: its first or its last segment
       const int slot = 2 * blockIdx.x + (it == it_begin ? 0 : 1);
       float *ws = p.ws + (int64_t)slot * BN * BM;
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(tbase + c0, v);
-        if (EPI == EPI_TC_PARTIAL) {
-          // [BN rows][128 features]: coalesced for this store and for the
-          // consumer, which reads along features
+      // up to 64 accumulator columns per TMEM round trip
+      constexpr int CH = BN < 64 ? BN : 64;
+      for (int cb = 0; cb < BN; cb += CH) {
+        float vv[CH / 16][16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) ws[(int64_t)(c0 + c) * BM + f_local] = v[c];
-        } else if (whole) {
-          finish16<EPI>(p, sm, v, f, tm, tn * BN + c0, q, lane);
-        } else {
-          // thread-major partial: this thread's BN columns are contiguous
-          float4 *dst = reinterpret_cast<float4 *>(ws + (int64_t)f_local * BN + c0);
+        for (int i = 0; i < CH / 16; ++i) tmem_ld16_nowait(tbase + cb + 16 * i, vv[i]);
+        tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        for (int i = 0; i < CH / 16; ++i) {
+          const int c0 = cb + 16 * i;
+          const float(&v)[16] = vv[i];
+          if (EPI == EPI_TC_PARTIAL) {
+            // [BN rows][128 features]: coalesced for this store and for the
+            // consumer, which reads along features
+#pragma unroll
+            for (int c = 0; c < 16; ++c) ws[(int64_t)(c0 + c) * BM + f_local] = v[c];
+          } else if (whole) {
+            finish16<EPI>(p, sm, v, f, tm, tn * BN + c0, q, lane);
+          } else {
+            // thread-major partial: this thread's BN columns are contiguous
+            float4 *dst = reinterpret_cast<float4 *>(ws + (int64_t)f_local * BN + c0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          }
         }
       }
       tc_fence_before();
@@ -598,6 +630,20 @@ bool make_map_2d(CUtensorMap *map, const void *base, bool fp8, int64_t rows, int
   return r == CUDA_SUCCESS;
 }
 
+bool make_map_3d(CUtensorMap *map, const void *base, const int64_t dims[3],
+                 const int64_t strides_bytes[2], const int box[3]) {
+  std::call_once(g_once, init_driver);
+  if (!g_encode) return false;
+  cuuint64_t d[3] = {(cuuint64_t)dims[0], (cuuint64_t)dims[1], (cuuint64_t)dims[2]};
+  cuuint64_t st[2] = {(cuuint64_t)strides_bytes[0], (cuuint64_t)strides_bytes[1]};
+  cuuint32_t bx[3] = {(cuuint32_t)box[0], (cuuint32_t)box[1], (cuuint32_t)box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), d, st,
+                        bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int pick_bn(int m_act) {
   if (m_act <= 16) return 16;
   if (m_act <= 32) return 32;
@@ -614,6 +660,29 @@ bool partial_ok(int m_act, int n_w, int k) {
   return grid > 0 && (total + grid - 1) / grid <= k / BK && total * grid < (1ll << 31);
 }
 
+int pick_bn_dp(int m_act, int n_w, int k) {
+  // Data-parallel tile width: the smallest modelled time of the tensor work
+  // (waves of whole tiles; an M 128 x N bn x K 16 MMA issues in bn / 2
+  // cycles at ~1.9 GHz) and of the operand stream out of L2 (~20 TB/s).
+  const int G = num_sms();
+  const int kb = k / BK;
+  const int cap = pick_bn(m_act);
+  int best = cap;
+  double best_t = 1e30;
+  for (int bn = cap; bn >= 64; bn /= 2) {
+    const int64_t tiles = (int64_t)((n_w + BM - 1) / BM) * ((m_act + bn - 1) / bn);
+    const int64_t waves = (tiles + G - 1) / G;
+    const double t_mma = (double)waves * kb * (BK / 16) * (bn / 2) / 1.9e9;
+    const double t_l2 = (double)tiles * kb * (A_BYTES + bn * BK * 2) / 20e12;
+    const double t = t_mma > t_l2 ? t_mma : t_l2;
+    if (t < best_t) {
+      best_t = t;
+      best = bn;
+    }
+  }
+  return best;
+}
+
 cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, GemmParams p,
                  cudaStream_t s, Partials *view) {
   if (p.m_act <= 0 || p.n_w <= 0) return cudaSuccess;
@@ -623,6 +692,12 @@ cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, Gem
   const int64_t total = (int64_t)p.tiles_m * p.tiles_n * (p.k / BK);
   int grid = num_sms();
   if (p.grid_cap > 0 && p.grid_cap < grid) grid = p.grid_cap;
+  if (p.dp) {
+    // whole tiles per CTA: fused epilogues only, no fixup
+    if (p.epi == EPI_TC_PARTIAL || p.epi == EPI_TC_LMHEAD) return cudaErrorInvalidValue;
+    const int tiles = p.tiles_m * p.tiles_n;
+    if (tiles < grid) grid = tiles;
+  }
   if (total < grid) grid = (int)total;
   if (grid < 1) grid = 1;
   if (p.epi == EPI_TC_PARTIAL) {

@@ -13,7 +13,7 @@ enum TcEpi {
   EPI_TC_STORE_BF16 = 2,  // out[a, f] = bf16(y)
   EPI_TC_LMHEAD = 3,      // per (row, 128-row vocab tile): max, lowest argmax, sum exp
   EPI_TC_QKV = 4,         // stitched q;k;v rows: per-head RMSNorm + RoPE for q and k, bf16 out
-  EPI_TC_SWIGLU = 5,      // gate/up rows interleaved by 64: u = silu(gate) * up, bf16 out
+  EPI_TC_SWIGLU = 5,      // gate/up rows alternating: u = silu(gate) * up, bf16 out
   EPI_TC_PARTIAL = 6,     // every k-segment writes its f32 partial; the consumer sums them
 };
 
@@ -94,6 +94,7 @@ struct GemmParams {
   float *ws;          // partial slots: 2 * grid * BN * 128 floats
   int *counters;      // per tile, zero between launches
   int grid_cap;       // 0 = one CTA per SM
+  int dp;             // 1: data-parallel whole tiles (fused epilogues), no stream-K split
   // lm_head
   const int32_t *bitmask;  // [n_seq][mask_words] or NULL
   int mask_words;
@@ -135,9 +136,15 @@ cudaError_t lmhead(const CUtensorMap &map_x, const CUtensorMap &map_w, const LmA
                    cudaStream_t s);
 int lmhead_vocab_tiles(int vocab);
 int pick_bn(int m_act);
+// Tile width for a data-parallel (whole-tile) launch of this shape.
+int pick_bn_dp(int m_act, int n_w, int k);
 // 2-D row-major map [rows, cols], box = 128 bytes of a row x box_rows rows, 128B swizzle.
 bool make_map_2d(CUtensorMap *map, const void *base, bool fp8, int64_t rows, int64_t cols,
                  int box_rows);
+// 3-D bf16 map (dims innermost first, byte strides of dims 1 and 2), 128B
+// swizzle; box[0] * 2 bytes must be 128.
+bool make_map_3d(CUtensorMap *map, const void *base, const int64_t dims[3],
+                 const int64_t strides_bytes[2], const int box[3]);
 // Launches the GEMM. For EPI_TC_PARTIAL, *view receives the partials' layout.
 cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, GemmParams p,
                  cudaStream_t s, Partials *view = nullptr);
