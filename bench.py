@@ -310,27 +310,40 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
     n_new = syn.uniform_ints(1, geom.gamma, n, seed, 2)
     work = []
 
-    def step(t):
-        nonlocal pos, n_new
+    # Every step's inputs (target rows, last tokens, accept counts) are drawn
+    # before the timed region; a step is one propose_batch plus the verify
+    # bookkeeping of every sequence.
+    plan = []
+    for t in range(W + K):
         rows = [tails[i][used[i]:used[i] + n_new[i]] for i in range(n)]
         for i in range(n):
             used[i] += n_new[i]
         newpos = [p + m for p, m in zip(pos, n_new)]
         toks = syn.uniform_ints(0, geom.vocab - 1, n, seed, 900 + t)
-        work.append(batched_work(geom, [p - m for p, m in zip(newpos, n_new)], n_new, nd,
-                                 1 if fp8 else 2))
-        head.propose_batch(states, toks, newpos, rows, nd, bitmask=mask)
         ks = syn.uniform_ints(0, nd, n, seed, 1900 + t)
-        for i in range(n):
-            head.after_verify(states[i], ks[i])
+        plan.append((rows, toks, newpos, ks))
+        if t >= W:
+            work.append(batched_work(geom, [p - m for p, m in zip(newpos, n_new)], n_new, nd,
+                                     1 if fp8 else 2))
         pos = newpos
         n_new = [k + 1 for k in ks]
+    host = [0.0, 0.0]
+
+    def step(t):
+        rows, toks, newpos, ks = plan[t]
+        t0 = time.perf_counter()
+        head.propose_batch(states, toks, newpos, rows, nd, bitmask=mask)
+        t1 = time.perf_counter()
+        for i in range(n):
+            head.after_verify(states[i], ks[i])
+        host[0] += t1 - t0
+        host[1] += time.perf_counter() - t1
 
     for t in range(W):
         step(t)
+    host[0] = host[1] = 0.0
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    work.clear()
     torch.cuda.synchronize()
     e0.record(s)
     for t in range(W, W + K):
@@ -346,6 +359,7 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
             "batch": n, "gamma": geom.gamma, "num_drafts": nd, "steps": K, "warmup": W,
             "ctx": f"U[{ctx_lo},{ctx_hi}]", "bitmask": use_mask, "fp8_kv_and_lm_head": fp8,
             "flops_per_step": flops, "bytes_per_step": byts,
+            "propose_call_us": 1e6 * host[0] / K, "verify_calls_us": 1e6 * host[1] / K,
             "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": tf,
                          "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / tf,
                          "peak_source": f"{src} bf16_tflops (burst)",

@@ -139,8 +139,9 @@ __device__ __forceinline__ void load_kv_tile(const AttnArgs &a, const AttnItem &
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
-  if ((int)blockIdx.x >= a.counts[0]) return;   // grid sized for the capacity
   pdl_trigger();
+  if (threadIdx.x == 0) l2_prefetch_part(a.pf, blockIdx.x, gridDim.x);
+  if ((int)blockIdx.x >= a.counts[0]) return;   // grid sized for the capacity
   pdl_wait();
   constexpr int LD = Smem<D>::LD;
   constexpr int NT = D / 8;          // n8 tiles across the head dim (output)

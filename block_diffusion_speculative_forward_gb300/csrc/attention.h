@@ -42,6 +42,7 @@ struct AttnArgs {
   // tensor-core kernel: CTA b runs items [cta_off[b], cta_off[b + 1])
   const int32_t *cta_off;
   int grid_tc;
+  L2Prefetch pf;              // weights of the next GEMMs
 };
 
 // TMA maps of the tensor-core kernel's operands (ok = false: not supported).

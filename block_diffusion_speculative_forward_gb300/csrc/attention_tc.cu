@@ -48,11 +48,11 @@ constexpr int TILE_BYTES = OFF_KV + KV_STAGES * STAGE_BYTES;   // 192 KB
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;               // two 64-column S buffers
-constexpr uint32_t TMEM_O = 128;             // two 128-column O buffers
+constexpr uint32_t TMEM_O = 128;             // two 128-column O accumulators (items alternate)
 
 struct Bars {
   uint64_t q_full[2], q_empty[2], kv_full[KV_STAGES], kv_empty[KV_STAGES];
-  uint64_t s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2], drain;
+  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_free[2], drain;
   uint32_t tmem_base;
   uint32_t q_issued, q_parity, kv_issued, kv_parity;
   int abort_flag;
@@ -115,6 +115,22 @@ __device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t lbo, 
   return d;
 }
 
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -140,8 +156,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&bar->s_full[b]), 1);
       mbar_init(smem_u32(&bar->s_empty[b]), 4);
       mbar_init(smem_u32(&bar->p_full[b]), 4);
-      mbar_init(smem_u32(&bar->o_full[b]), 1);
-      mbar_init(smem_u32(&bar->o_empty[b]), 4);
+      mbar_init(smem_u32(&bar->p_empty[b]), 1);
+      mbar_init(smem_u32(&bar->o_free[b]), 4);
     }
     for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(smem_u32(&bar->kv_full[s]), 1);
@@ -154,6 +170,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
+    l2_prefetch_part(a.pf, blockIdx.x, gridDim.x);
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_q) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_pool) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_kb) : "memory");
@@ -261,21 +278,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0;
       uint32_t kv_phase = 0;
       int T = 0, qi = 0;
-      bool have_prev = false;
-      int prev_T = 0, prev_stage = 0;
+      bool have_prev = false, prev_first = false;
+      int prev_T = 0, prev_stage = 0, prev_qi = 0;
       uint32_t prev_gm = 0;
       bool ok = true;
-      // O_T = P_T V_T for the tile issued before
-      auto issue_pv = [&](int t, int st, uint32_t gm) -> bool {
-        const int pb = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!mbar_wait(smem_u32(&bar->p_full[pb]), ph, abort_flag)) return false;
-        if (!mbar_wait(smem_u32(&bar->o_empty[pb]), ph ^ 1, abort_flag)) return false;
+      // O[item % 2] (+)= P_t V_t; the item's first tile starts the accumulator
+      auto issue_pv = [&](int t, int st, uint32_t gm, int item, bool first) -> bool {
+        const int pb = t & 1, ob = item & 1;
+        if (!mbar_wait(smem_u32(&bar->p_full[pb]), (t >> 1) & 1, abort_flag)) return false;
+        if (first && !mbar_wait(smem_u32(&bar->o_free[ob]), ((item >> 1) & 1) ^ 1, abort_flag))
+          return false;
         tc_fence_after();
-        const uint32_t d = tmem + TMEM_O + pb * AD;
+        const uint32_t d = tmem + TMEM_O + ob * AD;
         const uint32_t pa = base + OFF_P + pb * P_BYTES;
         const uint32_t vb = base + OFF_KV + st * STAGE_BYTES + KT_BYTES;
-        uint32_t acc = 0;
+        uint32_t acc = first ? 0u : 1u;
 #pragma unroll
         for (int kq = 0; kq < AK / 16; ++kq) {
           if (!((gm >> kq) & 1u)) continue;
@@ -283,7 +300,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     idesc_o, acc);
           acc = 1;
         }
-        umma_commit(smem_u32(&bar->o_full[pb]));
+        umma_commit(smem_u32(&bar->p_empty[pb]));
         umma_commit(smem_u32(&bar->kv_empty[st]));
         return true;
       };
@@ -311,53 +328,43 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           umma_commit(smem_u32(&bar->s_full[sbuf]));
           if (j == ig.ntiles - 1) umma_commit(smem_u32(&bar->q_empty[qb]));
-          if (have_prev && !issue_pv(prev_T, prev_stage, prev_gm)) { ok = false; break; }
+          if (have_prev && !issue_pv(prev_T, prev_stage, prev_gm, prev_qi, prev_first)) {
+            ok = false;
+            break;
+          }
           have_prev = true;
           prev_T = T;
           prev_stage = stage;
           prev_gm = group_mask(ig, j);
+          prev_qi = qi;
+          prev_first = (j == 0);
           if (++stage == KV_STAGES) {
             stage = 0;
             kv_phase ^= 1;
           }
         }
       }
-      if (ok && have_prev && !*abort_flag) issue_pv(prev_T, prev_stage, prev_gm);
+      if (ok && have_prev && !*abort_flag) issue_pv(prev_T, prev_stage, prev_gm, prev_qi, prev_first);
     }
   } else {
     // ------------------------------------------------ softmax -----------
+    // Scores in log2 units (x = s * scale * log2 e, p = 2^(x - m)). O
+    // accumulates in TMEM over the item's tiles relative to the reference
+    // max m; m moves (and O, l are rescaled) only when a tile's max exceeds
+    // it by more than 2^8, so P stays <= 256 and most tiles touch no O.
+    constexpr float TAU = 8.f;
+    const float scale2 = a.scale * 1.4426950408889634f;
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
     const int r = q4 * 32 + lane;            // query vector of this thread
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    int T = 0;
+    int T = 0, qi = 0;
     bool ok = true;
-    for (int c = c_begin; c < c_end && ok; ++c) {
+    for (int c = c_begin; c < c_end && ok; ++c, ++qi) {
       const AttnItem it = a.items[c];
       const ItemGeo ig = item_geo(it, a.seq[it.s], g.gamma);
-      float o[AD];
-#pragma unroll
-      for (int e = 0; e < AD; ++e) o[e] = 0.f;
-      float m = -INFINITY, l = 0.f, pend_corr = 0.f;
-      // folds O of tile t into o (o was relative to the previous max)
-      auto fold_o = [&](int t, float corr) -> bool {
-        const int ob = t & 1;
-        if (!mbar_wait(smem_u32(&bar->o_full[ob]), (t >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[64];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tmem_ld16_nowait(tmem + lane_off + TMEM_O + ob * AD + hh * 64 + 16 * i, v + 16 * i);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 64; ++e) o[hh * 64 + e] = fmaf(o[hh * 64 + e], corr, v[e]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar->o_empty[ob]));
-        return true;
-      };
+      const int ob = qi & 1;
+      const uint32_t o_col = tmem + lane_off + TMEM_O + ob * AD;
+      float m = -INFINITY, l = 0.f;
       for (int j = 0; j < ig.ntiles; ++j, ++T) {
         const int sbuf = T & 1;
         if (!mbar_wait(smem_u32(&bar->s_full[sbuf]), (T >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -372,16 +379,52 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(smem_u32(&bar->s_empty[sbuf]));
         const int kbase = ig.p0 + j * AK;
         float tmax = -INFINITY;
+        if (kbase >= ig.lo && kbase + AK <= ig.hi) {
 #pragma unroll
-        for (int cc = 0; cc < AK; ++cc) {
-          const int key = kbase + cc;
-          const float v = (key >= ig.lo && key < ig.hi) ? x[cc] * a.scale : -INFINITY;
-          x[cc] = v;
-          tmax = fmaxf(tmax, v);
+          for (int cc = 0; cc < AK; ++cc) {
+            x[cc] *= scale2;
+            tmax = fmaxf(tmax, x[cc]);
+          }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < AK; ++cc) {
+            const int key = kbase + cc;
+            x[cc] = (key >= ig.lo && key < ig.hi) ? x[cc] * scale2 : -INFINITY;
+            tmax = fmaxf(tmax, x[cc]);
+          }
         }
-        const float m_new = fmaxf(m, tmax);
-        const float mm = (m_new == -INFINITY) ? 0.f : m_new;
-        const float corr = __expf(m - mm);   // 0 while m is -inf
+        if (tmax > m + TAU) {
+          if (m != -INFINITY) {
+            // O holds tiles < T: wait for PV(T-1), then rescale it in TMEM
+            const int t1 = T - 1;
+            if (!mbar_wait(smem_u32(&bar->p_empty[t1 & 1]), (t1 >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float fac = ex2f(m - tmax);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float v[64];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) tmem_ld16_nowait(o_col + hh * 64 + 16 * i, v + 16 * i);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 64; ++e) v[e] *= fac;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) tmem_st16(o_col + hh * 64 + 16 * i, v + 16 * i);
+            }
+            tmem_wait_st();
+            l *= fac;
+          }
+          m = tmax;
+        }
+        const float mm = (m == -INFINITY) ? 0.f : m;
+        // P buffer of this tile was last read by PV(T-2)
+        if (T >= 2 && !mbar_wait(smem_u32(&bar->p_empty[sbuf]), ((T - 2) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         float s0 = 0.f, s1 = 0.f;
         // P row (bf16) in the 128B-swizzled K-major layout: 16-byte chunk ch
         // of row r sits at chunk position ch ^ (r % 8)
@@ -390,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int ch = 0; ch < AK / 8; ++ch) {
           float p[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) p[e] = __expf(x[ch * 8 + e] - mm);
+          for (int e = 0; e < 8; ++e) p[e] = ex2f(x[ch * 8 + e] - mm);
           s0 += (p[0] + p[1]) + (p[2] + p[3]);
           s1 += (p[4] + p[5]) + (p[6] + p[7]);
           const uint32_t w0 = pack_bf16(p[0], p[1]), w1 = pack_bf16(p[2], p[3]);
@@ -400,41 +443,56 @@ __global__ void __launch_bounds__(THREADS, 1)
                        "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                        : "memory");
         }
-        l = l * corr + (s0 + s1);
+        l += s0 + s1;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar->p_full[sbuf]));
-        if (j > 0 && !fold_o(T - 1, pend_corr)) { ok = false; break; }
-        pend_corr = corr;
-        m = m_new;
       }
-      if (!ok || !fold_o(T - 1, pend_corr)) {
+      if (!ok) break;
+      // the item's last PV, then O out of TMEM
+      const int tl = T - 1;
+      if (!mbar_wait(smem_u32(&bar->p_empty[tl & 1]), (tl >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
-      if (r < n_q) {
-        if (it.slot < 0) {
-          const float inv = 1.f / l;
-          bf16 *orow = a.o + ((int64_t)(it.s * g.gamma + r / grp) * g.nq + it.g * grp + r % grp) * AD;
+      tc_fence_after();
+      const float m_nat = m * 0.6931471805599453f;
+      const bool write = r < n_q;
+      const float inv = 1.f / l;
+      bf16 *orow = a.o + ((int64_t)(it.s * g.gamma + r / grp) * g.nq + it.g * grp + r % grp) * AD;
+      float *ws = a.ws + (int64_t)(it.slot < 0 ? 0 : it.slot) * a.slot_floats;
 #pragma unroll
-          for (int e = 0; e < AD; e += 8) {
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[64];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld16_nowait(o_col + hh * 64 + 16 * i, v + 16 * i);
+        tmem_wait_ld();
+        if (!write) continue;
+        if (it.slot < 0) {
+#pragma unroll
+          for (int e = 0; e < 64; e += 8) {
             uint4 w;
-            w.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
-            w.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
-            w.z = pack_bf16(o[e + 4] * inv, o[e + 5] * inv);
-            w.w = pack_bf16(o[e + 6] * inv, o[e + 7] * inv);
-            *reinterpret_cast<uint4 *>(orow + e) = w;
+            w.x = pack_bf16(v[e] * inv, v[e + 1] * inv);
+            w.y = pack_bf16(v[e + 2] * inv, v[e + 3] * inv);
+            w.z = pack_bf16(v[e + 4] * inv, v[e + 5] * inv);
+            w.w = pack_bf16(v[e + 6] * inv, v[e + 7] * inv);
+            *reinterpret_cast<uint4 *>(orow + hh * 64 + e) = w;
           }
         } else {
-          float *ws = a.ws + (int64_t)it.slot * a.slot_floats;
-          float *arow = ws + (int64_t)r * AD;
+          float *arow = ws + (int64_t)r * AD + hh * 64;
 #pragma unroll
-          for (int e = 0; e < AD; e += 4)
-            *reinterpret_cast<float4 *>(arow + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-          ws[(int64_t)n_q * AD + r] = m;
-          ws[(int64_t)n_q * AD + n_q + r] = l;
+          for (int e = 0; e < 64; e += 4)
+            *reinterpret_cast<float4 *>(arow + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
       }
+      if (write && it.slot >= 0) {
+        ws[(int64_t)n_q * AD + r] = m_nat;
+        ws[(int64_t)n_q * AD + n_q + r] = l;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar->o_free[ob]));
     }
   }
 

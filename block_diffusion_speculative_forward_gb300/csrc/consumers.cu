@@ -8,6 +8,8 @@
 // layers, rms_norm_eps, rotary_dim, yarn_inv_freq.
 #include "consumers.h"
 
+#include <cooperative_groups.h>
+
 namespace dfl {
 
 namespace {
@@ -21,6 +23,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // One block of 1024 threads per row: x[a] (+)= y[a]; out = bf16(g * x / rms(x)).
 __global__ void __launch_bounds__(1024) k_add_norm(AddNormArgs p) {
   pdl_trigger();
+  if (threadIdx.x == 0) l2_prefetch_part(p.pf, blockIdx.x, gridDim.x);
   pdl_wait();
   __shared__ float sh[32];
   __shared__ TileRange tr[32];
@@ -70,11 +73,87 @@ __global__ void __launch_bounds__(1024) k_add_norm(AddNormArgs p) {
   }
 }
 
+// Few rows: a cluster of CL CTAs per row, each CTA holding n / CL features
+// (a warp's 32 features lie in one 128-feature tile). Each CTA reduces its
+// sum of squares; the row total comes from the peers' shared memory.
+constexpr int NORM_CL = 8;
+__global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
+  namespace cg = cooperative_groups;
+  pdl_trigger();
+  if (threadIdx.x == 0) l2_prefetch_part(p.pf, blockIdx.x, gridDim.x);
+  pdl_wait();
+  __shared__ float red[8];
+  __shared__ float cta_ss;
+  cg::cluster_group cl = cg::this_cluster();
+  const int a = blockIdx.x / NORM_CL;
+  const int part = (int)cl.block_rank();
+  const int n = p.n, per = n / NORM_CL;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int MAXE = 2;   // up to 512 features per CTA
+  float xv[MAXE];
+  float ss = 0.f;
+#pragma unroll
+  for (int t = 0; t < MAXE; ++t) {
+    const int fl = threadIdx.x + t * 256;
+    const int f = part * per + fl;
+    xv[t] = 0.f;
+    if (fl < per) {
+      float v = p.x ? p.x[(int64_t)a * n + f] : 0.f;
+      if (p.has_y) {
+        if (p.y.ws) {
+          const TileRange tr = part_range(p.y, part_tile(p.y, a, f & ~31));
+          v += part_sum(p.y, tr, a, f);
+        } else {
+          v += p.y.dense[(int64_t)a * p.y.ld + f];
+        }
+      }
+      xv[t] = v;
+      ss += v * v;
+    }
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w];
+    cta_ss = t;
+  }
+  cl.sync();
+  float tot = 0.f;
+#pragma unroll
+  for (int r = 0; r < NORM_CL; ++r) tot += *cl.map_shared_rank(&cta_ss, r);
+  const float inv = rsqrtf(tot / (float)n + p.eps);
+  int drow = -1;
+  if (p.z) {
+    const int i = a % p.gamma;
+    if (i >= 1 && i <= p.nd) drow = (a / p.gamma) * p.nd + (i - 1);
+  }
+#pragma unroll
+  for (int t = 0; t < MAXE; ++t) {
+    const int fl = threadIdx.x + t * 256;
+    const int f = part * per + fl;
+    if (fl < per) {
+      const float v = xv[t];
+      if (p.x && p.has_y) p.x[(int64_t)a * n + f] = v;
+      if (p.x_tap) p.x_tap[(int64_t)a * n + f] = v;
+      const bf16 h = __float2bfloat16_rn(__bfloat162float(p.g[f]) * (v * inv));
+      if (p.out) p.out[(int64_t)a * n + f] = h;
+      if (p.z_tap) p.z_tap[(int64_t)a * n + f] = h;
+      if (drow >= 0) p.z[(int64_t)drow * n + f] = h;
+    }
+  }
+  cl.sync();   // peers have read cta_ss
+}
+
 // Warp per (row, head): q and k heads take RMSNorm with their gain and RoPE at
 // the row's position; v is rounded to bf16.
 template <int NP>
 __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
   pdl_trigger();
+  if (threadIdx.x == 0)
+    l2_prefetch_part(p.pf, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y);
   pdl_wait();
   const Geo &g = p.g;
   const int r = blockIdx.x;
@@ -85,12 +164,17 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
   if (head < g.nq + g.nkv) {
     const bool is_q = head < g.nq;
     const int base = is_q ? head * d : g.nq * d + (head - g.nq) * d;
+    // the head's features lie in one 128-feature tile (d divides 128 or
+    // equals it): one contributor range for the warp
+    TileRange tr{};
+    if (p.y.ws) tr = part_range(p.y, part_tile(p.y, r, base));
     float v[2 * NP];
     float ss = 0.f;
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
-      v[2 * t] = part_value(p.y, r, base + lane + 32 * t);
-      v[2 * t + 1] = part_value(p.y, r, base + lane + 32 * t + half);
+      const int f0 = base + lane + 32 * t, f1 = f0 + half;
+      v[2 * t] = p.y.ws ? part_sum(p.y, tr, r, f0) : p.y.dense[(int64_t)r * p.y.ld + f0];
+      v[2 * t + 1] = p.y.ws ? part_sum(p.y, tr, r, f1) : p.y.dense[(int64_t)r * p.y.ld + f1];
       ss += v[2 * t] * v[2 * t] + v[2 * t + 1] * v[2 * t + 1];
     }
     ss = warp_sum(ss);
@@ -118,10 +202,21 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
 // u[a, f] = silu(gate) * up with gate/up rows alternating (2f gate, 2f+1 up).
 __global__ void __launch_bounds__(256) k_swiglu_part(SwigluArgs p) {
   pdl_trigger();
+  if (threadIdx.x == 0)
+    l2_prefetch_part(p.pf, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y);
   pdl_wait();
   const int a = blockIdx.x;
   for (int f = blockIdx.y * 256 + threadIdx.x; f < p.I; f += gridDim.y * 256) {
-    const float gt = part_value(p.y, a, 2 * f), up = part_value(p.y, a, 2 * f + 1);
+    // a warp's 32 features are 64 consecutive gate/up rows: one 128-row tile
+    float gt, up;
+    if (p.y.ws) {
+      const TileRange tr = part_range(p.y, part_tile(p.y, a, 2 * (f & ~31)));
+      gt = part_sum(p.y, tr, a, 2 * f);
+      up = part_sum(p.y, tr, a, 2 * f + 1);
+    } else {
+      gt = p.y.dense[(int64_t)a * p.y.ld + 2 * f];
+      up = p.y.dense[(int64_t)a * p.y.ld + 2 * f + 1];
+    }
     p.u[(int64_t)a * p.I + f] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
   }
 }
@@ -131,6 +226,10 @@ __global__ void __launch_bounds__(256) k_swiglu_part(SwigluArgs p) {
 cudaError_t add_norm(const AddNormArgs &p, int rows, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (p.n > 4 * 1024) return cudaErrorInvalidValue;
+  // fewer rows than a quarter of the SMs: spread each row over a cluster
+  const int per = p.n / NORM_CL;
+  if (rows * 4 <= tc::num_sms() && p.n % NORM_CL == 0 && per % 32 == 0 && per <= 512)
+    return launch_pdl_cluster(k_add_norm_cl, dim3(rows * NORM_CL), dim3(256), 0, s, NORM_CL, p);
   return launch_pdl(k_add_norm, dim3(rows), dim3(1024), 0, s, p);
 }
 

@@ -761,14 +761,16 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
     m.ws = (int32_t)window_start(h, positions[i]);
     m.token = (int32_t)last_tokens[i];
     m.page_base = (int32_t)page_ids.size();
-    if (m.ws < m.pos)
-      for (int64_t b = m.ws / c.kv_block; b <= (m.pos - 1) / c.kv_block; ++b) {
-        auto it = st->pages.find(b);
-        if (it == st->pages.end())
+    if (m.ws < m.pos) {
+      // the window's pages are consecutive keys of the ordered page map
+      auto it = st->pages.lower_bound(m.ws / c.kv_block);
+      for (int64_t b = m.ws / c.kv_block; b <= (m.pos - 1) / c.kv_block; ++b, ++it) {
+        if (it == st->pages.end() || it->first != b)
           return fail(DFLASH_ESTATE, "internal: window page %lld of sequence %d missing",
                       (long long)b, i);
         page_ids.push_back(it->second);
       }
+    }
   }
   std::vector<AttnItem> items;
   std::vector<AttnPair> pairs;

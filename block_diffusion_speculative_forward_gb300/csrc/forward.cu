@@ -270,8 +270,9 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
 
 namespace {
 // One tensor-core GEMM: out[m_act, n_w] (epi)= act[m_act, k] * W[n_w, k]^T.
+// dp: whole tiles per CTA, tile width from the data-parallel cost model.
 cudaError_t tc_gemm(const Buffers &B, const CUtensorMap &map_w, ActBuf act, int m_act, int n_w,
-                    int k, int epi, void *out, int ldo, cudaStream_t s) {
+                    int k, int epi, void *out, int ldo, cudaStream_t s, bool dp = false) {
   GemmParams p{};
   p.m_act = m_act;
   p.n_w = n_w;
@@ -282,7 +283,8 @@ cudaError_t tc_gemm(const Buffers &B, const CUtensorMap &map_w, ActBuf act, int 
   p.ws = B.ws;
   p.counters = B.counters;
   p.status = B.status;
-  const int bn = tc::pick_bn(m_act);
+  p.dp = dp;
+  const int bn = dp ? tc::pick_bn_dp(m_act, n_w, k) : tc::pick_bn(m_act);
   return tc::gemm(map_w, B.act_map[act][bn_index(bn)], bn, p, s);
 }
 }  // namespace
@@ -367,6 +369,16 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   // does not fit the shape.
   Partials pending{};
   bool has_pending = false;
+  // weight bytes of each layer GEMM, prefetched into L2 by the latency-bound
+  // kernel before it
+  const uint64_t b_qkv = (uint64_t)g.qkv_w * g.H * 2, b_o = (uint64_t)g.H * qd * 2;
+  const uint64_t b_gu = (uint64_t)2 * g.I * g.H * 2, b_down = (uint64_t)g.H * g.I * 2;
+  auto pf1 = [](const void *p, uint64_t n) {
+    L2Prefetch f;
+    f.p[0] = p;
+    f.bytes[0] = n;
+    return f;
+  };
   for (int l = 0; l < g.L; ++l) {
     const LayerW &L = W.layers[l];
     {
@@ -379,6 +391,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       an.n = g.H;
       an.out = B.h;
       an.x_tap = B.tap_x ? B.tap_x + (size_t)l * R * g.H : nullptr;
+      an.pf = pf1(L.w_qkv, b_qkv);
       LK(add_norm(an, R, s));
     }
     const bool part = !dp && tc::partial_ok(R, g.qkv_w, g.H);
@@ -408,6 +421,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       qp.q = B.q;
       qp.kb = B.kb;
       qp.vb = B.vb;
+      qp.pf = pf1(L.w_o, b_o);
       LK(qkv_post(qp, R, s));
     } else if (part) {
       // QKV partials, then per-head q/k RMSNorm + RoPE
@@ -423,6 +437,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       qp.q = B.q;
       qp.kb = B.kb;
       qp.vb = B.vb;
+      qp.pf = pf1(L.w_o, b_o);
       LK(qkv_post(qp, R, s));
     } else {
       // QKV with per-head q/k RMSNorm + RoPE fused in the epilogue
@@ -472,6 +487,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       a.status = B.status;
       a.cta_off = cm.cta_off;
       a.grid_tc = B.attn_grid_tc;
+      a.pf = pf1(L.w_gu, b_gu);
       if (B.attn_maps.ok) {
         LK(attention_tc(a, B.attn_maps, s));
         LK(attention_merge(a, s));
@@ -505,6 +521,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       if (rc) return rc;
       sp.I = g.I;
       sp.u = B.u;
+      sp.pf = pf1(L.w_down, b_down);
       LK(swiglu_part(sp, R, s));
     } else {
       // gate/up with SwiGLU fused in the epilogue
