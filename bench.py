@@ -172,18 +172,21 @@ def run_ours(args):
     # captured per launch shape, and the probe is part of the shape)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pb, pe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    pb.record(stream)   # creates the events so their handles exist
-    pe.record(stream)
+    sb, se = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in (pb, pe, sb, se):
+        e.record(stream)   # creates the events so their handles exist
     torch.cuda.synchronize()
     import ctypes as C
     lib.dflash_debug_set_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
+    lib.dflash_debug_set_step_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
     lib.dflash_debug_launch_count.restype = C.c_int64
     lib.dflash_debug_set_probe(head.ptr, C.c_void_p(pb.cuda_event), C.c_void_p(pe.cuda_event))
+    lib.dflash_debug_set_step_probe(head.ptr, C.c_void_p(sb.cuda_event), C.c_void_p(se.cuda_event))
     for _ in range(W):
         step(rows_dev[used:used + 1])
         used += 1
     # device-timed region, inputs resident
-    probe_ms = []
+    probe_ms, dev_ms = [], []
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -194,10 +197,12 @@ def run_ours(args):
             step(rows_dev[used:used + 1])
             used += 1
             probe_ms.append(pb.elapsed_time(pe))
+            dev_ms.append(sb.elapsed_time(se))
         ev1.record(stream)
         torch.cuda.synchronize()
     launches = lib.dflash_debug_launch_count() - launches0
     lib.dflash_debug_set_probe(head.ptr, None, None)
+    lib.dflash_debug_set_step_probe(head.ptr, None, None)
     t_ms = ev0.elapsed_time(ev1)
     # end to end through the public call, host buffers: H2D of the step's new
     # row from pinned memory inside the timed region; drafts come back to host.
@@ -243,6 +248,7 @@ def run_ours(args):
                           "achieved_gbs": step_bytes(geom, ctx, 1) / (t_ms / K * 1e-3) / 1e9,
                           "frac_of_hbm": step_bytes(geom, ctx, 1) / (t_ms / K * 1e-3) / 1e9 / hbm},
         "propose_us": 1e3 * t_ms / K,
+        "device_us": 1e3 * statistics.median(dev_ms),
         "clocks": clk.summary(),
     }
     head.close()

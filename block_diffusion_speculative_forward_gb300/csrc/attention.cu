@@ -139,9 +139,8 @@ __device__ __forceinline__ void load_kv_tile(const AttnArgs &a, const AttnItem &
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
-  pdl_trigger();
-  if (threadIdx.x == 0) l2_prefetch_part(a.pf, blockIdx.x, gridDim.x);
   if ((int)blockIdx.x >= a.counts[0]) return;   // grid sized for the capacity
+  pdl_trigger();
   pdl_wait();
   constexpr int LD = Smem<D>::LD;
   constexpr int NT = D / 8;          // n8 tiles across the head dim (output)
@@ -330,8 +329,9 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
 }
 
 // One warp per (pair, query vector), 4 per block: combine the pair's chunks.
-// m and l of every chunk are read lane-parallel; the partial rows are read as
-// vectors, independent across chunks.
+// Lane c holds chunk c's (m, l) (32 chunks per round); the weights reach the
+// other lanes by shuffle, and every chunk's partial row is loaded before any
+// is used.
 template <int D>
 __global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
   if ((int)blockIdx.x >= a.counts[1]) return;   // grid sized for the capacity
@@ -346,39 +346,58 @@ __global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
   const int n_q = g.gamma * grp;
   if (qv >= n_q) return;
   const int64_t off_m = (int64_t)n_q * D + qv, off_l = (int64_t)n_q * D + n_q + qv;
+  // max over all chunks
   float M = -INFINITY;
-  for (int c = lane; c < pr.nc; c += 32)
-    M = fmaxf(M, __ldcg(a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats + off_m));
+  for (int c0 = 0; c0 < pr.nc; c0 += 32) {
+    const int c = c0 + lane;
+    if (c < pr.nc) M = fmaxf(M, __ldcg(a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats + off_m));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float l = 0.f;
-  for (int c = lane; c < pr.nc; c += 32) {
-    const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
-    const float m = __ldcg(ws + off_m);
-    l += (m == -INFINITY) ? 0.f : __expf(m - M) * __ldcg(ws + off_l);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   float acc[VPL];
 #pragma unroll
   for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < pr.nc; ++c) {
-    const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
-    const float m = __ldcg(ws + off_m);
-    const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
-    const float *row = ws + (int64_t)qv * D + lane * VPL;
-    if (VPL == 4) {
-      const float4 r = __ldcg(reinterpret_cast<const float4 *>(row));
-      acc[0] += w * r.x;
-      acc[1] += w * r.y;
-      acc[2] += w * r.z;
-      acc[3] += w * r.w;
-    } else {
+  for (int c0 = 0; c0 < pr.nc; c0 += 32) {
+    const int c = c0 + lane;
+    float w = 0.f;
+    if (c < pr.nc) {
+      const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
+      const float m = __ldcg(ws + off_m);
+      w = (m == -INFINITY) ? 0.f : __expf(m - M);
+      l += w * __ldcg(ws + off_l);
+    }
+    const int nc = pr.nc - c0 < 32 ? pr.nc - c0 : 32;
+    // rows of up to 8 chunks in flight, added in chunk order
+    for (int b = 0; b < nc; b += 8) {
+      float4 r[8];
 #pragma unroll
-      for (int e = 0; e < VPL; ++e) acc[e] += w * __ldcg(row + e);
+      for (int u = 0; u < 8; ++u) {
+        if (b + u < nc) {
+          const float *row = a.ws + (int64_t)(pr.slot0 + c0 + b + u) * a.slot_floats +
+                             (int64_t)qv * D + lane * VPL;
+          if constexpr (VPL == 4) r[u] = __ldcg(reinterpret_cast<const float4 *>(row));
+          else r[u] = make_float4(__ldcg(row), __ldcg(row + 1), 0.f, 0.f);
+        } else {
+          r[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, w, (b + u) & 31);
+        if (b + u < nc) {
+          acc[0] += wu * r[u].x;
+          acc[1] += wu * r[u].y;
+          if constexpr (VPL == 4) {
+            acc[2] += wu * r[u].z;
+            acc[3] += wu * r[u].w;
+          }
+        }
+      }
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = 1.f / l;
   bf16 *orow = a.o + ((int64_t)(pr.s * g.gamma + qv / grp) * g.nq + pr.g * grp + qv % grp) * D +
                lane * VPL;

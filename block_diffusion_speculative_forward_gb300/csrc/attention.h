@@ -37,12 +37,11 @@ struct AttnArgs {
   int n_pairs;                // grid size: at least the call's pair count
   const int *counts;          // device: [0] items, [1] pairs of this call
   float *ws;                  // partial slots
-  int64_t slot_floats;        // n_q*d + 2*n_q
+  int64_t slot_floats;        // n_q*d + 2*n_q, rounded up to a multiple of 4
   int *status;
   // tensor-core kernel: CTA b runs items [cta_off[b], cta_off[b + 1])
   const int32_t *cta_off;
   int grid_tc;
-  L2Prefetch pf;              // weights of the next GEMMs
 };
 
 // TMA maps of the tensor-core kernel's operands (ok = false: not supported).

@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
-    l2_prefetch_part(a.pf, blockIdx.x, gridDim.x);
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_q) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_pool) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_kb) : "memory");

@@ -23,7 +23,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 // One block of 1024 threads per row: x[a] (+)= y[a]; out = bf16(g * x / rms(x)).
 __global__ void __launch_bounds__(1024) k_add_norm(AddNormArgs p) {
   pdl_trigger();
-  if (threadIdx.x == 0) l2_prefetch_part(p.pf, blockIdx.x, gridDim.x);
   pdl_wait();
   __shared__ float sh[32];
   __shared__ TileRange tr[32];
@@ -80,7 +79,6 @@ constexpr int NORM_CL = 8;
 __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
   namespace cg = cooperative_groups;
   pdl_trigger();
-  if (threadIdx.x == 0) l2_prefetch_part(p.pf, blockIdx.x, gridDim.x);
   pdl_wait();
   __shared__ float red[8];
   __shared__ float cta_ss;
@@ -152,8 +150,6 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
 template <int NP>
 __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
   pdl_trigger();
-  if (threadIdx.x == 0)
-    l2_prefetch_part(p.pf, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y);
   pdl_wait();
   const Geo &g = p.g;
   const int r = blockIdx.x;
@@ -168,6 +164,17 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
     // equals it): one contributor range for the warp
     TileRange tr{};
     if (p.y.ws) tr = part_range(p.y, part_tile(p.y, r, base));
+    // gains and the rotation, loaded while the partials are in flight
+    const bf16 *gain = is_q ? p.q_norm : p.k_norm;
+    float gn[2 * NP], cs[NP], sn[NP];
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+      const int i = lane + 32 * t;
+      gn[2 * t] = __bfloat162float(gain[i]);
+      gn[2 * t + 1] = __bfloat162float(gain[i + half]);
+      cs[t] = p.cos_t[(int64_t)pos * half + i];
+      sn[t] = p.sin_t[(int64_t)pos * half + i];
+    }
     float v[2 * NP];
     float ss = 0.f;
 #pragma unroll
@@ -179,31 +186,33 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
     }
     ss = warp_sum(ss);
     const float inv = rsqrtf(ss / (float)d + g.eps);
-    const bf16 *gain = is_q ? p.q_norm : p.k_norm;
     bf16 *dst = is_q ? p.q + (int64_t)r * g.nq * d + head * d
                      : p.kb + (int64_t)r * g.kv + (head - g.nq) * d;
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
       const int i = lane + 32 * t;
-      const float x1 = __bfloat162float(gain[i]) * (v[2 * t] * inv);
-      const float x2 = __bfloat162float(gain[i + half]) * (v[2 * t + 1] * inv);
-      const float c = p.cos_t[(int64_t)pos * half + i], sn = p.sin_t[(int64_t)pos * half + i];
-      dst[i] = __float2bfloat16_rn(x1 * c - x2 * sn);
-      dst[i + half] = __float2bfloat16_rn(x2 * c + x1 * sn);
+      const float x1 = gn[2 * t] * (v[2 * t] * inv);
+      const float x2 = gn[2 * t + 1] * (v[2 * t + 1] * inv);
+      dst[i] = __float2bfloat16_rn(x1 * cs[t] - x2 * sn[t]);
+      dst[i + half] = __float2bfloat16_rn(x2 * cs[t] + x1 * sn[t]);
     }
   }
   if (blockIdx.y == 0) {
+    // v rows: a warp's 32 consecutive features share one tile
     const int vbase = g.nq * d + g.kv;
-    for (int e = threadIdx.x; e < g.kv; e += blockDim.x)
-      p.vb[(int64_t)r * g.kv + e] = __float2bfloat16_rn(part_value(p.y, r, vbase + e));
+    for (int e = threadIdx.x; e < g.kv; e += blockDim.x) {
+      const int f = vbase + e;
+      float y;
+      if (p.y.ws) y = part_sum(p.y, part_range(p.y, part_tile(p.y, r, f & ~31)), r, f);
+      else y = p.y.dense[(int64_t)r * p.y.ld + f];
+      p.vb[(int64_t)r * g.kv + e] = __float2bfloat16_rn(y);
+    }
   }
 }
 
 // u[a, f] = silu(gate) * up with gate/up rows alternating (2f gate, 2f+1 up).
 __global__ void __launch_bounds__(256) k_swiglu_part(SwigluArgs p) {
   pdl_trigger();
-  if (threadIdx.x == 0)
-    l2_prefetch_part(p.pf, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y);
   pdl_wait();
   const int a = blockIdx.x;
   for (int f = blockIdx.y * 256 + threadIdx.x; f < p.I; f += gridDim.y * 256) {

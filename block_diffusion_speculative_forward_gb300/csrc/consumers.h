@@ -18,7 +18,6 @@ struct AddNormArgs {
   bf16 *z_tap;          // [rows, n] copy of the normed rows (or NULL)
   bf16 *z;              // draft rows only: [n_seq * nd, n] (or NULL)
   int nd, gamma;
-  L2Prefetch pf;        // weights of the next GEMMs
 };
 
 struct QkvPostArgs {
@@ -28,14 +27,12 @@ struct QkvPostArgs {
   const bf16 *q_norm, *k_norm;
   const float *cos_t, *sin_t;
   bf16 *q, *kb, *vb;
-  L2Prefetch pf;
 };
 
 struct SwigluArgs {
   Partials y;           // [R, 2I], gate/up rows alternating
   int I;
   bf16 *u;              // [R, I]
-  L2Prefetch pf;
 };
 
 cudaError_t add_norm(const AddNormArgs &p, int rows, cudaStream_t s);

@@ -572,6 +572,13 @@ int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end) {
   return DFLASH_OK;
 }
 
+int dflash_debug_set_step_probe(dflash_handle *h, void *ev_begin, void *ev_end) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  h->b.step_begin = (cudaEvent_t)ev_begin;
+  h->b.step_end = (cudaEvent_t)ev_end;
+  return DFLASH_OK;
+}
+
 int64_t dflash_debug_launch_count(void) { return dfl::launch_count(); }
 
 int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t m, int32_t n_w, int32_t k,
@@ -666,7 +673,8 @@ int run_forward(dflash_handle *h, const CallMeta &cm, int nd, const int32_t *bit
     const std::vector<uintptr_t> key = {
         (uintptr_t)cm.n_seq, (uintptr_t)cm.n_rows, (uintptr_t)nd, (uintptr_t)bitmask,
         (uintptr_t)h->b.tap_x, (uintptr_t)h->b.tap_z, (uintptr_t)h->b.tap_logits,
-        (uintptr_t)h->b.probe_begin, (uintptr_t)h->b.probe_end};
+        (uintptr_t)h->b.probe_begin, (uintptr_t)h->b.probe_end,
+        (uintptr_t)h->b.step_begin,  (uintptr_t)h->b.step_end};
     auto it = h->graphs.find(key);
     if (it == h->graphs.end()) {
       const int64_t l0 = launch_count();

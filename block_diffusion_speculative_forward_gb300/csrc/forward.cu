@@ -214,7 +214,8 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
       g_build_err = "gamma * (num_q_heads / num_kv_heads) must be <= 128";
       return DFLASH_EINVAL;
     }
-    B->attn_slot_floats = (int64_t)n_q * g.d + 2 * n_q;
+    // slots start on 16 bytes (vector stores and loads of partial rows)
+    B->attn_slot_floats = ((int64_t)n_q * g.d + 2 * n_q + 3) & ~(int64_t)3;
     B->attn_slots = 3 * sms + 3 * c.max_batch * g.nkv + 64;
     BA(B->attn_ws, (size_t)B->attn_slots * B->attn_slot_floats);
     // The tensor-core kernel reads whole 16-row blocks of the block K/V
@@ -350,6 +351,7 @@ int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *
 
 int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffers &B,
             const CallMeta &cm, int nd, const int32_t *bitmask, int M_ctx, cudaStream_t s) {
+  if (B.step_begin && B.step_end) FK(cudaEventRecordWithFlags(B.step_begin, s, cudaEventRecordExternal));
   if (cm.n_rows) {
     int rc = ctx_append(g, W, B, cm.rows, cm.n_rows, M_ctx, s);
     if (rc) return rc;
@@ -360,6 +362,10 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   // Many rows: the fused QKV and gate/up GEMMs run whole tiles per CTA
   // (data-parallel, epilogue in the GEMM); few rows: split-K partials read by
   // the consumer kernels, so every SM streams weights.
+  // Many rows: QKV and gate/up run whole tiles per CTA (data-parallel; QKV
+  // stored dense for the q/k pass, SwiGLU in the epilogue). Few rows: every
+  // GEMM is split-K over all SMs (one SM streams only ~35 GB/s from HBM, so
+  // the weight stream needs them all) and the consumers read the partials.
   const bool dp = R > 64;
   const int bn_qkv = dp ? tc::pick_bn_dp(R, g.qkv_w, g.H) : bnR;
   const int bn_gu = dp ? tc::pick_bn_dp(R, 2 * g.I, g.H) : bnR;
@@ -369,16 +375,6 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   // does not fit the shape.
   Partials pending{};
   bool has_pending = false;
-  // weight bytes of each layer GEMM, prefetched into L2 by the latency-bound
-  // kernel before it
-  const uint64_t b_qkv = (uint64_t)g.qkv_w * g.H * 2, b_o = (uint64_t)g.H * qd * 2;
-  const uint64_t b_gu = (uint64_t)2 * g.I * g.H * 2, b_down = (uint64_t)g.H * g.I * 2;
-  auto pf1 = [](const void *p, uint64_t n) {
-    L2Prefetch f;
-    f.p[0] = p;
-    f.bytes[0] = n;
-    return f;
-  };
   for (int l = 0; l < g.L; ++l) {
     const LayerW &L = W.layers[l];
     {
@@ -391,7 +387,6 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       an.n = g.H;
       an.out = B.h;
       an.x_tap = B.tap_x ? B.tap_x + (size_t)l * R * g.H : nullptr;
-      an.pf = pf1(L.w_qkv, b_qkv);
       LK(add_norm(an, R, s));
     }
     const bool part = !dp && tc::partial_ok(R, g.qkv_w, g.H);
@@ -421,7 +416,6 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       qp.q = B.q;
       qp.kb = B.kb;
       qp.vb = B.vb;
-      qp.pf = pf1(L.w_o, b_o);
       LK(qkv_post(qp, R, s));
     } else if (part) {
       // QKV partials, then per-head q/k RMSNorm + RoPE
@@ -437,7 +431,6 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       qp.q = B.q;
       qp.kb = B.kb;
       qp.vb = B.vb;
-      qp.pf = pf1(L.w_o, b_o);
       LK(qkv_post(qp, R, s));
     } else {
       // QKV with per-head q/k RMSNorm + RoPE fused in the epilogue
@@ -487,7 +480,6 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       a.status = B.status;
       a.cta_off = cm.cta_off;
       a.grid_tc = B.attn_grid_tc;
-      a.pf = pf1(L.w_gu, b_gu);
       if (B.attn_maps.ok) {
         LK(attention_tc(a, B.attn_maps, s));
         LK(attention_merge(a, s));
@@ -515,13 +507,15 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       an.out = B.h;
       LK(add_norm(an, R, s));
     }
-    if (!dp && tc::partial_ok(R, 2 * g.I, g.H)) {
+    // gate/up: SwiGLU always in the GEMM's epilogue (whole tiles for many
+    // rows, the split-K fixup for few: one kernel instead of partials plus a
+    // SwiGLU pass)
+    if (false) {
       SwigluArgs sp{};
       int rc = project(B, W.map_gu[l], ACT_H, R, 2 * g.I, g.H, nullptr, &sp.y, s);
       if (rc) return rc;
       sp.I = g.I;
       sp.u = B.u;
-      sp.pf = pf1(L.w_down, b_down);
       LK(swiglu_part(sp, R, s));
     } else {
       // gate/up with SwiGLU fused in the epilogue
@@ -617,6 +611,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   LK(finalize(B.row_id, B.row_p1, n, nd, B.status, (uint32_t *)(B.out_dev + B.off_drafts),
               (int32_t *)(B.out_dev + B.off_nout), (float *)(B.out_dev + B.off_conf),
               (int32_t *)B.out_dev, s));
+  if (B.step_begin && B.step_end) FK(cudaEventRecordWithFlags(B.step_end, s, cudaEventRecordExternal));
   return DFLASH_OK;
 }
 

@@ -55,6 +55,7 @@ struct Buffers {
   bf16 *tap_z = nullptr;
   float *tap_logits = nullptr;
   cudaEvent_t probe_begin = nullptr, probe_end = nullptr;  // around the lm_head stage
+  cudaEvent_t step_begin = nullptr, step_end = nullptr;    // around the whole device step
   CUtensorMap act_map[ACT_COUNT][BN_COUNT];
   float *ws = nullptr;          // stream-K partials
   int *counters = nullptr;      // stream-K tile arrival counters (zero between launches)

@@ -169,59 +169,61 @@ __device__ __forceinline__ void finish16(const GemmParams &p, Smem *sm, const fl
   if (EPI == EPI_TC_QKV) {
     // Per-head RMSNorm (gain q_norm / k_norm) then RoPE over the full head for
     // q and k rows; v rows are stored as they are. A 128-row tile lies in one
-    // region and holds 128 / head_dim whole heads.
+    // region and holds 128 / head_dim whole heads. The rotation of the 16
+    // rows is loaded before the first barrier.
     const int fl = q * 32 + lane;
     const int d = p.head_dim;
     const int tile0 = tm * BM;
+    const int nrows = p.m_act - a0 < 16 ? p.m_act - a0 : 16;
     if (tile0 >= p.q_rows + p.k_rows) {
+      bf16 *dst = p.v_out + (int64_t)a0 * p.k_rows + (f - p.q_rows - p.k_rows);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int a = a0 + c;
-        if (a < p.m_act)
-          p.v_out[(int64_t)a * p.k_rows + (f - p.q_rows - p.k_rows)] = __float2bfloat16_rn(v[c]);
-      }
+      for (int c = 0; c < 16; ++c)
+        if (c < nrows) dst[(int64_t)c * p.k_rows] = __float2bfloat16_rn(v[c]);
       return;
     }
     const bool is_q = tile0 < p.q_rows;
     const bf16 *gain = is_q ? p.q_norm : p.k_norm;
     const int i = fl % d;
-    float ss[16];
+    const int half = d / 2;
+    float cs[16], sn[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      float x2 = v[c] * v[c];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x2 += __shfl_xor_sync(0xffffffffu, x2, o);
-      ss[c] = x2;
+      const int a = a0 + c;
+      const int pos = c < nrows ? p.seq[a / p.gamma].pos + a % p.gamma : 0;
+      cs[c] = p.cos_t[(int64_t)pos * half + (i % half)];
+      sn[c] = p.sin_t[(int64_t)pos * half + (i % half)];
     }
+    const float gi = __bfloat162float(gain[i]);
+    float ss[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) ss[c] = v[c] * v[c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) ss[c] += __shfl_xor_sync(0xffffffffu, ss[c], o);
     if (lane == 0) {
 #pragma unroll
       for (int c = 0; c < 16; ++c) sm->red_v[q][c] = ss[c];
     }
     epi_bar();
-    const float gi = __bfloat162float(gain[i]);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       float tot;
       if (d == 128) tot = sm->red_v[0][c] + sm->red_v[1][c] + sm->red_v[2][c] + sm->red_v[3][c];
       else tot = sm->red_v[q & 2][c] + sm->red_v[(q & 2) + 1][c];   // d == 64: warps {0,1} / {2,3}
-      const float y = gi * (v[c] * rsqrtf(tot / (float)d + p.eps));
-      sm->xch[c][fl] = y;
+      sm->xch[c][fl] = gi * (v[c] * rsqrtf(tot / (float)d + p.eps));
     }
     epi_bar();
-    const int half = d / 2;
+    bf16 *dst = is_q ? p.q_out + (int64_t)a0 * p.q_rows + f
+                     : p.k_out + (int64_t)a0 * p.k_rows + (f - p.q_rows);
+    const int ld = is_q ? p.q_rows : p.k_rows;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const int a = a0 + c;
       const float y = sm->xch[c][fl];
       const float other = sm->xch[c][fl ^ half];
-      if (a < p.m_act) {
-        const int pos = p.seq[a / p.gamma].pos + a % p.gamma;
-        const float cs = p.cos_t[(int64_t)pos * half + (i % half)];
-        const float sn = p.sin_t[(int64_t)pos * half + (i % half)];
-        const float o = (i < half) ? (y * cs - other * sn) : (y * cs + other * sn);
-        if (is_q) p.q_out[(int64_t)a * p.q_rows + f] = __float2bfloat16_rn(o);
-        else p.k_out[(int64_t)a * p.k_rows + (f - p.q_rows)] = __float2bfloat16_rn(o);
-      }
+      const float o = (i < half) ? (y * cs[c] - other * sn[c]) : (y * cs[c] + other * sn[c]);
+      if (c < nrows) dst[(int64_t)c * ld] = __float2bfloat16_rn(o);
     }
     epi_bar();
     return;

@@ -92,33 +92,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// --------------------------------------------------------- L2 prefetch --
-// Up to two byte ranges (weights of the GEMMs that come next) that a
-// latency-bound kernel pulls into L2 while HBM would otherwise idle. Part
-// `part` of `nparts` takes an equal slice of each range; one thread issues
-// it in 64 KB bulk prefetches (no data lands in the SM, nothing waits).
-struct L2Prefetch {
-  const void *p[2] = {nullptr, nullptr};
-  uint64_t bytes[2] = {0, 0};
-};
-__device__ __forceinline__ void l2_prefetch_part(const L2Prefetch &pf, int part, int nparts) {
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if (!pf.p[i] || pf.bytes[i] < 16) continue;
-    const uint64_t total = pf.bytes[i] & ~15ull;
-    const uint64_t slice = ((total + nparts - 1) / nparts + 15) & ~15ull;
-    uint64_t lo = (uint64_t)part * slice;
-    const uint64_t hi = lo + slice < total ? lo + slice : total;
-    for (; lo < hi; lo += 65536) {
-      const uint32_t n = (uint32_t)(hi - lo < 65536 ? hi - lo : 65536);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                       (const char *)pf.p[i] + lo),
-                   "r"(n)
-                   : "memory");
-    }
-  }
-}
-
 // The same with a thread-block cluster of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

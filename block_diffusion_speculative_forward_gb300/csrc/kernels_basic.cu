@@ -157,11 +157,23 @@ __global__ void k_ctx_kv_write(const Partials kv, const RowMeta *__restrict__ ro
     return;
   }
   const int kcol = l * 2 * g.kv + h * d, vcol = kcol + g.kv;
-  float v[2 * NP];
+  // a head's K (and V) columns lie in one 128-column tile: one contributor
+  // range each for the warp; every load is issued before the first use
+  auto val = [&](const TileRange &tr, int f) -> float {
+    return kv.ws ? part_sum(kv, tr, r, f) : kv.dense[(int64_t)r * kv.ld + f];
+  };
+  TileRange trk{}, trv{};
+  if (kv.ws) {
+    trk = part_range(kv, part_tile(kv, r, kcol));
+    trv = part_range(kv, part_tile(kv, r, vcol));
+  }
+  float v[2 * NP], vv[2 * NP];
 #pragma unroll
   for (int t = 0; t < NP; ++t) {
-    v[2 * t] = part_value(kv, r, kcol + lane + 32 * t);
-    v[2 * t + 1] = part_value(kv, r, kcol + lane + 32 * t + half);
+    v[2 * t] = val(trk, kcol + lane + 32 * t);
+    v[2 * t + 1] = val(trk, kcol + lane + 32 * t + half);
+    vv[2 * t] = val(trv, vcol + lane + 32 * t);
+    vv[2 * t + 1] = val(trv, vcol + lane + 32 * t + half);
   }
   norm_rope_warp<NP>(v, k_norm[l], g.eps, d, cos_t + (int64_t)rm.pos * half,
                      sin_t + (int64_t)rm.pos * half);
@@ -176,7 +188,12 @@ __global__ void k_ctx_kv_write(const Partials kv, const RowMeta *__restrict__ ro
       P[ko + i] = float_to_fp8(v[2 * t] / sk);
       P[ko + i + half] = float_to_fp8(v[2 * t + 1] / sk);
     }
-    for (int e = lane; e < d; e += 32) P[vo + e] = float_to_fp8(part_value(kv, r, vcol + e) / sv);
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+      const int i = lane + 32 * t;
+      P[vo + i] = float_to_fp8(vv[2 * t] / sv);
+      P[vo + i + half] = float_to_fp8(vv[2 * t + 1] / sv);
+    }
   } else {
     bf16 *P = (bf16 *)pool;
 #pragma unroll
@@ -185,7 +202,12 @@ __global__ void k_ctx_kv_write(const Partials kv, const RowMeta *__restrict__ ro
       P[ko + i] = __float2bfloat16_rn(v[2 * t]);
       P[ko + i + half] = __float2bfloat16_rn(v[2 * t + 1]);
     }
-    for (int e = lane; e < d; e += 32) P[vo + e] = __float2bfloat16_rn(part_value(kv, r, vcol + e));
+#pragma unroll
+    for (int t = 0; t < NP; ++t) {
+      const int i = lane + 32 * t;
+      P[vo + i] = __float2bfloat16_rn(vv[2 * t]);
+      P[vo + i + half] = __float2bfloat16_rn(vv[2 * t + 1]);
+    }
   }
 }
 

@@ -207,6 +207,9 @@ DFLASH_API int dflash_debug_gather_kv(dflash_handle *h, const dflash_state *st, 
  * and the per-row argmax/confidence reduction), on the call's stream. Events
  * are the caller's cudaEvent_t. NULL, NULL disables it. */
 DFLASH_API int dflash_debug_set_probe(dflash_handle *h, void *ev_begin, void *ev_end);
+/* The same around the whole device part of a propose* (from its first
+ * kernel to its last), separating device time from host time. */
+DFLASH_API int dflash_debug_set_step_probe(dflash_handle *h, void *ev_begin, void *ev_end);
 /* Propose calls replay a CUDA graph captured per launch shape (sequences,
  * new ctx rows, drafts, bitmask and tap/probe pointers); enable = 0 launches
  * the kernels one by one instead (same results). On by default. */
