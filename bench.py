@@ -45,6 +45,22 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(vals, dist, device):
+    """The slowest rank's value of each timing (the job is as slow as it)."""
+    if dist is None:
+        return list(vals)
+    t = torch.tensor([float(v) for v in vals], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def shard(n, rank, world):
+    """Sequences of a sequence-partitioned batch that this rank runs: every
+    sequence is independent given the (replicated) weights, so the shards
+    need no exchange on the data path."""
+    return list(range(rank, n, world))
+
+
 def head_cfg(geom, max_batch, max_seq_len, **kw):
     c = dict(num_layers=geom.num_layers, hidden=geom.hidden, intermediate=geom.intermediate,
              num_q_heads=geom.num_q_heads, num_kv_heads=geom.num_kv_heads,
@@ -216,10 +232,7 @@ def run_ours(args):
         used += 1
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
-    if dist:
-        tt = torch.tensor([t_ms, e2e_s], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms, e2e_s = float(tt[0]), float(tt[1])
+    t_ms, e2e_s = max_over_ranks([t_ms, e2e_s], dist, "cuda")
     hbm, tf, src = peaks()
     lm_ms = statistics.mean(probe_ms)
     lm_bytes = lm_head_bytes(geom, nd)

@@ -52,26 +52,18 @@ __device__ __forceinline__ TileRange part_range(const Partials &P, int t) {
   r.lo_second = part_begin(P.total, P.G, r.c_lo) < i0 ? 1 : 0;
   return r;
 }
-// Partial slots are laid out [slot][bn rows][128 features]. Up to 16
-// contributors are loaded at once (predicated, one memory round trip) and
-// added in ascending CTA order; longer ranges continue four at a time.
+// Partial slots are laid out [slot][bn rows][128 features]; contributors are
+// added in ascending CTA order, four loads in flight.
 __device__ __forceinline__ float part_sum(const Partials &P, const TileRange &r, int a, int f) {
   const float *base = P.ws + (a % P.bn) * 128 + (f & 127);
   const long long stride = (long long)P.bn * 128;
-  const int n = r.c_hi - r.c_lo + 1;
-  float v[16];
+  float s = __ldcg(base + (2 * r.c_lo + r.lo_second) * stride);
+  for (int c = r.c_lo + 1; c <= r.c_hi; c += 4) {
+    float v[4];
 #pragma unroll
-  for (int u = 0; u < 16; ++u)
-    v[u] = u < n ? __ldcg(base + (2 * (r.c_lo + u) + (u == 0 ? r.lo_second : 0)) * stride) : 0.f;
-  float s = v[0];
+    for (int u = 0; u < 4; ++u) v[u] = (c + u <= r.c_hi) ? __ldcg(base + 2 * (c + u) * stride) : 0.f;
 #pragma unroll
-  for (int u = 1; u < 16; ++u) s += v[u];
-  for (int c = r.c_lo + 16; c <= r.c_hi; c += 4) {
-    float w[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) w[u] = (c + u <= r.c_hi) ? __ldcg(base + 2 * (c + u) * stride) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) s += w[u];
+    for (int u = 0; u < 4; ++u) s += v[u];
   }
   return s;
 }
