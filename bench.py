@@ -87,7 +87,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -364,11 +364,12 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    e0.record(s)
-    for t in range(W, W + K):
-        step(t)
-    e1.record(s)
-    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record(s)
+        for t in range(W, W + K):
+            step(t)
+        e1.record(s)
+        torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / K
     flops = sum(f for f, _ in work) / K
     byts = sum(b for _, b in work) / K
@@ -379,6 +380,7 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
             "ctx": f"U[{ctx_lo},{ctx_hi}]", "bitmask": use_mask, "fp8_kv_and_lm_head": fp8,
             "flops_per_step": flops, "bytes_per_step": byts,
             "propose_call_us": 1e6 * host[0] / K, "verify_calls_us": 1e6 * host[1] / K,
+            "clocks": clk.summary(),
             "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": tf,
                          "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / tf,
                          "peak_source": f"{src} bf16_tflops (burst)",
@@ -515,7 +517,7 @@ def run_kernel_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-steps", type=int, default=4)
@@ -527,7 +529,10 @@ def main():
                     help="fp8_b128 adds the 128-sequence FP8 configuration")
     ap.add_argument("--kernel", default=None, choices=["lm_head", "lm_head_b32"],
                     help="time one kernel alone instead of the propose step")
-    ap.add_argument("--lm-traffic", type=float, default=None,
+    # dram__bytes_read.sum + dram__bytes_write.sum of one batch-1 lm_head GEMM
+    # launch (1,018,519,296 + 3,786,752 B), ncu at this workload; re-capture
+    # (or pass None) whenever that kernel changes.
+    ap.add_argument("--lm-traffic", type=float, default=1022306048.0,
                     help="ncu dram bytes per lm_head launch, when captured for this build")
     args = ap.parse_args()
     if args.warmup < 3:
