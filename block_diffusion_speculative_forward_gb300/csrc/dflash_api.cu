@@ -250,7 +250,7 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
                 cudaStream_t s, dfl::CallMeta *out,
                 const std::vector<dfl::AttnItem> &items = {},
                 const std::vector<dfl::AttnPair> &pairs = {},
-                const std::vector<int32_t> &cta_off = {}) {
+                const std::vector<int32_t> &cta_off = {}, size_t *defer_bytes = nullptr) {
   if ((int)seq.size() > h->cap_seq || (int)page_ids.size() > h->cap_pages ||
       (int)items.size() > h->cap_items || (int)pairs.size() > h->cap_pairs ||
       (int)cta_off.size() > h->cap_sched)
@@ -297,9 +297,13 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
     memcpy(h->meta_host + h->off_sched, cta_off.data(), cta_off.size() * sizeof(int32_t));
   if (!rows.empty())
     memcpy(h->meta_host + h->off_rows, rows.data(), rows.size() * sizeof(dfl::RowMeta));
-  CK(cudaMemcpyAsync(h->meta_dev, h->meta_host, total, cudaMemcpyHostToDevice, s));
-  CK(cudaEventRecord(h->meta_ev, s));
-  h->meta_ev_live = true;
+  if (defer_bytes) {
+    *defer_bytes = total;   // the caller's graph (or its own copy) moves it
+  } else {
+    CK(cudaMemcpyAsync(h->meta_dev, h->meta_host, total, cudaMemcpyHostToDevice, s));
+    CK(cudaEventRecord(h->meta_ev, s));
+    h->meta_ev_live = true;
+  }
   out->counts = (const int *)h->meta_dev;
   out->seq = (const dfl::SeqMeta *)(h->meta_dev + h->off_seq);
   out->rows = (const dfl::RowMeta *)(h->meta_dev + h->off_rows);
@@ -667,10 +671,25 @@ namespace dfl {
 // Runs the forward of a call: replays the graph captured for the call's launch
 // shape (capturing it on first use), or launches the kernels directly when
 // graphs are off or the capture fails.
+// The call's metadata upload (meta_bytes from the pinned staging buffer) and
+// the results' download are part of the same graph, so a replay is one
+// launch and one synchronisation.
 int run_forward(dflash_handle *h, const CallMeta &cm, int nd, const int32_t *bitmask,
-                cudaStream_t s) {
+                size_t meta_bytes, cudaStream_t s) {
+  auto body = [&](cudaStream_t st) -> int {
+    if (cudaMemcpyAsync(h->meta_dev, h->meta_host, meta_bytes, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return DFLASH_ECUDA;
+    int rc = forward(h->g, h->cfg, h->w, h->b, cm, nd, bitmask, h->M_ctx, st);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(h->b.out_host, h->b.out_dev, h->b.out_bytes, cudaMemcpyDeviceToHost, st) !=
+        cudaSuccess)
+      return DFLASH_ECUDA;
+    return DFLASH_OK;
+  };
   if (h->use_graphs) {
     const std::vector<uintptr_t> key = {
+        (uintptr_t)meta_bytes,
         (uintptr_t)cm.n_seq, (uintptr_t)cm.n_rows, (uintptr_t)nd, (uintptr_t)bitmask,
         (uintptr_t)h->b.tap_x, (uintptr_t)h->b.tap_z, (uintptr_t)h->b.tap_logits,
         (uintptr_t)h->b.probe_begin, (uintptr_t)h->b.probe_end,
@@ -681,8 +700,7 @@ int run_forward(dflash_handle *h, const CallMeta &cm, int nd, const int32_t *bit
       cudaGraph_t graph = nullptr;
       cudaGraphExec_t exec = nullptr;
       bool ok = cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed) == cudaSuccess;
-      int rc = ok ? forward(h->g, h->cfg, h->w, h->b, cm, nd, bitmask, h->M_ctx, h->cap_stream)
-                  : DFLASH_ECUDA;
+      int rc = ok ? body(h->cap_stream) : DFLASH_ECUDA;
       if (ok) ok = cudaStreamEndCapture(h->cap_stream, &graph) == cudaSuccess && rc == DFLASH_OK;
       if (ok) ok = cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
       if (graph) cudaGraphDestroy(graph);
@@ -702,8 +720,8 @@ int run_forward(dflash_handle *h, const CallMeta &cm, int nd, const int32_t *bit
       return DFLASH_OK;
     }
   }
-  const int rc = forward(h->g, h->cfg, h->w, h->b, cm, nd, bitmask, h->M_ctx, s);
-  if (rc) return fail(rc, "%s", last_build_error());
+  const int rc = body(s);
+  if (rc) return fail(rc, "%s", rc == DFLASH_ECUDA ? "cudaMemcpyAsync failed" : last_build_error());
   return DFLASH_OK;
 }
 
@@ -785,13 +803,13 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   std::vector<int32_t> cta_off;
   build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs, &cta_off);
   CallMeta cm;
-  int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off);
+  size_t meta_bytes = 0;
+  int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off, &meta_bytes);
   if (rc) return rc;
-  rc = run_forward(h, cm, num_drafts, bitmask, s);
+  rc = run_forward(h, cm, num_drafts, bitmask, meta_bytes, s);
   if (rc) return rc;
-  // Results to the host: one transfer, one synchronisation.
+  // Results are on the host after one synchronisation.
   size_t nd = (size_t)num_drafts;
-  CK(cudaMemcpyAsync(h->b.out_host, h->b.out_dev, h->b.out_bytes, cudaMemcpyDeviceToHost, s));
   CK(cudaStreamSynchronize(s));
   const int32_t *status = (const int32_t *)h->b.out_host;
   const uint32_t *dr = (const uint32_t *)(h->b.out_host + h->b.off_drafts);

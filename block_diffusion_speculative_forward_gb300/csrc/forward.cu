@@ -664,31 +664,40 @@ void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap
   cta_off->clear();
   if (grid_tc <= 0) return;
   // Longest-first onto the least-loaded CTA (cost: key tiles + one for the
-  // item's setup and output), then the items regrouped CTA by CTA.
+  // item's setup and output), then the items regrouped CTA by CTA (a
+  // counting sort; every buffer is reused across calls).
   const int n = (int)items->size();
-  std::vector<int> cost(n), order(n);
+  thread_local std::vector<int> cost, order, owner;
+  thread_local std::vector<std::pair<int64_t, int>> heap;
+  thread_local std::vector<AttnItem> regrouped;
+  cost.resize(n);
+  order.resize(n);
+  owner.resize(n);
   for (int i = 0; i < n; ++i) {
     cost[i] = attention_tc_tiles(g, seq[(*items)[i].s], (*items)[i]) + 1;
     order[i] = i;
   }
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
-  using Load = std::pair<int64_t, int>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int b = 0; b < grid_tc; ++b) heap.push({0, b});
-  std::vector<std::vector<int>> per(grid_tc);
+  // min-heap of (load, cta) in a flat array
+  auto greater = [](const std::pair<int64_t, int> &x, const std::pair<int64_t, int> &y) {
+    return x > y;
+  };
+  heap.clear();
+  for (int b = 0; b < grid_tc; ++b) heap.push_back({0, b});
+  std::make_heap(heap.begin(), heap.end(), greater);
+  cta_off->assign(grid_tc + 1, 0);
   for (int i : order) {
-    Load t = heap.top();
-    heap.pop();
-    per[t.second].push_back(i);
-    heap.push({t.first + cost[i], t.second});
+    std::pop_heap(heap.begin(), heap.end(), greater);
+    std::pair<int64_t, int> &t = heap.back();
+    owner[i] = t.second;
+    ++(*cta_off)[t.second + 1];
+    t.first += cost[i];
+    std::push_heap(heap.begin(), heap.end(), greater);
   }
-  std::vector<AttnItem> regrouped;
-  regrouped.reserve(n);
-  cta_off->push_back(0);
-  for (int b = 0; b < grid_tc; ++b) {
-    for (int i : per[b]) regrouped.push_back((*items)[i]);
-    cta_off->push_back((int32_t)regrouped.size());
-  }
+  for (int b = 0; b < grid_tc; ++b) (*cta_off)[b + 1] += (*cta_off)[b];
+  regrouped.resize(n);
+  std::vector<int32_t> fill(cta_off->begin(), cta_off->end() - 1);
+  for (int i : order) regrouped[fill[owner[i]]++] = (*items)[i];
   items->swap(regrouped);
 }
 
