@@ -93,8 +93,14 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+_HAS_CUDA = None
+
+
 def _stream() -> int | None:
-    return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    global _HAS_CUDA
+    if _HAS_CUDA is None:
+        _HAS_CUDA = torch.cuda.is_available()
+    return torch.cuda.current_stream().cuda_stream if _HAS_CUDA else None
 
 
 def config_struct(cfg: dict) -> Config:
@@ -154,6 +160,7 @@ class DraftHead:
         _check(L.dflash_create(C.byref(self._cfg_struct), wp, C.byref(h)))
         self.ptr = h.value
         self._results = (OK, BOOKKEEPING_ONLY)
+        self._outs = {}
 
     def close(self):
         if self.ptr:
@@ -193,15 +200,17 @@ class DraftHead:
         """Returns (drafts, n_out, conf). new_rows: device tensor [n_new, S] or
         None; a pinned CPU tensor is copied to the device first."""
         new_rows = self._to_device(new_rows)
-        drafts = (C.c_uint32 * num_drafts)()
-        n_out = C.c_int32()
-        conf = C.c_float()
+        out = self._outs.get(num_drafts)
+        if out is None:   # result buffers, reused by every call of this width
+            out = ((C.c_uint32 * num_drafts)(), C.c_int32(), C.c_float())
+            out = out + (C.byref(out[1]), C.byref(out[2]))
+            self._outs[num_drafts] = out
+        drafts, n_out, conf, n_ref, c_ref = out
         n_new = 0 if new_rows is None else int(new_rows.shape[0])
         _check(lib().dflash_propose(self.ptr, st.ptr, int(last_token), int(position),
                                     _ptr(new_rows), n_new, int(num_drafts), _ptr(bitmask), drafts,
-                                    C.byref(n_out), C.byref(conf) if want_conf else None,
-                                    _stream()), self._results)
-        return list(drafts)[:num_drafts], n_out.value, (conf.value if want_conf else None)
+                                    n_ref, c_ref if want_conf else None, _stream()), self._results)
+        return list(drafts), n_out.value, (conf.value if want_conf else None)
 
     def propose_batch(self, states, last_tokens, positions, new_rows, num_drafts: int,
                       bitmask=None, want_conf: bool = True):
