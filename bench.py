@@ -274,6 +274,9 @@ def run_ours(args):
         out["batch32"]["workload"] = ("full_b32: propose_batch of 32 sequences, ctx U[256,4096], "
                                       "new rows U[1,16], 50% bitmask, confidence on")
         torch.cuda.empty_cache()
+    if args.workload == "full_b1_window":
+        out["window"] = run_window(64, W)
+        torch.cuda.empty_cache()
     if args.workload == "fp8_b128":
         out["fp8_b128"] = run_batched(syn.FULL_G8, 1005, 128, 512, 4096, 7, True, False,
                                       max(3, K // 2), W)
@@ -385,6 +388,53 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
                          "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / tf,
                          "peak_source": f"{src} bf16_tflops (burst)",
                          "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm}}
+
+
+def run_window(K, W):
+    """C3: one sequence with an 8192-row prompt and a 4096-row window (rows
+    below the window are neither computed nor stored), then propose /
+    after_verify rounds with accept counts drawn U[0, 15]; every round brings
+    the k + 1 target rows the previous verify accepted."""
+    from block_diffusion_speculative_forward_gb300 import binding as B
+    geom, seed, prompt, window = syn.FULL, 1003, 8192, 4096
+    nd = geom.gamma - 1
+    rounds = K + W
+    w = syn.make_weights(geom, seed)
+    wd = B.weights_to_device(w)
+    del w
+    cfg = head_cfg(geom, 1, prompt + geom.gamma * (rounds + 2) + 64, ctx_window=window)
+    head = B.DraftHead(cfg, wd)
+    st = head.alloc_state()
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    stack = torch.randn((prompt + geom.gamma * (rounds + 2), geom.stack_width), device="cuda",
+                        generator=g).to(torch.bfloat16)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    head.prefill(st, stack[:prompt - 1])
+    torch.cuda.synchronize()
+    prefill_ms = 1e3 * (time.perf_counter() - t0)
+    ks = syn.uniform_ints(0, nd, rounds, seed, 7)
+    pos, used, n_new = prompt - 1, prompt - 1, 1
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for r in range(rounds):
+        if r == W:
+            torch.cuda.synchronize()
+            e0.record(s)
+        pos += n_new
+        got = head.propose(st, 1000 + r, pos, stack[used:used + n_new], nd)
+        used += n_new
+        k = min(ks[r], got[1])
+        head.after_verify(st, k)
+        n_new = k + 1
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    head.close()
+    return {"value": nd / (ms * 1e-3), "unit": UNIT, "propose_us": 1e3 * ms, "rounds": K,
+            "warmup": W, "prompt": prompt, "ctx_window": window, "prefill_ms": prefill_ms,
+            "workload": "full_b1_window: prompt 8192 (8191 prefilled, 4096-row window), then "
+                        "propose/after_verify rounds, k ~ U[0, 15], k + 1 new rows per round"}
 
 
 def cpu_baseline(w, cfg, geom, seed, ctx, n_steps):
@@ -525,8 +575,10 @@ def main():
     ap.add_argument("--no-batch", action="store_true", help="skip the batch-32 leg")
     ap.add_argument("--batch-only", action="store_true",
                     help="only the batch-32 leg (for profiling it alone)")
-    ap.add_argument("--workload", default="full_b1", choices=["full_b1", "fp8_b128"],
-                    help="fp8_b128 adds the 128-sequence FP8 configuration")
+    ap.add_argument("--workload", default="full_b1",
+                    choices=["full_b1", "fp8_b128", "full_b1_window"],
+                    help="fp8_b128 adds the 128-sequence FP8 configuration, full_b1_window the "
+                         "8192-row prompt with a 4096-row window (64 rounds)")
     ap.add_argument("--kernel", default=None, choices=["lm_head", "lm_head_b32"],
                     help="time one kernel alone instead of the propose step")
     # dram__bytes_read.sum + dram__bytes_write.sum of one batch-1 lm_head GEMM
