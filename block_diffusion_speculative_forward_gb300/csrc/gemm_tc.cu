@@ -47,12 +47,11 @@ template <int BN, int EPI>
 struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // Partial mode (the short batch-1 layer GEMMs): 5 stages and no exchange
-  // buffer, ~95 KB, so two GEMM CTAs fit on an SM and the next GEMM streams
-  // its first weight tiles while this one drains. Other modes: 8 x 16 KB of
-  // weight tiles in flight at the 16-row tile (the lm_head stream needs it).
+  // Up to 64 rows: 8 stages (8 x 16 KB of weight tiles in flight per SM,
+  // which the batch-1 weight stream needs; deeper rings measured no faster).
+  // Partial mode reserves no exchange buffer.
   static constexpr bool kPartial = (EPI == EPI_TC_PARTIAL);
-  static constexpr int STAGES = (kPartial && BN == 16) ? 5 : (BN <= 64) ? 8 : (BN <= 128 ? 6 : 4);
+  static constexpr int STAGES = (BN <= 64) ? 8 : (BN <= 128 ? 6 : 4);
   static_assert(STAGES <= 8, "the barrier arrays in Smem hold 8 stages");
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int EXTRA = kPartial ? 1536 : 10240;   // Smem (without / with xch)
