@@ -3,7 +3,6 @@
 // and applies the step that follows that projection in the layer:
 //   residual add + RMSNorm   (o_proj, down_proj, fc -> hidden_norm, final norm)
 //   per-head q/k RMSNorm + RoPE   (after the stitched QKV projection)
-//   SwiGLU                    (after the interleaved gate/up projection)
 // Sources: [P1] "Struct BlockDiffusionDraftHead" fields hidden_norm, norm,
 // layers, rms_norm_eps, rotary_dim, yarn_inv_freq.
 #include "consumers.h"
@@ -210,26 +209,6 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
   }
 }
 
-// u[a, f] = silu(gate) * up with gate/up rows alternating (2f gate, 2f+1 up).
-__global__ void __launch_bounds__(256) k_swiglu_part(SwigluArgs p) {
-  pdl_trigger();
-  pdl_wait();
-  const int a = blockIdx.x;
-  for (int f = blockIdx.y * 256 + threadIdx.x; f < p.I; f += gridDim.y * 256) {
-    // a warp's 32 features are 64 consecutive gate/up rows: one 128-row tile
-    float gt, up;
-    if (p.y.ws) {
-      const TileRange tr = part_range(p.y, part_tile(p.y, a, 2 * (f & ~31)));
-      gt = part_sum(p.y, tr, a, 2 * f);
-      up = part_sum(p.y, tr, a, 2 * f + 1);
-    } else {
-      gt = p.y.dense[(int64_t)a * p.y.ld + 2 * f];
-      up = p.y.dense[(int64_t)a * p.y.ld + 2 * f + 1];
-    }
-    p.u[(int64_t)a * p.I + f] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
-  }
-}
-
 }  // namespace
 
 cudaError_t add_norm(const AddNormArgs &p, int rows, cudaStream_t s) {
@@ -249,10 +228,5 @@ cudaError_t qkv_post(const QkvPostArgs &p, int R, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t swiglu_part(const SwigluArgs &p, int R, cudaStream_t s) {
-  const int per = (p.I + 255) / 256;
-  const int gy = per < 8 ? per : 8;
-  return launch_pdl(k_swiglu_part, dim3(R, gy), dim3(256), 0, s, p);
-}
 
 }  // namespace dfl

@@ -29,14 +29,8 @@ struct QkvPostArgs {
   bf16 *q, *kb, *vb;
 };
 
-struct SwigluArgs {
-  Partials y;           // [R, 2I], gate/up rows alternating
-  int I;
-  bf16 *u;              // [R, I]
-};
 
 cudaError_t add_norm(const AddNormArgs &p, int rows, cudaStream_t s);
 cudaError_t qkv_post(const QkvPostArgs &p, int R, cudaStream_t s);
-cudaError_t swiglu_part(const SwigluArgs &p, int R, cudaStream_t s);
 
 }  // namespace dfl

@@ -507,18 +507,10 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       an.out = B.h;
       LK(add_norm(an, R, s));
     }
-    // gate/up: SwiGLU always in the GEMM's epilogue (whole tiles for many
-    // rows, the split-K fixup for few: one kernel instead of partials plus a
-    // SwiGLU pass)
-    if (false) {
-      SwigluArgs sp{};
-      int rc = project(B, W.map_gu[l], ACT_H, R, 2 * g.I, g.H, nullptr, &sp.y, s);
-      if (rc) return rc;
-      sp.I = g.I;
-      sp.u = B.u;
-      LK(swiglu_part(sp, R, s));
-    } else {
-      // gate/up with SwiGLU fused in the epilogue
+    {
+      // gate/up with SwiGLU in the GEMM's epilogue: whole tiles for many rows,
+      // the split-K fixup for few (one kernel instead of partials plus a
+      // separate SwiGLU pass)
       GemmParams p{};
       p.m_act = R;
       p.n_w = 2 * g.I;

@@ -114,11 +114,6 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
 }
 
 // ------------------------------------------------------------- launchers --
-// out[i] = bf16(g * x[r] / sqrt(mean(x[r]^2) + eps)); r = i when nd == 0,
-// else the i-th draft row: (i / nd) * gamma + 1 + i % nd.
-cudaError_t rmsnorm_rows(const float *x, int rows, int n, const bf16 *g, float eps, int nd,
-                         int gamma, bf16 *out, cudaStream_t s);
-
 cudaError_t embed_block(const bf16 *E, const SeqMeta *seq, int n_seq, const Geo &g,
                         uint32_t mask_token, float *x, int *status, cudaStream_t s);
 

@@ -29,44 +29,6 @@ __device__ __forceinline__ uint8_t float_to_fp8(float v) {
   return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
 
-// Block-wide sum over blockDim.x threads (a multiple of 32, <= 1024).
-__device__ float block_sum(float v, float *sh) {
-  v = warp_sum(v);
-  int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) sh[w] = v;
-  __syncthreads();
-  float t = 0.f;
-  int nw = blockDim.x >> 5;
-  for (int i = 0; i < nw; ++i) t += sh[i];
-  return t;
-}
-
-// --------------------------------------------------------------- RMSNorm --
-// [P1] fields rms_norm_eps, hidden_norm, norm; the Qwen3 layer norms.
-__global__ void k_rmsnorm_rows(const float *__restrict__ x, int n, const bf16 *__restrict__ g,
-                               float eps, int nd, int gamma, bf16 *__restrict__ out) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float sh[32];
-  int i = blockIdx.x;
-  int r = nd > 0 ? (i / nd) * gamma + 1 + (i % nd) : i;
-  const float *xr = x + (int64_t)r * n;
-  float ss = 0.f;
-  for (int e = threadIdx.x; e < n; e += blockDim.x) ss += xr[e] * xr[e];
-  ss = block_sum(ss, sh);
-  float inv = rsqrtf(ss / (float)n + eps);
-  for (int e = threadIdx.x; e < n; e += blockDim.x)
-    out[(int64_t)i * n + e] = __float2bfloat16_rn(__bfloat162float(g[e]) * (xr[e] * inv));
-}
-
-cudaError_t rmsnorm_rows(const float *x, int rows, int n, const bf16 *g, float eps, int nd,
-                         int gamma, bf16 *out, cudaStream_t s) {
-  if (rows <= 0) return cudaSuccess;
-  launch_pdl(k_rmsnorm_rows, dim3(rows), dim3(256), 0, s, x, n, g, eps, nd, gamma, out);
-  return cudaGetLastError();
-}
-
 // ----------------------------------------------------------- block embed --
 // [P1] fields gamma, mask_token_id, embed_tokens_shared: row 0 of each
 // sequence's block embeds the last verified token, rows 1..gamma-1 the mask.
