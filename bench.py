@@ -350,12 +350,24 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
         pos = newpos
         n_new = [k + 1 for k in ks]
     host = [0.0, 0.0]
+    # device time of each propose_batch forward (events recorded at the first
+    # and after the last kernel of the forward, inside its graph)
+    import ctypes as C
+    lib = B.lib()
+    lib.dflash_debug_set_step_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
+    sb, se = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in (sb, se):
+        e.record(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    lib.dflash_debug_set_step_probe(head.ptr, C.c_void_p(sb.cuda_event), C.c_void_p(se.cuda_event))
+    dev_ms = []
 
     def step(t):
         rows, toks, newpos, ks = plan[t]
         t0 = time.perf_counter()
         head.propose_batch(states, toks, newpos, rows, nd, bitmask=mask)
         t1 = time.perf_counter()
+        dev_ms.append(sb.elapsed_time(se))
         for i in range(n):
             head.after_verify(states[i], ks[i])
         host[0] += t1 - t0
@@ -364,6 +376,7 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
     for t in range(W):
         step(t)
     host[0] = host[1] = 0.0
+    dev_ms.clear()
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -377,8 +390,10 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
     flops = sum(f for f, _ in work) / K
     byts = sum(b for _, b in work) / K
     hbm, tf, src = peaks()
+    lib.dflash_debug_set_step_probe(head.ptr, None, None)
     head.close()
     return {"value": n * nd / (ms * 1e-3), "unit": UNIT, "propose_us": 1e3 * ms,
+            "device_us": 1e3 * statistics.median(dev_ms),
             "batch": n, "gamma": geom.gamma, "num_drafts": nd, "steps": K, "warmup": W,
             "ctx": f"U[{ctx_lo},{ctx_hi}]", "bitmask": use_mask, "fp8_kv_and_lm_head": fp8,
             "flops_per_step": flops, "bytes_per_step": byts,

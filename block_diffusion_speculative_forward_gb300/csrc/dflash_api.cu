@@ -780,6 +780,16 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   std::vector<RowMeta> rows;
   std::vector<int32_t> page_ids;
   rows_of(h, plans, &rows);
+  // Calls whose new-row totals differ share a graph: above 16 rows the list
+  // is padded to a multiple of 32 with rows (seq -1) that are packed as
+  // zeros, carried through the projections and never stored.
+  if (rows.size() > 16) {
+    RowMeta pad{};
+    pad.page = -1;
+    pad.seq = -1;
+    pad.src = nullptr;
+    rows.resize((rows.size() + 31) / 32 * 32, pad);
+  }
   for (int i = 0; i < n; ++i) {
     dflash_state *st = states[i];
     SeqMeta &m = seq[i];

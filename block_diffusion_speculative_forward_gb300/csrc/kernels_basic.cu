@@ -57,13 +57,19 @@ cudaError_t embed_block(const bf16 *E, const SeqMeta *seq, int n_seq, const Geo 
 // ------------------------------------------------------------- row pack --
 // Gathers the ctx rows to compute from the callers' stacks into one
 // contiguous [m, S] buffer (16-byte vectors; S*2 is a multiple of 16).
+// Padding rows (seq < 0) become zero rows.
 __global__ void k_pack_rows(const RowMeta *__restrict__ rows, int S, bf16 *__restrict__ out) {
   pdl_trigger();
   pdl_wait();
   int r = blockIdx.x;
-  const uint4 *src = (const uint4 *)rows[r].src;
+  const RowMeta rm = rows[r];
+  const uint4 *src = (const uint4 *)rm.src;
   uint4 *dst = (uint4 *)(out + (int64_t)r * S);
   int nv = S / 8;
+  if (rm.seq < 0 || !src) {
+    for (int e = threadIdx.x; e < nv; e += blockDim.x) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   for (int e = threadIdx.x; e < nv; e += blockDim.x) dst[e] = src[e];
 }
 
@@ -114,6 +120,7 @@ __global__ void k_ctx_kv_write(const Partials kv, const RowMeta *__restrict__ ro
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = g.d, half = d / 2;
   const RowMeta rm = rows[r];
+  if (rm.seq < 0) return;   // padding row: computed, never stored
   if (rm.page < 0 || rm.page >= g.pages) {
     if (threadIdx.x == 0) atomicOr(status, ST_PAGE);
     return;
