@@ -6,7 +6,7 @@
 // Work: the same split-KV items as the mma.sync kernel (attention.cu), run by
 // one persistent CTA per SM over a host-balanced list of items. Per item the
 // group's gamma x (nq / nkv) <= 128 query vectors are the M = 128 operand;
-// keys stream in tiles of 64 (four 16-key pages) through a 3-stage TMA ring
+// keys stream in tiles of 64 (four 16-key pages) through a 4-stage TMA ring
 // straight from the paged pool. Per tile:
 //   S   = Q K^T   tcgen05, M 128 x N 64 x K 128, into TMEM (double buffered)
 //   P   = exp(S * scale - m)  by four softmax warps, one thread per query
@@ -34,7 +34,7 @@ using namespace tc;
 constexpr int AQ = 128;                      // query vectors per tile (MMA M)
 constexpr int AD = 128;                      // head dim
 constexpr int AK = 64;                       // keys per tile
-constexpr int KV_STAGES = 3;
+constexpr int KV_STAGES = 4;
 constexpr int Q_BYTES = AQ * AD * 2;         // 32 KB: two 64-column halves
 constexpr int Q_HALF = Q_BYTES / 2;
 constexpr int P_BYTES = AQ * AK * 2;         // 16 KB
@@ -44,7 +44,7 @@ constexpr int STAGE_BYTES = 2 * KT_BYTES;    // K tile then V tile
 constexpr int GROUP_BYTES = 16 * 128;        // one 16-key page half: 16 rows x 128 B
 constexpr int OFF_P = 2 * Q_BYTES;
 constexpr int OFF_KV = OFF_P + 2 * P_BYTES;
-constexpr int TILE_BYTES = OFF_KV + KV_STAGES * STAGE_BYTES;   // 192 KB
+constexpr int TILE_BYTES = OFF_KV + KV_STAGES * STAGE_BYTES;   // 224 KB
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;               // two 64-column S buffers
@@ -58,6 +58,7 @@ struct Bars {
   int abort_flag;
 };
 constexpr int SMEM = 1024 + TILE_BYTES + (int)sizeof(Bars);
+static_assert(SMEM <= 232448, "attention tile exceeds the 227 KB shared-memory limit");
 
 // Key range of an item in the tile's coordinates: ctx items count positions
 // (tile j starts at p0 + 64 j, p0 the item's first position rounded down to a
