@@ -262,6 +262,7 @@ def run_ours(args):
                           "frac_of_hbm": step_bytes(geom, ctx, 1) / (t_ms / K * 1e-3) / 1e9 / hbm},
         "propose_us": 1e3 * t_ms / K,
         "device_us": 1e3 * statistics.median(dev_ms),
+        "device_spread": spread(dev_ms),
         "clocks": clk.summary(),
     }
     head.close()
@@ -289,19 +290,45 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def batched_work(geom, ctx_list, n_new_list, nd, kv_elem):
-    """Algorithmic FLOPs and HBM bytes of one propose_batch step."""
+def batched_phases(geom, ctx_list, n_new_list, nd, kv_elem):
+    """Algorithmic (FLOPs, HBM bytes) of each phase of one propose_batch step:
+    the block rows through the layers' GEMMs, the lm_head over the draft rows,
+    the new ctx rows' projections (fc + fused K/V) and the attention over the
+    ctx windows; every weight and every stored ctx K/V row read once."""
     H, I, L, S = geom.hidden, geom.intermediate, geom.num_layers, geom.stack_width
     n = len(ctx_list)
     R, D, m = n * geom.gamma, n * nd, sum(n_new_list)
     layer_w = geom.q_dim * H + 2 * geom.kv_dim * H + H * geom.q_dim + 3 * I * H
-    flops = 2 * R * layer_w * L + 2 * D * geom.vocab * H + 2 * m * (H * S + L * 2 * geom.kv_dim * H)
-    keys = sum(c + geom.gamma for c in ctx_list)
-    flops += 4 * geom.gamma * geom.q_dim * keys * L
     wb = syn.weight_bytes(geom)
-    lm_bytes = geom.vocab * H * (1 if kv_elem == 1 else 2)
-    byts = wb["layers"] + wb["fc"] + lm_bytes + sum(ctx_list) * L * 2 * geom.kv_dim * kv_elem
-    return flops, byts
+    keys = sum(c + geom.gamma for c in ctx_list)
+    return {
+        "layers": (2 * R * layer_w * L, wb["layers"]),
+        "lm_head": (2 * D * geom.vocab * H, geom.vocab * H * (1 if kv_elem == 1 else 2)),
+        "ctx_rows": (2 * m * (H * S + L * 2 * geom.kv_dim * H), wb["fc"]),
+        "attention": (4 * geom.gamma * geom.q_dim * keys * L,
+                      sum(ctx_list) * L * 2 * geom.kv_dim * kv_elem),
+    }
+
+
+def phase_roofline(phases, t_ms, tf, hbm):
+    """T_roof = sum over phases of max(F / P, B / BW) against the measured step
+    time: the fraction of the roofline the whole step reaches when every phase
+    sits on its own bound."""
+    out, t_roof = {}, 0.0
+    for name, (f, b) in phases.items():
+        t_f, t_b = f / (tf * 1e12), b / (hbm * 1e9)
+        t_roof += max(t_f, t_b)
+        out[name] = {"tflop": f / 1e12, "gb": b / 1e9, "bound": "tensor" if t_f >= t_b else "hbm",
+                     "t_roof_us": 1e6 * max(t_f, t_b)}
+    return {"t_roof_us": 1e6 * t_roof, "frac": t_roof / (t_ms * 1e-3), "phases": out}
+
+
+def spread(ms):
+    """Median, 10th and 90th percentile of per-step times in ms, as us."""
+    if len(ms) < 2:
+        return {"median_us": 1e3 * ms[0], "p10_us": 1e3 * ms[0], "p90_us": 1e3 * ms[0]}
+    q = statistics.quantiles(ms, n=10, method="inclusive")
+    return {"median_us": 1e3 * statistics.median(ms), "p10_us": 1e3 * q[0], "p90_us": 1e3 * q[-1]}
 
 
 def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
@@ -345,8 +372,8 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
         ks = syn.uniform_ints(0, nd, n, seed, 1900 + t)
         plan.append((rows, toks, newpos, ks))
         if t >= W:
-            work.append(batched_work(geom, [p - m for p, m in zip(newpos, n_new)], n_new, nd,
-                                     1 if fp8 else 2))
+            work.append(batched_phases(geom, [p - m for p, m in zip(newpos, n_new)], n_new, nd,
+                                       1 if fp8 else 2))
         pos = newpos
         n_new = [k + 1 for k in ks]
     host = [0.0, 0.0]
@@ -387,13 +414,16 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
         e1.record(s)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / K
-    flops = sum(f for f, _ in work) / K
-    byts = sum(b for _, b in work) / K
+    phases = {name: (sum(w[name][0] for w in work) / K, sum(w[name][1] for w in work) / K)
+              for name in work[0]}
+    flops = sum(f for f, _ in phases.values())
+    byts = sum(b for _, b in phases.values())
     hbm, tf, src = peaks()
     lib.dflash_debug_set_step_probe(head.ptr, None, None)
     head.close()
     return {"value": n * nd / (ms * 1e-3), "unit": UNIT, "propose_us": 1e3 * ms,
             "device_us": 1e3 * statistics.median(dev_ms),
+            "device_spread": spread(dev_ms),
             "batch": n, "gamma": geom.gamma, "num_drafts": nd, "steps": K, "warmup": W,
             "ctx": f"U[{ctx_lo},{ctx_hi}]", "bitmask": use_mask, "fp8_kv_and_lm_head": fp8,
             "flops_per_step": flops, "bytes_per_step": byts,
@@ -402,7 +432,8 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
             "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": tf,
                          "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / tf,
                          "peak_source": f"{src} bf16_tflops (burst)",
-                         "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm}}
+                         "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm},
+            "phase_roofline": phase_roofline(phases, ms, tf, hbm)}
 
 
 def run_window(K, W):
