@@ -663,6 +663,41 @@ int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logit
   return DFLASH_OK;
 }
 
+int32_t dflash_debug_attn_work(int32_t n_seq, const int32_t *pos, const int32_t *ws,
+                               int32_t num_kv_heads, int32_t gamma, int32_t slot_cap,
+                               int32_t grid, int32_t sms, int32_t *items, int32_t cap_items,
+                               int32_t *cta_off, int32_t *n_pairs) {
+  if (n_seq < 0 || (n_seq > 0 && (!pos || !ws)) || num_kv_heads < 1 || gamma < 1 ||
+      slot_cap < 1 || grid < 0 || sms < 1 || cap_items < 0 || (cap_items > 0 && !items) ||
+      (grid > 0 && !cta_off))
+    return fail(DFLASH_EINVAL, "bad attention work arguments");
+  std::vector<dfl::SeqMeta> seq(n_seq);
+  for (int i = 0; i < n_seq; ++i) {
+    if (ws[i] < 0 || ws[i] > pos[i]) return fail(DFLASH_EINVAL, "window start outside 0..pos");
+    seq[i].pos = pos[i];
+    seq[i].ws = ws[i];
+  }
+  dfl::Geo g{};
+  g.nkv = num_kv_heads;
+  g.gamma = gamma;
+  std::vector<dfl::AttnItem> it;
+  std::vector<dfl::AttnPair> pr;
+  std::vector<int32_t> off;
+  dfl::build_attn_work_sms(g, seq, slot_cap, grid, sms, &it, &pr, &off);
+  if ((int64_t)it.size() > cap_items) return fail(DFLASH_EINVAL, "items beyond cap_items");
+  for (size_t i = 0; i < it.size(); ++i) {
+    int32_t *o = items + 5 * i;
+    o[0] = it[i].s;
+    o[1] = it[i].g;
+    o[2] = it[i].k0;
+    o[3] = it[i].k1;
+    o[4] = it[i].slot;
+  }
+  if (grid > 0) memcpy(cta_off, off.data(), sizeof(int32_t) * (size_t)(grid + 1));
+  if (n_pairs) *n_pairs = (int32_t)pr.size();
+  return (int32_t)it.size();
+}
+
 }  // extern "C"
 
 // ====================================================== propose driver ==

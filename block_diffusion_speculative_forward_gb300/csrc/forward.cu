@@ -620,9 +620,14 @@ namespace dfl {
 void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
                      std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
                      std::vector<int32_t> *cta_off) {
+  build_attn_work_sms(g, seq, slot_cap, grid_tc, tc::num_sms(), items, pairs, cta_off);
+}
+
+void build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
+                         int grid_tc, int sms, std::vector<AttnItem> *items,
+                         std::vector<AttnPair> *pairs, std::vector<int32_t> *cta_off) {
   int64_t total = 0;
   for (const SeqMeta &m : seq) total += (int64_t)(m.pos - m.ws) * g.nkv;
-  const int sms = tc::num_sms();
   // About three SM waves of ctx items, at least 64 keys each so the partial
   // merge stays cheap. Chunk boundaries fall on positions that are multiples
   // of 64, so every tile but a window's first starts on a page.

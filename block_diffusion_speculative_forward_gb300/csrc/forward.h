@@ -75,6 +75,11 @@ struct Buffers {
 void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
                      std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
                      std::vector<int32_t> *cta_off);
+// The same for a given SM count (the chunk size aims at three SM waves);
+// needs no device, so host-side tests can call it.
+void build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
+                         int grid_tc, int sms, std::vector<AttnItem> *items,
+                         std::vector<AttnPair> *pairs, std::vector<int32_t> *cta_off);
 
 struct CallMeta {
   const SeqMeta *seq = nullptr;

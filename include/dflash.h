@@ -247,6 +247,25 @@ DFLASH_API int dflash_gemm_noalloc(const void *w, const void *x, float *y, int32
 DFLASH_API int dflash_debug_lmhead(const void *w, const void *x, void *partials, int32_t m,
                                    int32_t n_w, int32_t k, void *stream);
 DFLASH_API int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits);
+/* Host-only inspection of the split of a call's attention into work items
+ * (needs no GPU): for n_seq sequences whose blocks sit at positions pos[i]
+ * and whose windows start at ws[i] (0 <= ws[i] <= pos[i]), each of the
+ * num_kv_heads key ranges (ctx keys ws..pos-1, then the gamma block keys) is
+ * cut into ctx chunks plus one block item, at most slot_cap partial slots in
+ * all; with grid > 0 the items are then balanced over grid persistent CTAs
+ * for a GPU of sms SMs, exactly as a propose* call does. Writes the items
+ * in the order the kernel reads them, 5 int32 each (sequence, kv head, first
+ * key, end key, partial slot; the slot is -1 for the block item of a
+ * sequence without ctx keys, which is then its only item)
+ * into items[cap_items][5], the CTA offsets into cta_off[grid + 1] (CTA b
+ * runs items cta_off[b] .. cta_off[b+1]-1) and the number of split pairs into
+ * *n_pairs (may be NULL). Keys count from the window start. Returns the item
+ * count, or DFLASH_EINVAL (nothing written) for a bad argument or more items
+ * than cap_items. Host pointers only. */
+DFLASH_API int32_t dflash_debug_attn_work(int32_t n_seq, const int32_t *pos, const int32_t *ws,
+                                          int32_t num_kv_heads, int32_t gamma, int32_t slot_cap,
+                                          int32_t grid, int32_t sms, int32_t *items,
+                                          int32_t cap_items, int32_t *cta_off, int32_t *n_pairs);
 
 #ifdef __cplusplus
 }
