@@ -129,13 +129,14 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- workloads --
-def build_b1(geom, seed, ctx, n_steps_total):
+def build_b1(geom, seed, ctx, n_steps_total, extra_positions=0):
     """Head + one sequence prefilled with ctx-1 rows; device rows for every
-    step's new target row; pinned host copies of the same rows."""
+    step's new target row; pinned host copies of the same rows. The state's
+    budget leaves extra_positions more positions for later steps."""
     from block_diffusion_speculative_forward_gb300 import binding as B
     w = syn.make_weights(geom, seed)
     wd = B.weights_to_device(w)
-    cfg = head_cfg(geom, 1, ctx + n_steps_total + 64)
+    cfg = head_cfg(geom, 1, ctx + n_steps_total + extra_positions + 64)
     head = B.DraftHead(cfg, wd)
     st = head.alloc_state()
     head.prefill(st, syn.make_stack(geom, ctx - 1, seed).cuda())
@@ -171,7 +172,9 @@ def run_ours(args):
     nd = geom.gamma - 1
     K, W = args.steps, args.warmup
     total = 2 * (K + W) + 2
-    w, wd, head, st, rows_dev, rows_host, cfg = build_b1(geom, seed, ctx, total)
+    K16, W16 = max(3, K // 10), 3
+    w, wd, head, st, rows_dev, rows_host, cfg = build_b1(geom, seed, ctx, total,
+                                                         geom.gamma * (K16 + W16 + 2))
     lib = B.lib()
     stream = torch.cuda.current_stream()
     pos = ctx
@@ -232,6 +235,10 @@ def run_ours(args):
         used += 1
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
+    try:
+        new16 = run_b1_new16(lib, head, st, pos, geom, seed, nd, K16, W16)
+    except Exception as e:   # reported in the line; never fatal for the metric's leg
+        new16 = {"error": f"{type(e).__name__}: {e}"[:300]}
     t_ms, e2e_s = max_over_ranks([t_ms, e2e_s], dist, "cuda")
     hbm, tf, src = peaks()
     lm_ms = statistics.mean(probe_ms)
@@ -264,6 +271,7 @@ def run_ours(args):
         "device_us": 1e3 * statistics.median(dev_ms),
         "device_spread": spread(dev_ms),
         "clocks": clk.summary(),
+        "b1_new16": new16,
     }
     head.close()
     del wd
@@ -288,6 +296,53 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def run_b1_new16(lib, head, st, pos, geom, seed, nd, K, W):
+    """The batch-1 propose when a round accepted every draft: each propose
+    brings gamma new ctx rows (the last token's and the accepted drafts'
+    target hiddens), so the fc, hidden_norm, fused K/V and paged write run
+    over 16 rows on top of the block forward. st must be due at position pos
+    with one new row; device rows, inputs resident."""
+    import ctypes as C
+    g = geom.gamma
+    rows = syn.make_stack(geom, g * (K + W + 2), seed, idx=2).cuda()
+    s = torch.cuda.current_stream()
+    sb, se = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in (sb, se):
+        e.record(s)
+    torch.cuda.synchronize()
+    lib.dflash_debug_set_step_probe(head.ptr, C.c_void_p(sb.cuda_event), C.c_void_p(se.cuda_event))
+    dev_ms, used = [], 0
+
+    def propose(n_rows):
+        nonlocal pos, used
+        _, n_out, _ = head.propose(st, 1000 + pos % 1000, pos, rows[used:used + n_rows], nd)
+        used += n_rows
+        if n_out != nd:
+            raise RuntimeError(f"{n_out} drafts where {nd} were expected")
+        head.after_verify(st, nd)
+        pos += nd + 1
+        dev_ms.append(sb.elapsed_time(se))
+
+    try:
+        propose(1)   # the round whose drafts are all accepted
+        for _ in range(W):
+            propose(g)
+        dev_ms.clear()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(K):
+            propose(g)
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / K
+    finally:
+        lib.dflash_debug_set_step_probe(head.ptr, None, None)
+    return {"n_new": g, "value": nd / (ms * 1e-3), "unit": UNIT, "propose_us": 1e3 * ms,
+            "device_spread": spread(dev_ms), "steps": K, "warmup": W,
+            "bytes_per_step": step_bytes(geom, pos - g, g)}
 
 
 def batched_phases(geom, ctx_list, n_new_list, nd, kv_elem):
