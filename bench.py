@@ -450,8 +450,7 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
         head.propose_batch(states, toks, newpos, rows, nd, bitmask=mask)
         t1 = time.perf_counter()
         dev_ms.append(sb.elapsed_time(se))
-        for i in range(n):
-            head.after_verify(states[i], ks[i])
+        head.after_verify_batch(states, ks)
         host[0] += t1 - t0
         host[1] += time.perf_counter() - t1
 

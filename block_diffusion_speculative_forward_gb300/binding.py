@@ -9,7 +9,9 @@ from __future__ import annotations
 
 import ctypes as C
 import os
+import threading
 
+import numpy as np
 import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdflash.so")
@@ -69,6 +71,7 @@ def lib() -> C.CDLL:
                                                vp, C.POINTER(u32), C.POINTER(i32),
                                                C.POINTER(C.c_float), vp]),
             "dflash_after_verify": (C.c_int, [vp, vp, i32]),
+            "dflash_after_verify_batch": (C.c_int, [vp, i32, C.POINTER(vp), C.POINTER(i32)]),
             "dflash_last_error": (C.c_char_p, []),
             "dflash_debug_state": (C.c_int, [vp, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), i32]),
             "dflash_debug_pool": (C.c_int, [vp, C.POINTER(i32), C.POINTER(i32)]),
@@ -161,6 +164,9 @@ class DraftHead:
         self.ptr = h.value
         self._results = (OK, BOOKKEEPING_ONLY)
         self._outs = {}
+        self._batch = {}
+        # the cached argument/result arrays serve one call at a time
+        self._lock = threading.Lock()
 
     def close(self):
         if self.ptr:
@@ -200,43 +206,59 @@ class DraftHead:
         """Returns (drafts, n_out, conf). new_rows: device tensor [n_new, S] or
         None; a pinned CPU tensor is copied to the device first."""
         new_rows = self._to_device(new_rows)
-        out = self._outs.get(num_drafts)
-        if out is None:   # result buffers, reused by every call of this width
-            out = ((C.c_uint32 * num_drafts)(), C.c_int32(), C.c_float())
-            out = out + (C.byref(out[1]), C.byref(out[2]))
-            self._outs[num_drafts] = out
-        drafts, n_out, conf, n_ref, c_ref = out
         n_new = 0 if new_rows is None else int(new_rows.shape[0])
-        _check(lib().dflash_propose(self.ptr, st.ptr, int(last_token), int(position),
-                                    _ptr(new_rows), n_new, int(num_drafts), _ptr(bitmask), drafts,
-                                    n_ref, c_ref if want_conf else None, _stream()), self._results)
-        return list(drafts), n_out.value, (conf.value if want_conf else None)
+        with self._lock:
+            out = self._outs.get(num_drafts)
+            if out is None:   # result buffers, reused by every call of this width
+                out = ((C.c_uint32 * num_drafts)(), C.c_int32(), C.c_float())
+                out = out + (C.byref(out[1]), C.byref(out[2]))
+                self._outs[num_drafts] = out
+            drafts, n_out, conf, n_ref, c_ref = out
+            _check(lib().dflash_propose(self.ptr, st.ptr, int(last_token), int(position),
+                                        _ptr(new_rows), n_new, int(num_drafts), _ptr(bitmask),
+                                        drafts, n_ref, c_ref if want_conf else None, _stream()),
+                   self._results)
+            return list(drafts), n_out.value, (conf.value if want_conf else None)
 
     def propose_batch(self, states, last_tokens, positions, new_rows, num_drafts: int,
                       bitmask=None, want_conf: bool = True):
         """Returns a list of (drafts, n_out, conf), or None when declined."""
         n = len(states)
         new_rows = [self._to_device(r) for r in new_rows]
-        st_arr = (C.c_void_p * n)(*[s.ptr for s in states])
-        tok = (C.c_uint32 * n)(*[int(t) for t in last_tokens])
-        pos = (C.c_int64 * n)(*[int(p) for p in positions])
-        rows = (C.c_void_p * n)(*[_ptr(r) for r in new_rows])
-        nn = (C.c_int32 * n)(*[0 if r is None else int(r.shape[0]) for r in new_rows])
-        drafts = (C.c_uint32 * (n * num_drafts))()
-        n_out = (C.c_int32 * n)()
-        conf = (C.c_float * n)()
-        rc = _check(lib().dflash_propose_batch(self.ptr, n, st_arr, tok, pos, rows, nn,
-                                               int(num_drafts), _ptr(bitmask), drafts, n_out,
-                                               conf if want_conf else None, _stream()),
-                    (OK, DECLINED, BOOKKEEPING_ONLY))
-        if rc == DECLINED:
-            return None
-        d = list(drafts)
-        return [(d[i * num_drafts:(i + 1) * num_drafts], n_out[i],
-                 conf[i] if want_conf else None) for i in range(n)]
+        with self._lock:
+            bufs = self._batch.get((n, num_drafts))
+            if bufs is None:   # argument and result arrays, reused by every call of this shape
+                bufs = ((C.c_void_p * n)(), (C.c_uint32 * n)(), (C.c_int64 * n)(),
+                        (C.c_void_p * n)(), (C.c_int32 * n)(), (C.c_uint32 * (n * num_drafts))(),
+                        (C.c_int32 * n)(), (C.c_float * n)())
+                self._batch[(n, num_drafts)] = bufs
+            st_arr, tok, pos, rows, nn, drafts, n_out, conf = bufs
+            st_arr[:] = [s.ptr for s in states]
+            tok[:] = [int(t) for t in last_tokens]
+            pos[:] = [int(p) for p in positions]
+            rows[:] = [None if r is None else r.data_ptr() for r in new_rows]
+            nn[:] = [0 if r is None else int(r.shape[0]) for r in new_rows]
+            rc = _check(lib().dflash_propose_batch(self.ptr, n, st_arr, tok, pos, rows, nn,
+                                                   int(num_drafts), _ptr(bitmask), drafts, n_out,
+                                                   conf if want_conf else None, _stream()),
+                        (OK, DECLINED, BOOKKEEPING_ONLY))
+            if rc == DECLINED:
+                return None
+            d = np.frombuffer(drafts, dtype=np.uint32).reshape(n, num_drafts).tolist()
+            no = np.frombuffer(n_out, dtype=np.int32).tolist()
+            cf = np.frombuffer(conf, dtype=np.float32).tolist() if want_conf else [None] * n
+        return [(d[i], no[i], cf[i]) for i in range(n)]
 
     def after_verify(self, st: State, num_accepted: int) -> None:
         _check(lib().dflash_after_verify(self.ptr, st.ptr, int(num_accepted)))
+
+    def after_verify_batch(self, states, num_accepted) -> None:
+        """after_verify for every state of a propose_batch in one call; on an
+        error no state changes."""
+        n = len(states)
+        st_arr = (C.c_void_p * n)(*[s.ptr for s in states])
+        ks = (C.c_int32 * n)(*[int(k) for k in num_accepted])
+        _check(lib().dflash_after_verify_batch(self.ptr, n, st_arr, ks))
 
     # -- inspection -----------------------------------------------------------
     def debug_state(self, st: State):

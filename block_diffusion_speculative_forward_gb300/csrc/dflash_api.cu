@@ -513,6 +513,30 @@ int dflash_after_verify(dflash_handle *h, dflash_state *st, int32_t num_accepted
   return DFLASH_OK;
 }
 
+int dflash_after_verify_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
+                              const int32_t *num_accepted) {
+  if (!h || n < 0 || (n > 0 && (!states || !num_accepted)))
+    return fail(DFLASH_EINVAL, "NULL argument");
+  std::lock_guard<std::mutex> lk(h->mu);
+  std::set<dflash_state *> seen;
+  for (int i = 0; i < n; ++i) {
+    dflash_state *st = states[i];
+    if (!st || !h->states.count(st)) return fail(DFLASH_EINVAL, "state %d unknown", i);
+    if (!seen.insert(st).second) return fail(DFLASH_EINVAL, "state %d repeated", i);
+    if (!st->pending) return fail(DFLASH_ESTATE, "state %d: after_verify without a propose", i);
+    if (num_accepted[i] < 0 || num_accepted[i] > st->pend_nout)
+      return fail(DFLASH_EINVAL, "state %d: num_accepted %d outside 0..%d", i, num_accepted[i],
+                  st->pend_nout);
+  }
+  for (int i = 0; i < n; ++i) {
+    dflash_state *st = states[i];
+    st->expected_next = st->pend_pos + num_accepted[i] + 1;
+    st->pending = false;
+    retire_below(h, st, window_start(h, st->expected_next));
+  }
+  return DFLASH_OK;
+}
+
 int dflash_debug_state(const dflash_state *st, int64_t *ctx_len, int32_t *first_block,
                        int32_t *table, int32_t cap) {
   if (!st) return fail(DFLASH_EINVAL, "NULL state");

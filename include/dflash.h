@@ -181,6 +181,13 @@ DFLASH_API int dflash_propose_batch(dflash_handle *h, int32_t n, dflash_state *c
  * position + num_accepted. Pages below that propose's window return to the
  * pool now. Host-only. Errors: EINVAL, ESTATE. */
 DFLASH_API int dflash_after_verify(dflash_handle *h, dflash_state *st, int32_t num_accepted);
+/* dflash_after_verify for the n states of one propose_batch in one call:
+ * num_accepted[i] (0..n_out of state i) applies to states[i]. Every state is
+ * checked first (known, not repeated, awaiting after_verify, count in range);
+ * on an error nothing changes and the message names the state's index.
+ * Host-only. Errors: EINVAL, ESTATE. */
+DFLASH_API int dflash_after_verify_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
+                                         const int32_t *num_accepted);
 
 /* Message of the last failing call on this thread ("" if none). */
 DFLASH_API const char *dflash_last_error(void);

@@ -167,3 +167,42 @@ def test_repeated_state_in_batch_is_rejected():
     with pytest.raises(B.DFlashError) as e:
         lib.propose_batch([a, a], [1, 1], [0, 0], [None, None], 3)
     assert e.value.code == "EINVAL"
+
+
+def test_after_verify_batch_matches_per_sequence_calls():
+    """[P3] after_verify applied to every state of a propose_batch in one call
+    leaves the same block tables and pool as one call per state, and on any
+    bad argument changes nothing."""
+    geom = replace(MICRO, gamma=8, ctx_window=64, kv_block=16, prefill_chunk=64)
+    n = 4
+    cfg = cfg_of(geom, max_batch=n, max_seq_len=2048)
+    one, many = B.DraftHead(cfg, None), B.DraftHead(cfg, None)
+    ctx = syn.uniform_ints(20, 120, n, 6, 1)
+    s1, s2 = [], []
+    for c in ctx:
+        a, b = one.alloc_state(), many.alloc_state()
+        one.prefill(a, _fake_rows(c))
+        many.prefill(b, _fake_rows(c))
+        s1.append(a)
+        s2.append(b)
+    pos, n_new = list(ctx), [0] * n
+    for rnd in range(10):
+        one.propose_batch(s1, [1] * n, pos, [_fake_rows(m) for m in n_new], 7)
+        many.propose_batch(s2, [1] * n, pos, [_fake_rows(m) for m in n_new], 7)
+        ks = syn.uniform_ints(0, 7, n, 6, 200 + rnd)
+        before = [many.debug_state(s) for s in s2]
+        for bad in ([0, 0, 8, 0], [0, -1, 0, 0]):          # a count outside 0..n_out
+            with pytest.raises(B.DFlashError, match="EINVAL"):
+                many.after_verify_batch(s2, bad)
+        with pytest.raises(B.DFlashError, match="EINVAL"):  # a state twice
+            many.after_verify_batch([s2[0], s2[1], s2[0]], ks[:3])
+        assert [many.debug_state(s) for s in s2] == before
+        for i in range(n):
+            one.after_verify(s1[i], ks[i])
+        many.after_verify_batch(s2, ks)
+        assert [one.debug_state(s) for s in s1] == [many.debug_state(s) for s in s2]
+        assert one.debug_pool() == many.debug_pool()
+        with pytest.raises(B.DFlashError, match="ESTATE"):  # no propose pending any more
+            many.after_verify_batch(s2, ks)
+        pos = [p + k + 1 for p, k in zip(pos, ks)]
+        n_new = [k + 1 for k in ks]
