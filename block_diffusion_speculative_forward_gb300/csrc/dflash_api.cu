@@ -486,7 +486,7 @@ int dflash_propose(dflash_handle *h, dflash_state *st, uint32_t last_token, int6
                    const void *new_rows, int32_t n_new, int32_t num_drafts, const int32_t *bitmask,
                    uint32_t *drafts, int32_t *n_out, float *conf, void *stream) {
   return dfl::propose_impl(h, 1, &st, &last_token, &position, &new_rows, &n_new, num_drafts,
-                           bitmask, drafts, n_out, conf, stream, true);
+                           bitmask, drafts, n_out, conf, stream);
 }
 
 int dflash_propose_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
@@ -497,7 +497,7 @@ int dflash_propose_batch(dflash_handle *h, int32_t n, dflash_state *const *state
   if (!h) return fail(DFLASH_EINVAL, "NULL handle");
   if (n < 2 || n > h->cfg.max_batch) return DFLASH_DECLINED;
   return dfl::propose_impl(h, n, states, last_tokens, positions, new_rows, n_new, num_drafts,
-                           bitmask, drafts, n_out, conf, stream, false);
+                           bitmask, drafts, n_out, conf, stream);
 }
 
 int dflash_after_verify(dflash_handle *h, dflash_state *st, int32_t num_accepted) {
@@ -788,7 +788,7 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
                  const uint32_t *last_tokens, const int64_t *positions,
                  const void *const *new_rows, const int32_t *n_new, int num_drafts,
                  const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
-                 void *stream, bool single) {
+                 void *stream) {
   if (!h) return fail(DFLASH_EINVAL, "NULL handle");
   if (!states || !last_tokens || !positions || !n_new || !drafts || !n_out)
     return fail(DFLASH_EINVAL, "NULL argument");
@@ -898,7 +898,6 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
     CK(cudaMemsetAsync(h->b.status, 0, sizeof(int), s));
     return fail(DFLASH_EDEVICE, "device bounds check tripped (status %d)", st_bits);
   }
-  (void)single;
   return DFLASH_OK;
 }
 

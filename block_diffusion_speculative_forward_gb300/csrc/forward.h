@@ -117,6 +117,6 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
                  const uint32_t *last_tokens, const int64_t *positions,
                  const void *const *new_rows, const int32_t *n_new, int num_drafts,
                  const int32_t *bitmask, uint32_t *drafts, int32_t *n_out, float *conf,
-                 void *stream, bool single);
+                 void *stream);
 
 }  // namespace dfl
