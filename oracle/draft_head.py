@@ -210,6 +210,9 @@ class DraftHeadOracle:
         self._lm = None
         self.pool = PagePool(self.n_pool_pages())
         self.states: list[SeqState] = []
+        # pages moved out of their states by take_drafter_kv and not yet
+        # installed or freed: tuple(page ids) -> (ctx_len, stored rows)
+        self.carried: dict[tuple, tuple] = {}
 
     # -- sizes ----------------------------------------------------------------
     def pages_per_seq(self) -> int:
@@ -432,6 +435,10 @@ class DraftHeadOracle:
             raise OracleError("EPOSITION", "position != expected next")
         if position > st.cap:
             raise OracleError("EINVAL", "ctx beyond state capacity")
+        if self.W > 0 and st.pages and max(0, position - self.W) < min(st.pages) * self.B:
+            # only an installed carry can get here: its window would reach
+            # below the first page it brought (rows retired before the take)
+            raise OracleError("EPOSITION", "window reaches below the installed pages")
         return n_new
 
     def propose_batch(self, states, last_tokens, positions, new_rows, num_drafts,
@@ -496,6 +503,62 @@ class DraftHeadOracle:
         for b in sorted(b for b in st.pages if (b + 1) * self.B <= ws):
             self.pool.give(st.pages.pop(b))
         self._drop_retired_rows(st, ws)
+
+    # -- drafter-KV carry across turns ----------------------------------------
+    def take_drafter_kv(self, st: SeqState):
+        """[P3] take_drafter_kv: move the sequence's KV pages out of its state,
+        so free_state releases none of them and the caller can carry them to
+        the next turn; the state then behaves as freshly allocated. Returns
+        (blocks, rows, last_pair_key), or None when there is nothing to carry.
+
+        reading: blocks = physical ids of the live pages in logical order,
+        rows = ctx_len (the first live logical page is ceil(rows/B) -
+        len(blocks)); the row space is positions, not compacted, so no pair
+        key is tracked (None); a propose awaiting after_verify cannot be
+        carried (ESTATE)."""
+        if st not in self.states:
+            raise OracleError("EINVAL", "unknown state")
+        if st.pending is not None:
+            raise OracleError("ESTATE", "take before after_verify")
+        if not st.pages:
+            return None
+        lo, hi = min(st.pages), max(st.pages)
+        blocks = [st.pages[b] for b in range(lo, hi + 1)]
+        self.carried[tuple(blocks)] = (st.ctx_len, st.rows)
+        st.ctx_len, st.pages, st.rows = 0, {}, {}
+        st.pending, st.expected_next = None, None
+        return blocks, self.carried[tuple(blocks)][0], None
+
+    def install_drafter_kv(self, st: SeqState, blocks, rows: int, last_pair_key=None) -> bool:
+        """[P3] install_drafter_kv: the inverse of take_drafter_kv, into a
+        fresh state. reading: the state then holds ctx_len = rows with the
+        carried pages as its live window; the next propose brings the rows of
+        positions rows..position-1 and may not place its window below the
+        first carried page. A bad bundle or a state that is not fresh is an
+        error that changes nothing (the caller still owns the pages)."""
+        key = tuple(int(b) for b in blocks)
+        if st not in self.states:
+            raise OracleError("EINVAL", "unknown state")
+        if key not in self.carried or self.carried[key][0] != rows:
+            raise OracleError("EINVAL", "pages not carried with these rows")
+        if st.ctx_len or st.pages or st.pending is not None or st.expected_next is not None:
+            raise OracleError("EINVAL", "state is not fresh")
+        if rows > st.cap:
+            raise OracleError("EINVAL", "rows beyond state capacity")
+        _, kv = self.carried.pop(key)
+        b0 = -(-rows // self.B) - len(key)
+        st.pages = {b0 + i: p for i, p in enumerate(key)}
+        st.rows, st.ctx_len = kv, rows
+        return True
+
+    def free_drafter_kv(self, blocks) -> None:
+        """[P3] free_drafter_kv: release carried pages that no state owns."""
+        key = tuple(int(b) for b in blocks)
+        if key not in self.carried:
+            raise OracleError("EINVAL", "pages not carried")
+        del self.carried[key]
+        for p in key:
+            self.pool.give(p)
 
     # -- views for parity checks ---------------------------------------------
     def block_table(self, st: SeqState):
