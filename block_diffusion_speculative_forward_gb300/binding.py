@@ -72,6 +72,10 @@ def lib() -> C.CDLL:
                                                C.POINTER(C.c_float), vp]),
             "dflash_after_verify": (C.c_int, [vp, vp, i32]),
             "dflash_after_verify_batch": (C.c_int, [vp, i32, C.POINTER(vp), C.POINTER(i32)]),
+            "dflash_take_drafter_kv": (C.c_int, [vp, vp, C.POINTER(i32), i32, C.POINTER(i32),
+                                                 C.POINTER(i64)]),
+            "dflash_install_drafter_kv": (C.c_int, [vp, vp, C.POINTER(i32), i32, i64]),
+            "dflash_free_drafter_kv": (C.c_int, [vp, C.POINTER(i32), i32]),
             "dflash_last_error": (C.c_char_p, []),
             "dflash_debug_state": (C.c_int, [vp, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), i32]),
             "dflash_debug_pool": (C.c_int, [vp, C.POINTER(i32), C.POINTER(i32)]),
@@ -259,6 +263,31 @@ class DraftHead:
         st_arr = (C.c_void_p * n)(*[s.ptr for s in states])
         ks = (C.c_int32 * n)(*[int(k) for k in num_accepted])
         _check(lib().dflash_after_verify_batch(self.ptr, n, st_arr, ks))
+
+    # -- drafter-KV carry across turns -----------------------------------------
+    def take_drafter_kv(self, st: State):
+        """[P3] take_drafter_kv: (blocks, rows, None), or None when the state
+        holds nothing to carry; the state then behaves as fresh."""
+        cap = self.debug_pool()[1]
+        blocks = (C.c_int32 * max(cap, 1))()
+        n, rows = C.c_int32(), C.c_int64()
+        rc = _check(lib().dflash_take_drafter_kv(self.ptr, st.ptr, blocks, cap, C.byref(n),
+                                                 C.byref(rows)), (OK, DECLINED))
+        if rc == DECLINED:
+            return None
+        return list(blocks[:n.value]), rows.value, None
+
+    def install_drafter_kv(self, st: State, blocks, rows: int, last_pair_key=None) -> bool:
+        """[P3] install_drafter_kv into a fresh state; raises on a bad bundle
+        (the caller then still owns it)."""
+        arr = (C.c_int32 * max(len(blocks), 1))(*[int(b) for b in blocks])
+        _check(lib().dflash_install_drafter_kv(self.ptr, st.ptr, arr, len(blocks), int(rows)))
+        return True
+
+    def free_drafter_kv(self, blocks) -> None:
+        """[P3] free_drafter_kv: release a carried bundle no state owns."""
+        arr = (C.c_int32 * max(len(blocks), 1))(*[int(b) for b in blocks])
+        _check(lib().dflash_free_drafter_kv(self.ptr, arr, len(blocks)))
 
     # -- inspection -----------------------------------------------------------
     def debug_state(self, st: State):

@@ -84,6 +84,9 @@ struct dflash_handle {
   PagePool pool;
   std::mutex mu;
   std::set<dflash_state *> states;
+  // pages taken out of their states (take_drafter_kv) and neither installed
+  // nor freed yet: first page id -> (the bundle's pages, its ctx length)
+  std::map<int32_t, std::pair<std::vector<int32_t>, int64_t>> carried;
   int R_max = 0, D_max = 0, M_ctx = 0;
   // per-call metadata staging
   char *meta_host = nullptr, *meta_dev = nullptr;
@@ -537,6 +540,63 @@ int dflash_after_verify_batch(dflash_handle *h, int32_t n, dflash_state *const *
   return DFLASH_OK;
 }
 
+int dflash_take_drafter_kv(dflash_handle *h, dflash_state *st, int32_t *blocks, int32_t cap,
+                           int32_t *n_blocks, int64_t *rows) {
+  if (!h || !st || !n_blocks || !rows || cap < 0 || (cap > 0 && !blocks))
+    return fail(DFLASH_EINVAL, "NULL argument");
+  std::lock_guard<std::mutex> lk(h->mu);
+  if (!h->states.count(st)) return fail(DFLASH_EINVAL, "state does not belong to this handle");
+  if (st->pending) return fail(DFLASH_ESTATE, "take_drafter_kv while a propose awaits after_verify");
+  if (st->pages.empty()) return DFLASH_DECLINED;
+  if ((int64_t)st->pages.size() > cap)
+    return fail(DFLASH_EINVAL, "%zu pages to carry, room for %d", st->pages.size(), cap);
+  // the live pages are consecutive logical pages: retirement removes from below
+  if (st->pages.rbegin()->first - st->pages.begin()->first + 1 != (int64_t)st->pages.size())
+    return fail(DFLASH_ESTATE, "internal: live pages are not consecutive");
+  std::vector<int32_t> ids;
+  for (auto &kv : st->pages) ids.push_back(kv.second);
+  std::copy(ids.begin(), ids.end(), blocks);
+  *n_blocks = (int32_t)ids.size();
+  *rows = st->ctx_len;
+  h->carried[ids.front()] = std::make_pair(ids, st->ctx_len);
+  st->pages.clear();
+  st->ctx_len = 0;
+  st->pending = false;
+  st->expected_next = -1;
+  return DFLASH_OK;
+}
+
+int dflash_install_drafter_kv(dflash_handle *h, dflash_state *st, const int32_t *blocks,
+                              int32_t n_blocks, int64_t rows) {
+  if (!h || !st || !blocks || n_blocks < 1) return fail(DFLASH_EINVAL, "NULL argument");
+  std::lock_guard<std::mutex> lk(h->mu);
+  if (!h->states.count(st)) return fail(DFLASH_EINVAL, "state does not belong to this handle");
+  auto it = h->carried.find(blocks[0]);
+  if (it == h->carried.end() || it->second.second != rows ||
+      it->second.first != std::vector<int32_t>(blocks, blocks + n_blocks))
+    return fail(DFLASH_EINVAL, "pages and rows are not a bundle taken by take_drafter_kv");
+  if (st->ctx_len != 0 || !st->pages.empty() || st->pending || st->expected_next >= 0)
+    return fail(DFLASH_EINVAL, "install_drafter_kv into a state that is not fresh");
+  if (rows > st->cap) return fail(DFLASH_EINVAL, "rows %lld beyond the state's budget", (long long)rows);
+  const int64_t B = h->cfg.kv_block;
+  const int64_t b0 = (rows + B - 1) / B - n_blocks;
+  for (int32_t i = 0; i < n_blocks; ++i) st->pages[b0 + i] = blocks[i];
+  st->ctx_len = rows;
+  h->carried.erase(it);
+  return DFLASH_OK;
+}
+
+int dflash_free_drafter_kv(dflash_handle *h, const int32_t *blocks, int32_t n_blocks) {
+  if (!h || !blocks || n_blocks < 1) return fail(DFLASH_EINVAL, "NULL argument");
+  std::lock_guard<std::mutex> lk(h->mu);
+  auto it = h->carried.find(blocks[0]);
+  if (it == h->carried.end() || it->second.first != std::vector<int32_t>(blocks, blocks + n_blocks))
+    return fail(DFLASH_EINVAL, "pages are not a bundle taken by take_drafter_kv");
+  for (int32_t p : it->second.first) h->pool.give(p);
+  h->carried.erase(it);
+  return DFLASH_OK;
+}
+
 int dflash_debug_state(const dflash_state *st, int64_t *ctx_len, int32_t *first_block,
                        int32_t *table, int32_t cap) {
   if (!st) return fail(DFLASH_EINVAL, "NULL state");
@@ -812,6 +872,12 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
       return fail(DFLASH_EPOSITION, "sequence %d: position %lld != %lld set by after_verify", i,
                   (long long)positions[i], (long long)st->expected_next);
     if (positions[i] > st->cap) return fail(DFLASH_EINVAL, "sequence %d: beyond its budget", i);
+    if (c.ctx_window > 0 && !st->pages.empty() &&
+        window_start(h, positions[i]) < st->pages.begin()->first * (int64_t)c.kv_block)
+      // only an installed carry can get here: rows below its first page are gone
+      return fail(DFLASH_EPOSITION,
+                  "sequence %d: the window of position %lld reaches below the installed pages",
+                  i, (long long)positions[i]);
     if (h->compute && n_new[i] > 0 &&
         (!new_rows || !new_rows[i] || !aligned16(new_rows[i])))
       return fail(DFLASH_EINVAL, "sequence %d: new rows must be a 16-byte aligned device pointer", i);

@@ -181,6 +181,36 @@ DFLASH_API int dflash_propose_batch(dflash_handle *h, int32_t n, dflash_state *c
  * position + num_accepted. Pages below that propose's window return to the
  * pool now. Host-only. Errors: EINVAL, ESTATE. */
 DFLASH_API int dflash_after_verify(dflash_handle *h, dflash_state *st, int32_t num_accepted);
+/* [P3] take_drafter_kv: move the sequence's KV pages out of st so that
+ * dflash_free_state releases none of them and the caller can carry them to
+ * the sequence's next turn; st then behaves as freshly allocated (ctx_len 0,
+ * no pages, no propose pending, no expected position). On DFLASH_OK the
+ * physical ids of the live pages, in logical order, are in
+ * blocks[0..*n_blocks) (host array of cap entries) and the ctx length in
+ * *rows: the bundle now belongs to the caller, who installs it with
+ * dflash_install_drafter_kv or releases it with dflash_free_drafter_kv. The
+ * page contents are those the state's earlier calls wrote on their streams.
+ * The row space is positions, so the trait's last_pair_key has no
+ * counterpart (None). Returns DFLASH_DECLINED, changing nothing, when st
+ * holds no pages (nothing to carry). Host-only. Errors (nothing changes):
+ * EINVAL (unknown state, cap too small), ESTATE (a propose awaits
+ * after_verify). */
+DFLASH_API int dflash_take_drafter_kv(dflash_handle *h, dflash_state *st, int32_t *blocks,
+                                      int32_t cap, int32_t *n_blocks, int64_t *rows);
+/* [P3] install_drafter_kv: install a bundle exactly as dflash_take_drafter_kv
+ * returned it (blocks[0..n_blocks), rows) into st, which must be fresh
+ * (nothing appended since dflash_alloc_state, or taken since). st then holds
+ * ctx_len = rows with the bundle as its live pages (logical pages
+ * ceil(rows/kv_block) - n_blocks onwards); its next propose brings the rows
+ * of positions rows..position-1, and a propose whose window would start
+ * below the first installed page fails with EPOSITION. Host-only. Errors
+ * (nothing changes, the caller still owns the bundle): EINVAL (not a carried
+ * bundle, rows differ, st not fresh or unknown, rows beyond st's budget). */
+DFLASH_API int dflash_install_drafter_kv(dflash_handle *h, dflash_state *st,
+                                         const int32_t *blocks, int32_t n_blocks, int64_t rows);
+/* [P3] free_drafter_kv: return a carried bundle that no state owns to the
+ * pool. Host-only. Errors: EINVAL (not a carried bundle); nothing changes. */
+DFLASH_API int dflash_free_drafter_kv(dflash_handle *h, const int32_t *blocks, int32_t n_blocks);
 /* dflash_after_verify for the n states of one propose_batch in one call:
  * num_accepted[i] (0..n_out of state i) applies to states[i]. Every state is
  * checked first (known, not repeated, awaiting after_verify, count in range);

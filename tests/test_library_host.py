@@ -206,3 +206,99 @@ def test_after_verify_batch_matches_per_sequence_calls():
             many.after_verify_batch(s2, ks)
         pos = [p + k + 1 for p, k in zip(pos, ks)]
         n_new = [k + 1 for k in ks]
+
+
+def test_drafter_kv_carry_matches_oracle_bookkeeping():
+    """[P3] take_drafter_kv / install_drafter_kv / free_drafter_kv on the
+    library's native scheduler against the oracle: the same bundles, block
+    tables and pool counts after every call, and the same errors."""
+    geom = replace(MICRO, gamma=8, ctx_window=40, kv_block=8, prefill_chunk=64)
+    cfg = cfg_of(geom, max_batch=3, max_seq_len=1024)
+    w = syn.make_weights(geom, 8)
+    ora = oracle.DraftHeadOracle(cfg, w)
+    lib = B.DraftHead(cfg, None)
+    so, sl, pos, carried = {}, {}, {}, {}
+    stack = syn.make_stack(geom, 96, 8)
+
+    def same(sid):
+        assert lib.debug_state(sl[sid]) == ora.block_table(so[sid]), sid
+        assert lib.debug_pool() == (ora.pool.n_pages - ora.pool.n_free(), ora.pool.n_pages)
+
+    script = [("new", 0, 70), ("new", 1, 9), ("turn", 0, 5), ("turn", 1, 7), ("take", 0, None),
+              ("turn", 0, None), ("new", 2, 30), ("install", 3, 0), ("turn", 3, 2),
+              ("take", 1, None), ("take", 2, None), ("free", 1, None), ("turn", 3, 7),
+              ("take", 3, None), ("install", 4, 3), ("install", 5, 2), ("turn", 4, 0),
+              ("turn", 5, 1)]
+    for op, sid, arg in script:
+        if op == "new" or (op == "turn" and arg is None):
+            if op == "new":
+                so[sid], sl[sid] = ora.alloc_state(), lib.alloc_state()
+            n = arg if op == "new" else 20
+            ora.prefill(so[sid], stack[:n])
+            lib.prefill(sl[sid], _fake_rows(n))
+            pos[sid] = so[sid].ctx_len
+        elif op == "turn":
+            p = pos[sid]
+            n_new = p - so[sid].ctx_len
+            ora.propose(so[sid], 3, p, stack[:n_new] if n_new else None, 7)
+            lib.propose(sl[sid], 3, p, _fake_rows(n_new), 7)
+            same(sid)
+            ora.after_verify(so[sid], arg)
+            lib.after_verify(sl[sid], arg)
+            pos[sid] = p + arg + 1
+        elif op == "take":
+            a, b = ora.take_drafter_kv(so[sid]), lib.take_drafter_kv(sl[sid])
+            assert a == b and a is not None
+            carried[sid] = (a[0], a[1], pos[sid])
+        elif op == "install":
+            blocks, rows, nxt = carried.pop(arg)
+            so[sid], sl[sid] = ora.alloc_state(), lib.alloc_state()
+            assert ora.install_drafter_kv(so[sid], blocks, rows)
+            assert lib.install_drafter_kv(sl[sid], blocks, rows)
+            pos[sid] = nxt
+        elif op == "free":
+            blocks = carried.pop(sid)[0]
+            ora.free_drafter_kv(blocks)
+            lib.free_drafter_kv(blocks)
+        for s_id in so:
+            same(s_id)
+    # nothing to carry; misuse changes nothing on either side
+    fresh_o, fresh_l = ora.alloc_state(), lib.alloc_state()
+    assert ora.take_drafter_kv(fresh_o) is None and lib.take_drafter_kv(fresh_l) is None
+    p = pos[4]
+    n_new = p - so[4].ctx_len
+    ora.propose(so[4], 3, p, stack[:n_new] if n_new else None, 7)
+    lib.propose(sl[4], 3, p, _fake_rows(n_new), 7)
+    with pytest.raises(B.DFlashError, match="ESTATE"):
+        lib.take_drafter_kv(sl[4])
+    ora.after_verify(so[4], 7)
+    lib.after_verify(sl[4], 7)
+    blocks, rows, _ = lib.take_drafter_kv(sl[4])
+    assert (blocks, rows, None) == ora.take_drafter_kv(so[4])
+    before = lib.debug_pool()
+    for bad in ([blocks, rows + 1], [blocks[:-1], rows], [[blocks[0] + 1000], rows]):
+        with pytest.raises(B.DFlashError, match="EINVAL"):
+            lib.install_drafter_kv(fresh_l, *bad)
+    with pytest.raises(B.DFlashError, match="EINVAL"):       # not a fresh state
+        lib.install_drafter_kv(sl[5], blocks, rows)
+    with pytest.raises(B.DFlashError, match="EINVAL"):       # part of a bundle
+        lib.free_drafter_kv(blocks[1:])
+    assert lib.debug_pool() == before and lib.debug_state(fresh_l) == (0, -1, [])
+    assert lib.install_drafter_kv(fresh_l, blocks, rows)
+    assert ora.install_drafter_kv(fresh_o, blocks, rows)
+    assert lib.debug_state(fresh_l) == ora.block_table(fresh_o)
+    with pytest.raises(B.DFlashError, match="EINVAL"):       # installed: no longer carried
+        lib.free_drafter_kv(blocks)
+    # a window reaching below the first installed page is refused like the oracle does
+    low = ora.block_table(fresh_o)[1] * geom.kv_block + geom.ctx_window - 1
+    assert low > rows     # reachable by a propose that brings low - rows rows
+    with pytest.raises(oracle.OracleError, match="EPOSITION"):
+        ora.propose(fresh_o, 3, low, stack[:low - rows], 7)
+    with pytest.raises(B.DFlashError, match="EPOSITION"):
+        lib.propose(fresh_l, 3, low, _fake_rows(low - rows), 7)
+    assert lib.debug_state(fresh_l) == ora.block_table(fresh_o)
+    for s_id in so:
+        lib.free_state(sl[s_id])
+    lib.free_state(fresh_l)
+    lib.free_state(lib.alloc_state())
+    assert lib.debug_pool()[0] == 0
