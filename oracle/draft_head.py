@@ -78,6 +78,41 @@ def rope(x: torch.Tensor, pos: torch.Tensor, inv_freq: torch.Tensor) -> torch.Te
     return torch.cat([x1 * c - x2 * s, x2 * c + x1 * s], dim=-1)
 
 
+def yarn_inv_freq(theta: float, d: int, factor: float, beta_fast: float, beta_slow: float,
+                  original_max_pos: int) -> torch.Tensor:
+    """YaRN inverse frequencies ([P1] field yarn_inv_freq: the drafter's
+    rope_scaling factor 64, beta_fast 32, beta_slow 1,
+    original_max_position_embeddings 4096), from the published YaRN method
+    ("NTK-by-parts"): pair i of the base table theta^(-2i/d) turns
+    original_max_pos / (2 pi theta^(2i/d)) times over the original context.
+    Pairs turning more than beta_fast times keep their frequency, pairs turning
+    fewer than beta_slow times are interpolated (frequency / factor), and the
+    pairs between blend the two along a linear ramp over the pair index.
+
+    reading: the ramp runs from floor(i_fast) to ceil(i_slow), i_r being the
+    (real) pair index that turns r times, clamped to the table, as config
+    files' rope_scaling is read; evaluated in double, stored f32."""
+    half = d // 2
+
+    def pair_turning(r):
+        return d * math.log(original_max_pos / (r * 2.0 * math.pi)) / (2.0 * math.log(theta))
+
+    lo = max(math.floor(pair_turning(beta_fast)), 0)
+    hi = min(math.ceil(pair_turning(beta_slow)), half - 1)
+    out = []
+    for i in range(half):
+        base = theta ** (-2.0 * i / d)
+        ramp = min(max((i - lo) / max(hi - lo, 1e-3), 0.0), 1.0)   # 0: keep, 1: interpolate
+        out.append(base * (1.0 - ramp) + (base / factor) * ramp)
+    return torch.tensor(out, dtype=F64).to(torch.float32)
+
+
+def yarn_attention_factor(factor: float) -> float:
+    """YaRN's attention temperature (the published 0.1 ln(s) + 1), applied by
+    scaling the rotated q and k, so the logits scale by its square."""
+    return 1.0 if factor <= 1.0 else 0.1 * math.log(factor) + 1.0
+
+
 def silu(a: torch.Tensor) -> torch.Tensor:
     return a / (1.0 + torch.exp(-a))
 
@@ -197,6 +232,9 @@ class DraftHeadOracle:
         self.fc = f(w["fc"])
         self.hidden_norm, self.norm = f(w["hidden_norm"]), f(w["norm"])
         self.inv_freq = w["inv_freq"].to(torch.float32)
+        # reading: the rotated q and k are scaled by the attention factor
+        # (YaRN's temperature; 0 or absent means none)
+        self.rope_scale = float(c.get("rope_attn_factor", 0.0) or 1.0)
         self.layers = [{k: f(v) for k, v in lay.items()} for lay in w["layers"]]
         # [P1]/[P2] field fused_kv_weight: rows [K0; V0; K1; V1; ...].
         self.w_kv = torch.cat([torch.cat([lay["k"], lay["v"]], 0) for lay in self.layers], 0)
@@ -289,7 +327,7 @@ class DraftHeadOracle:
             k = kv[:, base:base + self.kv].reshape(-1, self.nkv, self.d)
             v = kv[:, base + self.kv:base + 2 * self.kv].reshape(-1, self.nkv, self.d)
             k = rope(rms_norm(k, lay["k_norm"], self.eps).transpose(0, 1), pos,
-                     self.inv_freq).transpose(0, 1)
+                     self.inv_freq).transpose(0, 1) * self.rope_scale
             k_st, v_st = self._quant_kv(l, k), self._quant_kv(l, v, is_v=True)
             for r, j in enumerate(positions):
                 if j not in st.rows:
@@ -382,9 +420,9 @@ class DraftHeadOracle:
         k = (h @ lay["k"].T).reshape(g, self.nkv, self.d)
         v = (h @ lay["v"].T).reshape(g, self.nkv, self.d)
         q = rope(rms_norm(q, lay["q_norm"], self.eps).transpose(0, 1), pos,
-                 self.inv_freq).transpose(0, 1)
+                 self.inv_freq).transpose(0, 1) * self.rope_scale
         k = rope(rms_norm(k, lay["k_norm"], self.eps).transpose(0, 1), pos,
-                 self.inv_freq).transpose(0, 1)
+                 self.inv_freq).transpose(0, 1) * self.rope_scale
         q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)
         if ctx_pos:
             kc = torch.stack([st.rows[j][0][l] for j in ctx_pos])
