@@ -34,7 +34,7 @@ class Config(C.Structure):
         ("target_hidden", C.c_int32), ("fc_in_features", C.c_int32), ("rms_eps", C.c_float),
         ("ctx_window", C.c_int32), ("kv_block", C.c_int32), ("prefill_chunk", C.c_int32),
         ("max_batch", C.c_int32), ("max_seq_len", C.c_int32), ("kv_pool_blocks", C.c_int32),
-        ("kv_dtype", C.c_int32), ("lm_head_dtype", C.c_int32)]
+        ("kv_dtype", C.c_int32), ("lm_head_dtype", C.c_int32), ("rope_attn_factor", C.c_float)]
 
 
 class Weights(C.Structure):
@@ -76,6 +76,9 @@ def lib() -> C.CDLL:
                                                  C.POINTER(i64)]),
             "dflash_install_drafter_kv": (C.c_int, [vp, vp, C.POINTER(i32), i32, i64]),
             "dflash_free_drafter_kv": (C.c_int, [vp, C.POINTER(i32), i32]),
+            "dflash_yarn_inv_freq": (C.c_int, [C.c_double, i32, C.c_double, C.c_double,
+                                               C.c_double, i32, C.POINTER(C.c_float),
+                                               C.POINTER(C.c_float)]),
             "dflash_last_error": (C.c_char_p, []),
             "dflash_debug_state": (C.c_int, [vp, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32), i32]),
             "dflash_debug_pool": (C.c_int, [vp, C.POINTER(i32), C.POINTER(i32)]),
@@ -117,9 +120,23 @@ def config_struct(cfg: dict) -> Config:
             setattr(c, name, int(cfg.get(name, cfg["n_target_layers"] * cfg["target_hidden"])))
         elif name == "rms_eps":
             c.rms_eps = float(cfg[name])
+        elif name == "rope_attn_factor":
+            c.rope_attn_factor = float(cfg.get(name, 0.0))
         else:
             setattr(c, name, int(cfg.get(name, 0)))
     return c
+
+
+def yarn_inv_freq(theta: float, head_dim: int, factor: float, beta_fast: float,
+                  beta_slow: float, original_max_pos: int):
+    """The library's YaRN table (dflash_yarn_inv_freq): (f32 CPU tensor
+    [head_dim/2], attention factor for the config's rope_attn_factor)."""
+    out = (C.c_float * (head_dim // 2))()
+    att = C.c_float()
+    _check(lib().dflash_yarn_inv_freq(float(theta), int(head_dim), float(factor),
+                                      float(beta_fast), float(beta_slow), int(original_max_pos),
+                                      out, C.byref(att)))
+    return torch.tensor(list(out), dtype=torch.float32), att.value
 
 
 def weights_to_device(w: dict, device="cuda") -> dict:

@@ -230,6 +230,8 @@ int validate_config(const dflash_config *c) {
     return fail(DFLASH_EINVAL, "max_batch, max_seq_len >= 1 and kv_pool_blocks >= 0 required");
   if ((c->kv_dtype != 0 && c->kv_dtype != 1) || (c->lm_head_dtype != 0 && c->lm_head_dtype != 1))
     return fail(DFLASH_EINVAL, "kv_dtype and lm_head_dtype must be 0 or 1");
+  if (!(c->rope_attn_factor >= 0.f && c->rope_attn_factor < 1e4f))
+    return fail(DFLASH_EINVAL, "rope_attn_factor must be 0 (none) or positive");
   return DFLASH_OK;
 }
 
@@ -537,6 +539,29 @@ int dflash_after_verify_batch(dflash_handle *h, int32_t n, dflash_state *const *
     st->pending = false;
     retire_below(h, st, window_start(h, st->expected_next));
   }
+  return DFLASH_OK;
+}
+
+int dflash_yarn_inv_freq(double theta, int32_t head_dim, double factor, double beta_fast,
+                         double beta_slow, int32_t original_max_pos, float *inv_freq,
+                         float *attn_factor) {
+  if (!inv_freq || !(theta > 1.0) || head_dim < 2 || head_dim % 2 || !(factor >= 1.0) ||
+      !(beta_slow > 0.0) || !(beta_fast > beta_slow) || original_max_pos < 1)
+    return fail(DFLASH_EINVAL, "bad YaRN parameters");
+  const int half = head_dim / 2;
+  const double two_pi = 6.283185307179586476925286766559;
+  // the real pair index whose frequency turns r times over the original context
+  auto pair_turning = [&](double r) {
+    return head_dim * std::log(original_max_pos / (r * two_pi)) / (2.0 * std::log(theta));
+  };
+  const double lo = std::max(std::floor(pair_turning(beta_fast)), 0.0);
+  const double hi = std::min(std::ceil(pair_turning(beta_slow)), (double)(half - 1));
+  for (int i = 0; i < half; ++i) {
+    const double base = std::pow(theta, -2.0 * i / head_dim);
+    const double ramp = std::min(std::max((i - lo) / std::max(hi - lo, 1e-3), 0.0), 1.0);
+    inv_freq[i] = (float)(base * (1.0 - ramp) + (base / factor) * ramp);
+  }
+  if (attn_factor) *attn_factor = factor <= 1.0 ? 1.f : (float)(0.1 * std::log(factor) + 1.0);
   return DFLASH_OK;
 }
 

@@ -166,7 +166,9 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   const int max_pos = c.max_seq_len + g.gamma;
   BA(W->cos_t, (size_t)max_pos * (g.d / 2));
   BA(W->sin_t, (size_t)max_pos * (g.d / 2));
-  BK(rope_table(W->inv_freq, max_pos, g.d / 2, W->cos_t, W->sin_t, 0));
+  // YaRN's attention temperature scales every rotated q and k: folded into the table
+  const float rope_scale = c.rope_attn_factor > 0.f ? c.rope_attn_factor : 1.f;
+  BK(rope_table(W->inv_freq, max_pos, g.d / 2, rope_scale, W->cos_t, W->sin_t, 0));
   // KV pool.
   const size_t elem = g.kv_fp8 ? 1 : 2;
   const size_t pool_elems = (size_t)g.pages * g.L * 2 * g.nkv * g.B * g.d;

@@ -131,8 +131,8 @@ cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int 
 
 cudaError_t widen_fp8(const uint8_t *src, int64_t n, bf16 *dst, cudaStream_t s);
 
-cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float *cos_t, float *sin_t,
-                       cudaStream_t s);
+cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float scale, float *cos_t,
+                       float *sin_t, cudaStream_t s);
 
 cudaError_t gather_kv(const void *pool, const Geo &g, int layer, const RowMeta *rows, int n,
                       const float *kv_scale, float *k_out, float *v_out, cudaStream_t s);

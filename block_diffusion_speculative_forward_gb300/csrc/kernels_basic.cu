@@ -244,10 +244,11 @@ cudaError_t widen_fp8(const uint8_t *src, int64_t n, bf16 *dst, cudaStream_t s) 
 }
 
 // ------------------------------------------------------------ RoPE table --
-// cos/sin of pos * inv_freq[i] for every position the head can reach,
-// evaluated in double and stored f32 ([P1] field yarn_inv_freq).
+// cos/sin of pos * inv_freq[i] for every position the head can reach, times
+// the attention temperature scale (1 without YaRN), evaluated in double and
+// stored f32 ([P1] field yarn_inv_freq).
 __global__ void k_rope_table(const float *__restrict__ inv_freq, int max_pos, int half,
-                             float *__restrict__ cos_t, float *__restrict__ sin_t) {
+                             float scale, float *__restrict__ cos_t, float *__restrict__ sin_t) {
   pdl_trigger();
   pdl_wait();
   int64_t n = (int64_t)max_pos * half;
@@ -257,14 +258,15 @@ __global__ void k_rope_table(const float *__restrict__ inv_freq, int max_pos, in
     double a = (double)pos * (double)inv_freq[i];
     double sv, cv;
     sincos(a, &sv, &cv);
-    cos_t[t] = (float)cv;
-    sin_t[t] = (float)sv;
+    cos_t[t] = (float)(cv * (double)scale);
+    sin_t[t] = (float)(sv * (double)scale);
   }
 }
 
-cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float *cos_t, float *sin_t,
-                       cudaStream_t s) {
-  launch_pdl(k_rope_table, dim3(1024), dim3(256), 0, s, inv_freq, max_pos, half, cos_t, sin_t);
+cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float scale, float *cos_t,
+                       float *sin_t, cudaStream_t s) {
+  launch_pdl(k_rope_table, dim3(1024), dim3(256), 0, s, inv_freq, max_pos, half, scale, cos_t,
+             sin_t);
   return cudaGetLastError();
 }
 

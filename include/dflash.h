@@ -94,6 +94,9 @@ typedef struct {
     int32_t kv_pool_blocks;      /* pages in the pool; 0 = max_batch * (min(ctx_window, max_seq_len)/kv_block + 2) */
     int32_t kv_dtype;            /* 0 = bf16 cache ([P2] kv_cache), 1 = FP8 E4M3 with kv_scale ([P1] kv_cache) */
     int32_t lm_head_dtype;       /* 0 = bf16 lm_head, 1 = FP8 E4M3 codes + per-row scales */
+    float rope_attn_factor;      /* YaRN attention temperature: the rotated q and k (ctx keys
+                                    included) are scaled by it; 0 = none (1). For rope_scaling
+                                    factor s, dflash_yarn_inv_freq returns 0.1 ln(s) + 1 */
 } dflash_config;
 
 typedef struct {
@@ -211,6 +214,24 @@ DFLASH_API int dflash_install_drafter_kv(dflash_handle *h, dflash_state *st,
 /* [P3] free_drafter_kv: return a carried bundle that no state owns to the
  * pool. Host-only. Errors: EINVAL (not a carried bundle); nothing changes. */
 DFLASH_API int dflash_free_drafter_kv(dflash_handle *h, const int32_t *blocks, int32_t n_blocks);
+/* The YaRN-corrected RoPE inverse-frequency table of a drafter config's
+ * rope_scaling ([P1] field yarn_inv_freq: the shipped drafter has factor 64,
+ * beta_fast 32, beta_slow 1, original_max_position_embeddings 4096), by the
+ * published YaRN "NTK-by-parts" method: pair i of the base table
+ * theta^(-2i/head_dim) turns original_max_pos / (2 pi) * base_i times over
+ * the original context; pairs from ceil(i_slow) on are divided by factor,
+ * pairs up to floor(i_fast) are kept, and those between blend the two
+ * linearly in the pair index (i_r: the real pair index that turns r times,
+ * clamped to the table). Evaluated in double, written as f32 to the HOST
+ * array inv_freq[head_dim/2]; *attn_factor (may be NULL) receives the
+ * matching temperature 0.1 ln(factor) + 1 (1 when factor <= 1), to be set
+ * as dflash_config.rope_attn_factor. factor 1 gives the plain table.
+ * Host-only. Errors: EINVAL (theta <= 1, head_dim not even and positive,
+ * factor < 1, beta_slow <= 0, beta_fast <= beta_slow, original_max_pos < 1,
+ * NULL inv_freq). */
+DFLASH_API int dflash_yarn_inv_freq(double theta, int32_t head_dim, double factor,
+                                    double beta_fast, double beta_slow, int32_t original_max_pos,
+                                    float *inv_freq, float *attn_factor);
 /* dflash_after_verify for the n states of one propose_batch in one call:
  * num_accepted[i] (0..n_out of state i) applies to states[i]. Every state is
  * checked first (known, not repeated, awaiting after_verify, count in range);

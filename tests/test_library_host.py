@@ -302,3 +302,30 @@ def test_drafter_kv_carry_matches_oracle_bookkeeping():
     lib.free_state(fresh_l)
     lib.free_state(lib.alloc_state())
     assert lib.debug_pool()[0] == 0
+
+
+@pytest.mark.parametrize("theta,d,factor,fast,slow,orig", [
+    (1e7, 128, 64.0, 32.0, 1.0, 4096),     # the shipped drafter's rope_scaling
+    (1e6, 64, 16.0, 32.0, 1.0, 2048),
+    (1e4, 128, 4.0, 32.0, 1.0, 512),
+    (1e7, 128, 1.0, 32.0, 1.0, 4096)])     # no scaling: the plain table
+def test_yarn_table_matches_oracle(theta, d, factor, fast, slow, orig):
+    """The library's host-side YaRN table and temperature against the
+    oracle's own evaluation of the published method (both in double, f32
+    out): equal up to one f32 rounding of the same double."""
+    got, att = B.yarn_inv_freq(theta, d, factor, fast, slow, orig)
+    ref = oracle.yarn_inv_freq(theta, d, factor, fast, slow, orig)
+    assert torch.allclose(got, ref, rtol=2 ** -23, atol=0)
+    assert abs(att - oracle.yarn_attention_factor(factor)) <= 1e-6
+
+
+def test_yarn_arguments_and_factor_validation():
+    for bad in [(1.0, 128, 64.0, 32.0, 1.0, 4096), (1e7, 127, 64.0, 32.0, 1.0, 4096),
+                (1e7, 128, 0.5, 32.0, 1.0, 4096), (1e7, 128, 64.0, 1.0, 1.0, 4096),
+                (1e7, 128, 64.0, 32.0, 1.0, 0)]:
+        with pytest.raises(B.DFlashError, match="EINVAL"):
+            B.yarn_inv_freq(*bad)
+    for f in (-1.0, float("nan")):
+        with pytest.raises(B.DFlashError, match="EINVAL"):
+            B.DraftHead(cfg_of(MICRO, rope_attn_factor=f), None)
+    B.DraftHead(cfg_of(MICRO, rope_attn_factor=1.4158883), None).close()
