@@ -130,8 +130,11 @@ AppendPlan plan_append(const dflash_handle *h, dflash_state *st, int64_t n, cons
   p.lo = h->cfg.ctx_window > 0 ? std::max(p.old_len, p.ws) : p.new_len;
   p.src = (const bf16 *)src;
   const int64_t B = h->cfg.kv_block;
-  for (auto &kv : st->pages)
-    if ((kv.first + 1) * B <= p.ws) p.retire.push_back(kv.first);
+  // the pages map is ordered by logical page: the retiring ones are a prefix
+  for (auto &kv : st->pages) {
+    if ((kv.first + 1) * B > p.ws) break;
+    p.retire.push_back(kv.first);
+  }
   if (p.lo < p.new_len)
     for (int64_t b = p.lo / B; b <= (p.new_len - 1) / B; ++b)
       if (!st->pages.count(b)) p.need.push_back(b);
@@ -161,13 +164,10 @@ bool pool_can_cover(const dflash_handle *h, const std::vector<AppendPlan> &plans
 
 void retire_below(dflash_handle *h, dflash_state *st, int64_t ws) {
   const int64_t B = h->cfg.kv_block;
-  for (auto it = st->pages.begin(); it != st->pages.end();) {
-    if ((it->first + 1) * B <= ws) {
-      h->pool.give(it->second);
-      it = st->pages.erase(it);
-    } else {
-      ++it;
-    }
+  // ordered by logical page: stop at the first page that stays
+  for (auto it = st->pages.begin(); it != st->pages.end() && (it->first + 1) * B <= ws;) {
+    h->pool.give(it->second);
+    it = st->pages.erase(it);
   }
 }
 
