@@ -792,7 +792,8 @@ int32_t dflash_debug_attn_work(int32_t n_seq, const int32_t *pos, const int32_t 
   std::vector<dfl::AttnItem> it;
   std::vector<dfl::AttnPair> pr;
   std::vector<int32_t> off;
-  dfl::build_attn_work_sms(g, seq, slot_cap, grid, sms, &it, &pr, &off);
+  if (!dfl::build_attn_work_sms(g, seq, slot_cap, grid, sms, &it, &pr, &off))
+    return fail(DFLASH_EINVAL, "slot_cap %d cannot hold one chunk per window", slot_cap);
   if ((int64_t)it.size() > cap_items) return fail(DFLASH_EINVAL, "items beyond cap_items");
   for (size_t i = 0; i < it.size(); ++i) {
     int32_t *o = items + 5 * i;
@@ -961,7 +962,8 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   std::vector<AttnItem> items;
   std::vector<AttnPair> pairs;
   std::vector<int32_t> cta_off;
-  build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs, &cta_off);
+  if (!build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs, &cta_off))
+    return fail(DFLASH_EINVAL, "internal: attention work beyond the slot capacity");
   CallMeta cm;
   size_t meta_bytes = 0;
   int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off, &meta_bytes);

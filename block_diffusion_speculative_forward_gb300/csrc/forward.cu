@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <queue>
 #include <string>
 
@@ -619,17 +620,20 @@ cudaError_t gather_kv_rows(const Geo &g, const Weights &W, const Buffers &B, con
 
 namespace dfl {
 
-void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
+bool build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
                      std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
                      std::vector<int32_t> *cta_off) {
-  build_attn_work_sms(g, seq, slot_cap, grid_tc, tc::num_sms(), items, pairs, cta_off);
+  return build_attn_work_sms(g, seq, slot_cap, grid_tc, tc::num_sms(), items, pairs, cta_off);
 }
 
-void build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
+bool build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
                          int grid_tc, int sms, std::vector<AttnItem> *items,
                          std::vector<AttnPair> *pairs, std::vector<int32_t> *cta_off) {
-  int64_t total = 0;
-  for (const SeqMeta &m : seq) total += (int64_t)(m.pos - m.ws) * g.nkv;
+  int64_t total = 0, longest = 0;
+  for (const SeqMeta &m : seq) {
+    total += (int64_t)(m.pos - m.ws) * g.nkv;
+    longest = std::max<int64_t>(longest, (int64_t)(m.pos - m.ws) + m.ws % 64);
+  }
   // About three SM waves of ctx items, at least 64 keys each so the partial
   // merge stays cheap. Chunk boundaries fall on positions that are multiples
   // of 64, so every tile but a window's first starts on a page.
@@ -658,46 +662,55 @@ void build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot
       }
     }
     if (slots <= slot_cap) break;
+    if (chunk >= longest) {   // one chunk per window already: the call does not fit
+      items->clear();
+      pairs->clear();
+      cta_off->clear();
+      return false;
+    }
     chunk *= 2;
   }
   cta_off->clear();
-  if (grid_tc <= 0) return;
-  // Longest-first onto the least-loaded CTA (cost: key tiles + one for the
-  // item's setup and output), then the items regrouped CTA by CTA (a
-  // counting sort; every buffer is reused across calls).
+  if (grid_tc <= 0) return true;
+  // Longest first (a stable counting sort on the cost: key tiles + one for
+  // the item's setup and output) onto the least-loaded CTA (ties: lowest
+  // CTA), then the items regrouped CTA by CTA. Every buffer is reused.
   const int n = (int)items->size();
-  thread_local std::vector<int> cost, order, owner;
-  thread_local std::vector<std::pair<int64_t, int>> heap;
+  thread_local std::vector<int> cost, order, owner, bucket;
+  thread_local std::vector<int32_t> fill;
+  thread_local std::vector<int64_t> heap;   // load << 16 | cta, a min-heap
   thread_local std::vector<AttnItem> regrouped;
   cost.resize(n);
   order.resize(n);
   owner.resize(n);
+  int max_cost = 1;
   for (int i = 0; i < n; ++i) {
     cost[i] = attention_tc_tiles(g, seq[(*items)[i].s], (*items)[i]) + 1;
-    order[i] = i;
+    max_cost = std::max(max_cost, cost[i]);
   }
-  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
-  // min-heap of (load, cta) in a flat array
-  auto greater = [](const std::pair<int64_t, int> &x, const std::pair<int64_t, int> &y) {
-    return x > y;
-  };
-  heap.clear();
-  for (int b = 0; b < grid_tc; ++b) heap.push_back({0, b});
-  std::make_heap(heap.begin(), heap.end(), greater);
+  bucket.assign(max_cost + 2, 0);
+  for (int i = 0; i < n; ++i) ++bucket[max_cost - cost[i] + 1];
+  for (int c = 0; c <= max_cost; ++c) bucket[c + 1] += bucket[c];
+  for (int i = 0; i < n; ++i) order[bucket[max_cost - cost[i]]++] = i;
+  heap.resize(grid_tc);
+  for (int b = 0; b < grid_tc; ++b) heap[b] = b;
+  std::make_heap(heap.begin(), heap.end(), std::greater<int64_t>());
   cta_off->assign(grid_tc + 1, 0);
   for (int i : order) {
-    std::pop_heap(heap.begin(), heap.end(), greater);
-    std::pair<int64_t, int> &t = heap.back();
-    owner[i] = t.second;
-    ++(*cta_off)[t.second + 1];
-    t.first += cost[i];
-    std::push_heap(heap.begin(), heap.end(), greater);
+    std::pop_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+    int64_t &t = heap.back();
+    const int b = (int)(t & 0xFFFF);
+    owner[i] = b;
+    ++(*cta_off)[b + 1];
+    t += (int64_t)cost[i] << 16;
+    std::push_heap(heap.begin(), heap.end(), std::greater<int64_t>());
   }
   for (int b = 0; b < grid_tc; ++b) (*cta_off)[b + 1] += (*cta_off)[b];
   regrouped.resize(n);
-  std::vector<int32_t> fill(cta_off->begin(), cta_off->end() - 1);
+  fill.assign(cta_off->begin(), cta_off->end() - 1);
   for (int i : order) regrouped[fill[owner[i]]++] = (*items)[i];
   items->swap(regrouped);
+  return true;
 }
 
 }  // namespace dfl

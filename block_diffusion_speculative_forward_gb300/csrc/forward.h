@@ -72,12 +72,14 @@ struct Buffers {
 // (ctx chunks plus one block-key item) within the workspace's slot capacity.
 // With grid_tc > 0 the items are also balanced over grid_tc persistent CTAs
 // of the tensor-core kernel: CTA b runs items [cta_off[b], cta_off[b + 1]).
-void build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
+// Returns false (and no items) when even one chunk per window needs more
+// slots than slot_cap; a handle's capacity always holds its widest call.
+bool build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
                      std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
                      std::vector<int32_t> *cta_off);
 // The same for a given SM count (the chunk size aims at three SM waves);
 // needs no device, so host-side tests can call it.
-void build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
+bool build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap,
                          int grid_tc, int sms, std::vector<AttnItem> *items,
                          std::vector<AttnPair> *pairs, std::vector<int32_t> *cta_off);
 

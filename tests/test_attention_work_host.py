@@ -160,3 +160,7 @@ def test_bad_arguments(fn):
     assert attn_work(fn, [10], [0], 0, 4, 100, 8)[0] == EINVAL       # no kv heads
     assert attn_work(fn, [10], [0], 2, 4, 100, 8, sms=0)[0] == EINVAL
     assert attn_work(fn, [5000] * 4, [0] * 4, 4, 16, 1000, 8, cap=3)[0] == EINVAL
+    # 16 split pairs need at least 32 slots: refused, not silently truncated
+    assert attn_work(fn, [5000] * 4, [0] * 4, 4, 16, 31, 8)[0] == EINVAL
+    items, _, _ = attn_work(fn, [5000] * 4, [0] * 4, 4, 16, 32, 8)
+    assert len(items) == 32
