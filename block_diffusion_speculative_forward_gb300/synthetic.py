@@ -19,6 +19,10 @@ Recipe (every tensor has its own ``torch.Generator`` seeded with
   * target hidden stacks: N(0, 1) bf16, ``[rows, n_target_layers * target_hidden]``;
   * inv_freq[i] = theta ** (-2 i / head_dim), evaluated in double, stored f32;
   * FP8 lm_head: per-row scale amax/448, codes = e4m3(w / scale) (torch cast);
+  * NVFP4 lm_head: a power-of-two global scale at or above amax/(448*6), one
+    E4M3 scale per 16 elements of a row = e4m3(block amax / (6 * global))
+    (torch cast), E2M1 codes of w / (scale * global) at the nearest magnitude
+    (ties to the smaller), packed two per byte, element 2j in the low nibble;
   * FP8 KV scales: U[6, 10] / 448 per (layer, kv head, K|V).
 """
 from __future__ import annotations
@@ -103,7 +107,7 @@ def make_inv_freq(head_dim: int, theta: float) -> torch.Tensor:
 
 
 def make_weights(geom: Geometry, seed: int, *, lm_head_fp8: bool = False,
-                 kv_fp8: bool = False) -> dict:
+                 kv_fp8: bool = False, lm_head_nvfp4: bool = False) -> dict:
     """All drafter weights (CPU tensors). bf16 unless noted."""
     H, I, S = geom.hidden, geom.intermediate, geom.stack_width
     w = {
@@ -135,11 +139,38 @@ def make_weights(geom: Geometry, seed: int, *, lm_head_fp8: bool = False,
         codes = (lm / scale[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
         w["lm_head_fp8"] = codes
         w["lm_head_scale"] = scale.to(torch.float32)
+    if lm_head_nvfp4:
+        p, sc, g = quantize_nvfp4(w["lm_head"])
+        w["lm_head_nvfp4"], w["lm_head_nvfp4_scale"] = p, sc
+        w["lm_head_nvfp4_global"] = torch.tensor(g, dtype=torch.float32)
     if kv_fp8:
         u = torch.rand((geom.num_layers, geom.num_kv_heads, 2), generator=_gen(seed, 7),
                        dtype=torch.float32)
         w["kv_scale"] = ((6.0 + 4.0 * u) / 448.0).to(torch.float32)
     return w
+
+
+def quantize_nvfp4(w: torch.Tensor, rows_per_pass: int = 8192):
+    """NVFP4 encoding of a [rows, k] table (k % 16 == 0), the way a
+    checkpoint carries an NVFP4 lm_head: (packed E2M1 codes [rows, k/2] uint8,
+    E4M3 block scales [rows, k/16] uint8, f32 global scale)."""
+    rows, k = w.shape
+    top = float(w.to(torch.float32).abs().max()) if w.numel() else 0.0
+    # the smallest power of two that keeps every block scale within E4M3's 448
+    g = 2.0 ** math.ceil(math.log2(top / (448.0 * 6.0))) if top > 0 else 1.0
+    mids = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])   # between E2M1 magnitudes
+    packed = torch.empty((rows, k // 2), dtype=torch.uint8)
+    scales = torch.empty((rows, k // 16), dtype=torch.uint8)
+    for r0 in range(0, rows, rows_per_pass):
+        x = w[r0:r0 + rows_per_pass].to(torch.float32).reshape(-1, k // 16, 16)
+        s8 = (x.abs().amax(dim=2) / (6.0 * g)).clamp(max=448.0).to(torch.float8_e4m3fn)
+        sv = s8.to(torch.float32)
+        q = (x / (torch.where(sv > 0, sv, torch.ones_like(sv))[..., None] * g)).clamp(-6.0, 6.0)
+        code = torch.bucketize(q.abs(), mids) | ((q < 0).to(torch.int64) << 3)
+        code = code.reshape(x.shape[0], k)
+        packed[r0:r0 + x.shape[0]] = (code[:, 0::2] | (code[:, 1::2] << 4)).to(torch.uint8)
+        scales[r0:r0 + x.shape[0]] = s8.view(torch.uint8)
+    return packed, scales, g
 
 
 def make_stack(geom: Geometry, n_rows: int, seed: int, idx: int = 0) -> torch.Tensor:

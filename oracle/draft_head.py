@@ -54,6 +54,41 @@ def e4m3_codes(x32: torch.Tensor) -> torch.Tensor:
     return x32.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).to(F64)
 
 
+def e2m1_value(code: int) -> float:
+    """OCP MX FP4 E2M1 code -> value: sign bit 3, exponent bits 2..1 (bias
+    1), mantissa bit 0; exponent 0 is subnormal (m * 0.5). Magnitudes 0, 0.5,
+    1, 1.5, 2, 3, 4, 6."""
+    sign = -1.0 if code & 8 else 1.0
+    e, m = (code >> 1) & 3, code & 1
+    return sign * (0.5 * m if e == 0 else 2.0 ** (e - 1) * (1.0 + 0.5 * m))
+
+
+def e4m3_value(code: int) -> float:
+    """OCP FP8 E4M3 byte -> value: sign bit 7, exponent bits 6..3 (bias 7),
+    mantissa bits 2..0; exponent 0 is subnormal (m * 2^-9); S.1111.111 is
+    NaN (no infinities)."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 15, code & 7
+    if e == 15 and m == 7:
+        return math.nan
+    return sign * (m * 2.0 ** -9 if e == 0 else 2.0 ** (e - 7) * (1.0 + m / 8.0))
+
+
+def nvfp4_dequant(packed: torch.Tensor, scales: torch.Tensor, global_scale: float) -> torch.Tensor:
+    """NVFP4 table -> float64 values ([P1] field lm_head_nvfp4: the target's
+    NVFP4 lm_head, 'packed + scales'). reading: the NVFP4 format: E2M1 codes
+    two per byte (element 2j in the low nibble, 2j+1 in the high one) in
+    packed [rows, k/2] uint8, one E4M3 scale per 16 consecutive elements of a
+    row in scales [rows, k/16] uint8, and one f32 global scale: value =
+    e2m1 * e4m3(scale) * global."""
+    lut4 = torch.tensor([e2m1_value(c) for c in range(16)], dtype=F64)
+    lut8 = torch.tensor([e4m3_value(c) for c in range(256)], dtype=F64)
+    p = packed.to(torch.int64)
+    q = torch.stack([lut4[p & 15], lut4[p >> 4]], dim=-1).reshape(packed.shape[0], -1)
+    sc = lut8[scales.to(torch.int64)].repeat_interleave(16, dim=1)
+    return q * sc * float(global_scale)
+
+
 # --------------------------------------------------------------- the math --
 def rms_norm(x: torch.Tensor, g: torch.Tensor, eps: float) -> torch.Tensor:
     """RMSNorm over the last axis: g * x / sqrt(mean(x^2) + eps).
@@ -212,7 +247,7 @@ class DraftHeadOracle:
     cfg keys: num_layers hidden intermediate num_q_heads num_kv_heads head_dim
     vocab gamma mask_token_id n_target_layers target_hidden rms_eps ctx_window
     kv_block prefill_chunk max_batch max_seq_len kv_pool_blocks kv_dtype
-    (0 bf16, 1 fp8) lm_head_dtype (0 bf16, 1 fp8)."""
+    (0 bf16, 1 fp8) lm_head_dtype (0 bf16, 1 fp8, 2 nvfp4)."""
 
     def __init__(self, cfg: dict, w: dict):
         self.cfg = dict(cfg)
@@ -240,11 +275,18 @@ class DraftHeadOracle:
         self.w_kv = torch.cat([torch.cat([lay["k"], lay["v"]], 0) for lay in self.layers], 0)
         self.kv_fp8 = c.get("kv_dtype", 0) == 1
         self.lm_fp8 = c.get("lm_head_dtype", 0) == 1
+        # reading: the NVFP4 head is weight-only like the FP8 one (the
+        # final-normed z is not quantised), with the block and global scales
+        # folded into the dequantised table
+        self.lm_nvfp4 = c.get("lm_head_dtype", 0) == 2
         if self.kv_fp8:
             self.kv_scale = w["kv_scale"].to(torch.float32)   # [L, nkv, 2]
         if self.lm_fp8:
             self.lm_codes = w["lm_head_fp8"]
             self.lm_scale = w["lm_head_scale"].to(F64)
+        if self.lm_nvfp4:
+            self.lm_nv = (w["lm_head_nvfp4"], w["lm_head_nvfp4_scale"],
+                          float(w["lm_head_nvfp4_global"]))
         self._lm = None
         self.pool = PagePool(self.n_pool_pages())
         self.states: list[SeqState] = []
@@ -265,11 +307,15 @@ class DraftHeadOracle:
         return max(1, c["max_batch"]) * self.pages_per_seq()
 
     def lm_head(self) -> torch.Tensor:
-        """Float64 lm_head rows, built once: bf16 table, or the FP8 codes
-        (weight-only; the per-row scale is applied to the logits)."""
+        """Float64 lm_head rows, built once: bf16 table, the FP8 codes
+        (weight-only; the per-row scale is applied to the logits) or the
+        dequantised NVFP4 table."""
         if self._lm is None:
-            src = self.lm_codes if self.lm_fp8 else self.lm_head_bf16
-            self._lm = src.to(F64)
+            if self.lm_nvfp4:
+                self._lm = nvfp4_dequant(*self.lm_nv)
+            else:
+                src = self.lm_codes if self.lm_fp8 else self.lm_head_bf16
+                self._lm = src.to(F64)
         return self._lm
 
     # -- state ----------------------------------------------------------------
