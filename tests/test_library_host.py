@@ -329,3 +329,19 @@ def test_yarn_arguments_and_factor_validation():
         with pytest.raises(B.DFlashError, match="EINVAL"):
             B.DraftHead(cfg_of(MICRO, rope_attn_factor=f), None)
     B.DraftHead(cfg_of(MICRO, rope_attn_factor=1.4158883), None).close()
+
+
+def test_noalloc_gemm_rejects_bad_arguments_without_touching_memory():
+    """dflash_gemm_noalloc's argument checks run before any CUDA call, so they
+    are checked here with pointers that are never dereferenced."""
+    f = C.CDLL(B._LIB_PATH).dflash_gemm_noalloc
+    f.restype = C.c_int
+    f.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
+                  C.c_void_p]
+    w, x, y, odd = 0x10000, 0x20000, 0x30000, 0x20008
+    EINVAL = -1
+    for args in [(None, x, y, 16, 128, 64), (w, None, y, 16, 128, 64), (w, x, None, 16, 128, 64),
+                 (w, x, y, 0, 128, 64), (w, x, y, 17, 128, 64), (w, x, y, 16, 0, 64),
+                 (w, x, y, 16, 4096 * 128 + 1, 64), (w, x, y, 16, 128, 0), (w, x, y, 16, 128, 96),
+                 (w, odd, y, 16, 128, 64), (odd, x, y, 16, 128, 64)]:
+        assert f(*args, None) == EINVAL, args
