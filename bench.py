@@ -250,6 +250,8 @@ def run_ours(args):
     lm_bytes = lm_head_bytes(geom, nd)
     achieved = lm_bytes / (lm_ms * 1e-3) / 1e9
     traffic = args.lm_traffic
+    sbytes = step_bytes(geom, ctx, 1)
+    dev_med = statistics.median(dev_ms)
     out = {
         "metric": METRIC, "value": world * K * nd / (t_ms * 1e-3), "unit": UNIT,
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": t_ms / K,
@@ -264,14 +266,24 @@ def run_ours(args):
                 "h2d_bytes_per_step": geom.stack_width * 2,
                 "d2h_bytes_per_step": 4 * nd + 12},
         "gpu_launches": int(launches),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "lm_head stage (GEMM over the vocab + argmax/confidence)",
+        # the whole propose step as the roofline's unit: every weight and the
+        # window's K/V read once, over the device time of the step's kernels
+        # (CUDA events at its first and after its last kernel, on its stream)
+        "roofline": {"bound": "hbm", "achieved": sbytes / (dev_med * 1e-3) / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": sbytes / (dev_med * 1e-3) / 1e9 / hbm,
+                     "traffic": None,
+                     "traffic_note": "per-kernel ncu DRAM bytes are in profiles/ (launch lists)",
+                     "kernel": "whole propose step (all kernels of one dflash_propose)",
                      "peak_source": f"{src} hbm_gbs",
-                     "algorithmic_bytes_per_launch": lm_bytes, "avg_ms": lm_ms},
-        "step_roofline": {"bytes_per_step": step_bytes(geom, ctx, 1),
-                          "achieved_gbs": step_bytes(geom, ctx, 1) / (t_ms / K * 1e-3) / 1e9,
-                          "frac_of_hbm": step_bytes(geom, ctx, 1) / (t_ms / K * 1e-3) / 1e9 / hbm},
+                     "algorithmic_bytes_per_launch": sbytes, "avg_ms": dev_med,
+                     "wall_frac": sbytes / (t_ms / K * 1e-3) / 1e9 / hbm},
+        "lm_head_roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                             "frac": achieved / hbm, "traffic": traffic,
+                             "traffic_note": "ncu constant for the build named in profiles/"
+                                             "lm_head_b1_dram_traffic.md, or null",
+                             "kernel": "lm_head stage (GEMM over the vocab + argmax/confidence)",
+                             "peak_source": f"{src} hbm_gbs",
+                             "algorithmic_bytes_per_launch": lm_bytes, "avg_ms": lm_ms},
         "propose_us": 1e3 * t_ms / K,
         "device_us": 1e3 * statistics.median(dev_ms),
         "device_spread": spread(dev_ms),
@@ -288,12 +300,16 @@ def run_ours(args):
         out["batch32"]["workload"] = ("full_b32: propose_batch of 32 sequences, ctx U[256,4096], "
                                       "new rows U[1,16], 50% bitmask, confidence on")
         torch.cuda.empty_cache()
-    if args.workload == "full_b1_window":
+    if not args.no_window:
+        # the ctx_window cap: 8192-row prompt, 4096-row window, 64 rounds
         out["window"] = run_window(64, W)
         torch.cuda.empty_cache()
-    if args.workload == "fp8_b128":
-        out["fp8_b128"] = run_batched(syn.FULL_G8, 1005, 128, 512, 4096, 7, True, False,
-                                      max(3, K // 2), W)
+    if not args.no_fp8:
+        # FP8 lm_head and FP8 KV cache, 128 sequences, gamma 8, 32 rounds
+        out["fp8_b128"] = run_batched(syn.FULL_G8, 1005, 128, 512, 4096, 7, True, False, 32, W)
+        out["fp8_b128"]["workload"] = ("fp8_b128: propose_batch of 128 sequences, gamma 8, "
+                                       "ctx U[512,4096], FP8 E4M3 lm_head (row scales) and KV "
+                                       "cache (per-head scales), 32 propose/after_verify rounds")
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(w, cfg, geom, seed, ctx, args.cpu_steps)
@@ -504,15 +520,16 @@ def run_window(K, W):
     geom, seed, prompt, window = syn.FULL, 1003, 8192, 4096
     nd = geom.gamma - 1
     rounds = K + W
+    probed = 16                       # further rounds with the device-time probe
     w = syn.make_weights(geom, seed)
     wd = B.weights_to_device(w)
     del w
-    cfg = head_cfg(geom, 1, prompt + geom.gamma * (rounds + 2) + 64, ctx_window=window)
+    cfg = head_cfg(geom, 1, prompt + geom.gamma * (rounds + probed + 2) + 64, ctx_window=window)
     head = B.DraftHead(cfg, wd)
     st = head.alloc_state()
     g = torch.Generator(device="cuda").manual_seed(seed)
-    stack = torch.randn((prompt + geom.gamma * (rounds + 2), geom.stack_width), device="cuda",
-                        generator=g).to(torch.bfloat16)
+    stack = torch.randn((prompt + geom.gamma * (rounds + probed + 2), geom.stack_width),
+                        device="cuda", generator=g).to(torch.bfloat16)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     head.prefill(st, stack[:prompt - 1])
@@ -522,24 +539,62 @@ def run_window(K, W):
     pos, used, n_new = prompt - 1, prompt - 1, 1
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    import ctypes as C
+    lib = B.lib()
+    lib.dflash_debug_set_step_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
+    sb, se = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in (sb, se):
+        e.record(s)
+    torch.cuda.synchronize()
+    dev_ms, round_bytes = [], []
+    # the timed rounds and the device-time probe are separate passes over the
+    # same call sequence shape: rounds W.. are timed without probes, then a
+    # second set of rounds is probed
+    clk = ClockSampler(torch.cuda.current_device())
     for r in range(rounds):
         if r == W:
             torch.cuda.synchronize()
+            clk.__enter__()
             e0.record(s)
         pos += n_new
         got = head.propose(st, 1000 + r, pos, stack[used:used + n_new], nd)
+        if r >= W:
+            round_bytes.append(step_bytes(geom, min(window, pos - n_new), n_new))
         used += n_new
         k = min(ks[r], got[1])
         head.after_verify(st, k)
         n_new = k + 1
     e1.record(s)
     torch.cuda.synchronize()
+    clk.__exit__()
     ms = e0.elapsed_time(e1) / K
+    lib.dflash_debug_set_step_probe(head.ptr, C.c_void_p(sb.cuda_event), C.c_void_p(se.cuda_event))
+    ks2 = syn.uniform_ints(0, nd, probed, seed, 8)
+    for r in range(probed):
+        pos += n_new
+        got = head.propose(st, 2000 + r, pos, stack[used:used + n_new], nd)
+        used += n_new
+        if r >= 2:
+            dev_ms.append(sb.elapsed_time(se))
+        k = min(ks2[r], got[1])
+        head.after_verify(st, k)
+        n_new = k + 1
+    lib.dflash_debug_set_step_probe(head.ptr, None, None)
     head.close()
+    hbm, _, src = peaks()
+    byts = statistics.mean(round_bytes)
+    dev = statistics.median(dev_ms)
     return {"value": nd / (ms * 1e-3), "unit": UNIT, "propose_us": 1e3 * ms, "rounds": K,
             "warmup": W, "prompt": prompt, "ctx_window": window, "prefill_ms": prefill_ms,
+            "device_us": 1e3 * dev, "device_spread": spread(dev_ms),
+            "bytes_per_round": byts, "clocks": clk.summary(),
+            "roofline": {"bound": "hbm", "achieved": byts / (dev * 1e-3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": byts / (dev * 1e-3) / 1e9 / hbm,
+                         "wall_frac": byts / (ms * 1e-3) / 1e9 / hbm,
+                         "peak_source": f"{src} hbm_gbs",
+                         "kernel": "whole propose round (device time of its kernels)"},
             "workload": "full_b1_window: prompt 8192 (8191 prefilled, 4096-row window), then "
-                        "propose/after_verify rounds, k ~ U[0, 15], k + 1 new rows per round"}
+                        "64 propose/after_verify rounds, k ~ U[0, 15], k + 1 new rows per round"}
 
 
 def cpu_baseline(w, cfg, geom, seed, ctx, n_steps):
@@ -680,10 +735,10 @@ def main():
     ap.add_argument("--no-batch", action="store_true", help="skip the batch-32 leg")
     ap.add_argument("--batch-only", action="store_true",
                     help="only the batch-32 leg (for profiling it alone)")
-    ap.add_argument("--workload", default="full_b1",
-                    choices=["full_b1", "fp8_b128", "full_b1_window"],
-                    help="fp8_b128 adds the 128-sequence FP8 configuration, full_b1_window the "
-                         "8192-row prompt with a 4096-row window (64 rounds)")
+    ap.add_argument("--no-window", action="store_true",
+                    help="skip the 8192-row prompt / 4096-row window leg (64 rounds)")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the 128-sequence FP8 leg (32 rounds)")
     ap.add_argument("--kernel", default=None, choices=["lm_head", "lm_head_b32"],
                     help="time one kernel alone instead of the propose step")
     # dram__bytes_read.sum + dram__bytes_write.sum of one batch-1 lm_head GEMM

@@ -85,6 +85,8 @@ def lib() -> C.CDLL:
             "dflash_debug_gather_kv": (C.c_int, [vp, vp, i32, i64, i32, vp, vp, vp]),
             "dflash_debug_set_taps": (C.c_int, [vp, vp, vp, vp]),
             "dflash_debug_set_graphs": (C.c_int, [vp, i32]),
+            "dflash_debug_set_fault": (C.c_int, [vp, i64]),
+            "dflash_debug_rows": (C.c_int, [vp, i32, C.POINTER(i32), C.POINTER(C.c_float), vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -333,6 +335,18 @@ class DraftHead:
     def set_graphs(self, enable: bool):
         """Replay captured CUDA graphs (default) or launch kernels one by one."""
         _check(lib().dflash_debug_set_graphs(self.ptr, 1 if enable else 0))
+
+    def set_fault(self, wait_ns: int):
+        """Test hook: every GEMM of later proposes aborts after waiting wait_ns
+        on a barrier nothing arrives on (0 = off)."""
+        _check(lib().dflash_debug_set_fault(self.ptr, int(wait_ns)))
+
+    def debug_rows(self, n_rows: int):
+        """(ids, p1) of the last propose's draft rows, sequence-major."""
+        ids = (C.c_int32 * max(n_rows, 1))()
+        p1 = (C.c_float * max(n_rows, 1))()
+        _check(lib().dflash_debug_rows(self.ptr, int(n_rows), ids, p1, _stream()))
+        return list(ids)[:n_rows], list(p1)[:n_rows]
 
     def set_taps(self, x_taps=None, z=None, logits=None):
         self._taps = (x_taps, z, logits)

@@ -348,6 +348,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------ softmax -----------
+    // Every wait here is taken with one answer per warp (the TMEM loads and
+    // stores after it are warp-collective).
     // Scores in log2 units (x = s * scale * log2 e, p = 2^(x - m)). O
     // accumulates in TMEM over the item's tiles relative to the reference
     // max m; m moves (and O, l are rescaled) only when a tile's max exceeds
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < ig.ntiles; ++j, ++T) {
         const int sbuf = T & 1;
-        if (!mbar_wait(smem_u32(&bar->s_full[sbuf]), (T >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(smem_u32(&bar->s_full[sbuf]), (T >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         float x[AK];
 #pragma unroll
@@ -397,7 +399,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (m != -INFINITY) {
             // O holds tiles < T: wait for PV(T-1), then rescale it in TMEM
             const int t1 = T - 1;
-            if (!mbar_wait(smem_u32(&bar->p_empty[t1 & 1]), (t1 >> 1) & 1, abort_flag)) {
+            if (!mbar_wait_warp(smem_u32(&bar->p_empty[t1 & 1]), (t1 >> 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const float mm = (m == -INFINITY) ? 0.f : m;
         // P buffer of this tile was last read by PV(T-2)
-        if (T >= 2 && !mbar_wait(smem_u32(&bar->p_empty[sbuf]), ((T - 2) >> 1) & 1, abort_flag)) {
+        if (T >= 2 && !mbar_wait_warp(smem_u32(&bar->p_empty[sbuf]), ((T - 2) >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       // the item's last PV, then O out of TMEM
       const int tl = T - 1;
-      if (!mbar_wait(smem_u32(&bar->p_empty[tl & 1]), (tl >> 1) & 1, abort_flag)) {
+      if (!mbar_wait_warp(smem_u32(&bar->p_empty[tl & 1]), (tl >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }

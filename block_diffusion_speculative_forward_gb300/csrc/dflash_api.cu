@@ -59,6 +59,7 @@ struct PagePool {
     return id;
   }
   void give(int32_t id) { free_ids.insert(id); }
+  void take_id(int32_t id) { free_ids.erase(id); }
   int32_t n_free() const { return (int32_t)free_ids.size(); }
 };
 
@@ -168,6 +169,52 @@ void retire_below(dflash_handle *h, dflash_state *st, int64_t ws) {
   for (auto it = st->pages.begin(); it != st->pages.end() && (it->first + 1) * B <= ws;) {
     h->pool.give(it->second);
     it = st->pages.erase(it);
+  }
+}
+
+// The host state of the states a call touches, taken before it commits
+// anything: a call that fails after its commit (a CUDA error, or a device
+// status word raised by its kernels) puts every state and the pool back.
+struct Snapshot {
+  struct One {
+    dflash_state *st;
+    int64_t ctx_len;
+    std::map<int64_t, int32_t> pages;
+    bool pending;
+    int64_t pend_pos;
+    int32_t pend_nout;
+    int64_t expected_next;
+  };
+  std::vector<One> states;
+};
+
+Snapshot snapshot(dflash_state *const *states, int n) {
+  Snapshot s;
+  for (int i = 0; i < n; ++i) {
+    dflash_state *st = states[i];
+    s.states.push_back({st, st->ctx_len, st->pages, st->pending, st->pend_pos, st->pend_nout,
+                        st->expected_next});
+  }
+  return s;
+}
+
+void rollback(dflash_handle *h, const Snapshot &snap) {
+  std::set<int32_t> now, then;
+  for (const auto &o : snap.states) {
+    for (auto &kv : o.st->pages) now.insert(kv.second);
+    for (auto &kv : o.pages) then.insert(kv.second);
+  }
+  for (int32_t id : now)
+    if (!then.count(id)) h->pool.give(id);       // taken by the failed call
+  for (int32_t id : then)
+    if (!now.count(id)) h->pool.take_id(id);     // retired by it
+  for (const auto &o : snap.states) {
+    o.st->ctx_len = o.ctx_len;
+    o.st->pages = o.pages;
+    o.st->pending = o.pending;
+    o.st->pend_pos = o.pend_pos;
+    o.st->pend_nout = o.pend_nout;
+    o.st->expected_next = o.expected_next;
   }
 }
 
@@ -464,6 +511,7 @@ int dflash_prefill(dflash_handle *h, dflash_state *st, const void *stack, int32_
     return fail(DFLASH_EINVAL, "stack must be a 16-byte aligned device pointer");
   std::vector<AppendPlan> plans{plan_append(h, st, n_rows, stack)};
   if (!pool_can_cover(h, plans)) return fail(DFLASH_ENOMEM, "KV pool exhausted");
+  const Snapshot snap = snapshot(&st, 1);
   commit_plans(h, plans);
   st->ctx_len = plans[0].new_len;
   if (!h->compute) return DFLASH_BOOKKEEPING_ONLY;
@@ -474,9 +522,14 @@ int dflash_prefill(dflash_handle *h, dflash_state *st, const void *stack, int32_
     std::vector<dfl::RowMeta> chunk(rows.begin() + a, rows.begin() + a + nb);
     dfl::CallMeta cm;
     int rc = upload_meta(h, {}, chunk, {}, s, &cm);
-    if (rc) return rc;
-    rc = dfl::ctx_append(h->g, h->w, h->b, cm.rows, cm.n_rows, h->M_ctx, s);
-    if (rc) return fail(rc, "%s", dfl::last_build_error());
+    if (rc == DFLASH_OK) {
+      rc = dfl::ctx_append(h->g, h->w, h->b, cm.rows, cm.n_rows, h->M_ctx, s);
+      if (rc) fail(rc, "%s", dfl::last_build_error());
+    }
+    if (rc) {
+      rollback(h, snap);   // no state claims rows that were never written
+      return rc;
+    }
   }
   return DFLASH_OK;
 }
@@ -694,6 +747,23 @@ int dflash_debug_set_step_probe(dflash_handle *h, void *ev_begin, void *ev_end) 
 
 int64_t dflash_debug_launch_count(void) { return dfl::launch_count(); }
 
+int dflash_debug_set_fault(dflash_handle *h, int64_t wait_ns) {
+  if (!h || wait_ns < 0 || wait_ns > 2000000000ll)
+    return fail(DFLASH_EINVAL, "NULL handle or wait outside 0..2e9 ns");
+  h->b.fault_ns = wait_ns;
+  return DFLASH_OK;
+}
+
+int dflash_debug_rows(dflash_handle *h, int32_t n_rows, int32_t *ids, float *p1, void *stream) {
+  if (!h || !h->compute || n_rows < 0 || n_rows > h->D_max || (n_rows > 0 && (!ids || !p1)))
+    return fail(DFLASH_EINVAL, "NULL argument, no device side, or rows outside 0..%d", h ? h->D_max : 0);
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(cudaMemcpyAsync(ids, h->b.row_id, sizeof(int32_t) * (size_t)n_rows, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(p1, h->b.row_p1, sizeof(float) * (size_t)n_rows, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  return DFLASH_OK;
+}
+
 int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t m, int32_t n_w, int32_t k,
                       int32_t grid_cap, void *stream) {
   if (!w || !x || !y || m <= 0 || n_w <= 0 || k <= 0 || k % 64)
@@ -838,7 +908,7 @@ int run_forward(dflash_handle *h, const CallMeta &cm, int nd, const int32_t *bit
         (uintptr_t)cm.n_seq, (uintptr_t)cm.n_rows, (uintptr_t)nd, (uintptr_t)bitmask,
         (uintptr_t)h->b.tap_x, (uintptr_t)h->b.tap_z, (uintptr_t)h->b.tap_logits,
         (uintptr_t)h->b.probe_begin, (uintptr_t)h->b.probe_end,
-        (uintptr_t)h->b.step_begin,  (uintptr_t)h->b.step_end};
+        (uintptr_t)h->b.step_begin,  (uintptr_t)h->b.step_end, (uintptr_t)h->b.fault_ns};
     auto it = h->graphs.find(key);
     if (it == h->graphs.end()) {
       const int64_t l0 = launch_count();
@@ -912,6 +982,7 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   for (int i = 0; i < n; ++i)
     plans.push_back(plan_append(h, states[i], n_new[i], new_rows ? new_rows[i] : nullptr));
   if (!pool_can_cover(h, plans)) return fail(DFLASH_ENOMEM, "KV pool exhausted");
+  const Snapshot snap = snapshot(states, n);
   commit_plans(h, plans);
   for (auto &p : plans) p.st->ctx_len = p.new_len;
   if (!h->compute) {
@@ -952,9 +1023,11 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
       // the window's pages are consecutive keys of the ordered page map
       auto it = st->pages.lower_bound(m.ws / c.kv_block);
       for (int64_t b = m.ws / c.kv_block; b <= (m.pos - 1) / c.kv_block; ++b, ++it) {
-        if (it == st->pages.end() || it->first != b)
+        if (it == st->pages.end() || it->first != b) {
+          rollback(h, snap);
           return fail(DFLASH_ESTATE, "internal: window page %lld of sequence %d missing",
                       (long long)b, i);
+        }
         page_ids.push_back(it->second);
       }
     }
@@ -962,21 +1035,42 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   std::vector<AttnItem> items;
   std::vector<AttnPair> pairs;
   std::vector<int32_t> cta_off;
-  if (!build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs, &cta_off))
+  if (!build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs, &cta_off)) {
+    rollback(h, snap);
     return fail(DFLASH_EINVAL, "internal: attention work beyond the slot capacity");
+  }
   CallMeta cm;
   size_t meta_bytes = 0;
   int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off, &meta_bytes);
-  if (rc) return rc;
-  rc = run_forward(h, cm, num_drafts, bitmask, meta_bytes, s);
-  if (rc) return rc;
-  // Results are on the host after one synchronisation.
+  if (rc == DFLASH_OK) rc = run_forward(h, cm, num_drafts, bitmask, meta_bytes, s);
+  if (rc == DFLASH_OK) {
+    // Results are on the host after one synchronisation.
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+      rc = fail(DFLASH_ECUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  }
+  if (rc) {
+    rollback(h, snap);
+    return rc;
+  }
   size_t nd = (size_t)num_drafts;
-  CK(cudaStreamSynchronize(s));
   const int32_t *status = (const int32_t *)h->b.out_host;
   const uint32_t *dr = (const uint32_t *)(h->b.out_host + h->b.off_drafts);
   const int32_t *no = (const int32_t *)(h->b.out_host + h->b.off_nout);
   const float *cf = (const float *)(h->b.out_host + h->b.off_conf);
+  if (*status) {
+    // The device abandoned or rejected part of the call's work: nothing of it
+    // is returned and every state goes back to where it was. The status word
+    // and the stream-K tile counters (an aborted CTA may have left a tile's
+    // count behind) start from zero again.
+    int st_bits = *status;
+    rollback(h, snap);
+    CK(cudaMemsetAsync(h->b.status, 0, sizeof(int), s));
+    CK(cudaMemsetAsync(h->b.counters, 0, sizeof(int) * (size_t)h->b.n_counters, s));
+    CK(cudaStreamSynchronize(s));
+    return fail(DFLASH_EDEVICE, "device status %d (%s)", st_bits,
+                (st_bits & dfl::ST_TIMEOUT) ? "a bounded wait ran out" : "a bounds check tripped");
+  }
   for (int i = 0; i < n; ++i) {
     n_out[i] = no[i];
     memcpy(drafts + i * nd, dr + i * nd, nd * sizeof(uint32_t));
@@ -985,11 +1079,6 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
     states[i]->pend_pos = positions[i];
     states[i]->pend_nout = no[i];
     states[i]->expected_next = -1;
-  }
-  if (*status) {
-    int st_bits = *status;
-    CK(cudaMemsetAsync(h->b.status, 0, sizeof(int), s));
-    return fail(DFLASH_EDEVICE, "device bounds check tripped (status %d)", st_bits);
   }
   return DFLASH_OK;
 }

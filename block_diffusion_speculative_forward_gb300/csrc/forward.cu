@@ -287,6 +287,7 @@ cudaError_t tc_gemm(const Buffers &B, const CUtensorMap &map_w, ActBuf act, int 
   p.ws = B.ws;
   p.counters = B.counters;
   p.status = B.status;
+  p.fault_ns = B.fault_ns;
   p.dp = dp;
   const int bn = dp ? tc::pick_bn_dp(m_act, n_w, k) : tc::pick_bn(m_act);
   return tc::gemm(map_w, B.act_map[act][bn_index(bn)], bn, p, s);
@@ -307,6 +308,7 @@ int project(const Buffers &B, const CUtensorMap &map_w, ActBuf act, int m_act, i
   p.ws = B.ws;
   p.counters = B.counters;
   p.status = B.status;
+  p.fault_ns = B.fault_ns;
   const int bn = tc::pick_bn(m_act);
   if (tc::partial_ok(m_act, n_w, k)) {
     p.epi = EPI_TC_PARTIAL;
@@ -405,6 +407,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       p.ws = B.ws;
       p.counters = B.counters;
       p.status = B.status;
+      p.fault_ns = B.fault_ns;
       p.dp = 1;
       LK(tc::gemm(W.map_qkv[l], B.act_map[ACT_H][bn_index(bn_qkv)], bn_qkv, p, s));
       QkvPostArgs qp{};
@@ -445,6 +448,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       p.ws = B.ws;
       p.counters = B.counters;
       p.status = B.status;
+      p.fault_ns = B.fault_ns;
       p.seq = cm.seq;
       p.gamma = g.gamma;
       p.head_dim = g.d;
@@ -522,6 +526,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       p.ws = B.ws;
       p.counters = B.counters;
       p.status = B.status;
+      p.fault_ns = B.fault_ns;
       p.u_out = B.u;
       p.dp = dp;
       LK(tc::gemm(W.map_gu[l], B.act_map[ACT_H][bn_index(bn_gu)], bn_gu, p, s));
@@ -564,6 +569,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     p.ws = B.ws;
     p.counters = B.counters;
     p.status = B.status;
+    p.fault_ns = B.fault_ns;
     p.bitmask = bitmask;
     p.mask_words = (g.V + 31) / 32;
     p.nd = nd;
@@ -600,6 +606,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     p.ws = B.ws;
     p.counters = B.counters;
     p.status = B.status;
+    p.fault_ns = B.fault_ns;
     const int bn = tc::pick_bn(D);
     LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
   }

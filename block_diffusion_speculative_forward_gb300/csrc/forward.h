@@ -66,6 +66,7 @@ struct Buffers {
   int attn_grid_tc = 0;         // persistent CTAs of the tensor-core attention
   int attn_slots = 0;           // slot capacity
   int64_t attn_slot_floats = 0; // n_q*d + 2*n_q per slot
+  int64_t fault_ns = 0;         // test hook of every GEMM launch (GemmParams::fault_ns)
 };
 
 // Cuts every (sequence, kv head) key range of the call into split-KV items

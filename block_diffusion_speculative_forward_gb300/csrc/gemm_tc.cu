@@ -74,7 +74,7 @@ struct Part {
 
 // ----------------------------------------------------------- epilogues --
 struct Smem {
-  uint64_t full[8], empty[8], acc_full[2], acc_empty[2], drain;
+  uint64_t full[8], empty[8], acc_full[2], acc_empty[2], drain, never;
   uint32_t tmem_base;
   uint32_t drain_issued, drain_parity;
   int abort_flag;
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&sm->acc_empty[b]), 4);
     }
     mbar_init(smem_u32(&sm->drain), 1);
+    mbar_init(smem_u32(&sm->never), 1);   // nothing ever arrives (test hook)
     sm->abort_flag = 0;
     sm->drain_issued = 0;
     sm->drain_parity = 0;
@@ -427,14 +428,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int f_local = q * 32 + lane;       // weight row within the tile
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t it = it_begin; it < it_end;) {
+    // test hook: one epilogue thread waits on a barrier nothing arrives on
+    // until the limit runs out, which aborts the CTA mid-stream
+    bool live = true;
+    if (p.fault_ns > 0 && threadIdx.x == 64)
+      live = fault_wait(smem_u32(&sm->never), (uint64_t)p.fault_ns, abort_flag);
+    live = epi_all(live);
+    for (int64_t it = it_begin; live && it < it_end;) {
       const int t = dp ? (int)blockIdx.x + (int)(it / kb) * (int)gridDim.x : (int)(it / kb);
       const int k0 = (int)(it % kb);
       const int k1 = (int)((int64_t)kb < (int64_t)k0 + (it_end - it) ? (int64_t)kb : (int64_t)k0 + (it_end - it));
       const int tm = t % p.tiles_m, tn = t / p.tiles_m;
       const int f = tm * BM + f_local;
       const bool whole = (k0 == 0 && k1 == kb);
-      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), acc_phase, abort_flag)) break;
+      // all 128 epilogue threads take the same decision (named barriers and
+      // warp-collective TMEM loads follow)
+      if (!epi_all(mbar_wait(smem_u32(&sm->acc_full[acc]), acc_phase, abort_flag))) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
       // partial slot of this CTA for this tile: its first or its last segment

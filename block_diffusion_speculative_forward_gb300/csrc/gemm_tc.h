@@ -113,6 +113,9 @@ struct GemmParams {
   bf16 *q_out, *k_out, *v_out;   // [m_act, q_rows], [m_act, k_rows], [m_act, k_rows]
   // SwiGLU epilogue: u[m_act, n_w / 2]
   bf16 *u_out;
+  // test hook: > 0 makes every CTA abort after waiting this long (ns) on a
+  // barrier that nothing arrives on (the bounded-wait abort path)
+  int64_t fault_ns;
   // filled by the launcher
   int tiles_m, tiles_n;
 };

@@ -226,7 +226,8 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                   : 0xffffffffu;
         }
       }
-      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), acc_phase, abort_flag)) break;
+      // one decision per warp: the TMEM loads below are warp-collective
+      if (!mbar_wait_warp(smem_u32(&sm->acc_full[acc]), acc_phase, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * LM_N;
       float m = -INFINITY, s = 0.f;

@@ -55,6 +55,44 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     }
   }
 }
+// The same wait by every lane of a warp, with one answer for the whole warp:
+// a lane that gives up (abort or timeout) makes every lane give up, so the
+// warp-collective tcgen05 loads after a wait stay convergent even when a
+// barrier completes while another lane is already aborting.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int *abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+// Agreement of the four epilogue warps (named barrier 1, 128 threads): true
+// on every thread only when every thread passes true. Used after each
+// per-thread wait so that the epilogue's named barriers and warp-collective
+// loads are reached by all 128 threads or by none.
+__device__ __forceinline__ bool epi_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+// Test hook: waits up to limit_ns on a barrier that nothing arrives on, then
+// raises the abort flag (the CTA then takes its ordinary abort path).
+__device__ __forceinline__ bool fault_wait(uint32_t never_bar, uint64_t limit_ns,
+                                           volatile int *abort_flag) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_test(never_bar, 0)) {
+    if (global_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t bar, int x,
                                             int y, uint64_t policy) {
   asm volatile(

@@ -10,7 +10,15 @@
  * Conventions for every call:
  *   - Every call returns a status (DFLASH_OK or a code below). On any error
  *     the handle and every state are unchanged: a call checks all arguments
- *     and the KV pool's capacity before it mutates anything.
+ *     and the KV pool's capacity before it mutates anything, and a call that
+ *     fails after that point (a CUDA error, or DFLASH_EDEVICE: a kernel's
+ *     bounds check or bounded wait gave up) puts every state it touched and
+ *     the pool back as they were. After DFLASH_EDEVICE the call's outputs
+ *     are not written and the device work it started has been abandoned:
+ *     K/V slots past a restored ctx_len may hold partial writes (the next
+ *     append of those positions overwrites them), and a page that the call
+ *     retired and took again may have lost rows below the window, which no
+ *     later propose of that state attends. The handle stays usable.
  *   - dflash_last_error() returns a message for the last failing call on the
  *     calling thread.
  *   - "dev" marks a device pointer, "host" a host pointer. Device work runs on
@@ -73,7 +81,7 @@ enum {
     DFLASH_ESTATE = -3,           /* call out of order (propose twice, after_verify without propose) */
     DFLASH_EPOSITION = -4,        /* position != ctx_len + n_new, or != the position after_verify set */
     DFLASH_ECUDA = -5,            /* a CUDA call failed */
-    DFLASH_EDEVICE = -6           /* a kernel's own bounds check tripped (device status word) */
+    DFLASH_EDEVICE = -6           /* a kernel's bounds check or bounded wait gave up (device status word) */
 };
 
 typedef struct {
@@ -272,6 +280,20 @@ DFLASH_API int dflash_debug_set_step_probe(dflash_handle *h, void *ev_begin, voi
  * new ctx rows, drafts, bitmask and tap/probe pointers); enable = 0 launches
  * the kernels one by one instead (same results). On by default. */
 DFLASH_API int dflash_debug_set_graphs(dflash_handle *h, int32_t enable);
+/* Test hook of the bounded-wait abort path: with wait_ns > 0, every
+ * tensor-core GEMM of later propose* calls has one thread of each CTA wait up
+ * to wait_ns (<= 2e9) on a barrier that nothing arrives on; the wait runs
+ * out, the CTA raises the device status word, drains its own copies and
+ * MMAs, frees its TMEM and exits, and the call returns DFLASH_EDEVICE with
+ * its states put back. 0 turns it off. Errors: EINVAL. */
+DFLASH_API int dflash_debug_set_fault(dflash_handle *h, int64_t wait_ns);
+/* Per draft row of the last propose* call, sequence-major (n*num_drafts
+ * rows): the argmax token id (-1 when the bitmask allows nothing) and the
+ * top-1 softmax probability 1 / sum_v exp(l_v - max l), as the chain
+ * confidence takes its minimum over them. ids, p1: host [n_rows].
+ * Synchronises the stream. Errors: EINVAL, ECUDA. */
+DFLASH_API int dflash_debug_rows(dflash_handle *h, int32_t n_rows, int32_t *ids, float *p1,
+                                 void *stream);
 /* Kernels this library has launched since it was loaded (all handles). */
 DFLASH_API int64_t dflash_debug_launch_count(void);
 /* One tensor-core GEMM in isolation, for kernel tests: y[m, n_w] = x[m, k] *
@@ -291,8 +313,11 @@ DFLASH_API int dflash_debug_gemm(const void *w, const void *x, float *y, int32_t
  * Limits: 1 <= m <= 16, k % 64 == 0, n_w <= 524288 (4096 tiles of 128 rows);
  * w and x 16-byte aligned dev pointers, y a dev pointer. Larger sizes return
  * DFLASH_EINVAL. The first call on each device looks up the array's device
- * address with that device current; make that first call before any stream
- * capture. All calls share the array, so calls that overlap on the GPU race:
+ * address with that device current and keeps it for later calls; make that
+ * first call before any stream capture. The kept address belongs to the
+ * device's current context: after cudaDeviceReset (or any other end of that
+ * context) do not call this entry point again in the same process, since
+ * the kept address would no longer be valid. All calls share the array, so calls that overlap on the GPU race:
  * order them. Synchronises the stream; returns DFLASH_OK, DFLASH_EINVAL,
  * DFLASH_ECUDA or DFLASH_EDEVICE (dflash_last_error is not updated). */
 DFLASH_API int dflash_gemm_noalloc(const void *w, const void *x, float *y, int32_t m, int32_t n_w,

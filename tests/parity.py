@@ -5,7 +5,9 @@ tolerances of the parity gate:
   * residual taps, final z, gathered ctx K/V: max-abs 3e-2;
   * logits: per row max|diff| / max|ref| <= 2e-2 (5e-2 on FP8 paths);
   * draft ids: exact wherever the oracle's masked top-1 - top-2 gap > 1e-2;
-  * confidence: |diff| <= 1e-2.
+  * confidence: |diff| <= 1e-2 end to end; and, teacher-forced (the
+    oracle's logits from the GPU's own final-normed rows), every draft row's
+    top-1 probability and the chain minimum within 1e-2 relative.
 Deep stacks are compared layer by layer (teacher-forced), see E2E_* below."""
 from __future__ import annotations
 
@@ -23,6 +25,11 @@ LOGIT_TOL = 2e-2
 LOGIT_TOL_FP8 = 5e-2
 GAP = 1e-2
 CONF_TOL = 1e-2
+# Teacher-forced top-1 probabilities (oracle logits from the GPU's own z):
+# relative, so that probabilities of 1e-3 .. 1e-6 (random weights, full
+# vocab) are checked as strictly as probabilities near one.
+CONF_REL = 1e-2
+P1_FLOOR = 1e-12
 # End to end over many layers, an fp32 evaluation of the method drifts from the
 # fp64 oracle (measured: the oracle in fp32 vs fp64 at the shipped geometry,
 # 8 layers: max residual diff 0.09, logits ~1.3% of max|l|). End-to-end
@@ -99,6 +106,38 @@ def check_abs(ref, got, tol, what):
     return err
 
 
+def check_rows(lg_ref, allowed, ids, p1, got_out=None):
+    """The lm_head stage row by row, teacher-forced: lg_ref are the oracle's
+    logits of the draft rows computed from the GPU's own final-normed rows, so
+    the only difference left is the stage's own arithmetic (the GEMM's fp32
+    accumulation and the per-tile max / argmax / sum-exp merge). Every row's
+    id matches where the top-1/top-2 gap exceeds GAP (elsewhere the GPU's id
+    must be within GAP of the max); every row's top-1 probability and the
+    chain confidence match within CONF_REL relative. Returns the p1 values."""
+    d_ref, n_ref, c_ref, p1_ref = oracle.select_drafts(lg_ref, allowed)
+    lg = lg_ref.to(torch.float64)
+    if allowed is not None:
+        lg = torch.where(allowed[None, :], lg, torch.full_like(lg, -math.inf))
+    g = gaps(lg_ref, allowed)
+    for i in range(n_ref):
+        if g[i] > GAP:
+            assert ids[i] == d_ref[i], f"row {i}: id {ids[i]} vs oracle {d_ref[i]} (gap {float(g[i]):.4f})"
+        else:
+            assert 0 <= ids[i] < lg.shape[1] and float(lg[i].max() - lg[i, ids[i]]) <= GAP, \
+                f"row {i}: id {ids[i]} is not within {GAP} of the row's max"
+        rel = abs(p1[i] - p1_ref[i]) / max(p1_ref[i], P1_FLOOR)
+        assert rel <= CONF_REL, f"row {i}: p1 {p1[i]:.6e} vs oracle {p1_ref[i]:.6e} (rel {rel:.2e})"
+    for i in range(n_ref, len(ids)):
+        assert ids[i] == -1 and p1[i] == 0.0, f"row {i} after the chain ended: {ids[i]}, {p1[i]}"
+    if got_out is not None:
+        got_d, got_n, got_c = got_out
+        assert got_n == n_ref, (got_n, n_ref)
+        if got_c is not None:
+            ref_c = min(p1_ref[:n_ref]) if n_ref else 0.0
+            assert abs(got_c - ref_c) <= CONF_REL * max(ref_c, P1_FLOOR), (got_c, ref_c)
+    return p1_ref
+
+
 def check_seq(pair: Pair, ref_tap: dict, ref_out, got_out, seq_idx: int, n_seq: int,
               nd: int, allowed=None, hidden=True):
     """Compare one sequence of a propose call: taps, logits, drafts, conf."""
@@ -118,6 +157,12 @@ def check_seq(pair: Pair, ref_tap: dict, ref_out, got_out, seq_idx: int, n_seq: 
     n = check_drafts(ref_d[:ref_n], got_d[:got_n], ref_tap["logits"], allowed)
     if got_c is not None:
         assert abs(ref_c - got_c) <= CONF_TOL, (ref_c, got_c)
+    # the lm_head stage teacher-forced from the GPU's own final-normed rows
+    g = pair.geom.gamma
+    ids, p1 = pair.lib.debug_rows(n_seq * nd)
+    z_got = pair.tz[seq_idx * g:(seq_idx + 1) * g].double().cpu()
+    check_rows(pair.ora.draft_logits(z_got, nd), allowed, ids[seq_idx * nd:(seq_idx + 1) * nd],
+               p1[seq_idx * nd:(seq_idx + 1) * nd], got_out)
     return n
 
 

@@ -68,16 +68,25 @@ def bench(monkeypatch):
 def test_batch1_leg(bench):
     args = bench.argparse.Namespace(gpus=1, steps=12, warmup=3, impl="ours", cpu_steps=1,
                                     no_cpu=True, no_batch=True, batch_only=False,
-                                    workload="full_b1", kernel=None, lm_traffic=1.0)
+                                    no_window=True, no_fp8=True, kernel=None, lm_traffic=1.0)
     out = {}
     bench.print = lambda s, **k: out.setdefault("line", s)
     bench.run_ours(args)
     line = bench.json.loads(out["line"])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e",
-                "gpu_launches", "roofline", "clocks", "device_spread"):
+                "gpu_launches", "roofline", "clocks", "device_spread", "lm_head_roofline"):
         assert key in line, key
+    assert line["roofline"]["kernel"].startswith("whole propose step")
     assert "error" not in line["b1_new16"], line["b1_new16"]
+
+
+def test_window_leg(bench):
+    r = bench.run_window(5, 3)
+    assert r["rounds"] == 5 and r["ctx_window"] == 4096
+    for key in ("roofline", "clocks", "device_spread", "workload", "device_us"):
+        assert key in r, key
+    assert r["roofline"]["frac"] > 0
 
 
 @pytest.mark.parametrize("fp8", [False, True])

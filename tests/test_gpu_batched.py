@@ -15,7 +15,8 @@ import oracle
 from block_diffusion_speculative_forward_gb300 import binding as B
 from block_diffusion_speculative_forward_gb300 import synthetic as syn
 from tests.parity import (CONF_TOL, E2E_GAP, E2E_LOGIT_TOL, HIDDEN_TOL, LOGIT_TOL, LOGIT_TOL_FP8,
-                          cfg_for, check_abs, check_drafts, check_fp8_kv, check_logits, gaps)
+                          cfg_for, check_abs, check_drafts, check_fp8_kv, check_logits,
+                          check_rows, gaps)
 from tests.test_oracle_state import PositionSim
 
 pytestmark = pytest.mark.gpu
@@ -89,6 +90,7 @@ class Batch:
         g, H, L = geom.gamma, geom.hidden, geom.num_layers
         R = self.n * g
         tx = self.tx[:(L + 1) * R * H].reshape(L + 1, R, H)
+        ids, p1 = self.lib.debug_rows(self.n * nd)
         for i in self.sampled:
             allowed = None if bitmask is None else oracle.bitmask_allowed(bitmask[i], geom.vocab)
             taps = {}
@@ -105,6 +107,7 @@ class Batch:
             lg_ref = self.ora.draft_logits(z_got, nd)
             lg_got = self.tl[i * nd:(i + 1) * nd]
             check_logits(lg_ref, lg_got, LOGIT_TOL_FP8 if self.fp8 else LOGIT_TOL)
+            check_rows(lg_ref, allowed, ids[i * nd:(i + 1) * nd], p1[i * nd:(i + 1) * nd], got[i])
             d_ref, n_ref, c_ref, _ = oracle.select_drafts(lg_ref, allowed)
             assert got[i][1] == n_ref == ref[1]
             check_drafts(d_ref, got[i][0], lg_ref, allowed)

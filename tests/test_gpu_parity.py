@@ -10,7 +10,7 @@ import torch
 from block_diffusion_speculative_forward_gb300 import synthetic as syn
 from tests.parity import (CONF_TOL, E2E_GAP, E2E_LOGIT_TOL, HIDDEN_TOL, LOGIT_TOL, Pair,
                           assert_tables, check_abs, check_drafts, check_kv, check_logits,
-                          check_seq, gaps)
+                          check_rows, check_seq, gaps)
 from tests.test_oracle_pins import MICRO
 import oracle
 
@@ -193,6 +193,8 @@ def test_full_geometry_single_sequence():
     lg_ref = pair.ora.draft_logits(z_got, 15)
     lg_got = pair.tl[:15]
     check_logits(lg_ref, lg_got, LOGIT_TOL)
+    ids, p1 = pair.lib.debug_rows(15)
+    check_rows(lg_ref, None, ids, p1, got)
     d_ref, n_ref, c_ref, _ = oracle.select_drafts(lg_ref, None)
     assert got[1] == n_ref == 15
     n = check_drafts(d_ref, got[0], lg_ref, None)

@@ -58,6 +58,21 @@ def test_attention_temperature():
     assert abs(oracle.yarn_attention_factor(64.0) - 1.4158883083359671) < 1e-12
 
 
+def test_attention_temperature_shape():
+    """The published temperature is affine in ln(s) with slope 1/10 and value
+    1 at s = 1: checked through properties that fix such a function (no
+    scaling is the identity; the excess over one adds across a product of
+    factors; a factor of e^10 doubles the scale; shrinking (s < 1) never
+    applies, the factor only grows), not through the formula itself."""
+    f = oracle.yarn_attention_factor
+    for a, b in [(2.0, 32.0), (4.0, 16.0), (8.0, 8.0), (3.0, 21.0)]:
+        assert abs((f(a * b) - 1) - ((f(a) - 1) + (f(b) - 1))) < 1e-12
+    assert abs(f(math.exp(10.0)) - 2.0) < 1e-12
+    xs = [1.0, 1.5, 2.0, 16.0, 64.0, 1e3]
+    assert all(f(x) < f(y) for x, y in zip(xs, xs[1:]))
+    assert f(0.5) == 1.0
+
+
 def test_factor_two_equals_doubled_qk_norm_gains():
     """The factor scales the rotated q and k (ctx keys included): with 2 the
     whole propose equals a head whose q_norm / k_norm gains are doubled."""

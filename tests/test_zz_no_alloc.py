@@ -1,9 +1,10 @@
 """dflash_gemm_noalloc: the GEMM for callers that may not allocate device
 memory while running (an engine whose arena already owns the GPU, or a decode
-loop that cannot take cudaMalloc's device-wide synchronisation). It must give
-the same result as the allocating GEMM entry point, on two calls in a row,
-since its fixed scratch array keeps the previous call's contents. Collected
-last so that a stop-at-first-failure run has run every other test first."""
+loop that cannot take cudaMalloc's device-wide synchronisation). On two calls
+in a row (its fixed scratch array keeps the previous call's contents) it must
+give the same result as the allocating GEMM entry point, and both must match
+an fp32 matmul of the same bf16 inputs. Collected last so that a
+stop-at-first-failure run has run every other test first."""
 import ctypes as C
 
 import pytest
@@ -48,6 +49,11 @@ def test_noalloc_matches_allocating_gemm_twice(lib):
         got = _run(lib, "noalloc", w, x, m, n, k)
         err = (got - ref).abs().max().item()
         assert err <= 1e-3 * max(1.0, ref.abs().max().item()), (i, err)
+        # both against an fp32 matmul of the bf16 operands
+        mm = x.float() @ w.float().T
+        tol = 1e-3 * max(1.0, mm.abs().max().item())
+        assert (got - mm).abs().max().item() <= tol, (i, "noalloc vs fp32 matmul")
+        assert (ref - mm).abs().max().item() <= tol, (i, "allocating GEMM vs fp32 matmul")
 
 
 def test_noalloc_rejects_oversize(lib):
