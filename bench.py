@@ -248,8 +248,18 @@ def run_ours(args):
     hbm, tf, src = peaks()
     lm_ms = statistics.mean(probe_ms)
     lm_bytes = lm_head_bytes(geom, nd)
+    lm_kernel = "lm_head stage (GEMM over the vocab + argmax/confidence)"
+    lib.dflash_debug_last_path.argtypes = [C.c_void_p]
+    chained = lib.dflash_debug_last_path(head.ptr) == 1
+    if chained:
+        # the chained path runs the lm_head in the last layer's launch, after
+        # that layer's o_proj, gate/up and down: the probe spans all four
+        H, I = geom.hidden, geom.intermediate
+        lm_bytes += 2 * (H * geom.q_dim + 3 * I * H)
+        lm_kernel = ("last chained launch (o_proj, gate/up, down of the last layer, then the "
+                     "lm_head with argmax/confidence) + the row merge")
     achieved = lm_bytes / (lm_ms * 1e-3) / 1e9
-    traffic = args.lm_traffic
+    traffic = None if chained else args.lm_traffic
     sbytes = step_bytes(geom, ctx, 1)
     dev_med = statistics.median(dev_ms)
     out = {
@@ -281,9 +291,10 @@ def run_ours(args):
                              "frac": achieved / hbm, "traffic": traffic,
                              "traffic_note": "ncu constant for the build named in profiles/"
                                              "lm_head_b1_dram_traffic.md, or null",
-                             "kernel": "lm_head stage (GEMM over the vocab + argmax/confidence)",
+                             "kernel": lm_kernel,
                              "peak_source": f"{src} hbm_gbs",
                              "algorithmic_bytes_per_launch": lm_bytes, "avg_ms": lm_ms},
+        "path": "chained" if chained else "kernel per step",
         "propose_us": 1e3 * t_ms / K,
         "device_us": 1e3 * statistics.median(dev_ms),
         "device_spread": spread(dev_ms),

@@ -86,6 +86,8 @@ def lib() -> C.CDLL:
             "dflash_debug_set_taps": (C.c_int, [vp, vp, vp, vp]),
             "dflash_debug_set_graphs": (C.c_int, [vp, i32]),
             "dflash_debug_set_fault": (C.c_int, [vp, i64]),
+            "dflash_debug_set_chain": (C.c_int, [vp, i32]),
+            "dflash_debug_last_path": (C.c_int, [vp]),
             "dflash_debug_rows": (C.c_int, [vp, i32, C.POINTER(i32), C.POINTER(C.c_float), vp]),
         }
         for name, (res, args) in sig.items():
@@ -340,6 +342,14 @@ class DraftHead:
         """Test hook: every GEMM of later proposes aborts after waiting wait_ns
         on a barrier nothing arrives on (0 = off)."""
         _check(lib().dflash_debug_set_fault(self.ptr, int(wait_ns)))
+
+    def set_chain(self, enable: bool):
+        """Few-row proposes take the chained path (default) or the
+        kernel-per-step path."""
+        _check(lib().dflash_debug_set_chain(self.ptr, 1 if enable else 0))
+
+    def last_path_chained(self) -> bool:
+        return lib().dflash_debug_last_path(self.ptr) == 1
 
     def debug_rows(self, n_rows: int):
         """(ids, p1) of the last propose's draft rows, sequence-major."""

@@ -1,0 +1,650 @@
+// Few-row proposes (one sequence, or a handful of short blocks) as a few
+// persistent launches: each launch walks several weight-streaming GEMMs of
+// the layer stack back to back ("phases"), so the weight stream of the next
+// projection starts while the current one finishes, and the norms, the q/k
+// RoPE, SwiGLU, the residual updates and the lm_head reductions run inside
+// the GEMMs instead of as separate kernels ([P1] fields fc, hidden_norm,
+// fused_kv_weight, kv_cache, layers, norm, lm_head_shared).
+//
+// A batch-1 propose of the shipped geometry is
+//   prologue (block embed, pack of the new ctx rows)
+//   chain [fc, fused K/V + paged write, QKV of layer 0]
+//   for each layer l: attention(l); chain [o(l), gate/up(l), down(l), QKV(l+1) or lm_head]
+// where every GEMM is "swap AB" (128 weight rows are the MMA's M, the 16
+// block rows its N) and is split over all SMs by stream-K, as in gemm_tc.cu.
+//
+// Warp roles of a CTA (224 threads):
+//   warp 0     issues the weight TMA loads of every phase into an 8-stage ring;
+//              weights depend on nothing, so it runs ahead across phases
+//   warp 1     owns TMEM and issues the MMAs (one thread)
+//   warp 2     provides the B operand of each stage: a TMA load of a bf16
+//              activation written by an earlier kernel or phase (after the
+//              producing tile's ready flag), or, for a normed input, the whole
+//              RMSNorm(x) rows built once per phase into a 64 KB shared-memory
+//              region from the f32 residual and its per-tile sums of squares
+//   warps 3-6  drain the accumulators and run the phase's epilogue; a tile cut
+//              between CTAs is finished by its last arriving contributor,
+//              which sums the partials in CTA order
+// Phases depend only on earlier phases. A phase's dependency is a count of
+// finished tiles (or one tile's flag) in global memory, polled with
+// acquire loads; every wait here is bounded (2 s), after which the CTA raises
+// the status word and takes the same abort path as gemm_tc.cu. All CTAs are
+// resident at once (one per SM), so waiting on another CTA is safe.
+#include <cuda.h>
+
+#include <cstddef>
+
+#include "chain.h"
+#include "gemm_epi.h"
+#include "tc_ptx.h"
+
+namespace dfl {
+namespace tc {
+
+namespace {
+
+constexpr int CH_THREADS = 224;
+constexpr int CH_STAGES = 8;
+constexpr int CH_B_BYTES = CHAIN_BN * BK * 2;                 // 2 KB
+constexpr int CH_STAGE_BYTES = A_BYTES + CH_B_BYTES;          // 18 KB (1024-aligned)
+constexpr int CH_REGION_BYTES = (CHAIN_MAX_K_NORM / BK) * CH_B_BYTES;   // 64 KB
+constexpr int CH_EPI_T0 = 96;
+constexpr uint32_t CH_TMEM_COLS = 32;
+
+struct ChainSmem {
+  uint64_t full[CH_STAGES], empty[CH_STAGES], acc_full[2], acc_empty[2], b_free, drain, never;
+  uint32_t tmem_base;
+  uint32_t drain_issued, drain_parity;
+  int abort_flag;
+  int is_last;
+  EpiScratch epi;
+};
+constexpr int CH_SMEM = 1024 + CH_STAGES * CH_STAGE_BYTES + CH_REGION_BYTES + (int)sizeof(ChainSmem);
+static_assert(CH_SMEM <= 232448, "chain CTA exceeds the 227 KB shared-memory limit");
+static_assert(CH_STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+static_assert(sizeof(ChainMaps) + sizeof(ChainArgs) <= 32000, "chain parameters exceed the launch limit");
+
+__device__ __forceinline__ int64_t range_begin(int64_t total, int G, int c) {
+  return total * c / G;
+}
+// The CTA whose range holds iteration i.
+__device__ __forceinline__ int range_owner(int64_t total, int G, int64_t i) {
+  int c = (int)((i * G) / total);
+  while (c + 1 < G && range_begin(total, G, c + 1) <= i) ++c;
+  while (c > 0 && range_begin(total, G, c) > i) --c;
+  return c;
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Every lane of the warp polls until *ctr >= target (one answer per warp).
+// False when the CTA aborts or the wait runs past the limit (then it aborts).
+__device__ bool wait_count_warp(const int *ctr, int target, volatile int *abort_flag) {
+  bool ok = true;
+  if (ld_acquire(ctr) < target) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (ld_acquire(ctr) >= target) break;
+      if ((i & 15) == 0) {
+        if (*abort_flag) { ok = false; break; }
+        if (global_ns() - t0 > TIMEOUT_NS) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// ------------------------------------------------------- phase epilogues --
+// Residual / ctx-row outputs: out[a, f] (+)= y, the residual tap, and the
+// per-tile sums of squares of the updated rows (the next RMSNorm's input).
+__device__ __forceinline__ void finish_rows(const ChainPhase &P, EpiScratch *sm,
+                                            const float (&v)[16], int f, int tm, int q, int lane,
+                                            int et) {
+  const bool add = P.kind != CK_FC;
+  const bool f_ok = f < P.n_w;
+  float sq[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    float y = 0.f;
+    if (f_ok && c < P.rows) {
+      float *o = P.out + (int64_t)c * P.n_w + f;
+      y = (add ? __ldcg(o) : 0.f) + v[c];
+      *o = y;
+      if (P.x_tap) P.x_tap[(int64_t)c * P.n_w + f] = y;
+    }
+    sq[c] = y * y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int c = 0; c < 16; ++c) sq[c] += __shfl_xor_sync(0xffffffffu, sq[c], o);
+  if (lane == 0) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) sm->red_v[q][c] = sq[c];
+  }
+  epi_bar();
+  if (et < 16)
+    P.out_ss[tm * 16 + et] = sm->red_v[0][et] + sm->red_v[1][et] + sm->red_v[2][et] + sm->red_v[3][et];
+  epi_bar();
+}
+
+// Fused ctx K/V rows ([P1] fields fused_kv_weight, kv_cache, yarn_inv_freq):
+// W_kv row f is element i of head h of layer l's K (or V). A 128-row tile
+// holds whole heads of one kind. K: per-head RMSNorm (k_norm of layer l),
+// then RoPE at the row's position; V as it is; both written to the row's
+// (page, slot) of the pool, bf16 or E4M3 with the head's scale.
+__device__ __forceinline__ void finish_kv(const ChainPhase &P, EpiScratch *sm, const float (&v)[16],
+                                          int f, int q, int lane, int *status) {
+  const Geo &g = P.geo;
+  const int d = g.d, half = d / 2;
+  const int fl = q * 32 + lane;
+  const int l = f / (2 * g.kv), within = f % (2 * g.kv);
+  const int kind = within / g.kv, h = (within % g.kv) / d, i = within % d;
+  const int nrows = P.rows < 16 ? P.rows : 16;
+  float y[16];
+  if (kind == 0) {
+    float ss[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) ss[c] = v[c] * v[c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) ss[c] += __shfl_xor_sync(0xffffffffu, ss[c], o);
+    if (lane == 0) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) sm->red_v[q][c] = ss[c];
+    }
+  }
+  epi_bar();
+  if (kind == 0) {
+    const float gi = __bfloat162float(P.k_norm[l][i]);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float tot;
+      if (d == 128) tot = sm->red_v[0][c] + sm->red_v[1][c] + sm->red_v[2][c] + sm->red_v[3][c];
+      else tot = sm->red_v[q & 2][c] + sm->red_v[(q & 2) + 1][c];
+      sm->xch[c][fl] = gi * (v[c] * rsqrtf(tot / (float)d + g.eps));
+    }
+  }
+  epi_bar();
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    if (kind == 0) {
+      const int pos = c < nrows ? P.ctx_rows[c].pos : 0;
+      const float cs = P.ep.cos_t[(int64_t)pos * half + (i % half)];
+      const float sn = P.ep.sin_t[(int64_t)pos * half + (i % half)];
+      const float a = sm->xch[c][fl], b = sm->xch[c][fl ^ half];
+      y[c] = (i < half) ? (a * cs - b * sn) : (a * cs + b * sn);
+    } else {
+      y[c] = v[c];
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    if (c >= nrows) break;
+    const RowMeta rm = P.ctx_rows[c];
+    if (rm.seq < 0) continue;   // padding row: computed, never stored
+    if (rm.page < 0 || rm.page >= g.pages) {
+      if (i == 0) atomicOr(status, ST_PAGE);
+      continue;
+    }
+    const int64_t off = kv_offset(g, rm.page, l, kind, h, rm.slot) + i;
+    if (g.kv_fp8) {
+      const float s = P.kv_scale[(l * g.nkv + h) * 2 + kind];
+      ((uint8_t *)P.pool)[off] = (uint8_t)__nv_cvt_float_to_fp8(y[c] / s, __NV_SATFINITE, __NV_E4M3);
+    } else {
+      ((bf16 *)P.pool)[off] = __float2bfloat16_rn(y[c]);
+    }
+  }
+  epi_bar();
+}
+
+// ---------------------------------------------------------------- kernel --
+__global__ void __launch_bounds__(CH_THREADS, 1)
+    k_chain(const __grid_constant__ ChainMaps maps, const __grid_constant__ ChainArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  const uint32_t region = base + CH_STAGES * CH_STAGE_BYTES;
+  ChainSmem *sm = (ChainSmem *)(gbase + CH_STAGES * CH_STAGE_BYTES + CH_REGION_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = (int)gridDim.x, cta = (int)blockIdx.x;
+  const int np = a.n_phases;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < CH_STAGES; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 2);   // the weight copy's arrival + the B operand's
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sm->acc_full[b]), 1);
+      mbar_init(smem_u32(&sm->acc_empty[b]), 4);
+    }
+    mbar_init(smem_u32(&sm->b_free), 1);
+    mbar_init(smem_u32(&sm->drain), 1);
+    mbar_init(smem_u32(&sm->never), 1);   // nothing ever arrives (test hook)
+    sm->abort_flag = 0;
+    sm->drain_issued = 0;
+    sm->drain_parity = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    pdl_trigger();
+  }
+  if (warp == 0 && lane < np) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.w[lane]) : "memory");
+    if (!a.ph[lane].b_norm) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.b[lane]) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sm->tmem_base)),
+                 "r"(CH_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int *abort_flag = &sm->abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------- weight producer ------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, parity = 0;
+      bool ok = true;
+      for (int p = 0; p < np && ok; ++p) {
+        const ChainPhase &P = a.ph[p];
+        const int64_t total = (int64_t)P.tiles_m * P.kb;
+        const int64_t e = range_begin(total, G, cta + 1);
+        for (int64_t it = range_begin(total, G, cta); it < e; ++it) {
+          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&sm->full[stage]);
+          mbar_expect_tx(fb, A_BYTES);
+          tma_load_2d(base + stage * CH_STAGE_BYTES, &maps.w[p], fb, (int)(it % P.kb) * BK,
+                      (int)(it / P.kb) * BM, pol);
+          issued |= 1u << stage;
+          parity = (parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      sm->drain_issued = issued;
+      sm->drain_parity = parity;
+    }
+    pdl_wait();
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer -----------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_mn<BM, CHAIN_BN>();
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int p = 0; p < np && ok; ++p) {
+        const ChainPhase &P = a.ph[p];
+        const int64_t total = (int64_t)P.tiles_m * P.kb;
+        const int64_t b = range_begin(total, G, cta), e = range_begin(total, G, cta + 1);
+        for (int64_t it = b; it < e && ok;) {
+          const int k0 = (int)(it % P.kb);
+          const int k1 = (int)((int64_t)P.kb < k0 + (e - it) ? (int64_t)P.kb : k0 + (e - it));
+          if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), acc_phase ^ 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + acc * CHAIN_BN;
+          for (int k = k0; k < k1; ++k) {
+            if (!mbar_wait(smem_u32(&sm->full[stage]), phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = base + stage * CH_STAGE_BYTES;
+            const uint32_t sb = P.b_norm ? region + k * CH_B_BYTES : sa + A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), idesc,
+                        (k > k0 || kk > 0) ? 1u : 0u);
+            umma_commit(smem_u32(&sm->empty[stage]));
+            if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&sm->acc_full[acc]));
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+          it += k1 - k0;
+        }
+        // the normed region is free again once this phase's MMAs completed
+        if (ok && P.b_norm && e > b) umma_commit(smem_u32(&sm->b_free));
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------- B operand ------------
+    pdl_wait();
+    const uint64_t pol_b = policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0, free_phase = 0;
+    bool region_used = false, ok = true;
+    for (int p = 0; p < np && ok; ++p) {
+      const ChainPhase &P = a.ph[p];
+      const int64_t total = (int64_t)P.tiles_m * P.kb;
+      const int64_t b = range_begin(total, G, cta), e = range_begin(total, G, cta + 1);
+      if (b == e) continue;
+      if (P.dep >= 0 && !P.dep_tile &&
+          !wait_count_warp(a.ph[P.dep].done, a.ph[P.dep].tiles_m, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (P.b_norm) {
+        // the previous normed phase's MMAs must be done with the region
+        if (region_used) {
+          if (!mbar_wait_warp(smem_u32(&sm->b_free), free_phase, abort_flag)) { ok = false; break; }
+          free_phase ^= 1;
+        }
+        region_used = true;
+        // rinv of row r (lanes 0..15): 1 / sqrt(mean of squares + eps)
+        float rinv = 0.f;
+        if (lane < 16 && lane < P.rows) {
+          float t = 0.f;
+          for (int j = 0; j < P.k / 128; ++j) t += __ldcg(P.nss + j * 16 + lane);
+          rinv = rsqrtf(t / (float)P.k + a.ph[p].ep.eps);
+        }
+        // lane: row r = lane / 2, 32 consecutive features (four 16-byte chunks)
+        const int r = lane >> 1, hh = lane & 1;
+        const float rr = __shfl_sync(0xffffffffu, rinv, r);
+        const bool live = r < P.rows;
+        const bool tap = P.kind == CK_LM && cta == 0 && live;
+        int drow = -1;
+        if (tap && P.z_rows) {
+          const int gm = P.ep.lm_gamma, j = r % gm - P.ep.lm_first;
+          if (j >= 0 && j < P.ep.nd) drow = (r / gm) * P.ep.nd + j;
+        }
+        for (int kb = 0; kb < P.kb; ++kb) {
+          const int f0 = kb * BK + hh * 32;
+          uint32_t w[16];
+          if (live) {
+            const float4 *xs = reinterpret_cast<const float4 *>(P.nsrc + (int64_t)r * P.k + f0);
+            const uint4 *gs = reinterpret_cast<const uint4 *>(P.ngain + f0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float4 x0 = __ldcg(xs + 2 * u), x1 = __ldcg(xs + 2 * u + 1);
+              const uint4 gw = __ldg(gs + u);
+              const bf16 *gv = reinterpret_cast<const bf16 *>(&gw);
+              const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                    __bfloat162float(gv[2 * e2]) * (xv[2 * e2] * rr),
+                    __bfloat162float(gv[2 * e2 + 1]) * (xv[2 * e2 + 1] * rr));
+                w[4 * u + e2] = *reinterpret_cast<uint32_t *>(&h2);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) w[u] = 0u;
+          }
+          // 128-byte swizzle: chunk ch of row r sits at chunk ch ^ (r % 8)
+          const uint32_t rowb = region + kb * CH_B_BYTES + r * 128;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t ch = (uint32_t)(hh * 4 + u);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             rowb + ((ch ^ (uint32_t)(r & 7)) << 4)),
+                         "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                         : "memory");
+          }
+          if (tap) {
+            if (P.z_tap) {
+              uint4 *zt = reinterpret_cast<uint4 *>(P.z_tap + (int64_t)r * P.k + f0);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) zt[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            }
+            if (drow >= 0) {
+              uint4 *zr = reinterpret_cast<uint4 *>(P.z_rows + (int64_t)drow * P.k + f0);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) zr[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            }
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        for (int64_t it = b; it < e; ++it) {
+          if (!mbar_wait_warp(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
+          if (lane == 0) mbar_arrive(smem_u32(&sm->full[stage]));
+          if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
+        }
+      } else {
+        const ChainPhase *D = P.dep >= 0 ? &a.ph[P.dep] : nullptr;
+        for (int64_t it = b; it < e; ++it) {
+          const int k = (int)(it % P.kb);
+          if (!mbar_wait_warp(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
+          if (P.dep_tile && D && !wait_count_warp(D->flag + k, 1, abort_flag)) { ok = false; break; }
+          if (lane == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint32_t fb = smem_u32(&sm->full[stage]);
+            mbar_expect_tx(fb, CH_B_BYTES);
+            tma_load_2d(base + stage * CH_STAGE_BYTES + A_BYTES, &maps.b[p], fb, k * BK, 0, pol_b);
+          }
+          if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------- epilogue -------------
+    pdl_wait();
+    const int et = (int)threadIdx.x - CH_EPI_T0;
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int f_local = q * 32 + lane;       // weight row within the tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool live = true;
+    if (a.fault_ns > 0 && et == 0)
+      live = fault_wait(smem_u32(&sm->never), (uint64_t)a.fault_ns, abort_flag);
+    live = epi_all(live);
+    for (int p = 0; p < np && live; ++p) {
+      const ChainPhase &P = a.ph[p];
+      const int64_t total = (int64_t)P.tiles_m * P.kb;
+      const int64_t b = range_begin(total, G, cta), e = range_begin(total, G, cta + 1);
+      bool res_seen = P.res_dep < 0;
+      for (int64_t it = b; it < e;) {
+        const int t = (int)(it / P.kb);
+        const int k0 = (int)(it % P.kb);
+        const int k1 = (int)((int64_t)P.kb < k0 + (e - it) ? (int64_t)P.kb : k0 + (e - it));
+        const bool whole = (k0 == 0 && k1 == P.kb);
+        const int f = t * BM + f_local;
+        if (!epi_all(mbar_wait(smem_u32(&sm->acc_full[acc]), acc_phase, abort_flag))) {
+          live = false;
+          break;
+        }
+        tc_fence_after();
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * CHAIN_BN, v);
+        tc_fence_before();
+        if (lane == 0) mbar_arrive(smem_u32(&sm->acc_empty[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        bool finisher = whole;
+        if (!whole) {
+          // this CTA's partial of the tile, thread-major (16 contiguous floats)
+          const int slot = 2 * (p * G + cta) + (it == b ? 0 : 1);
+          float4 *dst = reinterpret_cast<float4 *>(a.ws + ((int64_t)slot * BM + f_local) * CHAIN_BN);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          __threadfence();
+          epi_bar();
+          const int c_lo = range_owner(total, G, (int64_t)t * P.kb);
+          const int c_hi = range_owner(total, G, (int64_t)t * P.kb + P.kb - 1);
+          if (et == 0) sm->is_last = (atomicAdd(&P.arrive[t], 1) == c_hi - c_lo);
+          epi_bar();
+          finisher = sm->is_last != 0;
+          if (finisher) {
+            __threadfence();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = 0.f;
+            for (int cc = c_lo; cc <= c_hi; ++cc) {
+              const int sl = 2 * (p * G + cc) +
+                             ((cc == c_lo && range_begin(total, G, cc) < (int64_t)t * P.kb) ? 1 : 0);
+              const float4 *src =
+                  reinterpret_cast<const float4 *>(a.ws + ((int64_t)sl * BM + f_local) * CHAIN_BN);
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const float4 r = __ldcg(src + c);
+                v[4 * c] += r.x;
+                v[4 * c + 1] += r.y;
+                v[4 * c + 2] += r.z;
+                v[4 * c + 3] += r.w;
+              }
+            }
+          }
+        }
+        if (finisher && !res_seen) {
+          // the residual rows this epilogue adds to were written by another
+          // phase's epilogues: take their count with acquire semantics
+          bool ok = true;
+          if (warp == 3) ok = wait_count_warp(a.ph[P.res_dep].done, a.ph[P.res_dep].tiles_m, abort_flag);
+          if (!epi_all(ok)) {
+            live = false;
+            break;
+          }
+          res_seen = true;
+        }
+        if (finisher) {
+          switch (P.kind) {
+            case CK_FC:
+            case CK_O:
+            case CK_DOWN: finish_rows(P, &sm->epi, v, f, t, q, lane, et); break;
+            case CK_KV: finish_kv(P, &sm->epi, v, f, q, lane, a.status); break;
+            case CK_QKV: finish16<EPI_TC_QKV>(P.ep, &sm->epi, v, f, t, 0, q, lane, et); break;
+            case CK_GU: finish16<EPI_TC_SWIGLU>(P.ep, &sm->epi, v, f, t, 0, q, lane, et); break;
+            default: finish16<EPI_TC_LMHEAD>(P.ep, &sm->epi, v, f, t, 0, q, lane, et); break;
+          }
+          // publish: every thread's stores, then the tile's flag and count
+          __threadfence();
+          epi_bar();
+          if (et == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(P.flag + t), "r"(1) : "memory");
+            asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(P.done), "r"(1) : "memory");
+          }
+        }
+        if (!whole) epi_bar();   // is_last is reused by the next split tile
+        it += k1 - k0;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------- teardown ----
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      atomicOr(a.status, ST_TIMEOUT);
+      // let this CTA's own copies land (bounded: a stage whose B arrival is
+      // missing never completes, and its weight copy has long landed)
+      for (int s = 0; s < CH_STAGES; ++s) {
+        if (!((sm->drain_issued >> s) & 1u)) continue;
+        const uint32_t par = (sm->drain_parity >> s) & 1u;
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(smem_u32(&sm->full[s]), par) && global_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+    if (threadIdx.x == 32) {
+      umma_commit(smem_u32(&sm->drain));
+      const uint64_t t0 = global_ns();
+      while (!mbar_test(smem_u32(&sm->drain), 0) && global_ns() - t0 < 100000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(CH_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// -------------------------------------------------------------- prologue --
+// Block embed ([P1] fields gamma, mask_token_id, embed_tokens_shared) with
+// the per-tile sums of squares of each row (the first RMSNorm's input), and
+// the pack of the new ctx rows from the callers' stacks (zero for padding).
+__global__ void k_chain_prologue(const bf16 *__restrict__ E, const SeqMeta *__restrict__ seq,
+                                 int R, int gamma, int H, int V, uint32_t mask_token,
+                                 float *__restrict__ x, float *__restrict__ ss, float *x_tap,
+                                 const RowMeta *__restrict__ rows, int S, bf16 *__restrict__ pack,
+                                 int *status) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  if (b >= R) {
+    const RowMeta rm = rows[b - R];
+    uint4 *dst = reinterpret_cast<uint4 *>(pack + (int64_t)(b - R) * S);
+    const uint4 *src = reinterpret_cast<const uint4 *>(rm.src);
+    for (int e = threadIdx.x; e < S / 8; e += blockDim.x)
+      dst[e] = (rm.seq < 0 || !src) ? make_uint4(0u, 0u, 0u, 0u) : src[e];
+    return;
+  }
+  const int i = b % gamma;
+  uint32_t tok = i == 0 ? (uint32_t)seq[b / gamma].token : mask_token;
+  if (tok >= (uint32_t)V) {
+    if (threadIdx.x == 0) atomicOr(status, ST_TOKEN);
+    tok = 0;
+  }
+  // thread t: features 8t .. 8t+7; 16 threads per 128-feature tile
+  const int f0 = 8 * threadIdx.x;
+  float s = 0.f;
+  if (f0 < H) {
+    const uint4 raw = *reinterpret_cast<const uint4 *>(E + (int64_t)tok * H + f0);
+    const bf16 *e = reinterpret_cast<const bf16 *>(&raw);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = __bfloat162float(e[j]);
+      s += v[j] * v[j];
+    }
+    float4 *xo = reinterpret_cast<float4 *>(x + (int64_t)b * H + f0);
+    xo[0] = make_float4(v[0], v[1], v[2], v[3]);
+    xo[1] = make_float4(v[4], v[5], v[6], v[7]);
+    if (x_tap) {
+      float4 *to = reinterpret_cast<float4 *>(x_tap + (int64_t)b * H + f0);
+      to[0] = xo[0];
+      to[1] = xo[1];
+    }
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (f0 < H && (threadIdx.x & 15) == 0) ss[(threadIdx.x >> 4) * 16 + b] = s;
+}
+
+}  // namespace
+
+int chain_smem() { return CH_SMEM; }
+
+cudaError_t chain(const ChainMaps &maps, const ChainArgs &a, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaError_t e = launch_pdl(k_chain, dim3(num_sms()), dim3(CH_THREADS), CH_SMEM, s, maps, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t chain_prologue(const bf16 *E, const SeqMeta *seq, int R, const Geo &g,
+                           uint32_t mask_token, float *x, float *ss, float *x_tap,
+                           const RowMeta *rows, int m, bf16 *pack, int *status, cudaStream_t s) {
+  if (g.H > 8 * 256 || g.H % 128) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(tc::k_chain_prologue, dim3(R + m), dim3(256), 0, s, E, seq, R,
+                             g.gamma, g.H, g.V, mask_token, x, ss, x_tap, rows, g.S, pack, status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

@@ -98,6 +98,8 @@ struct dflash_handle {
   int cap_seq = 0, cap_pages = 0, cap_items = 0, cap_pairs = 0;
   size_t off_seq = 0, off_pages = 0, off_items = 0, off_pairs = 0, off_sched = 0, off_rows = 0;
   int cap_sched = 0;
+  bool chain_ok = false;    // the head can take the chained few-row path
+  int last_chained = 0;     // the last propose took it
   // captured propose graphs, keyed by the call's launch shape
   bool use_graphs = true;
   cudaStream_t cap_stream = nullptr;
@@ -457,6 +459,7 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_ha
     delete h;
     return rc;
   }
+  h->chain_ok = h->b.use_chain;
   h->cap_items = h->b.attn_slots + h->cap_pairs;
   h->off_pairs = (h->off_items + sizeof(dfl::AttnItem) * h->cap_items + 15) & ~(size_t)15;
   h->cap_sched = h->b.attn_grid_tc + 1;
@@ -747,6 +750,19 @@ int dflash_debug_set_step_probe(dflash_handle *h, void *ev_begin, void *ev_end) 
 
 int64_t dflash_debug_launch_count(void) { return dfl::launch_count(); }
 
+int dflash_debug_set_chain(dflash_handle *h, int32_t enable) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  if (!h->compute) return DFLASH_OK;
+  h->b.use_chain = enable != 0 && h->chain_ok;
+  drop_graphs(h);
+  return DFLASH_OK;
+}
+
+int dflash_debug_last_path(const dflash_handle *h) {
+  if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  return h->last_chained;
+}
+
 int dflash_debug_set_fault(dflash_handle *h, int64_t wait_ns) {
   if (!h || wait_ns < 0 || wait_ns > 2000000000ll)
     return fail(DFLASH_EINVAL, "NULL handle or wait outside 0..2e9 ns");
@@ -836,6 +852,8 @@ int dflash_debug_lmhead(const void *w, const void *x, void *partials, int32_t m,
 
 int dflash_debug_set_taps(dflash_handle *h, float *x_taps, void *z, float *logits) {
   if (!h) return fail(DFLASH_EINVAL, "NULL handle");
+  if (((uintptr_t)x_taps | (uintptr_t)z | (uintptr_t)logits) & 15)
+    return fail(DFLASH_EINVAL, "tap buffers must be 16-byte aligned");
   h->b.tap_x = x_taps;
   h->b.tap_z = (bf16 *)z;
   h->b.tap_logits = logits;
@@ -1043,6 +1061,7 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   size_t meta_bytes = 0;
   int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off, &meta_bytes);
   if (rc == DFLASH_OK) rc = run_forward(h, cm, num_drafts, bitmask, meta_bytes, s);
+  h->last_chained = chain_applies(h->g, h->b, cm.n_rows, n * h->g.gamma) ? 1 : 0;
   if (rc == DFLASH_OK) {
     // Results are on the host after one synchronisation.
     cudaError_t e = cudaStreamSynchronize(s);

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include "chain.h"
 #include "consumers.h"
 #include "forward.h"
 
@@ -163,6 +164,13 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
       return DFLASH_ECUDA;
     }
   }
+  // The chained few-row path reads norm gains 16 bytes at a time.
+  {
+    auto al = [](const void *q) { return ((uintptr_t)q & 15) == 0; };
+    bool ok = al(W->hidden_norm) && al(W->norm);
+    for (const LayerW &L : W->layers) ok = ok && al(L.in_norm) && al(L.post_norm);
+    B->use_chain = ok;
+  }
   // RoPE table for every position a block row can reach.
   const int max_pos = c.max_seq_len + g.gamma;
   BA(W->cos_t, (size_t)max_pos * (g.d / 2));
@@ -209,6 +217,16 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->counters, (size_t)B->n_counters);
   BK(cudaMemset(B->counters, 0, sizeof(int) * (size_t)B->n_counters));
   BA(B->lm_part, (size_t)D_max * vt);
+  // Few-row chained proposes: per-tile sums of squares of the residual and
+  // of the new ctx rows, and every launch's tile counters and flags.
+  {
+    const int ht = (g.H + 127) / 128;
+    BA(B->ss_in, (size_t)ht * 16);
+    BA(B->ss_mid, (size_t)ht * 16);
+    BA(B->ss_c, (size_t)ht * 16);
+    B->chain_sync_ints = chain_sync_capacity(g);
+    BA(B->chain_sync, (size_t)B->chain_sync_ints);
+  }
   // Split-KV attention partials: at most two ctx chunks per (sequence, kv
   // head) beyond 3 x SMs, plus one block-key item each.
   {
@@ -354,8 +372,245 @@ int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *
   return DFLASH_OK;
 }
 
+int chain_sync_capacity(const Geo &g) {
+  auto t = [](int64_t n) { return (int)((n + 127) / 128); };
+  // per phase: arrival counters and flags per tile, one tile count (+ padding)
+  auto ph = [](int tiles) { return 2 * tiles + 4; };
+  const int first = ph(t(g.H)) + ph(t((int64_t)g.L * 2 * g.kv)) + ph(t(g.qkv_w));
+  const int layer = ph(t(g.H)) + ph(t(2 * (int64_t)g.I)) + ph(t(g.H)) +
+                    std::max(ph(t(g.qkv_w)), ph(t(g.V)));
+  return first + g.L * layer + 64;
+}
+
+bool chain_applies(const Geo &g, const Buffers &B, int n_rows, int R) {
+  return B.use_chain && R <= CHAIN_BN && n_rows <= CHAIN_BN && g.H <= CHAIN_MAX_K_NORM &&
+         g.H % 128 == 0 && g.S % CHAIN_BK == 0 && g.I % CHAIN_BK == 0 && B.chain_sync;
+}
+
+namespace {
+
+// The chained propose of few rows (see chain.cu): prologue, one launch for
+// the new ctx rows and layer 0's QKV, then per layer the attention and one
+// launch for o_proj, gate/up, down and the next QKV (or the lm_head), then
+// the row merge of the lm_head partials and the chain of drafts.
+int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const Buffers &B,
+                  const CallMeta &cm, int nd, const int32_t *bitmask, cudaStream_t s) {
+  if (B.step_begin && B.step_end) FK(cudaEventRecordWithFlags(B.step_begin, s, cudaEventRecordExternal));
+  const int n = cm.n_seq, R = n * g.gamma, D = n * nd, m = cm.n_rows;
+  const int qd = g.nq * g.d;
+  FK(cudaMemsetAsync(B.chain_sync, 0, sizeof(int) * (size_t)B.chain_sync_ints, s));
+  LK(chain_prologue(W.embed, cm.seq, R, g, c.mask_token_id, B.x, B.ss_in, B.tap_x, cm.rows, m,
+                    B.ctx_pack, B.status, s));
+  int *sync = B.chain_sync;
+  auto phase = [&](int kind, int n_w, int k, int rows) {
+    ChainPhase P{};
+    P.kind = kind;
+    P.n_w = n_w;
+    P.k = k;
+    P.rows = rows;
+    P.tiles_m = (n_w + 127) / 128;
+    P.kb = k / CHAIN_BK;
+    P.dep = -1;
+    P.res_dep = -1;
+    P.arrive = sync;
+    P.flag = sync + P.tiles_m;
+    P.done = sync + 2 * P.tiles_m;
+    sync += 2 * P.tiles_m + 4;
+    P.geo = g;
+    P.ep.m_act = rows;
+    P.ep.n_w = n_w;
+    P.ep.k = k;
+    P.ep.eps = g.eps;
+    P.ep.status = B.status;
+    P.ep.tiles_m = P.tiles_m;
+    P.ep.tiles_n = 1;
+    P.ep.cos_t = W.cos_t;
+    P.ep.sin_t = W.sin_t;
+    return P;
+  };
+  auto normed = [](ChainPhase &P, const float *src, const float *ss, const bf16 *gain) {
+    P.b_norm = 1;
+    P.nsrc = src;
+    P.nss = ss;
+    P.ngain = gain;
+  };
+  auto qkv_phase = [&](int l) {
+    ChainPhase P = phase(CK_QKV, g.qkv_w, g.H, R);
+    normed(P, B.x, B.ss_in, W.layers[l].in_norm);
+    P.ep.seq = cm.seq;
+    P.ep.gamma = g.gamma;
+    P.ep.head_dim = g.d;
+    P.ep.q_rows = qd;
+    P.ep.k_rows = g.kv;
+    P.ep.q_norm = W.layers[l].q_norm;
+    P.ep.k_norm = W.layers[l].k_norm;
+    P.ep.q_out = B.q;
+    P.ep.k_out = B.kb;
+    P.ep.v_out = B.vb;
+    return P;
+  };
+  const CUtensorMap empty_map{};
+  auto launch = [&](ChainPhase *ph, const CUtensorMap *const *wm, const CUtensorMap *const *bm,
+                    int np) -> int {
+    ChainArgs a{};
+    ChainMaps maps;
+    a.n_phases = np;
+    for (int i = 0; i < np; ++i) {
+      a.ph[i] = ph[i];
+      maps.w[i] = *wm[i];
+      maps.b[i] = bm[i] ? *bm[i] : empty_map;
+    }
+    for (int i = np; i < CHAIN_MAX_PHASES; ++i) {
+      maps.w[i] = empty_map;
+      maps.b[i] = empty_map;
+    }
+    a.ws = B.ws;
+    a.status = B.status;
+    a.fault_ns = B.fault_ns;
+    LK(tc::chain(maps, a, s));
+    return DFLASH_OK;
+  };
+  const CUtensorMap *act16_o = &B.act_map[ACT_O][bn_index(16)];
+  const CUtensorMap *act16_u = &B.act_map[ACT_U][bn_index(16)];
+  const CUtensorMap *act16_pack = &B.act_map[ACT_PACK][bn_index(16)];
+  {
+    // new ctx rows (fc, hidden_norm, fused K/V with the paged write) and layer 0's QKV
+    ChainPhase ph[3];
+    const CUtensorMap *wm[3], *bm[3];
+    int np = 0;
+    if (m > 0) {
+      ChainPhase fc = phase(CK_FC, g.H, g.S, m);
+      fc.out = B.ctx_fc;
+      fc.out_ss = B.ss_c;
+      ph[np] = fc;
+      wm[np] = &W.map_fc;
+      bm[np++] = act16_pack;
+      ChainPhase kv = phase(CK_KV, g.L * 2 * g.kv, g.H, m);
+      normed(kv, B.ctx_fc, B.ss_c, W.hidden_norm);
+      kv.dep = 0;
+      kv.ctx_rows = cm.rows;
+      kv.k_norm = W.k_norm_dev;
+      kv.pool = W.pool;
+      kv.kv_scale = W.kv_scale;
+      ph[np] = kv;
+      wm[np] = &W.map_wkv;
+      bm[np++] = nullptr;
+    }
+    ph[np] = qkv_phase(0);
+    wm[np] = &W.map_qkv[0];
+    bm[np++] = nullptr;
+    int rc = launch(ph, wm, bm, np);
+    if (rc) return rc;
+  }
+  for (int l = 0; l < g.L; ++l) {
+    const LayerW &L = W.layers[l];
+    {
+      AttnArgs a{};
+      a.g = g;
+      a.q = B.q;
+      a.kb = B.kb;
+      a.vb = B.vb;
+      a.o = B.o;
+      a.seq = cm.seq;
+      a.page_ids = cm.page_ids;
+      a.pool = W.pool;
+      a.kv_scale = W.kv_scale;
+      a.layer = l;
+      a.scale = (float)(1.0 / std::sqrt((double)g.d));
+      a.items = cm.items;
+      a.n_items = cm.cap_items;
+      a.pairs = cm.pairs;
+      a.n_pairs = cm.cap_pairs;
+      a.counts = cm.counts;
+      a.ws = B.attn_ws;
+      a.slot_floats = B.attn_slot_floats;
+      a.status = B.status;
+      a.cta_off = cm.cta_off;
+      a.grid_tc = B.attn_grid_tc;
+      if (B.attn_maps.ok) {
+        LK(attention_tc(a, B.attn_maps, s));
+        LK(attention_merge(a, s));
+      } else {
+        LK(attention_split(a, s));
+      }
+      if (cm.cap_pairs) count_launches(1);
+    }
+    ChainPhase ph[4];
+    const CUtensorMap *wm[4], *bm[4];
+    ph[0] = phase(CK_O, g.H, qd, R);
+    ph[0].out = B.x;
+    ph[0].out_ss = B.ss_mid;
+    wm[0] = &W.map_o[l];
+    bm[0] = act16_o;
+    ph[1] = phase(CK_GU, 2 * g.I, g.H, R);
+    normed(ph[1], B.x, B.ss_mid, L.post_norm);
+    ph[1].dep = 0;
+    ph[1].ep.u_out = B.u;
+    wm[1] = &W.map_gu[l];
+    bm[1] = nullptr;
+    ph[2] = phase(CK_DOWN, g.H, g.I, R);
+    ph[2].dep = 1;
+    ph[2].dep_tile = 1;
+    ph[2].res_dep = 0;
+    ph[2].out = B.x;
+    ph[2].out_ss = B.ss_in;
+    ph[2].x_tap = B.tap_x ? B.tap_x + (size_t)(l + 1) * R * g.H : nullptr;
+    wm[2] = &W.map_down[l];
+    bm[2] = act16_u;
+    if (l + 1 < g.L) {
+      ph[3] = qkv_phase(l + 1);
+      wm[3] = &W.map_qkv[l + 1];
+    } else {
+      ph[3] = phase(CK_LM, g.V, g.H, R);
+      normed(ph[3], B.x, B.ss_in, W.norm);
+      ph[3].ep.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+      ph[3].ep.bitmask = bitmask;
+      ph[3].ep.mask_words = (g.V + 31) / 32;
+      ph[3].ep.nd = nd;
+      ph[3].ep.lm_gamma = g.gamma;
+      ph[3].ep.lm_first = 1;
+      ph[3].ep.lm_part = B.lm_part;
+      ph[3].z_rows = B.z;
+      ph[3].z_tap = B.tap_z;
+      wm[3] = &W.map_lm;
+      if (B.probe_begin && B.probe_end)
+        FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));
+    }
+    ph[3].dep = 2;
+    bm[3] = nullptr;
+    int rc = launch(ph, wm, bm, 4);
+    if (rc) return rc;
+  }
+  LK(lm_reduce(B.lm_part, D, (g.V + 127) / 128, B.row_id, B.row_p1, s));
+  if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_end, s, cudaEventRecordExternal));
+  if (B.tap_logits) {
+    GemmParams p{};
+    p.m_act = D;
+    p.n_w = g.V;
+    p.k = g.H;
+    p.epi = EPI_TC_STORE_F32;
+    p.out = B.tap_logits;
+    p.ldo = g.V;
+    p.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+    p.ws = B.ws;
+    p.counters = B.counters;
+    p.status = B.status;
+    const int bn = tc::pick_bn(D);
+    LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
+  }
+  LK(finalize(B.row_id, B.row_p1, n, nd, B.status, (uint32_t *)(B.out_dev + B.off_drafts),
+              (int32_t *)(B.out_dev + B.off_nout), (float *)(B.out_dev + B.off_conf),
+              (int32_t *)B.out_dev, s));
+  if (B.step_begin && B.step_end) FK(cudaEventRecordWithFlags(B.step_end, s, cudaEventRecordExternal));
+  return DFLASH_OK;
+}
+
+}  // namespace
+
 int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffers &B,
             const CallMeta &cm, int nd, const int32_t *bitmask, int M_ctx, cudaStream_t s) {
+  if (chain_applies(g, B, cm.n_rows, cm.n_seq * g.gamma))
+    return forward_chain(g, c, W, B, cm, nd, bitmask, s);
   if (B.step_begin && B.step_end) FK(cudaEventRecordWithFlags(B.step_begin, s, cudaEventRecordExternal));
   if (cm.n_rows) {
     int rc = ctx_append(g, W, B, cm.rows, cm.n_rows, M_ctx, s);

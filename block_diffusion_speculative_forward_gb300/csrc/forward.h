@@ -67,6 +67,14 @@ struct Buffers {
   int attn_slots = 0;           // slot capacity
   int64_t attn_slot_floats = 0; // n_q*d + 2*n_q per slot
   int64_t fault_ns = 0;         // test hook of every GEMM launch (GemmParams::fault_ns)
+  // few-row (chained) proposes
+  float *ss_in = nullptr;       // [H/128][16] per-tile sums of squares of the residual entering a layer
+  float *ss_mid = nullptr;      // [H/128][16] ... of the residual after o_proj
+  float *ss_c = nullptr;        // [H/128][16] ... of the new ctx rows (hidden_norm's input)
+  int *chain_sync = nullptr;    // per launch and phase: arrival counters, tile flags, tile count
+  int chain_sync_ints = 0;
+  bool use_chain = true;        // few-row proposes take the chained path when it applies
+  int last_chained = 0;         // the last forward took the chained path
 };
 
 // Cuts every (sequence, kv head) key range of the call into split-KV items
@@ -95,6 +103,11 @@ struct CallMeta {
   int n_seq = 0, n_rows = 0, n_items = 0, n_pairs = 0;
   int cap_items = 0, cap_pairs = 0;
 };
+
+// Ints of chained-propose counters a head needs (every launch of one forward).
+int chain_sync_capacity(const Geo &g);
+// Whether a call of n_rows new ctx rows and R block rows takes the chained path.
+bool chain_applies(const Geo &g, const Buffers &B, int n_rows, int R);
 
 int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights *w, int R_max,
                       int D_max, int M_ctx, Weights *W, Buffers *B, std::vector<void *> *dev,

@@ -100,7 +100,9 @@ struct GemmParams {
   const int32_t *bitmask;  // [n_seq][mask_words] or NULL
   int mask_words;
   int nd;             // draft rows per sequence (row a belongs to sequence a / nd)
-  LmPartial *lm_part; // [m_act][tiles_m]
+  int lm_gamma;       // 0: activations are draft rows; > 0: blocks of lm_gamma rows whose
+  int lm_first;       //   rows lm_first .. lm_first + nd - 1 are the draft rows
+  LmPartial *lm_part; // [draft rows][tiles_m]
   int *status;
   // QKV epilogue: rows [0, q_rows) are q heads, [q_rows, q_rows + k_rows) k
   // heads, the rest v; row a of the activations is block row a % gamma of

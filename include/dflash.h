@@ -263,7 +263,7 @@ DFLASH_API int dflash_debug_pool(const dflash_handle *h, int32_t *in_use, int32_
  * dequantised to f32: k_out, v_out dev [n, num_kv_heads, head_dim]. */
 DFLASH_API int dflash_debug_gather_kv(dflash_handle *h, const dflash_state *st, int32_t layer, int64_t pos0,
                            int32_t n, float *k_out, float *v_out, void *stream);
-/* Taps filled by every later propose* (NULL disables each):
+/* Taps filled by every later propose* (NULL disables each; 16-byte aligned):
  * x_taps dev f32 [num_layers+1][rows][hidden] (the residual entering each
  * layer and leaving the last); z dev bf16 [rows][hidden] (final norm);
  * logits dev f32 [n*num_drafts][vocab] (draft rows, sequence-major).
@@ -280,6 +280,13 @@ DFLASH_API int dflash_debug_set_step_probe(dflash_handle *h, void *ev_begin, voi
  * new ctx rows, drafts, bitmask and tap/probe pointers); enable = 0 launches
  * the kernels one by one instead (same results). On by default. */
 DFLASH_API int dflash_debug_set_graphs(dflash_handle *h, int32_t enable);
+/* Few-row proposes (at most 16 block rows and 16 new ctx rows, hidden at
+ * most 2048) run as a chained sequence of persistent launches by default;
+ * enable = 0 makes them take the kernel-per-step path that many-row proposes
+ * take (same results within rounding). Errors: EINVAL. */
+DFLASH_API int dflash_debug_set_chain(dflash_handle *h, int32_t enable);
+/* 1 when the last propose* call took the chained few-row path, else 0. */
+DFLASH_API int dflash_debug_last_path(const dflash_handle *h);
 /* Test hook of the bounded-wait abort path: with wait_ns > 0, every
  * tensor-core GEMM of later propose* calls has one thread of each CTA wait up
  * to wait_ns (<= 2e9) on a barrier that nothing arrives on; the wait runs

@@ -209,3 +209,26 @@ def test_full_geometry_single_sequence():
     assert abs(ref[2] - got[2]) <= CONF_TOL
     assert_tables(pair, so, sl)
     check_kv(pair, so, sl, list(range(1019, 1024)))
+
+
+@pytest.mark.parametrize("chained", [True, False])
+def test_few_row_paths_match_oracle(chained):
+    """Few-row proposes run chained (persistent multi-phase launches) by
+    default; the kernel-per-step path serves them too when the chain is
+    switched off. Both against the oracle, over rounds with new rows."""
+    pair = Pair(syn.TINY, 1051)
+    pair.lib.set_chain(chained)
+    so, sl, _ = _prefill(pair, 45, 1051)
+    rows = syn.make_stack(syn.TINY, 20, 1051, idx=4)
+    p, n_new, used = 45, 0, 0
+    for k in [2, 0, 3, 1]:
+        r = rows[used:used + n_new] if n_new else None
+        used += n_new
+        tap, ref, got = _propose(pair, so, sl, (13 * p) % syn.TINY.vocab, p, r, 3)
+        assert pair.lib.last_path_chained() == chained
+        check_seq(pair, tap, ref, got, 0, 1, 3)
+        assert_tables(pair, so, sl)
+        pair.ora.after_verify(so, k)
+        pair.lib.after_verify(sl, k)
+        p, n_new = p + k + 1, k + 1
+    check_kv(pair, so, sl, range(0, p - n_new))
