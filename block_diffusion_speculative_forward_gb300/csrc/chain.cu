@@ -17,11 +17,12 @@
 //   warp 0     issues the weight TMA loads of every phase into an 8-stage ring;
 //              weights depend on nothing, so it runs ahead across phases
 //   warp 1     owns TMEM and issues the MMAs (one thread)
-//   warp 2     provides the B operand of each stage: a TMA load of a bf16
-//              activation written by an earlier kernel or phase (after the
-//              producing tile's ready flag), or, for a normed input, the whole
-//              RMSNorm(x) rows built once per phase into a 64 KB shared-memory
-//              region from the f32 residual and its per-tile sums of squares
+//   warp 2     provides the B operand of each stage by a TMA load of a bf16
+//              activation: one written by an earlier kernel, or by an earlier
+//              phase (after the producing tile's ready flag), or a normed
+//              input RMSNorm(x), which CTA j writes for k-block j (from the f32
+//              residual and its per-tile sums of squares) before raising that
+//              k-block's ready flag
 //   warps 3-6  drain the accumulators and run the phase's epilogue; a tile cut
 //              between CTAs is finished by its last arriving contributor,
 //              which sums the partials in CTA order
@@ -44,36 +45,45 @@ namespace tc {
 namespace {
 
 constexpr int CH_THREADS = 224;
-constexpr int CH_STAGES = 8;
-constexpr int CH_B_BYTES = CHAIN_BN * BK * 2;                 // 2 KB
+constexpr int CH_STAGES = 11;
+constexpr int CH_B_BYTES = CHAIN_BN * BK * 2;                 // 2 KB: bf16 B operand
 constexpr int CH_STAGE_BYTES = A_BYTES + CH_B_BYTES;          // 18 KB (1024-aligned)
-constexpr int CH_REGION_BYTES = (CHAIN_MAX_K_NORM / BK) * CH_B_BYTES;   // 64 KB
 constexpr int CH_EPI_T0 = 96;
 constexpr uint32_t CH_TMEM_COLS = 32;
 
 struct ChainSmem {
-  uint64_t full[CH_STAGES], empty[CH_STAGES], acc_full[2], acc_empty[2], b_free, drain, never;
+  uint64_t full[CH_STAGES], empty[CH_STAGES], acc_full[2], acc_empty[2], drain, never;
   uint32_t tmem_base;
   uint32_t drain_issued, drain_parity;
   int abort_flag;
   int is_last;
   EpiScratch epi;
 };
-constexpr int CH_SMEM = 1024 + CH_STAGES * CH_STAGE_BYTES + CH_REGION_BYTES + (int)sizeof(ChainSmem);
+constexpr int CH_SMEM = 1024 + CH_STAGES * CH_STAGE_BYTES + (int)sizeof(ChainSmem);
 static_assert(CH_SMEM <= 232448, "chain CTA exceeds the 227 KB shared-memory limit");
 static_assert(CH_STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 static_assert(sizeof(ChainMaps) + sizeof(ChainArgs) <= 32000, "chain parameters exceed the launch limit");
 
-__device__ __forceinline__ int64_t range_begin(int64_t total, int G, int c) {
-  return total * c / G;
-}
-// The CTA whose range holds iteration i.
-__device__ __forceinline__ int range_owner(int64_t total, int G, int64_t i) {
-  int c = (int)((i * G) / total);
-  while (c + 1 < G && range_begin(total, G, c + 1) <= i) ++c;
-  while (c > 0 && range_begin(total, G, c) > i) --c;
-  return c;
-}
+// Stream-K split of one phase's (tile, k-block) iterations over the first
+// G = min(CTAs, iterations) CTAs, so that every participating CTA holds at
+// least one iteration (a tile's contributors are then exactly the CTAs
+// owner(first) .. owner(last)); later CTAs hold none of this phase.
+struct Split {
+  int64_t total;
+  int G;
+  __device__ __forceinline__ Split(int64_t total_, int ctas)
+      : total(total_), G(total_ < ctas ? (int)total_ : ctas) {}
+  __device__ __forceinline__ int64_t begin(int c) const {
+    return c >= G ? total : total * c / G;
+  }
+  // The CTA whose range holds iteration i.
+  __device__ __forceinline__ int owner(int64_t i) const {
+    int c = (int)((i * G) / total);
+    while (c + 1 < G && begin(c + 1) <= i) ++c;
+    while (c > 0 && begin(c) > i) --c;
+    return c;
+  }
+};
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
@@ -110,14 +120,17 @@ __device__ __forceinline__ void finish_rows(const ChainPhase &P, EpiScratch *sm,
                                             int et) {
   const bool add = P.kind != CK_FC;
   const bool f_ok = f < P.n_w;
-  float sq[16];
+  // every load first (one round trip), then the stores
+  float old[16], sq[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    old[c] = (add && f_ok && c < P.rows) ? __ldcg(P.out + (int64_t)c * P.n_w + f) : 0.f;
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
     float y = 0.f;
     if (f_ok && c < P.rows) {
-      float *o = P.out + (int64_t)c * P.n_w + f;
-      y = (add ? __ldcg(o) : 0.f) + v[c];
-      *o = y;
+      y = old[c] + v[c];
+      P.out[(int64_t)c * P.n_w + f] = y;
       if (P.x_tap) P.x_tap[(int64_t)c * P.n_w + f] = y;
     }
     sq[c] = y * y;
@@ -214,8 +227,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
-  const uint32_t region = base + CH_STAGES * CH_STAGE_BYTES;
-  ChainSmem *sm = (ChainSmem *)(gbase + CH_STAGES * CH_STAGE_BYTES + CH_REGION_BYTES);
+  ChainSmem *sm = (ChainSmem *)(gbase + CH_STAGES * CH_STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (int)gridDim.x, cta = (int)blockIdx.x;
   const int np = a.n_phases;
@@ -229,7 +241,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       mbar_init(smem_u32(&sm->acc_full[b]), 1);
       mbar_init(smem_u32(&sm->acc_empty[b]), 4);
     }
-    mbar_init(smem_u32(&sm->b_free), 1);
     mbar_init(smem_u32(&sm->drain), 1);
     mbar_init(smem_u32(&sm->never), 1);   // nothing ever arrives (test hook)
     sm->abort_flag = 0;
@@ -241,7 +252,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   }
   if (warp == 0 && lane < np) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.w[lane]) : "memory");
-    if (!a.ph[lane].b_norm) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.b[lane]) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.b[lane]) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -265,14 +276,15 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       bool ok = true;
       for (int p = 0; p < np && ok; ++p) {
         const ChainPhase &P = a.ph[p];
-        const int64_t total = (int64_t)P.tiles_m * P.kb;
-        const int64_t e = range_begin(total, G, cta + 1);
-        for (int64_t it = range_begin(total, G, cta); it < e; ++it) {
+        const Split sp((int64_t)P.tiles_m * P.kb, G);
+        const int64_t e = sp.begin(cta + 1);
+        int t = (int)(sp.begin(cta) / P.kb), k = (int)(sp.begin(cta) % P.kb);
+        for (int64_t it = sp.begin(cta); it < e; ++it) {
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&sm->full[stage]);
           mbar_expect_tx(fb, A_BYTES);
-          tma_load_2d(base + stage * CH_STAGE_BYTES, &maps.w[p], fb, (int)(it % P.kb) * BK,
-                      (int)(it / P.kb) * BM, pol);
+          tma_load_2d(base + stage * CH_STAGE_BYTES, &maps.w[p], fb, k * BK, t * BM, pol);
+          if (++k == P.kb) { k = 0; ++t; }
           issued |= 1u << stage;
           parity = (parity & ~(1u << stage)) | (phase << stage);
           if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
@@ -291,8 +303,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       bool ok = true;
       for (int p = 0; p < np && ok; ++p) {
         const ChainPhase &P = a.ph[p];
-        const int64_t total = (int64_t)P.tiles_m * P.kb;
-        const int64_t b = range_begin(total, G, cta), e = range_begin(total, G, cta + 1);
+        const Split sp((int64_t)P.tiles_m * P.kb, G);
+        const int64_t b = sp.begin(cta), e = sp.begin(cta + 1);
         for (int64_t it = b; it < e && ok;) {
           const int k0 = (int)(it % P.kb);
           const int k1 = (int)((int64_t)P.kb < k0 + (e - it) ? (int64_t)P.kb : k0 + (e - it));
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             if (!mbar_wait(smem_u32(&sm->full[stage]), phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = base + stage * CH_STAGE_BYTES;
-            const uint32_t sb = P.b_norm ? region + k * CH_B_BYTES : sa + A_BYTES;
+            const uint32_t sb = sa + A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               umma_bf16(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), idesc,
@@ -317,8 +329,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           if (acc == 0) acc_phase ^= 1;
           it += k1 - k0;
         }
-        // the normed region is free again once this phase's MMAs completed
-        if (ok && P.b_norm && e > b) umma_commit(smem_u32(&sm->b_free));
       }
     }
   } else if (warp == 2) {
@@ -326,110 +336,123 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     pdl_wait();
     const uint64_t pol_b = policy_evict_last();
     int stage = 0;
-    uint32_t phase = 0, free_phase = 0;
-    bool region_used = false, ok = true;
+    uint32_t phase = 0;
+    bool ok = true;
     for (int p = 0; p < np && ok; ++p) {
       const ChainPhase &P = a.ph[p];
-      const int64_t total = (int64_t)P.tiles_m * P.kb;
-      const int64_t b = range_begin(total, G, cta), e = range_begin(total, G, cta + 1);
+      const Split sp((int64_t)P.tiles_m * P.kb, G);
+      const int64_t b = sp.begin(cta), e = sp.begin(cta + 1);
+      const bool need_dep = P.dep >= 0 && !P.dep_tile;
+      if (P.b_norm && cta < P.kb) {
+        // this CTA's share of the normed operand: k-block cta of
+        // h = bf16(gain * x * rinv(row)), written once to the phase's bf16
+        // buffer, then its ready flag
+        if (need_dep && !wait_count_warp(a.ph[P.dep].done, a.ph[P.dep].tiles_m, abort_flag)) {
+          ok = false;
+          break;
+        }
+        float rinv = 0.f;   // lane r < 16: 1 / sqrt(mean square of row r + eps)
+        if (lane < 16 && lane < P.rows) {
+          // the row's per-tile sums (at most 16 tiles), all loads in flight at once
+          const int nt = P.k / 128;
+          float sv[CHAIN_MAX_K_NORM / 128];
+#pragma unroll
+          for (int j = 0; j < CHAIN_MAX_K_NORM / 128; ++j) sv[j] = j < nt ? __ldcg(P.nss + j * 16 + lane) : 0.f;
+          float t = 0.f;
+#pragma unroll
+          for (int j = 0; j < CHAIN_MAX_K_NORM / 128; ++j) t += sv[j];
+          rinv = rsqrtf(t / (float)P.k + P.ep.eps);
+        }
+        // lane: row r, 32 consecutive features (half hh of the k-block)
+        const int r = lane & 15, hh = lane >> 4;
+        const float rr = __shfl_sync(0xffffffffu, rinv, r);
+        const int f0 = cta * BK + hh * 32;
+        uint32_t w[16];
+        if (r < P.rows) {
+          const float4 *xs = reinterpret_cast<const float4 *>(P.nsrc + (int64_t)r * P.k + f0);
+          const uint4 *gs = reinterpret_cast<const uint4 *>(P.ngain + f0);
+          float4 xv[8];
+          uint4 gw[4];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) xv[u] = __ldcg(xs + u);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) gw[u] = __ldg(gs + u);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bf16 *gv = reinterpret_cast<const bf16 *>(&gw[u]);
+            const float x8[8] = {xv[2 * u].x, xv[2 * u].y, xv[2 * u].z, xv[2 * u].w,
+                                 xv[2 * u + 1].x, xv[2 * u + 1].y, xv[2 * u + 1].z, xv[2 * u + 1].w};
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                  __bfloat162float(gv[2 * e2]) * (x8[2 * e2] * rr),
+                  __bfloat162float(gv[2 * e2 + 1]) * (x8[2 * e2 + 1] * rr));
+              w[4 * u + e2] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) w[u] = 0u;   // rows past the call's rows: zero
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(P.hbuf + (int64_t)r * P.k + f0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        if (P.kind == CK_LM && r < P.rows) {
+          // the lm_head's normed rows for the debug taps
+          if (P.z_tap) {
+            uint4 *zt = reinterpret_cast<uint4 *>(P.z_tap + (int64_t)r * P.k + f0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) zt[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+          }
+          const int j = r % P.ep.lm_gamma - P.ep.lm_first;
+          if (P.z_rows && j >= 0 && j < P.ep.nd) {
+            uint4 *zr = reinterpret_cast<uint4 *>(P.z_rows +
+                                                  (int64_t)((r / P.ep.lm_gamma) * P.ep.nd + j) * P.k + f0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) zr[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+          }
+        }
+        // publish: the warp's stores are ordered before lane 0's release by
+        // the warp barrier (release is cumulative); consumers acquire, then
+        // fence the async proxy before their TMA reads
+        __syncwarp();
+        if (lane == 0) {
+          asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(P.hflag + cta), "r"(1) : "memory");
+          asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(P.hdone), "r"(1) : "memory");
+        }
+      }
       if (b == e) continue;
-      if (P.dep >= 0 && !P.dep_tile &&
+      if (need_dep && !P.b_norm &&
           !wait_count_warp(a.ph[P.dep].done, a.ph[P.dep].tiles_m, abort_flag)) {
         ok = false;
         break;
       }
-      if (P.b_norm) {
-        // the previous normed phase's MMAs must be done with the region
-        if (region_used) {
-          if (!mbar_wait_warp(smem_u32(&sm->b_free), free_phase, abort_flag)) { ok = false; break; }
-          free_phase ^= 1;
+      // B = a bf16 activation, TMA per stage. A normed operand's k-block k
+      // waits for its ready flag; with a tile dependency, k-block k waits for
+      // tile k of phase dep; either until every k-block or tile is ready.
+      const ChainPhase *D = (P.dep >= 0 && P.dep_tile) ? &a.ph[P.dep] : nullptr;
+      const int *rflag = P.b_norm ? P.hflag : D ? D->flag : nullptr;
+      const int *rdone = P.b_norm ? P.hdone : D ? D->done : nullptr;
+      const int rall = P.b_norm ? P.kb : D ? D->tiles_m : 0;
+      bool all_ready = rflag == nullptr;
+      int k = (int)(b % P.kb);
+      for (int64_t it = b; it < e; ++it) {
+        if (!mbar_wait_warp(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
+        bool acquired = false;
+        if (!all_ready) {
+          acquired = true;
+          if (ld_acquire(rdone) >= rall) all_ready = true;
+          else if (!wait_count_warp(rflag + k, 1, abort_flag)) { ok = false; break; }
         }
-        region_used = true;
-        // rinv of row r (lanes 0..15): 1 / sqrt(mean of squares + eps)
-        float rinv = 0.f;
-        if (lane < 16 && lane < P.rows) {
-          float t = 0.f;
-          for (int j = 0; j < P.k / 128; ++j) t += __ldcg(P.nss + j * 16 + lane);
-          rinv = rsqrtf(t / (float)P.k + a.ph[p].ep.eps);
+        if (lane == 0) {
+          // what the acquire made visible to the generic proxy, for the TMA
+          if (acquired) asm volatile("fence.proxy.async.global;" ::: "memory");
+          const uint32_t fb = smem_u32(&sm->full[stage]);
+          mbar_expect_tx(fb, CH_B_BYTES);
+          tma_load_2d(base + stage * CH_STAGE_BYTES + A_BYTES, &maps.b[p], fb, k * BK, 0, pol_b);
         }
-        // lane: row r = lane / 2, 32 consecutive features (four 16-byte chunks)
-        const int r = lane >> 1, hh = lane & 1;
-        const float rr = __shfl_sync(0xffffffffu, rinv, r);
-        const bool live = r < P.rows;
-        const bool tap = P.kind == CK_LM && cta == 0 && live;
-        int drow = -1;
-        if (tap && P.z_rows) {
-          const int gm = P.ep.lm_gamma, j = r % gm - P.ep.lm_first;
-          if (j >= 0 && j < P.ep.nd) drow = (r / gm) * P.ep.nd + j;
-        }
-        for (int kb = 0; kb < P.kb; ++kb) {
-          const int f0 = kb * BK + hh * 32;
-          uint32_t w[16];
-          if (live) {
-            const float4 *xs = reinterpret_cast<const float4 *>(P.nsrc + (int64_t)r * P.k + f0);
-            const uint4 *gs = reinterpret_cast<const uint4 *>(P.ngain + f0);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float4 x0 = __ldcg(xs + 2 * u), x1 = __ldcg(xs + 2 * u + 1);
-              const uint4 gw = __ldg(gs + u);
-              const bf16 *gv = reinterpret_cast<const bf16 *>(&gw);
-              const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                    __bfloat162float(gv[2 * e2]) * (xv[2 * e2] * rr),
-                    __bfloat162float(gv[2 * e2 + 1]) * (xv[2 * e2 + 1] * rr));
-                w[4 * u + e2] = *reinterpret_cast<uint32_t *>(&h2);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 16; ++u) w[u] = 0u;
-          }
-          // 128-byte swizzle: chunk ch of row r sits at chunk ch ^ (r % 8)
-          const uint32_t rowb = region + kb * CH_B_BYTES + r * 128;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t ch = (uint32_t)(hh * 4 + u);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             rowb + ((ch ^ (uint32_t)(r & 7)) << 4)),
-                         "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
-                         : "memory");
-          }
-          if (tap) {
-            if (P.z_tap) {
-              uint4 *zt = reinterpret_cast<uint4 *>(P.z_tap + (int64_t)r * P.k + f0);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) zt[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            }
-            if (drow >= 0) {
-              uint4 *zr = reinterpret_cast<uint4 *>(P.z_rows + (int64_t)drow * P.k + f0);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) zr[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            }
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        for (int64_t it = b; it < e; ++it) {
-          if (!mbar_wait_warp(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
-          if (lane == 0) mbar_arrive(smem_u32(&sm->full[stage]));
-          if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
-        }
-      } else {
-        const ChainPhase *D = P.dep >= 0 ? &a.ph[P.dep] : nullptr;
-        for (int64_t it = b; it < e; ++it) {
-          const int k = (int)(it % P.kb);
-          if (!mbar_wait_warp(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
-          if (P.dep_tile && D && !wait_count_warp(D->flag + k, 1, abort_flag)) { ok = false; break; }
-          if (lane == 0) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            const uint32_t fb = smem_u32(&sm->full[stage]);
-            mbar_expect_tx(fb, CH_B_BYTES);
-            tma_load_2d(base + stage * CH_STAGE_BYTES + A_BYTES, &maps.b[p], fb, k * BK, 0, pol_b);
-          }
-          if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
-        }
+        if (++k == P.kb) k = 0;
+        if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
       }
     }
   } else {
@@ -446,8 +469,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     live = epi_all(live);
     for (int p = 0; p < np && live; ++p) {
       const ChainPhase &P = a.ph[p];
-      const int64_t total = (int64_t)P.tiles_m * P.kb;
-      const int64_t b = range_begin(total, G, cta), e = range_begin(total, G, cta + 1);
+      const Split sp((int64_t)P.tiles_m * P.kb, G);
+      const int64_t b = sp.begin(cta), e = sp.begin(cta + 1);
       bool res_seen = P.res_dep < 0;
       for (int64_t it = b; it < e;) {
         const int t = (int)(it / P.kb);
@@ -473,30 +496,50 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           float4 *dst = reinterpret_cast<float4 *>(a.ws + ((int64_t)slot * BM + f_local) * CHAIN_BN);
 #pragma unroll
           for (int c = 0; c < 4; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-          __threadfence();
+          // arrival: the partial stores of all 128 threads are ordered before
+          // one thread's acquire-release add by the barrier; the last
+          // contributor's add acquires every earlier contributor's partials,
+          // and the barrier after it carries that to the other threads
           epi_bar();
-          const int c_lo = range_owner(total, G, (int64_t)t * P.kb);
-          const int c_hi = range_owner(total, G, (int64_t)t * P.kb + P.kb - 1);
-          if (et == 0) sm->is_last = (atomicAdd(&P.arrive[t], 1) == c_hi - c_lo);
+          const int c_lo = sp.owner((int64_t)t * P.kb);
+          const int c_hi = sp.owner((int64_t)t * P.kb + P.kb - 1);
+          if (et == 0) {
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(P.arrive + t) : "memory");
+            sm->is_last = (old == c_hi - c_lo);
+          }
           epi_bar();
           finisher = sm->is_last != 0;
           if (finisher) {
-            __threadfence();
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] = 0.f;
-            for (int cc = c_lo; cc <= c_hi; ++cc) {
-              const int sl = 2 * (p * G + cc) +
-                             ((cc == c_lo && range_begin(total, G, cc) < (int64_t)t * P.kb) ? 1 : 0);
-              const float4 *src =
-                  reinterpret_cast<const float4 *>(a.ws + ((int64_t)sl * BM + f_local) * CHAIN_BN);
+            // contributors in ascending order, four partials in flight
+            for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
+              float4 r[4][4];
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const float4 r = __ldcg(src + c);
-                v[4 * c] += r.x;
-                v[4 * c + 1] += r.y;
-                v[4 * c + 2] += r.z;
-                v[4 * c + 3] += r.w;
+              for (int u = 0; u < 4; ++u) {
+                const int cc = c0 + u;
+                if (cc <= c_hi) {
+                  const int sl = 2 * (p * G + cc) +
+                                 ((cc == c_lo && sp.begin(cc) < (int64_t)t * P.kb) ? 1 : 0);
+                  const float4 *src = reinterpret_cast<const float4 *>(
+                      a.ws + ((int64_t)sl * BM + f_local) * CHAIN_BN);
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) r[u][c] = __ldcg(src + c);
+                } else {
+#pragma unroll
+                  for (int c = 0; c < 4; ++c) r[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
               }
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  v[4 * c] += r[u][c].x;
+                  v[4 * c + 1] += r[u][c].y;
+                  v[4 * c + 2] += r[u][c].z;
+                  v[4 * c + 3] += r[u][c].w;
+                }
             }
           }
         }
@@ -521,11 +564,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             case CK_GU: finish16<EPI_TC_SWIGLU>(P.ep, &sm->epi, v, f, t, 0, q, lane, et); break;
             default: finish16<EPI_TC_LMHEAD>(P.ep, &sm->epi, v, f, t, 0, q, lane, et); break;
           }
-          // publish: every thread's stores, then the tile's flag and count
-          __threadfence();
+          // publish: every thread's stores (ordered by the barrier), then
+          // the tile's flag and count with release semantics
           epi_bar();
           if (et == 0) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
             asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(P.flag + t), "r"(1) : "memory");
             asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(P.done), "r"(1) : "memory");
           }

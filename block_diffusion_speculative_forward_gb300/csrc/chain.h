@@ -23,20 +23,25 @@ enum ChainKind : int {
 constexpr int CHAIN_MAX_PHASES = 6;
 constexpr int CHAIN_BN = 16;        // activation rows of every phase (one MMA N)
 constexpr int CHAIN_BK = 64;        // reduction elements per stage
-constexpr int CHAIN_MAX_K_NORM = 2048;   // a normed B operand is held whole in shared memory
+constexpr int CHAIN_MAX_K_NORM = 2048;   // the widest normed input (hidden) the chain takes
 
 struct ChainPhase {
   int kind;
   int n_w, k;            // weight rows (outputs), reduction length (multiple of 64)
   int rows;              // valid activation rows (<= 16)
   int tiles_m, kb;       // n_w / 128 rounded up, k / 64
-  // B operand: 1 = RMSNorm(nsrc; ngain) built in shared memory from the f32
-  // rows nsrc [rows, k] and their per-tile sums of squares nss [k/128][16];
-  // 0 = TMA of the bf16 activation map of this phase
+  // B operand: TMA of the bf16 activation map b of this phase. b_norm = 1:
+  // that activation is hbuf = RMSNorm(nsrc; ngain) [16, k], which CTA j
+  // writes for k-block j from the f32 rows nsrc [rows, k] and their per-tile
+  // sums of squares nss [k/128][16] (rows past `rows` are zero), then sets
+  // hflag[j] and counts hdone
   int b_norm;
   const float *nsrc;
   const float *nss;
   const bf16 *ngain;
+  bf16 *hbuf;
+  int *hflag;            // [kb] (zero at launch)
+  int *hdone;            // (zero at launch)
   // dependency of the B operand on an earlier phase of the same launch:
   // dep < 0 none; dep_tile 0: every tile of phase dep finished; 1: k-block j
   // waits for tile j of phase dep
@@ -75,7 +80,7 @@ struct ChainArgs {
 
 struct ChainMaps {
   CUtensorMap w[CHAIN_MAX_PHASES];   // weights, box 128 rows x 64
-  CUtensorMap b[CHAIN_MAX_PHASES];   // activations (TMA-fed B operands), box 16 rows x 64
+  CUtensorMap b[CHAIN_MAX_PHASES];   // bf16 activations (the B operands), box 16 rows x 64
 };
 
 namespace tc {

@@ -203,7 +203,7 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->row_p1, (size_t)D_max);
   BA(B->ctx_pack, (size_t)M_ctx * g.S);
   BA(B->ctx_fc, (size_t)M_ctx * H);
-  BA(B->ctx_c, (size_t)M_ctx * H);
+  BA(B->ctx_c, (size_t)std::max(M_ctx, CHAIN_BN) * H);   // the chained path writes 16 rows
   BA(B->ctx_kv, (size_t)M_ctx * g.L * 2 * kv);
   BA(B->status, 4);
   BK(cudaMemset(B->status, 0, 16));
@@ -226,6 +226,12 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     BA(B->ss_c, (size_t)ht * 16);
     B->chain_sync_ints = chain_sync_capacity(g);
     BA(B->chain_sync, (size_t)B->chain_sync_ints);
+    BA(B->hn, (size_t)2 * CHAIN_BN * H);
+    if (!tc::make_map_2d(&B->map_hn[0], B->hn, false, CHAIN_BN, H, CHAIN_BN) ||
+        !tc::make_map_2d(&B->map_hn[1], B->hn + (size_t)CHAIN_BN * H, false, CHAIN_BN, H, CHAIN_BN)) {
+      g_build_err = "cuTensorMapEncodeTiled failed for a normed activation";
+      return DFLASH_ECUDA;
+    }
   }
   // Split-KV attention partials: at most two ctx chunks per (sequence, kv
   // head) beyond 3 x SMs, plus one block-key item each.
@@ -374,11 +380,12 @@ int ctx_append(const Geo &g, const Weights &W, const Buffers &B, const RowMeta *
 
 int chain_sync_capacity(const Geo &g) {
   auto t = [](int64_t n) { return (int)((n + 127) / 128); };
-  // per phase: arrival counters and flags per tile, one tile count (+ padding)
-  auto ph = [](int tiles) { return 2 * tiles + 4; };
-  const int first = ph(t(g.H)) + ph(t((int64_t)g.L * 2 * g.kv)) + ph(t(g.qkv_w));
-  const int layer = ph(t(g.H)) + ph(t(2 * (int64_t)g.I)) + ph(t(g.H)) +
-                    std::max(ph(t(g.qkv_w)), ph(t(g.V)));
+  // per phase: arrival counters and flags per tile, the tile count, the
+  // normed operand's k-block count and flags (+ padding); see forward_chain
+  auto ph = [](int tiles, int k) { return 2 * tiles + 4 + (k / CHAIN_BK + 3) / 4 * 4; };
+  const int first = ph(t(g.H), g.S) + ph(t((int64_t)g.L * 2 * g.kv), g.H) + ph(t(g.qkv_w), g.H);
+  const int layer = ph(t(g.H), g.nq * g.d) + ph(t(2 * (int64_t)g.I), g.H) + ph(t(g.H), g.I) +
+                    std::max(ph(t(g.qkv_w), g.H), ph(t(g.V), g.H));
   return first + g.L * layer + 64;
 }
 
@@ -415,7 +422,9 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
     P.arrive = sync;
     P.flag = sync + P.tiles_m;
     P.done = sync + 2 * P.tiles_m;
-    sync += 2 * P.tiles_m + 4;
+    P.hdone = P.done + 1;
+    P.hflag = sync + 2 * P.tiles_m + 4;
+    sync += 2 * P.tiles_m + 4 + (P.kb + 3) / 4 * 4;
     P.geo = g;
     P.ep.m_act = rows;
     P.ep.n_w = n_w;
@@ -428,15 +437,17 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
     P.ep.sin_t = W.sin_t;
     return P;
   };
-  auto normed = [](ChainPhase &P, const float *src, const float *ss, const bf16 *gain) {
+  auto normed = [](ChainPhase &P, const float *src, const float *ss, const bf16 *gain, bf16 *h) {
     P.b_norm = 1;
     P.nsrc = src;
     P.nss = ss;
     P.ngain = gain;
+    P.hbuf = h;
   };
+  bf16 *const hn_mid = B.hn, *const hn_in = B.hn + (size_t)CHAIN_BN * g.H;
   auto qkv_phase = [&](int l) {
     ChainPhase P = phase(CK_QKV, g.qkv_w, g.H, R);
-    normed(P, B.x, B.ss_in, W.layers[l].in_norm);
+    normed(P, B.x, B.ss_in, W.layers[l].in_norm, hn_in);
     P.ep.seq = cm.seq;
     P.ep.gamma = g.gamma;
     P.ep.head_dim = g.d;
@@ -458,7 +469,7 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
     for (int i = 0; i < np; ++i) {
       a.ph[i] = ph[i];
       maps.w[i] = *wm[i];
-      maps.b[i] = bm[i] ? *bm[i] : empty_map;
+      maps.b[i] = *bm[i];
     }
     for (int i = np; i < CHAIN_MAX_PHASES; ++i) {
       maps.w[i] = empty_map;
@@ -486,7 +497,7 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
       wm[np] = &W.map_fc;
       bm[np++] = act16_pack;
       ChainPhase kv = phase(CK_KV, g.L * 2 * g.kv, g.H, m);
-      normed(kv, B.ctx_fc, B.ss_c, W.hidden_norm);
+      normed(kv, B.ctx_fc, B.ss_c, W.hidden_norm, B.ctx_c);
       kv.dep = 0;
       kv.ctx_rows = cm.rows;
       kv.k_norm = W.k_norm_dev;
@@ -494,11 +505,11 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
       kv.kv_scale = W.kv_scale;
       ph[np] = kv;
       wm[np] = &W.map_wkv;
-      bm[np++] = nullptr;
+      bm[np++] = &B.act_map[ACT_C][bn_index(16)];
     }
     ph[np] = qkv_phase(0);
     wm[np] = &W.map_qkv[0];
-    bm[np++] = nullptr;
+    bm[np++] = &B.map_hn[1];
     int rc = launch(ph, wm, bm, np);
     if (rc) return rc;
   }
@@ -543,11 +554,11 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
     wm[0] = &W.map_o[l];
     bm[0] = act16_o;
     ph[1] = phase(CK_GU, 2 * g.I, g.H, R);
-    normed(ph[1], B.x, B.ss_mid, L.post_norm);
+    normed(ph[1], B.x, B.ss_mid, L.post_norm, hn_mid);
     ph[1].dep = 0;
     ph[1].ep.u_out = B.u;
     wm[1] = &W.map_gu[l];
-    bm[1] = nullptr;
+    bm[1] = &B.map_hn[0];
     ph[2] = phase(CK_DOWN, g.H, g.I, R);
     ph[2].dep = 1;
     ph[2].dep_tile = 1;
@@ -562,7 +573,7 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
       wm[3] = &W.map_qkv[l + 1];
     } else {
       ph[3] = phase(CK_LM, g.V, g.H, R);
-      normed(ph[3], B.x, B.ss_in, W.norm);
+      normed(ph[3], B.x, B.ss_in, W.norm, hn_in);
       ph[3].ep.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
       ph[3].ep.bitmask = bitmask;
       ph[3].ep.mask_words = (g.V + 31) / 32;
@@ -577,7 +588,7 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
         FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));
     }
     ph[3].dep = 2;
-    bm[3] = nullptr;
+    bm[3] = &B.map_hn[1];
     int rc = launch(ph, wm, bm, 4);
     if (rc) return rc;
   }

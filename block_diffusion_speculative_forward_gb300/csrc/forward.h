@@ -72,6 +72,8 @@ struct Buffers {
   float *ss_mid = nullptr;      // [H/128][16] ... of the residual after o_proj
   float *ss_c = nullptr;        // [H/128][16] ... of the new ctx rows (hidden_norm's input)
   int *chain_sync = nullptr;    // per launch and phase: arrival counters, tile flags, tile count
+  bf16 *hn = nullptr;           // [2][16][H] normed residual rows (gate/up input; QKV or lm_head input)
+  CUtensorMap map_hn[2];        // their B-operand maps, box 16 rows x 64
   int chain_sync_ints = 0;
   bool use_chain = true;        // few-row proposes take the chained path when it applies
   int last_chained = 0;         // the last forward took the chained path
