@@ -344,8 +344,8 @@ class DraftHead:
         _check(lib().dflash_debug_set_fault(self.ptr, int(wait_ns)))
 
     def set_chain(self, enable: bool):
-        """Few-row proposes take the chained path (default) or the
-        kernel-per-step path."""
+        """Few-row proposes take the chained single launch (True) or the
+        kernel-per-step path (False, the default)."""
         _check(lib().dflash_debug_set_chain(self.ptr, 1 if enable else 0))
 
     def last_path_chained(self) -> bool:

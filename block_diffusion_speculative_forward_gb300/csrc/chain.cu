@@ -38,6 +38,7 @@
 #include "chain.h"
 #include "gemm_epi.h"
 #include "tc_ptx.h"
+#include "chain_attn.cuh"
 
 namespace dfl {
 namespace tc {
@@ -45,7 +46,7 @@ namespace tc {
 namespace {
 
 constexpr int CH_THREADS = 224;
-constexpr int CH_STAGES = 11;
+constexpr int CH_STAGES = 8;
 constexpr int CH_B_BYTES = CHAIN_BN * BK * 2;                 // 2 KB: bf16 B operand
 constexpr int CH_STAGE_BYTES = A_BYTES + CH_B_BYTES;          // 18 KB (1024-aligned)
 constexpr int CH_EPI_T0 = 96;
@@ -53,16 +54,18 @@ constexpr uint32_t CH_TMEM_COLS = 32;
 
 struct ChainSmem {
   uint64_t full[CH_STAGES], empty[CH_STAGES], acc_full[2], acc_empty[2], drain, never;
+  uint64_t kvb[8];   // attention: two K/V buffers per epilogue warp
   uint32_t tmem_base;
   uint32_t drain_issued, drain_parity;
   int abort_flag;
   int is_last;
   EpiScratch epi;
 };
-constexpr int CH_SMEM = 1024 + CH_STAGES * CH_STAGE_BYTES + (int)sizeof(ChainSmem);
+constexpr int CH_ATTN_OFF = CH_STAGES * CH_STAGE_BYTES;   // the attention area (1024-aligned)
+constexpr int CH_SMEM = 1024 + CH_ATTN_OFF + CA_BYTES + (int)sizeof(ChainSmem);
 static_assert(CH_SMEM <= 232448, "chain CTA exceeds the 227 KB shared-memory limit");
 static_assert(CH_STAGE_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
-static_assert(sizeof(ChainMaps) + sizeof(ChainArgs) <= 32000, "chain parameters exceed the launch limit");
+static_assert(sizeof(ChainArgs) <= 32000, "chain parameters exceed the launch limit");
 
 // Stream-K split of one phase's (tile, k-block) iterations over the first
 // G = min(CTAs, iterations) CTAs, so that every participating CTA holds at
@@ -222,12 +225,12 @@ __device__ __forceinline__ void finish_kv(const ChainPhase &P, EpiScratch *sm, c
 
 // ---------------------------------------------------------------- kernel --
 __global__ void __launch_bounds__(CH_THREADS, 1)
-    k_chain(const __grid_constant__ ChainMaps maps, const __grid_constant__ ChainArgs a) {
+    k_chain(const __grid_constant__ ChainArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
-  ChainSmem *sm = (ChainSmem *)(gbase + CH_STAGES * CH_STAGE_BYTES);
+  ChainSmem *sm = (ChainSmem *)(gbase + CH_ATTN_OFF + CA_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (int)gridDim.x, cta = (int)blockIdx.x;
   const int np = a.n_phases;
@@ -243,6 +246,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     }
     mbar_init(smem_u32(&sm->drain), 1);
     mbar_init(smem_u32(&sm->never), 1);   // nothing ever arrives (test hook)
+    for (int b = 0; b < 8; ++b) mbar_init(smem_u32(&sm->kvb[b]), 1);
     sm->abort_flag = 0;
     sm->drain_issued = 0;
     sm->drain_parity = 0;
@@ -250,9 +254,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     pdl_trigger();
   }
-  if (warp == 0 && lane < np) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.w[lane]) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.b[lane]) : "memory");
+  if (warp == 0) {
+    for (int p = lane; p < np; p += 32)
+      if (a.ph[p].kind != CK_ATTN) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(a.maps + a.ph[p].map_w) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(a.maps + a.ph[p].map_b) : "memory");
+      }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -278,12 +285,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         const ChainPhase &P = a.ph[p];
         const Split sp((int64_t)P.tiles_m * P.kb, G);
         const int64_t e = sp.begin(cta + 1);
+        if (sp.begin(cta) >= e) continue;   // no weights here (attention, or a short phase)
         int t = (int)(sp.begin(cta) / P.kb), k = (int)(sp.begin(cta) % P.kb);
         for (int64_t it = sp.begin(cta); it < e; ++it) {
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t fb = smem_u32(&sm->full[stage]);
           mbar_expect_tx(fb, A_BYTES);
-          tma_load_2d(base + stage * CH_STAGE_BYTES, &maps.w[p], fb, k * BK, t * BM, pol);
+          tma_load_2d(base + stage * CH_STAGE_BYTES, a.maps + P.map_w, fb, k * BK, t * BM, pol);
           if (++k == P.kb) { k = 0; ++t; }
           issued |= 1u << stage;
           parity = (parity & ~(1u << stage)) | (phase << stage);
@@ -434,6 +442,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       const int *rflag = P.b_norm ? P.hflag : D ? D->flag : nullptr;
       const int *rdone = P.b_norm ? P.hdone : D ? D->done : nullptr;
       const int rall = P.b_norm ? P.kb : D ? D->tiles_m : 0;
+      const int rdiv = P.b_norm ? 1 : P.dep_div, rneed = P.b_norm ? 1 : P.dep_need;
       bool all_ready = rflag == nullptr;
       int k = (int)(b % P.kb);
       for (int64_t it = b; it < e; ++it) {
@@ -442,14 +451,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         if (!all_ready) {
           acquired = true;
           if (ld_acquire(rdone) >= rall) all_ready = true;
-          else if (!wait_count_warp(rflag + k, 1, abort_flag)) { ok = false; break; }
+          else if (!wait_count_warp(rflag + k / rdiv, rneed, abort_flag)) { ok = false; break; }
         }
         if (lane == 0) {
           // what the acquire made visible to the generic proxy, for the TMA
           if (acquired) asm volatile("fence.proxy.async.global;" ::: "memory");
           const uint32_t fb = smem_u32(&sm->full[stage]);
           mbar_expect_tx(fb, CH_B_BYTES);
-          tma_load_2d(base + stage * CH_STAGE_BYTES + A_BYTES, &maps.b[p], fb, k * BK, 0, pol_b);
+          tma_load_2d(base + stage * CH_STAGE_BYTES + A_BYTES, a.maps + P.map_b, fb, k * BK, 0, pol_b);
         }
         if (++k == P.kb) k = 0;
         if (++stage == CH_STAGES) { stage = 0; phase ^= 1; }
@@ -467,8 +476,33 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     if (a.fault_ns > 0 && et == 0)
       live = fault_wait(smem_u32(&sm->never), (uint64_t)a.fault_ns, abort_flag);
     live = epi_all(live);
+    uint32_t kv_par = 0;   // per warp and buffer: parity of the next K/V arrival
     for (int p = 0; p < np && live; ++p) {
       const ChainPhase &P = a.ph[p];
+      if (P.kind == CK_ATTN) {
+        // block attention: items cta, cta + G, ... of the call, once the QKV
+        // phase (and the fused ctx K/V phase of this launch, if any) is done
+        bool ok = true;
+        if (warp == 3) {
+          if (P.dep >= 0) ok = wait_count_warp(a.ph[P.dep].done, a.ph[P.dep].tiles_m, abort_flag);
+          if (ok && P.dep2 >= 0) ok = wait_count_warp(a.ph[P.dep2].done, a.ph[P.dep2].tiles_m, abort_flag);
+        }
+        live = epi_all(ok);
+        const int n_items = live ? *a.attn.count : 0;
+        uint8_t *abase = gbase + CH_ATTN_OFF;
+        const uint32_t abase_s = base + CH_ATTN_OFF;
+        const uint32_t kvb0 = smem_u32(&sm->kvb[0]);
+        for (int i = cta; i < n_items && live; i += G) {
+          const ChainAttnItem it = a.attn.items[i];
+          live = a.attn.geo.d == 128
+                     ? ca_item<128>(a.attn, a.maps + a.map_pool, P.attn_layer, P, it, abase, abase_s, kvb0, kv_par, &sm->epi,
+                                    &sm->is_last, abort_flag, a.status, et, q, lane)
+                     : ca_item<64>(a.attn, a.maps + a.map_pool, P.attn_layer, P, it, abase, abase_s, kvb0, kv_par, &sm->epi,
+                                   &sm->is_last, abort_flag, a.status, et, q, lane);
+          live = epi_all(live);
+        }
+        continue;
+      }
       const Split sp((int64_t)P.tiles_m * P.kb, G);
       const int64_t b = sp.begin(cta), e = sp.begin(cta + 1);
       bool res_seen = P.res_dep < 0;
@@ -492,7 +526,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         bool finisher = whole;
         if (!whole) {
           // this CTA's partial of the tile, thread-major (16 contiguous floats)
-          const int slot = 2 * (p * G + cta) + (it == b ? 0 : 1);
+          const int slot = 2 * (P.slot_set * G + cta) + (it == b ? 0 : 1);
           float4 *dst = reinterpret_cast<float4 *>(a.ws + ((int64_t)slot * BM + f_local) * CHAIN_BN);
 #pragma unroll
           for (int c = 0; c < 4; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
@@ -520,7 +554,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
               for (int u = 0; u < 4; ++u) {
                 const int cc = c0 + u;
                 if (cc <= c_hi) {
-                  const int sl = 2 * (p * G + cc) +
+                  const int sl = 2 * (P.slot_set * G + cc) +
                                  ((cc == c_lo && sp.begin(cc) < (int64_t)t * P.kb) ? 1 : 0);
                   const float4 *src = reinterpret_cast<const float4 *>(
                       a.ws + ((int64_t)sl * BM + f_local) * CHAIN_BN);
@@ -665,14 +699,14 @@ __global__ void k_chain_prologue(const bf16 *__restrict__ E, const SeqMeta *__re
 
 int chain_smem() { return CH_SMEM; }
 
-cudaError_t chain(const ChainMaps &maps, const ChainArgs &a, cudaStream_t s) {
+cudaError_t chain(const ChainArgs &a, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaError_t e = launch_pdl(k_chain, dim3(num_sms()), dim3(CH_THREADS), CH_SMEM, s, maps, a);
+  cudaError_t e = launch_pdl(k_chain, dim3(num_sms()), dim3(CH_THREADS), CH_SMEM, s, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

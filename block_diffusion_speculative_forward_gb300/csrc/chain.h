@@ -18,15 +18,41 @@ enum ChainKind : int {
   CK_GU,       // gate/up: SwiGLU into u (bf16), tile-ready flags for the down phase
   CK_DOWN,     // down: residual x += y, per-tile sums of squares, residual tap
   CK_LM,       // lm_head: per (draft row, vocab tile) max / lowest argmax / sum exp
+  CK_ATTN,     // block attention (no weights): o rows per head, head-ready counts in flag
 };
 
-constexpr int CHAIN_MAX_PHASES = 6;
+// One attention item: sequence s, query head j, key tiles [t0, t1) of the
+// sequence (ctx tiles of 16 positions from the window start's page, then one
+// tile of block keys); its partial goes to slot `slot`; the pair (s, j) has
+// nc items in slots slot0 .. slot0 + nc - 1.
+struct ChainAttnItem {
+  int32_t s, j, t0, t1, slot, slot0, nc, pad;
+};
+
+// The attention phase of a launch (at most one, and first in its launch).
+struct ChainAttn {
+  Geo geo;
+  int layer;
+  float scale;               // 1 / sqrt(head_dim)
+  const SeqMeta *seq;
+  const int32_t *page_ids;
+  const int *count;          // device: items of the call
+  const ChainAttnItem *items;
+  const bf16 *q;             // [R, nq * d]
+  bf16 *o;                   // [R, nq * d]
+  float *ws;                 // item partials: [16 * d + 32] f32 each
+};
+
+constexpr int CHAIN_MAX_PHASES = 48;
 constexpr int CHAIN_BN = 16;        // activation rows of every phase (one MMA N)
 constexpr int CHAIN_BK = 64;        // reduction elements per stage
 constexpr int CHAIN_MAX_K_NORM = 2048;   // the widest normed input (hidden) the chain takes
 
 struct ChainPhase {
   int kind;
+  int map_w, map_b;      // tensor maps (indices into ChainArgs::maps) of the weight and the B operand
+  int slot_set;          // which of the three stream-K partial sets the phase uses
+  int attn_layer;        // CK_ATTN: the layer
   int n_w, k;            // weight rows (outputs), reduction length (multiple of 64)
   int rows;              // valid activation rows (<= 16)
   int tiles_m, kb;       // n_w / 128 rounded up, k / 64
@@ -46,6 +72,12 @@ struct ChainPhase {
   // dep < 0 none; dep_tile 0: every tile of phase dep finished; 1: k-block j
   // waits for tile j of phase dep
   int dep, dep_tile;
+  // with dep_tile: k-block j waits until flag[j / dep_div] of phase dep
+  // reaches dep_need (1 for a tile flag; the sequence count for a head)
+  int dep_div, dep_need;
+  // CK_ATTN: a second phase whose tiles must all be finished first (the
+  // fused ctx K/V of the same launch), or -1
+  int dep2;
   // the epilogue reads residual rows another phase of the launch wrote
   // (res_dep >= 0): it takes that phase's finished-tile count (all of them)
   // with acquire semantics before its first finished tile
@@ -73,14 +105,12 @@ struct ChainPhase {
 struct ChainArgs {
   int n_phases;
   ChainPhase ph[CHAIN_MAX_PHASES];
-  float *ws;             // stream-K partials: phase p uses slots [2 G p, 2 G (p + 1)) of 16 x 128 f32
+  ChainAttn attn;        // the CK_ATTN phases' work (their layer is per phase)
+  const CUtensorMap *maps;   // device table of the launch's tensor maps
+  int map_pool, map_kb, map_vb;   // attention: KV pool rows, block K and V
+  float *ws;             // stream-K partials: set s uses slots [2 G s, 2 G (s + 1)) of 16 x 128 f32
   int *status;
   int64_t fault_ns;      // test hook, as GemmParams::fault_ns
-};
-
-struct ChainMaps {
-  CUtensorMap w[CHAIN_MAX_PHASES];   // weights, box 128 rows x 64
-  CUtensorMap b[CHAIN_MAX_PHASES];   // bf16 activations (the B operands), box 16 rows x 64
 };
 
 namespace tc {
@@ -88,7 +118,7 @@ namespace tc {
 int chain_smem();
 // Launches one chain over every SM (one persistent CTA each). The phases run
 // in order; each CTA walks its stream-K range of every phase.
-cudaError_t chain(const ChainMaps &maps, const ChainArgs &a, cudaStream_t s);
+cudaError_t chain(const ChainArgs &a, cudaStream_t s);
 }  // namespace tc
 
 // The rows of a chained propose before its first chain: block embed (x,

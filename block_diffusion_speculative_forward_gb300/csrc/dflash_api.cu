@@ -98,6 +98,8 @@ struct dflash_handle {
   int cap_seq = 0, cap_pages = 0, cap_items = 0, cap_pairs = 0;
   size_t off_seq = 0, off_pages = 0, off_items = 0, off_pairs = 0, off_sched = 0, off_rows = 0;
   int cap_sched = 0;
+  int cap_citems = 0;
+  size_t off_citems = 0;
   bool chain_ok = false;    // the head can take the chained few-row path
   int last_chained = 0;     // the last propose took it
   // captured propose graphs, keyed by the call's launch shape
@@ -304,10 +306,11 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
                 cudaStream_t s, dfl::CallMeta *out,
                 const std::vector<dfl::AttnItem> &items = {},
                 const std::vector<dfl::AttnPair> &pairs = {},
-                const std::vector<int32_t> &cta_off = {}, size_t *defer_bytes = nullptr) {
+                const std::vector<int32_t> &cta_off = {}, size_t *defer_bytes = nullptr,
+                const std::vector<dfl::ChainAttnItem> &citems = {}) {
   if ((int)seq.size() > h->cap_seq || (int)page_ids.size() > h->cap_pages ||
       (int)items.size() > h->cap_items || (int)pairs.size() > h->cap_pairs ||
-      (int)cta_off.size() > h->cap_sched)
+      (int)cta_off.size() > h->cap_sched || (int)citems.size() > h->cap_citems)
     return fail(DFLASH_EINVAL, "internal: call metadata beyond the handle's capacity");
   size_t total = h->off_rows + rows.size() * sizeof(dfl::RowMeta) + 16;
   if (h->meta_ev_live) {
@@ -340,6 +343,9 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
   int32_t *counts = (int32_t *)h->meta_host;
   counts[0] = (int32_t)items.size();
   counts[1] = (int32_t)pairs.size();
+  counts[2] = (int32_t)citems.size();
+  if (!citems.empty())
+    memcpy(h->meta_host + h->off_citems, citems.data(), citems.size() * sizeof(dfl::ChainAttnItem));
   if (!seq.empty()) memcpy(h->meta_host + h->off_seq, seq.data(), seq.size() * sizeof(dfl::SeqMeta));
   if (!page_ids.empty())
     memcpy(h->meta_host + h->off_pages, page_ids.data(), page_ids.size() * sizeof(int32_t));
@@ -365,6 +371,7 @@ int upload_meta(dflash_handle *h, const std::vector<dfl::SeqMeta> &seq,
   out->items = (const dfl::AttnItem *)(h->meta_dev + h->off_items);
   out->pairs = (const dfl::AttnPair *)(h->meta_dev + h->off_pairs);
   out->cta_off = (const int32_t *)(h->meta_dev + h->off_sched);
+  out->citems = (const dfl::ChainAttnItem *)(h->meta_dev + h->off_citems);
   out->n_seq = (int)seq.size();
   out->n_rows = (int)rows.size();
   out->n_items = (int)items.size();
@@ -460,11 +467,17 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_ha
     return rc;
   }
   h->chain_ok = h->b.use_chain;
+  // the chained launch is opt-in: at the shipped drafter geometry it ran
+  // slower than the kernel-per-step path (its cross-CTA hand-offs between
+  // phases are L2 round trips taken while every other SM streams weights)
+  h->b.use_chain = false;
   h->cap_items = h->b.attn_slots + h->cap_pairs;
   h->off_pairs = (h->off_items + sizeof(dfl::AttnItem) * h->cap_items + 15) & ~(size_t)15;
   h->cap_sched = h->b.attn_grid_tc + 1;
   h->off_sched = (h->off_pairs + sizeof(dfl::AttnPair) * h->cap_pairs + 15) & ~(size_t)15;
-  h->off_rows = (h->off_sched + sizeof(int32_t) * h->cap_sched + 15) & ~(size_t)15;
+  h->cap_citems = dfl::chain_attn_capacity(h->g);
+  h->off_citems = (h->off_sched + sizeof(int32_t) * h->cap_sched + 15) & ~(size_t)15;
+  h->off_rows = (h->off_citems + sizeof(dfl::ChainAttnItem) * h->cap_citems + 15) & ~(size_t)15;
   *out = h;
   return DFLASH_OK;
 }
@@ -1053,15 +1066,26 @@ int propose_impl(dflash_handle *h, int n, dflash_state *const *states,
   std::vector<AttnItem> items;
   std::vector<AttnPair> pairs;
   std::vector<int32_t> cta_off;
-  if (!build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs, &cta_off)) {
+  thread_local std::vector<ChainAttnItem> citems;
+  citems.clear();
+  const bool chained = chain_applies(h->g, h->b, (int)rows.size(), n * h->g.gamma);
+  if (chained) {
+    // the chained path runs the attention inside its launches
+    build_chain_attn_items(h->g, seq, tc::num_sms(), &citems);
+    if ((int)citems.size() > h->cap_citems) {
+      rollback(h, snap);
+      return fail(DFLASH_EINVAL, "internal: chained attention items beyond the capacity");
+    }
+  } else if (!build_attn_work(h->g, seq, h->b.attn_slots, h->b.attn_grid_tc, &items, &pairs,
+                              &cta_off)) {
     rollback(h, snap);
     return fail(DFLASH_EINVAL, "internal: attention work beyond the slot capacity");
   }
   CallMeta cm;
   size_t meta_bytes = 0;
-  int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off, &meta_bytes);
+  int rc = upload_meta(h, seq, rows, page_ids, s, &cm, items, pairs, cta_off, &meta_bytes, citems);
   if (rc == DFLASH_OK) rc = run_forward(h, cm, num_drafts, bitmask, meta_bytes, s);
-  h->last_chained = chain_applies(h->g, h->b, cm.n_rows, n * h->g.gamma) ? 1 : 0;
+  h->last_chained = chained ? 1 : 0;
   if (rc == DFLASH_OK) {
     // Results are on the host after one synchronisation.
     cudaError_t e = cudaStreamSynchronize(s);

@@ -227,7 +227,14 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     B->chain_sync_ints = chain_sync_capacity(g);
     BA(B->chain_sync, (size_t)B->chain_sync_ints);
     BA(B->hn, (size_t)2 * CHAIN_BN * H);
-    if (!tc::make_map_2d(&B->map_hn[0], B->hn, false, CHAIN_BN, H, CHAIN_BN) ||
+    BA(B->ca_ws, (size_t)chain_attn_capacity(g) * (16 * g.d + 32));
+    B->ca_pool_ok = W->pool != nullptr;
+    if ((B->ca_pool_ok &&
+         !tc::make_map_2d(&B->ca_pool, W->pool, false, (int64_t)g.pages * g.L * 2 * g.nkv * g.B,
+                          g.d, 16)) ||
+        !tc::make_map_2d(&B->ca_kb, B->kb, false, R_max, kv, 16) ||
+        !tc::make_map_2d(&B->ca_vb, B->vb, false, R_max, kv, 16) ||
+        !tc::make_map_2d(&B->map_hn[0], B->hn, false, CHAIN_BN, H, CHAIN_BN) ||
         !tc::make_map_2d(&B->map_hn[1], B->hn + (size_t)CHAIN_BN * H, false, CHAIN_BN, H, CHAIN_BN)) {
       g_build_err = "cuTensorMapEncodeTiled failed for a normed activation";
       return DFLASH_ECUDA;
@@ -268,6 +275,32 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
           g_build_err = "cuTensorMapEncodeTiled failed for an activation operand";
           return DFLASH_ECUDA;
         }
+  }
+  // the chained path's tensor maps, in device memory (its launch parameters
+  // hold only their rows)
+  {
+    std::vector<CUtensorMap> t(mt_count(g.L));
+    memset(t.data(), 0, sizeof(CUtensorMap) * t.size());
+    if (B->ca_pool_ok) t[MT_POOL] = B->ca_pool;
+    t[MT_KB] = B->ca_kb;
+    t[MT_VB] = B->ca_vb;
+    t[MT_FC] = W->map_fc;
+    t[MT_WKV] = W->map_wkv;
+    t[MT_LM] = W->map_lm;
+    t[MT_PACK] = B->act_map[ACT_PACK][bn_index(16)];
+    t[MT_CTXC] = B->act_map[ACT_C][bn_index(16)];
+    t[MT_HN_MID] = B->map_hn[0];
+    t[MT_HN_IN] = B->map_hn[1];
+    t[MT_O16] = B->act_map[ACT_O][bn_index(16)];
+    t[MT_U16] = B->act_map[ACT_U][bn_index(16)];
+    for (int l = 0; l < g.L; ++l) {
+      t[mt_layer(l, 0)] = W->map_qkv[l];
+      t[mt_layer(l, 1)] = W->map_o[l];
+      t[mt_layer(l, 2)] = W->map_gu[l];
+      t[mt_layer(l, 3)] = W->map_down[l];
+    }
+    BA(B->map_table, t.size());
+    BK(cudaMemcpy(B->map_table, t.data(), sizeof(CUtensorMap) * t.size(), cudaMemcpyHostToDevice));
   }
   const int nb = c.max_batch;
   B->off_drafts = 16;
@@ -384,22 +417,49 @@ int chain_sync_capacity(const Geo &g) {
   // normed operand's k-block count and flags (+ padding); see forward_chain
   auto ph = [](int tiles, int k) { return 2 * tiles + 4 + (k / CHAIN_BK + 3) / 4 * 4; };
   const int first = ph(t(g.H), g.S) + ph(t((int64_t)g.L * 2 * g.kv), g.H) + ph(t(g.qkv_w), g.H);
-  const int layer = ph(t(g.H), g.nq * g.d) + ph(t(2 * (int64_t)g.I), g.H) + ph(t(g.H), g.I) +
-                    std::max(ph(t(g.qkv_w), g.H), ph(t(g.V), g.H));
+  // the attention phase counts (sequence, head) pairs: at most 16 sequences
+  const int layer = ph(16 * g.nq, 0) + ph(t(g.H), g.nq * g.d) + ph(t(2 * (int64_t)g.I), g.H) +
+                    ph(t(g.H), g.I) + std::max(ph(t(g.qkv_w), g.H), ph(t(g.V), g.H));
   return first + g.L * layer + 64;
 }
 
 bool chain_applies(const Geo &g, const Buffers &B, int n_rows, int R) {
-  return B.use_chain && R <= CHAIN_BN && n_rows <= CHAIN_BN && g.H <= CHAIN_MAX_K_NORM &&
-         g.H % 128 == 0 && g.S % CHAIN_BK == 0 && g.I % CHAIN_BK == 0 && B.chain_sync;
+  // bf16 cache in pages of 16 for the in-launch attention; every phase of
+  // the forward in one launch
+  return B.use_chain && 3 + 5 * g.L <= CHAIN_MAX_PHASES && R <= CHAIN_BN && n_rows <= CHAIN_BN && g.H <= CHAIN_MAX_K_NORM &&
+         g.H % 128 == 0 && g.S % CHAIN_BK == 0 && g.I % CHAIN_BK == 0 && B.chain_sync &&
+         !g.kv_fp8 && g.B == 16 && (g.d == 64 || g.d == 128) && g.gamma <= CHAIN_BN;
+}
+
+int chain_attn_capacity(const Geo &g) { return tc::num_sms() + (CHAIN_BN / 2) * g.nq + 16; }
+
+void build_chain_attn_items(const Geo &g, const std::vector<SeqMeta> &seq, int ctas,
+                            std::vector<ChainAttnItem> *items) {
+  items->clear();
+  const int pairs = (int)seq.size() * g.nq;
+  const int nc_target = std::max(1, ctas / std::max(1, pairs));
+  for (int s = 0; s < (int)seq.size(); ++s) {
+    const int n_ctx = seq[s].pos - seq[s].ws;
+    const int p0 = seq[s].ws & ~15;
+    const int T = (n_ctx > 0 ? (seq[s].pos - p0 + 15) / 16 : 0) + 1;   // + the block tile
+    int nc = std::min(nc_target, T);
+    const int chunk = (T + nc - 1) / nc;
+    nc = (T + chunk - 1) / chunk;
+    for (int j = 0; j < g.nq; ++j) {
+      const int slot0 = (int)items->size();
+      for (int c = 0; c < nc; ++c)
+        items->push_back({s, j, c * chunk, std::min(T, (c + 1) * chunk), slot0 + c, slot0, nc, 0});
+    }
+  }
 }
 
 namespace {
 
-// The chained propose of few rows (see chain.cu): prologue, one launch for
-// the new ctx rows and layer 0's QKV, then per layer the attention and one
-// launch for o_proj, gate/up, down and the next QKV (or the lm_head), then
-// the row merge of the lm_head partials and the chain of drafts.
+// The chained propose of few rows (see chain.cu): the prologue (block embed,
+// pack of the new ctx rows), then one persistent launch whose phases are the
+// new ctx rows (fc, fused K/V), layer 0's QKV, and per layer the attention,
+// o_proj, gate/up, down and the next QKV (or the lm_head); then the row merge
+// of the lm_head partials and the chain of drafts.
 int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const Buffers &B,
                   const CallMeta &cm, int nd, const int32_t *bitmask, cudaStream_t s) {
   if (B.step_begin && B.step_end) FK(cudaEventRecordWithFlags(B.step_begin, s, cudaEventRecordExternal));
@@ -409,15 +469,27 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
   LK(chain_prologue(W.embed, cm.seq, R, g, c.mask_token_id, B.x, B.ss_in, B.tap_x, cm.rows, m,
                     B.ctx_pack, B.status, s));
   int *sync = B.chain_sync;
-  auto phase = [&](int kind, int n_w, int k, int rows) {
-    ChainPhase P{};
+  ChainArgs a{};
+  int np = 0, weight_phases = 0;
+  // appends a phase: its counters from the sync area, its tensor maps, and
+  // (weight phases) the next of three stream-K partial sets in turn, so a set
+  // is reused only by a phase that depends on the set's previous user
+  auto add = [&](int kind, int n_w, int k, int rows, int map_w, int map_b) -> ChainPhase & {
+    ChainPhase &P = a.ph[np++];
+    P = ChainPhase{};
     P.kind = kind;
     P.n_w = n_w;
     P.k = k;
     P.rows = rows;
-    P.tiles_m = (n_w + 127) / 128;
+    // the attention phase has no weights; its "tiles" are the (sequence,
+    // head) pairs, whose count `done` reaches when every pair is merged
+    P.tiles_m = kind == CK_ATTN ? n * g.nq : (n_w + 127) / 128;
     P.kb = k / CHAIN_BK;
+    P.map_w = map_w;
+    P.map_b = map_b;
+    P.slot_set = kind == CK_ATTN ? 0 : weight_phases++ % 3;
     P.dep = -1;
+    P.dep2 = -1;
     P.res_dep = -1;
     P.arrive = sync;
     P.flag = sync + P.tiles_m;
@@ -445,8 +517,8 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
     P.hbuf = h;
   };
   bf16 *const hn_mid = B.hn, *const hn_in = B.hn + (size_t)CHAIN_BN * g.H;
-  auto qkv_phase = [&](int l) {
-    ChainPhase P = phase(CK_QKV, g.qkv_w, g.H, R);
+  auto add_qkv = [&](int l) -> int {
+    ChainPhase &P = add(CK_QKV, g.qkv_w, g.H, R, mt_layer(l, 0), MT_HN_IN);
     normed(P, B.x, B.ss_in, W.layers[l].in_norm, hn_in);
     P.ep.seq = cm.seq;
     P.ep.gamma = g.gamma;
@@ -458,142 +530,94 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
     P.ep.q_out = B.q;
     P.ep.k_out = B.kb;
     P.ep.v_out = B.vb;
-    return P;
+    return np - 1;
   };
-  const CUtensorMap empty_map{};
-  auto launch = [&](ChainPhase *ph, const CUtensorMap *const *wm, const CUtensorMap *const *bm,
-                    int np) -> int {
-    ChainArgs a{};
-    ChainMaps maps;
-    a.n_phases = np;
-    for (int i = 0; i < np; ++i) {
-      a.ph[i] = ph[i];
-      maps.w[i] = *wm[i];
-      maps.b[i] = *bm[i];
-    }
-    for (int i = np; i < CHAIN_MAX_PHASES; ++i) {
-      maps.w[i] = empty_map;
-      maps.b[i] = empty_map;
-    }
-    a.ws = B.ws;
-    a.status = B.status;
-    a.fault_ns = B.fault_ns;
-    LK(tc::chain(maps, a, s));
-    return DFLASH_OK;
-  };
-  const CUtensorMap *act16_o = &B.act_map[ACT_O][bn_index(16)];
-  const CUtensorMap *act16_u = &B.act_map[ACT_U][bn_index(16)];
-  const CUtensorMap *act16_pack = &B.act_map[ACT_PACK][bn_index(16)];
-  {
-    // new ctx rows (fc, hidden_norm, fused K/V with the paged write) and layer 0's QKV
-    ChainPhase ph[3];
-    const CUtensorMap *wm[3], *bm[3];
-    int np = 0;
-    if (m > 0) {
-      ChainPhase fc = phase(CK_FC, g.H, g.S, m);
-      fc.out = B.ctx_fc;
-      fc.out_ss = B.ss_c;
-      ph[np] = fc;
-      wm[np] = &W.map_fc;
-      bm[np++] = act16_pack;
-      ChainPhase kv = phase(CK_KV, g.L * 2 * g.kv, g.H, m);
-      normed(kv, B.ctx_fc, B.ss_c, W.hidden_norm, B.ctx_c);
-      kv.dep = 0;
-      kv.ctx_rows = cm.rows;
-      kv.k_norm = W.k_norm_dev;
-      kv.pool = W.pool;
-      kv.kv_scale = W.kv_scale;
-      ph[np] = kv;
-      wm[np] = &W.map_wkv;
-      bm[np++] = &B.act_map[ACT_C][bn_index(16)];
-    }
-    ph[np] = qkv_phase(0);
-    wm[np] = &W.map_qkv[0];
-    bm[np++] = &B.map_hn[1];
-    int rc = launch(ph, wm, bm, np);
-    if (rc) return rc;
+  // new ctx rows: fc, hidden_norm, fused K/V with the paged write
+  int kv_phase = -1;
+  if (m > 0) {
+    ChainPhase &fc = add(CK_FC, g.H, g.S, m, MT_FC, MT_PACK);
+    fc.out = B.ctx_fc;
+    fc.out_ss = B.ss_c;
+    const int fc_i = np - 1;
+    ChainPhase &kv = add(CK_KV, g.L * 2 * g.kv, g.H, m, MT_WKV, MT_CTXC);
+    normed(kv, B.ctx_fc, B.ss_c, W.hidden_norm, B.ctx_c);
+    kv.dep = fc_i;
+    kv.ctx_rows = cm.rows;
+    kv.k_norm = W.k_norm_dev;
+    kv.pool = W.pool;
+    kv.kv_scale = W.kv_scale;
+    kv_phase = np - 1;
   }
+  int qkv_i = add_qkv(0);
   for (int l = 0; l < g.L; ++l) {
     const LayerW &L = W.layers[l];
-    {
-      AttnArgs a{};
-      a.g = g;
-      a.q = B.q;
-      a.kb = B.kb;
-      a.vb = B.vb;
-      a.o = B.o;
-      a.seq = cm.seq;
-      a.page_ids = cm.page_ids;
-      a.pool = W.pool;
-      a.kv_scale = W.kv_scale;
-      a.layer = l;
-      a.scale = (float)(1.0 / std::sqrt((double)g.d));
-      a.items = cm.items;
-      a.n_items = cm.cap_items;
-      a.pairs = cm.pairs;
-      a.n_pairs = cm.cap_pairs;
-      a.counts = cm.counts;
-      a.ws = B.attn_ws;
-      a.slot_floats = B.attn_slot_floats;
-      a.status = B.status;
-      a.cta_off = cm.cta_off;
-      a.grid_tc = B.attn_grid_tc;
-      if (B.attn_maps.ok) {
-        LK(attention_tc(a, B.attn_maps, s));
-        LK(attention_merge(a, s));
-      } else {
-        LK(attention_split(a, s));
-      }
-      if (cm.cap_pairs) count_launches(1);
-    }
-    ChainPhase ph[4];
-    const CUtensorMap *wm[4], *bm[4];
-    ph[0] = phase(CK_O, g.H, qd, R);
-    ph[0].out = B.x;
-    ph[0].out_ss = B.ss_mid;
-    wm[0] = &W.map_o[l];
-    bm[0] = act16_o;
-    ph[1] = phase(CK_GU, 2 * g.I, g.H, R);
-    normed(ph[1], B.x, B.ss_mid, L.post_norm, hn_mid);
-    ph[1].dep = 0;
-    ph[1].ep.u_out = B.u;
-    wm[1] = &W.map_gu[l];
-    bm[1] = &B.map_hn[0];
-    ph[2] = phase(CK_DOWN, g.H, g.I, R);
-    ph[2].dep = 1;
-    ph[2].dep_tile = 1;
-    ph[2].res_dep = 0;
-    ph[2].out = B.x;
-    ph[2].out_ss = B.ss_in;
-    ph[2].x_tap = B.tap_x ? B.tap_x + (size_t)(l + 1) * R * g.H : nullptr;
-    wm[2] = &W.map_down[l];
-    bm[2] = act16_u;
+    // attention of layer l once its QKV (and the new ctx rows' K/V) are in
+    ChainPhase &at = add(CK_ATTN, 0, 0, R, MT_EMPTY, MT_EMPTY);
+    at.dep = qkv_i;
+    at.dep2 = l == 0 ? kv_phase : -1;
+    at.attn_layer = l;
+    const int at_i = np - 1;
+    ChainPhase &o = add(CK_O, g.H, qd, R, mt_layer(l, 1), MT_O16);
+    o.dep = at_i;
+    o.dep_tile = 1;
+    o.dep_div = g.d / CHAIN_BK;   // k-block j reads head j * 64 / d
+    o.dep_need = n;               // every sequence's rows of that head
+    o.out = B.x;
+    o.out_ss = B.ss_mid;
+    const int o_i = np - 1;
+    ChainPhase &gu = add(CK_GU, 2 * g.I, g.H, R, mt_layer(l, 2), MT_HN_MID);
+    normed(gu, B.x, B.ss_mid, L.post_norm, hn_mid);
+    gu.dep = o_i;
+    gu.ep.u_out = B.u;
+    const int gu_i = np - 1;
+    ChainPhase &dn = add(CK_DOWN, g.H, g.I, R, mt_layer(l, 3), MT_U16);
+    dn.dep = gu_i;
+    dn.dep_tile = 1;
+    dn.dep_div = 1;
+    dn.dep_need = 1;
+    dn.res_dep = o_i;
+    dn.out = B.x;
+    dn.out_ss = B.ss_in;
+    dn.x_tap = B.tap_x ? B.tap_x + (size_t)(l + 1) * R * g.H : nullptr;
+    const int dn_i = np - 1;
     if (l + 1 < g.L) {
-      ph[3] = qkv_phase(l + 1);
-      wm[3] = &W.map_qkv[l + 1];
+      qkv_i = add_qkv(l + 1);
+      a.ph[qkv_i].dep = dn_i;
     } else {
-      ph[3] = phase(CK_LM, g.V, g.H, R);
-      normed(ph[3], B.x, B.ss_in, W.norm, hn_in);
-      ph[3].ep.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
-      ph[3].ep.bitmask = bitmask;
-      ph[3].ep.mask_words = (g.V + 31) / 32;
-      ph[3].ep.nd = nd;
-      ph[3].ep.lm_gamma = g.gamma;
-      ph[3].ep.lm_first = 1;
-      ph[3].ep.lm_part = B.lm_part;
-      ph[3].z_rows = B.z;
-      ph[3].z_tap = B.tap_z;
-      wm[3] = &W.map_lm;
-      if (B.probe_begin && B.probe_end)
-        FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));
+      ChainPhase &lm = add(CK_LM, g.V, g.H, R, MT_LM, MT_HN_IN);
+      normed(lm, B.x, B.ss_in, W.norm, hn_in);
+      lm.dep = dn_i;
+      lm.ep.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+      lm.ep.bitmask = bitmask;
+      lm.ep.mask_words = (g.V + 31) / 32;
+      lm.ep.nd = nd;
+      lm.ep.lm_gamma = g.gamma;
+      lm.ep.lm_first = 1;
+      lm.ep.lm_part = B.lm_part;
+      lm.z_rows = B.z;
+      lm.z_tap = B.tap_z;
     }
-    ph[3].dep = 2;
-    bm[3] = &B.map_hn[1];
-    int rc = launch(ph, wm, bm, 4);
-    if (rc) return rc;
   }
+  a.n_phases = np;
+  a.attn.geo = g;
+  a.attn.scale = (float)(1.0 / std::sqrt((double)g.d));
+  a.attn.seq = cm.seq;
+  a.attn.page_ids = cm.page_ids;
+  a.attn.count = cm.counts + 2;
+  a.attn.items = cm.citems;
+  a.attn.q = B.q;
+  a.attn.o = B.o;
+  a.attn.ws = B.ca_ws;
+  a.maps = B.map_table;
+  a.map_pool = MT_POOL;
+  a.map_kb = MT_POOL + 1;
+  a.map_vb = MT_POOL + 2;
+  a.ws = B.ws;
+  a.status = B.status;
+  a.fault_ns = B.fault_ns;
+  LK(tc::chain(a, s));
   LK(lm_reduce(B.lm_part, D, (g.V + 127) / 128, B.row_id, B.row_p1, s));
-  if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_end, s, cudaEventRecordExternal));
+  // (the lm_head runs inside the single launch: no separate lm_head probe here)
   if (B.tap_logits) {
     GemmParams p{};
     p.m_act = D;

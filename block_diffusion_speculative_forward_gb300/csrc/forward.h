@@ -5,6 +5,7 @@
 #include <vector>
 
 #include "attention.h"
+#include "chain.h"
 #include "dflash.h"
 #include "gemm_tc.h"
 #include "internal.h"
@@ -74,6 +75,10 @@ struct Buffers {
   int *chain_sync = nullptr;    // per launch and phase: arrival counters, tile flags, tile count
   bf16 *hn = nullptr;           // [2][16][H] normed residual rows (gate/up input; QKV or lm_head input)
   CUtensorMap map_hn[2];        // their B-operand maps, box 16 rows x 64
+  float *ca_ws = nullptr;       // chained attention partials: [16 * d + 32] f32 per item
+  CUtensorMap *map_table = nullptr;   // device: the chained path's tensor maps (MT_* rows)
+  CUtensorMap ca_pool, ca_kb, ca_vb;   // chained attention operands, box 16 rows x 64
+  bool ca_pool_ok = false;
   int chain_sync_ints = 0;
   bool use_chain = true;        // few-row proposes take the chained path when it applies
   int last_chained = 0;         // the last forward took the chained path
@@ -101,10 +106,30 @@ struct CallMeta {
   const AttnItem *items = nullptr;
   const AttnPair *pairs = nullptr;
   const int32_t *cta_off = nullptr;   // tensor-core attention schedule (grid_tc + 1)
-  const int *counts = nullptr;   // device: items, pairs
+  const int *counts = nullptr;   // device: items, pairs, chained attention items
+  const ChainAttnItem *citems = nullptr;   // chained path: attention items of the call
   int n_seq = 0, n_rows = 0, n_items = 0, n_pairs = 0;
   int cap_items = 0, cap_pairs = 0;
 };
+
+// The attention work of a chained call: per (sequence, query head), its key
+// tiles (the window's ctx pages, then one tile of block keys) cut into at
+// most `ctas` / pairs chunks. Items are listed pair by pair.
+void build_chain_attn_items(const Geo &g, const std::vector<SeqMeta> &seq, int ctas,
+                            std::vector<ChainAttnItem> *items);
+// Item capacity of a head's chained calls.
+int chain_attn_capacity(const Geo &g);
+
+// Rows of the device table of a head's chained-path tensor maps: fixed
+// operands, then per layer l its QKV, o_proj, gate/up and down weights.
+enum : int {
+  MT_EMPTY = 0, MT_POOL = 1, MT_KB = 2, MT_VB = 3,   // pool, kb, vb consecutive (attention)
+  MT_FC = 4, MT_WKV = 5, MT_LM = 6,
+  MT_PACK = 7, MT_CTXC = 8, MT_HN_MID = 9, MT_HN_IN = 10, MT_O16 = 11, MT_U16 = 12,
+  MT_LAYERS = 13
+};
+inline int mt_layer(int l, int which) { return MT_LAYERS + 4 * l + which; }
+inline int mt_count(int L) { return MT_LAYERS + 4 * L; }
 
 // Ints of chained-propose counters a head needs (every launch of one forward).
 int chain_sync_capacity(const Geo &g);

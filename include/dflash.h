@@ -280,10 +280,12 @@ DFLASH_API int dflash_debug_set_step_probe(dflash_handle *h, void *ev_begin, voi
  * new ctx rows, drafts, bitmask and tap/probe pointers); enable = 0 launches
  * the kernels one by one instead (same results). On by default. */
 DFLASH_API int dflash_debug_set_graphs(dflash_handle *h, int32_t enable);
-/* Few-row proposes (at most 16 block rows and 16 new ctx rows, hidden at
- * most 2048) run as a chained sequence of persistent launches by default;
- * enable = 0 makes them take the kernel-per-step path that many-row proposes
- * take (same results within rounding). Errors: EINVAL. */
+/* enable = 1 makes few-row proposes (one sequence of 16 block rows, at most
+ * 16 new ctx rows, hidden at most 2048, bf16 KV) run as one persistent
+ * launch that walks every layer's phases with cross-CTA dependency counters;
+ * enable = 0 (the default) keeps them on the kernel-per-step path that every
+ * other propose takes (same results within rounding). A shape the chained
+ * launch does not take stays on the kernel-per-step path. Errors: EINVAL. */
 DFLASH_API int dflash_debug_set_chain(dflash_handle *h, int32_t enable);
 /* 1 when the last propose* call took the chained few-row path, else 0. */
 DFLASH_API int dflash_debug_last_path(const dflash_handle *h);

@@ -65,15 +65,18 @@ def _check_lm_stage(head, ora, tz, tl, seq_rows, n, nd, masks, gamma, got):
     _spread(seen)
 
 
+@pytest.mark.parametrize("chained", [False, True])
 @pytest.mark.parametrize("masked", [False, True])
-def test_sharp_confidence_batch1(masked):
+def test_sharp_confidence_batch1(masked, chained):
     """One sequence at the shipped geometry: the stream-K GEMM with the fused
-    lm_head epilogue over 128-row vocab tiles, then the row merge."""
+    lm_head epilogue over 128-row vocab tiles, then the row merge; on the
+    kernel-per-step path and inside the chained single launch."""
     geom, seed, nd = syn.FULL, 1102, 15
     cfg = cfg_for(geom, max_batch=1, max_seq_len=256)
     w = _sharp_weights(geom, seed)
     ora = oracle.DraftHeadOracle(cfg, w)
     head = B.DraftHead(cfg, B.weights_to_device(w))
+    head.set_chain(chained)
     g = geom.gamma
     tz = torch.zeros((g, geom.hidden), dtype=torch.bfloat16, device="cuda")
     tl = torch.zeros((nd, geom.vocab), device="cuda")
@@ -84,6 +87,7 @@ def test_sharp_confidence_batch1(masked):
     got = head.propose(st, 4242, 41, syn.make_stack(geom, 1, seed, idx=1).cuda(), nd,
                        bitmask=None if masks is None else masks[0].cuda())
     torch.cuda.synchronize()
+    assert head.last_path_chained() == chained
     _check_lm_stage(head, ora, tz, tl, [0], 1, nd, masks, g, [got])
     head.close()
 

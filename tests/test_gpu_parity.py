@@ -213,9 +213,10 @@ def test_full_geometry_single_sequence():
 
 @pytest.mark.parametrize("chained", [True, False])
 def test_few_row_paths_match_oracle(chained):
-    """Few-row proposes run chained (persistent multi-phase launches) by
-    default; the kernel-per-step path serves them too when the chain is
-    switched off. Both against the oracle, over rounds with new rows."""
+    """Few-row proposes take the kernel-per-step path by default and the
+    chained single launch (every layer's phases in one persistent launch)
+    when it is switched on. Both against the oracle, over rounds with new
+    rows."""
     pair = Pair(syn.TINY, 1051)
     pair.lib.set_chain(chained)
     so, sl, _ = _prefill(pair, 45, 1051)
