@@ -247,7 +247,8 @@ class DraftHeadOracle:
     cfg keys: num_layers hidden intermediate num_q_heads num_kv_heads head_dim
     vocab gamma mask_token_id n_target_layers target_hidden rms_eps ctx_window
     kv_block prefill_chunk max_batch max_seq_len kv_pool_blocks kv_dtype
-    (0 bf16, 1 fp8) lm_head_dtype (0 bf16, 1 fp8, 2 nvfp4)."""
+    (0 bf16, 1 fp8) lm_head_dtype (0 bf16, 1 fp8, 2 nvfp4) shifted_rows (0/1,
+    optional)."""
 
     def __init__(self, cfg: dict, w: dict):
         self.cfg = dict(cfg)
@@ -287,6 +288,12 @@ class DraftHeadOracle:
         if self.lm_nvfp4:
             self.lm_nv = (w["lm_head_nvfp4"], w["lm_head_nvfp4_scale"],
                           float(w["lm_head_nvfp4_global"]))
+        # [P1]/[P2] field shifted_rows (the DSpark convention): block row j's
+        # logits give the token at position p + j + 1, so the draft vector is
+        # the full-row argmax vector rotated right by one; the verify indexing
+        # then reads drafts 1..nd from block rows 0..nd-1. Otherwise row i
+        # gives draft i (rows 1..nd).
+        self.draft0 = 0 if c.get("shifted_rows", 0) else 1
         self._lm = None
         self.pool = PagePool(self.n_pool_pages())
         self.states: list[SeqState] = []
@@ -434,7 +441,8 @@ class DraftHeadOracle:
         gamma-1 mask rows), embed_tokens_shared (shared embed table), layers
         (Qwen3-style layer stack), norm (final RMSNorm), lm_head_shared (argmax
         over the block's logits). reading: rows 1..num_drafts give drafts
-        1..num_drafts; queries see the windowed ctx and every block key."""
+        1..num_drafts (rows 0..num_drafts-1 with shifted_rows); queries see the
+        windowed ctx and every block key."""
         g = self.gamma
         toks = [last_token] + [self.cfg["mask_token_id"]] * (g - 1)
         x = self.embed[torch.tensor(toks)].to(F64)                # [g, H]
@@ -483,9 +491,10 @@ class DraftHeadOracle:
         return x + u @ lay["down"].T
 
     def draft_logits(self, z: torch.Tensor, num_drafts: int) -> torch.Tensor:
-        """lm_head logits of block rows 1..num_drafts of the final-normed z
-        ([P1] field lm_head_shared; FP8 mirror: scale_v * <z, codes_v>)."""
-        logits = z[1:1 + num_drafts] @ self.lm_head().T
+        """lm_head logits of the draft rows of the final-normed z: block rows
+        1..num_drafts, or 0..num_drafts-1 with shifted_rows ([P1] field
+        lm_head_shared; FP8 mirror: scale_v * <z, codes_v>)."""
+        logits = z[self.draft0:self.draft0 + num_drafts] @ self.lm_head().T
         if self.lm_fp8:
             logits = logits * self.lm_scale[None, :]
         return logits
@@ -587,6 +596,64 @@ class DraftHeadOracle:
         for b in sorted(b for b in st.pages if (b + 1) * self.B <= ws):
             self.pool.give(st.pages.pop(b))
         self._drop_retired_rows(st, ws)
+
+    def catchup_batch(self, states, rows, first_pos, tokens=None) -> int:
+        """[P2]/[P3] catchup_batch (catchup_drafter for one state): append,
+        for each state, the ctx rows of target hiddens paired with tokens
+        accepted by the last verify, at explicit RoPE positions first_pos[i],
+        first_pos[i] + 1, ... Returns the rows appended (their sum).
+
+        reading: this head keeps one ctx row per target position (the row
+        space is positions, never compacted), so a state's append slot and
+        the RoPE position of its next row coincide: first_pos[i] must equal
+        the state's ctx_len. The rows are the ones the next propose would
+        otherwise bring as new rows (the last verified token's and those of
+        the accepted drafts), so after after_verify(k) at most k + 1 rows fit
+        before the expected position. The ctx rows depend on the hiddens
+        alone; tokens (when given) are only range-checked. Pages: all states
+        retire first, then take pages, in state order; a batch that cannot
+        get its pages changes nothing."""
+        n = len(states)
+        if len(rows) != n or len(first_pos) != n or (tokens is not None and len(tokens) != n):
+            raise OracleError("EINVAL", "array lengths differ")
+        if len(set(map(id, states))) != n:
+            raise OracleError("EINVAL", "duplicate state")
+        counts = []
+        for i, st in enumerate(states):
+            m = 0 if rows[i] is None else rows[i].shape[0]
+            if st not in self.states:
+                raise OracleError("EINVAL", "unknown state")
+            if st.pending is not None:
+                raise OracleError("ESTATE", "catch-up before after_verify")
+            if tokens is not None and (len(tokens[i]) != m or
+                                       any(not (0 <= t < self.V) for t in tokens[i])):
+                raise OracleError("EINVAL", "tokens do not pair with the rows")
+            if first_pos[i] != st.ctx_len:
+                raise OracleError("EPOSITION", "first position != the state's append point")
+            if st.expected_next is not None and st.ctx_len + m > st.expected_next:
+                raise OracleError("EPOSITION", "rows past the position after_verify set")
+            if st.ctx_len + m > st.cap:
+                raise OracleError("EINVAL", "ctx beyond state capacity")
+            counts.append(m)
+        plans = [self._plan_append(st, m) for st, m in zip(states, counts)]
+        need = sum(len(pl[3]) for pl in plans)
+        retire = sum(len(pl[2]) for pl in plans)
+        if need > self.pool.n_free() + retire:
+            raise OracleError("ENOMEM", "KV pool exhausted")
+        for st, pl in zip(states, plans):
+            for b in pl[2]:
+                self.pool.give(st.pages.pop(b))
+        for st, pl in zip(states, plans):
+            for b in pl[3]:
+                st.pages[b] = self.pool.take()
+        for st, r, m, f, pl in zip(states, rows, counts, first_pos, plans):
+            new_len, lo = pl[0], pl[1]
+            self._drop_retired_rows(st, max(0, new_len - self.W) if self.W > 0 else new_len)
+            if m:
+                # explicit positions: row r of the feed sits at first_pos + r
+                self._store_rows(st, r[lo - st.ctx_len:], range(f + (lo - st.ctx_len), f + m))
+            st.ctx_len = new_len
+        return sum(counts)
 
     # -- drafter-KV carry across turns ----------------------------------------
     def take_drafter_kv(self, st: SeqState):
