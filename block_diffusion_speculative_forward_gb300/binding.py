@@ -34,7 +34,8 @@ class Config(C.Structure):
         ("target_hidden", C.c_int32), ("fc_in_features", C.c_int32), ("rms_eps", C.c_float),
         ("ctx_window", C.c_int32), ("kv_block", C.c_int32), ("prefill_chunk", C.c_int32),
         ("max_batch", C.c_int32), ("max_seq_len", C.c_int32), ("kv_pool_blocks", C.c_int32),
-        ("kv_dtype", C.c_int32), ("lm_head_dtype", C.c_int32), ("rope_attn_factor", C.c_float)]
+        ("kv_dtype", C.c_int32), ("lm_head_dtype", C.c_int32), ("rope_attn_factor", C.c_float),
+        ("shifted_rows", C.c_int32)]
 
 
 class Weights(C.Structure):
@@ -72,6 +73,9 @@ def lib() -> C.CDLL:
                                                C.POINTER(C.c_float), vp]),
             "dflash_after_verify": (C.c_int, [vp, vp, i32]),
             "dflash_after_verify_batch": (C.c_int, [vp, i32, C.POINTER(vp), C.POINTER(i32)]),
+            "dflash_catchup_batch": (C.c_int, [vp, i32, C.POINTER(vp), C.POINTER(vp),
+                                               C.POINTER(vp), C.POINTER(i32), C.POINTER(i64),
+                                               C.POINTER(i64), vp]),
             "dflash_take_drafter_kv": (C.c_int, [vp, vp, C.POINTER(i32), i32, C.POINTER(i32),
                                                  C.POINTER(i64)]),
             "dflash_install_drafter_kv": (C.c_int, [vp, vp, C.POINTER(i32), i32, i64]),
@@ -284,6 +288,33 @@ class DraftHead:
         st_arr = (C.c_void_p * n)(*[s.ptr for s in states])
         ks = (C.c_int32 * n)(*[int(k) for k in num_accepted])
         _check(lib().dflash_after_verify_batch(self.ptr, n, st_arr, ks))
+
+    def catchup_batch(self, states, rows, first_pos, tokens=None) -> int:
+        """[P2]/[P3] catchup_batch: append rows[i] (device [m, S] or None)
+        to states[i] at RoPE positions first_pos[i].. (the state's append
+        point); tokens[i] (the paired token ids) are range-checked. Returns
+        the rows appended."""
+        n = len(states)
+        rows = [self._to_device(r) for r in rows]
+        st_arr = (C.c_void_p * n)(*[s.ptr for s in states])
+        ptrs = (C.c_void_p * n)(*[None if r is None else r.data_ptr() for r in rows])
+        counts = (C.c_int32 * n)(*[0 if r is None else int(r.shape[0]) for r in rows])
+        fp = (C.c_int64 * n)(*[int(f) for f in first_pos])
+        keep, tok = [], None
+        if tokens is not None:
+            tok = (C.c_void_p * n)()
+            for i, t in enumerate(tokens):
+                if t is not None and len(t) != counts[i]:
+                    # the library reads n_rows[i] ids from the array
+                    raise DFlashError(-1, f"state {i}: {len(t)} tokens for {counts[i]} rows")
+                if t is not None:
+                    a = (C.c_uint32 * max(len(t), 1))(*[int(v) for v in t])
+                    keep.append(a)
+                    tok[i] = C.cast(a, C.c_void_p)
+        written = C.c_int64()
+        _check(lib().dflash_catchup_batch(self.ptr, n, st_arr, tok, ptrs, counts, fp,
+                                          C.byref(written), _stream()), self._results)
+        return written.value
 
     # -- drafter-KV carry across turns -----------------------------------------
     def take_drafter_kv(self, st: State):

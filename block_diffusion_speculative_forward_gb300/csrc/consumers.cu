@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(1024) k_add_norm(AddNormArgs p) {
   // draft-row index of this row, or -1
   int drow = -1;
   if (p.z) {
-    const int i = a % p.gamma;
-    if (i >= 1 && i <= p.nd) drow = (a / p.gamma) * p.nd + (i - 1);
+    const int i = a % p.gamma - p.first;
+    if (i >= 0 && i < p.nd) drow = (a / p.gamma) * p.nd + i;
   }
 #pragma unroll
   for (int t = 0; t < MAXE; ++t) {
@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
   const float inv = rsqrtf(tot / (float)n + p.eps);
   int drow = -1;
   if (p.z) {
-    const int i = a % p.gamma;
-    if (i >= 1 && i <= p.nd) drow = (a / p.gamma) * p.nd + (i - 1);
+    const int i = a % p.gamma - p.first;
+    if (i >= 0 && i < p.nd) drow = (a / p.gamma) * p.nd + i;
   }
 #pragma unroll
   for (int t = 0; t < MAXE; ++t) {

@@ -18,6 +18,7 @@ struct AddNormArgs {
   bf16 *z_tap;          // [rows, n] copy of the normed rows (or NULL)
   bf16 *z;              // draft rows only: [n_seq * nd, n] (or NULL)
   int nd, gamma;
+  int first;            // block row of a sequence's first draft row
 };
 
 struct QkvPostArgs {

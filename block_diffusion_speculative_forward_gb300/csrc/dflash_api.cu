@@ -279,6 +279,8 @@ int validate_config(const dflash_config *c) {
     return fail(DFLASH_EINVAL, "ctx_window >= 0, 1 <= kv_block <= 256, prefill_chunk >= 1 required");
   if (c->max_batch < 1 || c->max_seq_len < 1 || c->kv_pool_blocks < 0)
     return fail(DFLASH_EINVAL, "max_batch, max_seq_len >= 1 and kv_pool_blocks >= 0 required");
+  if (c->shifted_rows != 0 && c->shifted_rows != 1)
+    return fail(DFLASH_EINVAL, "shifted_rows must be 0 or 1");
   if ((c->kv_dtype != 0 && c->kv_dtype != 1) || (c->lm_head_dtype != 0 && c->lm_head_dtype != 1))
     return fail(DFLASH_EINVAL, "kv_dtype and lm_head_dtype must be 0 or 1");
   if (!(c->rope_attn_factor >= 0.f && c->rope_attn_factor < 1e4f))
@@ -431,6 +433,7 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *wts, dflash_ha
   g.qkv_w = g.nq * g.d + 2 * g.kv;
   g.kv_fp8 = cfg->kv_dtype;
   g.eps = cfg->rms_eps;
+  g.draft0 = cfg->shifted_rows ? 0 : 1;
   g.pages = pool_pages_for(cfg);
   h->pool.init(g.pages);
   h->R_max = cfg->max_batch * g.gamma;
@@ -607,6 +610,69 @@ int dflash_after_verify_batch(dflash_handle *h, int32_t n, dflash_state *const *
     st->expected_next = st->pend_pos + num_accepted[i] + 1;
     st->pending = false;
     retire_below(h, st, window_start(h, st->expected_next));
+  }
+  return DFLASH_OK;
+}
+
+int dflash_catchup_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
+                         const uint32_t *const *tokens, const void *const *rows,
+                         const int32_t *n_rows, const int64_t *first_pos, int64_t *written,
+                         void *stream) {
+  if (written) *written = 0;
+  if (!h || n < 0 || (n > 0 && (!states || !rows || !n_rows || !first_pos)))
+    return fail(DFLASH_EINVAL, "NULL argument");
+  cudaStream_t s = (cudaStream_t)stream;
+  std::lock_guard<std::mutex> lk(h->mu);
+  std::set<dflash_state *> seen;
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    dflash_state *st = states[i];
+    const int32_t m = n_rows[i];
+    if (!st || !h->states.count(st)) return fail(DFLASH_EINVAL, "state %d unknown", i);
+    if (!seen.insert(st).second) return fail(DFLASH_EINVAL, "state %d repeated", i);
+    if (m < 0) return fail(DFLASH_EINVAL, "state %d: n_rows < 0", i);
+    if (st->pending) return fail(DFLASH_ESTATE, "state %d: catch-up while a propose awaits after_verify", i);
+    if (tokens && tokens[i])
+      for (int32_t r = 0; r < m; ++r)
+        if (tokens[i][r] >= (uint32_t)h->cfg.vocab)
+          return fail(DFLASH_EINVAL, "state %d: token %d outside the vocab", i, r);
+    if (first_pos[i] != st->ctx_len)
+      return fail(DFLASH_EPOSITION, "state %d: first position %lld != its append point %lld", i,
+                  (long long)first_pos[i], (long long)st->ctx_len);
+    if (st->expected_next >= 0 && st->ctx_len + m > st->expected_next)
+      return fail(DFLASH_EPOSITION, "state %d: rows past the position after_verify set (%lld)", i,
+                  (long long)st->expected_next);
+    if (st->ctx_len + m > st->cap) return fail(DFLASH_EINVAL, "state %d: ctx beyond its budget", i);
+    if (h->compute && m > 0 && (!rows[i] || !aligned16(rows[i])))
+      return fail(DFLASH_EINVAL, "state %d: rows must be a 16-byte aligned device pointer", i);
+    total += m;
+  }
+  std::vector<AppendPlan> plans;
+  for (int i = 0; i < n; ++i) plans.push_back(plan_append(h, states[i], n_rows[i], rows[i]));
+  if (!pool_can_cover(h, plans)) return fail(DFLASH_ENOMEM, "KV pool exhausted");
+  const Snapshot snap = snapshot(states, n);
+  commit_plans(h, plans);
+  for (auto &p : plans) p.st->ctx_len = p.new_len;
+  if (written) *written = total;
+  if (!h->compute) return DFLASH_BOOKKEEPING_ONLY;
+  // the rows sit at their states' append points, so the row metadata of an
+  // append (position j at slot j) carries the explicit positions as they are
+  std::vector<dfl::RowMeta> meta;
+  rows_of(h, plans, &meta);
+  for (size_t a = 0; a < meta.size(); a += (size_t)h->cfg.prefill_chunk) {
+    size_t nb = std::min(meta.size() - a, (size_t)h->cfg.prefill_chunk);
+    std::vector<dfl::RowMeta> chunk(meta.begin() + a, meta.begin() + a + nb);
+    dfl::CallMeta cm;
+    int rc = upload_meta(h, {}, chunk, {}, s, &cm);
+    if (rc == DFLASH_OK) {
+      rc = dfl::ctx_append(h->g, h->w, h->b, cm.rows, cm.n_rows, h->M_ctx, s);
+      if (rc) fail(rc, "%s", dfl::last_build_error());
+    }
+    if (rc) {
+      rollback(h, snap);
+      if (written) *written = 0;
+      return rc;
+    }
   }
   return DFLASH_OK;
 }

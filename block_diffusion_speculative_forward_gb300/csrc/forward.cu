@@ -592,7 +592,7 @@ int forward_chain(const Geo &g, const dflash_config &c, const Weights &W, const 
       lm.ep.mask_words = (g.V + 31) / 32;
       lm.ep.nd = nd;
       lm.ep.lm_gamma = g.gamma;
-      lm.ep.lm_first = 1;
+      lm.ep.lm_first = g.draft0;
       lm.ep.lm_part = B.lm_part;
       lm.z_rows = B.z;
       lm.z_tap = B.tap_z;
@@ -844,6 +844,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     an.z = B.z;
     an.nd = nd;
     an.gamma = g.gamma;
+    an.first = g.draft0;
     LK(add_norm(an, R, s));
   }
   if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));

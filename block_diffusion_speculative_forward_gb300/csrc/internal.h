@@ -21,6 +21,7 @@ struct Geo {
   int qkv_w;     // nq*d + 2*kv: width of the stitched QKV output
   int pages;     // pages in the KV pool
   int kv_fp8;    // cache dtype
+  int draft0;    // block row of the first draft: 1, or 0 with shifted rows
   float eps;
 };
 

@@ -105,6 +105,10 @@ typedef struct {
     float rope_attn_factor;      /* YaRN attention temperature: the rotated q and k (ctx keys
                                     included) are scaled by it; 0 = none (1). For rope_scaling
                                     factor s, dflash_yarn_inv_freq returns 0.1 ln(s) + 1 */
+    int32_t shifted_rows;        /* [P1]/[P2] field shifted_rows (the DSpark convention): 1 = block
+                                    row j predicts the token at position+j+1, so drafts 1..n come
+                                    from block rows 0..n-1 (the all-rows argmax vector rotated
+                                    right by one); 0 = drafts from rows 1..n */
 } dflash_config;
 
 typedef struct {
@@ -155,7 +159,8 @@ DFLASH_API int dflash_prefill(dflash_handle *h, dflash_state *st, const void *st
  * ctx_len..position-1 (as dflash_prefill), then run the gamma-row block
  * (last_token at `position`, mask_token_id at position+1..position+gamma-1)
  * through the layers, the final norm and the lm_head, and return the argmax
- * of block rows 1..num_drafts. position must equal ctx_len + n_new, and,
+ * of block rows 1..num_drafts (rows 0..num_drafts-1 with shifted_rows).
+ * position must equal ctx_len + n_new, and,
  * after dflash_after_verify(k), the previous position + k + 1.
  *   new_rows: dev [n_new, stack width] bf16 or NULL when n_new == 0
  *   num_drafts: 1 .. gamma-1
@@ -240,6 +245,33 @@ DFLASH_API int dflash_free_drafter_kv(dflash_handle *h, const int32_t *blocks, i
 DFLASH_API int dflash_yarn_inv_freq(double theta, int32_t head_dim, double factor,
                                     double beta_fast, double beta_slow, int32_t original_max_pos,
                                     float *inv_freq, float *attn_factor);
+/* [P2] catchup_batch / [P3] catchup_drafter: append, for each of n states,
+ * n_rows[i] ctx rows (the target hiddens paired with the tokens the last
+ * verify settled) at RoPE positions first_pos[i] .. first_pos[i]+n_rows[i]-1,
+ * exactly as dflash_prefill computes and stores them (rows below the window
+ * are neither computed nor stored). This head keeps one ctx row per target
+ * position, so a state's KV slot and the RoPE position of its next row
+ * coincide: first_pos[i] must equal the state's ctx_len. After
+ * dflash_after_verify(k) the rows of positions position..position+k (the
+ * last verified token's and the accepted drafts') may come here, all or a
+ * first part of them, and the next propose then brings only the rest as
+ * new_rows (none when all came here).
+ *   states: host [n], distinct; tokens: host [n] array of host [n_rows[i]]
+ *     u32 arrays (or NULL, or NULL entries): checked < vocab only, the ctx
+ *     rows depend on the hiddens alone;
+ *   rows: host [n] array of dev [n_rows[i], stack width] bf16 (16-byte
+ *     aligned; NULL where n_rows[i] == 0); n_rows, first_pos: host [n];
+ *   written: host, may be NULL: rows appended (their sum), 0 on an error.
+ * Pages: all states retire first, then take pages, in state order; on an
+ * error nothing changes and the message names the state's index. Asynchronous
+ * on the stream. Errors: EINVAL (unknown or repeated state, negative count,
+ * token outside the vocab, budget, pointer), ESTATE (a propose awaits
+ * after_verify), EPOSITION (first_pos != ctx_len, or rows past the position
+ * after_verify set), ENOMEM (pool), ECUDA. */
+DFLASH_API int dflash_catchup_batch(dflash_handle *h, int32_t n, dflash_state *const *states,
+                                    const uint32_t *const *tokens, const void *const *rows,
+                                    const int32_t *n_rows, const int64_t *first_pos,
+                                    int64_t *written, void *stream);
 /* dflash_after_verify for the n states of one propose_batch in one call:
  * num_accepted[i] (0..n_out of state i) applies to states[i]. Every state is
  * checked first (known, not repeated, awaiting after_verify, count in range);

@@ -121,6 +121,90 @@ def test_batched_script_matches_oracle_bookkeeping():
     assert lib.propose_batch(sl * 2, [1] * 10, pos * 2, [None] * 10, 7) is None  # n > max_batch
 
 
+def test_catchup_script_matches_oracle_bookkeeping():
+    """[P2] catchup_batch in rounds: propose_batch, after_verify(k_i), then
+    the first j_i of each sequence's k_i + 1 rows through the catch-up feed
+    and the rest as the next propose's new rows; block tables after every
+    call equal the oracle's."""
+    geom = replace(MICRO, gamma=8, ctx_window=40, kv_block=8, prefill_chunk=64)
+    n = 4
+    cfg = cfg_of(geom, max_batch=n, max_seq_len=2048)
+    ora = oracle.DraftHeadOracle(cfg, syn.make_weights(geom, 6))
+    lib = B.DraftHead(cfg, None)
+    ctx = syn.uniform_ints(5, 60, n, 6, 1)
+    so, sl = [], []
+    for i, c in enumerate(ctx):
+        a, b = ora.alloc_state(), lib.alloc_state()
+        ora.prefill(a, syn.make_stack(geom, c, 6, idx=i))
+        lib.prefill(b, _fake_rows(c))
+        so.append(a)
+        sl.append(b)
+    pos, pend = list(ctx), [0] * n
+    for rnd in range(10):
+        ora.propose_batch(so, [1] * n, pos,
+                          [syn.make_stack(geom, m, 6, idx=1000 + rnd * n + i) if m else None
+                           for i, m in enumerate(pend)], 7)
+        lib.propose_batch(sl, [1] * n, pos, [_fake_rows(m) for m in pend], 7)
+        ks = syn.uniform_ints(0, 7, n, 6, 100 + rnd)
+        lib.after_verify_batch(sl, ks)
+        for i in range(n):
+            ora.after_verify(so[i], ks[i])
+        js = [min(j, k + 1) for j, k in zip(syn.uniform_ints(0, 8, n, 6, 200 + rnd), ks)]
+        first = [st.ctx_len for st in so]
+        assert ora.catchup_batch(so, [syn.make_stack(geom, j, 6, idx=5000 + rnd * n + i)
+                                      if j else None for i, j in enumerate(js)], first) == sum(js)
+        assert lib.catchup_batch(sl, [_fake_rows(j) for j in js], first,
+                                 tokens=[[3] * j for j in js]) == sum(js)
+        for i in range(n):
+            assert lib.debug_state(sl[i]) == ora.block_table(so[i])
+        assert lib.debug_pool() == (ora.pool.n_pages - ora.pool.n_free(), ora.pool.n_pages)
+        pos = [p + k + 1 for p, k in zip(pos, ks)]
+        pend = [k + 1 - j for k, j in zip(ks, js)]
+
+
+def test_catchup_errors_match_oracle_and_change_nothing():
+    cfg = cfg_of(MICRO, kv_pool_blocks=6)
+    ora = oracle.DraftHeadOracle(cfg, syn.make_weights(MICRO, 7))
+    lib = B.DraftHead(cfg, None)
+    o1, o2 = ora.alloc_state(), ora.alloc_state()
+    l1, l2 = lib.alloc_state(), lib.alloc_state()
+    ora.prefill(o1, syn.make_stack(MICRO, 18, 7))
+    lib.prefill(l1, _fake_rows(18))
+    rows = syn.make_stack(MICRO, 33, 7)
+    cases = [
+        ("EPOSITION", ([0], [2], [19], None)),
+        ("EPOSITION", ([0], [2], [17], None)),
+        ("EINVAL", ([0, 0], [1, 1], [18, 18], None)),
+        ("EINVAL", ([0], [2], [18], [[1]])),
+        ("EINVAL", ([0], [2], [18], [[1, 256]])),
+        ("ENOMEM", ([0, 1], [1, 33], [18, 0], None)),
+    ]
+    for code, (idx, counts, first, toks) in cases:
+        before = (lib.debug_state(l1), lib.debug_state(l2), lib.debug_pool())
+        with pytest.raises(oracle.OracleError) as eo:
+            ora.catchup_batch([(o1, o2)[i] for i in idx], [rows[:m] for m in counts], first, toks)
+        with pytest.raises(B.DFlashError) as el:
+            lib.catchup_batch([(l1, l2)[i] for i in idx], [_fake_rows(m) for m in counts], first,
+                              tokens=toks)
+        assert eo.value.code == el.value.code == code
+        assert (lib.debug_state(l1), lib.debug_state(l2), lib.debug_pool()) == before
+    ora.propose(o1, 4, 18, None, 3)
+    lib.propose(l1, 4, 18, None, 3)
+    with pytest.raises(B.DFlashError) as el:
+        lib.catchup_batch([l1], [_fake_rows(1)], [18])
+    assert el.value.code == "ESTATE"
+    ora.after_verify(o1, 1)
+    lib.after_verify(l1, 1)
+    with pytest.raises(B.DFlashError) as el:
+        lib.catchup_batch([l1], [_fake_rows(3)], [18])
+    assert el.value.code == "EPOSITION"
+    assert ora.catchup_batch([o1], [rows[:2]], [18]) == lib.catchup_batch([l1], [_fake_rows(2)],
+                                                                            [18]) == 2
+    assert lib.debug_state(l1) == ora.block_table(o1)
+    with pytest.raises(B.DFlashError):
+        B.DraftHead(cfg_of(MICRO, shifted_rows=2), None)
+
+
 def test_errors_leave_state_unchanged():
     cfg = cfg_of(MICRO, kv_pool_blocks=3)
     lib = B.DraftHead(cfg, None)
