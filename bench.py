@@ -314,6 +314,11 @@ def run_ours(args):
         # the ctx_window cap: 8192-row prompt, 4096-row window, 64 rounds
         out["window"] = run_window(64, W)
         torch.cuda.empty_cache()
+    if not args.no_lowp:
+        # the metric's batch-1 step with the lm_head streamed as FP8 / NVFP4 codes
+        for fmt in ("fp8", "nvfp4"):
+            out[f"b1_lm_{fmt}"] = run_b1_lowp(fmt, max(5, K // 2), W)
+            torch.cuda.empty_cache()
     if not args.no_fp8:
         # FP8 lm_head and FP8 KV cache, 128 sequences, gamma 8, 32 rounds
         out["fp8_b128"] = run_batched(syn.FULL_G8, 1005, 128, 512, 4096, 7, True, False, 32, W)
@@ -607,6 +612,94 @@ def run_window(K, W):
                         "64 propose/after_verify rounds, k ~ U[0, 15], k + 1 new rows per round"}
 
 
+def lm_lowp_bytes(geom, fmt, n_rows):
+    """Algorithmic bytes of the streamed lm_head stage: the codes and their
+    scales once, the draft rows' z in, (id, p1) per row out."""
+    V, H = geom.vocab, geom.hidden
+    table = V * H + 4 * V if fmt == "fp8" else V * H // 2 + V * H // 16
+    return table + 2 * n_rows * H + 8 * n_rows
+
+
+def run_b1_lowp(fmt, K, W):
+    """The batch-1 propose of the metric's workload with the lm_head
+    streamed as codes: FP8 E4M3 with per-row scales, or NVFP4 (E2M1 codes,
+    E4M3 scales per 16 elements, global scale). Device time per step and of
+    the lm_head stage (CUDA events inside the replayed graph)."""
+    from block_diffusion_speculative_forward_gb300 import binding as B
+    import ctypes as C
+    geom, seed, ctx = syn.FULL, 1002, 1024
+    nd = geom.gamma - 1
+    w = syn.make_weights(geom, seed, lm_head_fp8=fmt == "fp8", lm_head_nvfp4=fmt == "nvfp4")
+    del w["lm_head"]
+    w["lm_head"] = torch.empty(0, dtype=torch.bfloat16)   # not needed: the codes stream
+    wd = B.weights_to_device(w)
+    del w
+    n_steps = K + W + 4
+    cfg = head_cfg(geom, 1, ctx + n_steps + 64, lm_head_dtype=1 if fmt == "fp8" else 2)
+    head = B.DraftHead(cfg, wd)
+    st = head.alloc_state()
+    head.prefill(st, syn.make_stack(geom, ctx - 1, seed).cuda())
+    rows = syn.make_stack(geom, n_steps + 1, seed, idx=1).cuda()
+    lib = B.lib()
+    lib.dflash_debug_set_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
+    lib.dflash_debug_set_step_probe.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p]
+    s = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record(s)
+    torch.cuda.synchronize()
+    pos, used = ctx, 0
+
+    def step():
+        nonlocal pos, used
+        head.propose(st, 1000 + pos % 1000, pos, rows[used:used + 1], nd)
+        head.after_verify(st, 0)
+        pos += 1
+        used += 1
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev[0].record(s)
+        for _ in range(K):
+            step()
+        ev[1].record(s)
+        torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / K
+    lib.dflash_debug_set_probe(head.ptr, C.c_void_p(ev[2].cuda_event), C.c_void_p(ev[3].cuda_event))
+    lib.dflash_debug_set_step_probe(head.ptr, C.c_void_p(ev[4].cuda_event),
+                                    C.c_void_p(ev[5].cuda_event))
+    lm_ms, dev_ms = [], []
+    for i in range(4):
+        step()
+        if i >= 2:
+            lm_ms.append(ev[2].elapsed_time(ev[3]))
+            dev_ms.append(ev[4].elapsed_time(ev[5]))
+    lib.dflash_debug_set_probe(head.ptr, None, None)
+    lib.dflash_debug_set_step_probe(head.ptr, None, None)
+    head.close()
+    hbm, _, src = peaks()
+    lm_b = lm_lowp_bytes(geom, fmt, nd)
+    wb = syn.weight_bytes(geom)
+    sbytes = (sum(wb.values()) - wb["lm_head"] + lm_b + ctx * geom.num_layers * 2 * geom.kv_dim * 2
+              + geom.stack_width * 2)
+    lm, dev = statistics.mean(lm_ms), statistics.median(dev_ms)
+    return {"value": nd / (ms * 1e-3), "unit": UNIT, "propose_us": 1e3 * ms, "steps": K,
+            "warmup": W, "device_us": 1e3 * dev, "clocks": clk.summary(),
+            "roofline": {"bound": "hbm", "achieved": sbytes / (dev * 1e-3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": sbytes / (dev * 1e-3) / 1e9 / hbm,
+                         "peak_source": f"{src} hbm_gbs", "algorithmic_bytes_per_launch": sbytes,
+                         "kernel": "whole propose step (device time of its kernels)"},
+            "lm_head_roofline": {"bound": "hbm", "achieved": lm_b / (lm * 1e-3) / 1e9,
+                                 "peak": hbm, "unit": "GB/s",
+                                 "frac": lm_b / (lm * 1e-3) / 1e9 / hbm, "avg_ms": lm,
+                                 "algorithmic_bytes_per_launch": lm_b, "traffic": None,
+                                 "kernel": "k_lm_lowp (codes dequantised into TMEM) + merge"},
+            "workload": f"full_b1 with the lm_head streamed as {fmt.upper()} codes "
+                        f"(no bf16 table): ctx 1024, one new row, 15 drafts"}
+
+
 def cpu_baseline(w, cfg, geom, seed, ctx, n_steps):
     """The oracle, as it stands, on the host cores: prefill untimed, then a
     bounded number of single-sequence proposes of the same workload."""
@@ -747,6 +840,8 @@ def main():
                     help="only the batch-32 leg (for profiling it alone)")
     ap.add_argument("--no-window", action="store_true",
                     help="skip the 8192-row prompt / 4096-row window leg (64 rounds)")
+    ap.add_argument("--no-lowp", action="store_true",
+                    help="skip the batch-1 legs with the lm_head streamed as FP8 / NVFP4 codes")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the 128-sequence FP8 leg (32 rounds)")
     ap.add_argument("--path", default="auto", choices=["auto", "per-step", "chained"],

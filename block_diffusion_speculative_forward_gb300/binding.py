@@ -42,7 +42,8 @@ class Weights(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("lm_head_fp8", C.c_void_p),
                 ("lm_head_scale", C.c_void_p), ("fc", C.c_void_p), ("hidden_norm", C.c_void_p),
                 ("norm", C.c_void_p), ("inv_freq", C.c_void_p), ("kv_scale", C.c_void_p),
-                ("layers", C.POINTER(C.c_void_p))]
+                ("layers", C.POINTER(C.c_void_p)), ("lm_head_nvfp4", C.c_void_p),
+                ("lm_head_nvfp4_scale", C.c_void_p), ("lm_head_nvfp4_global", C.c_float)]
 
 
 _lib = None
@@ -183,6 +184,10 @@ class DraftHead:
             if "lm_head_fp8" in weights:
                 ws.lm_head_fp8 = weights["lm_head_fp8"].data_ptr()
                 ws.lm_head_scale = weights["lm_head_scale"].data_ptr()
+            if "lm_head_nvfp4" in weights:
+                ws.lm_head_nvfp4 = weights["lm_head_nvfp4"].data_ptr()
+                ws.lm_head_nvfp4_scale = weights["lm_head_nvfp4_scale"].data_ptr()
+                ws.lm_head_nvfp4_global = float(weights["lm_head_nvfp4_global"])
             if "kv_scale" in weights:
                 ws.kv_scale = weights["kv_scale"].data_ptr()
             ws.layers = C.cast(self._layer_arr, C.POINTER(C.c_void_p))

@@ -37,7 +37,7 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     deps.append(os.path.join(INCLUDE, "dflash.h"))
     newest_dep = max(os.path.getmtime(p) for p in deps)
 

@@ -8,6 +8,7 @@
 #include "consumers.h"
 
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 
 namespace dfl {
 
@@ -66,7 +67,10 @@ __global__ void __launch_bounds__(1024) k_add_norm(AddNormArgs p) {
       const bf16 h = __float2bfloat16_rn(__bfloat162float(p.g[f]) * (v * inv));
       if (p.out) p.out[(int64_t)a * n + f] = h;
       if (p.z_tap) p.z_tap[(int64_t)a * n + f] = h;
-      if (drow >= 0) p.z[(int64_t)drow * n + f] = h;
+      if (drow >= 0) {
+        p.z[(int64_t)drow * n + f] = h;
+        if (p.z16) p.z16[(int64_t)drow * n + f] = __half_as_ushort(__float2half_rn(__bfloat162float(h)));
+      }
     }
   }
 }
@@ -138,7 +142,10 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
       const bf16 h = __float2bfloat16_rn(__bfloat162float(p.g[f]) * (v * inv));
       if (p.out) p.out[(int64_t)a * n + f] = h;
       if (p.z_tap) p.z_tap[(int64_t)a * n + f] = h;
-      if (drow >= 0) p.z[(int64_t)drow * n + f] = h;
+      if (drow >= 0) {
+        p.z[(int64_t)drow * n + f] = h;
+        if (p.z16) p.z16[(int64_t)drow * n + f] = __half_as_ushort(__float2half_rn(__bfloat162float(h)));
+      }
     }
   }
   cl.sync();   // peers have read cta_ss

@@ -19,6 +19,7 @@ struct AddNormArgs {
   bf16 *z;              // draft rows only: [n_seq * nd, n] (or NULL)
   int nd, gamma;
   int first;            // block row of a sequence's first draft row
+  uint16_t *z16;        // draft rows again as f16 bits (or NULL)
 };
 
 struct QkvPostArgs {

@@ -281,8 +281,10 @@ int validate_config(const dflash_config *c) {
     return fail(DFLASH_EINVAL, "max_batch, max_seq_len >= 1 and kv_pool_blocks >= 0 required");
   if (c->shifted_rows != 0 && c->shifted_rows != 1)
     return fail(DFLASH_EINVAL, "shifted_rows must be 0 or 1");
-  if ((c->kv_dtype != 0 && c->kv_dtype != 1) || (c->lm_head_dtype != 0 && c->lm_head_dtype != 1))
-    return fail(DFLASH_EINVAL, "kv_dtype and lm_head_dtype must be 0 or 1");
+  if ((c->kv_dtype != 0 && c->kv_dtype != 1) || c->lm_head_dtype < 0 || c->lm_head_dtype > 2)
+    return fail(DFLASH_EINVAL, "kv_dtype must be 0 or 1 and lm_head_dtype 0, 1 or 2");
+  if (c->lm_head_dtype != 0 && c->hidden % 256)
+    return fail(DFLASH_EINVAL, "a streamed FP8 or NVFP4 lm_head needs hidden a multiple of 256");
   if (!(c->rope_attn_factor >= 0.f && c->rope_attn_factor < 1e4f))
     return fail(DFLASH_EINVAL, "rope_attn_factor must be 0 (none) or positive");
   return DFLASH_OK;

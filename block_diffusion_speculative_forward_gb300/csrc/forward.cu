@@ -64,13 +64,18 @@ void count_launches(int n) { g_launches += n; }
 int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights *w, int R_max,
                       int D_max, int M_ctx, Weights *W, Buffers *B, std::vector<void *> *dev,
                       std::vector<void *> *host) {
-  if (!w->embed || !w->lm_head || !w->fc || !w->hidden_norm || !w->norm || !w->inv_freq ||
-      !w->layers) {
+  if (!w->embed || (c.lm_head_dtype == 0 && !w->lm_head) || !w->fc || !w->hidden_norm ||
+      !w->norm || !w->inv_freq || !w->layers) {
     g_build_err = "a required weight pointer is NULL";
     return DFLASH_EINVAL;
   }
   if (c.lm_head_dtype == 1 && (!w->lm_head_fp8 || !w->lm_head_scale)) {
     g_build_err = "lm_head_dtype 1 needs lm_head_fp8 and lm_head_scale";
+    return DFLASH_EINVAL;
+  }
+  if (c.lm_head_dtype == 2 && (!w->lm_head_nvfp4 || !w->lm_head_nvfp4_scale ||
+                               !(w->lm_head_nvfp4_global > 0.f))) {
+    g_build_err = "lm_head_dtype 2 needs lm_head_nvfp4, lm_head_nvfp4_scale and a positive global";
     return DFLASH_EINVAL;
   }
   if (c.kv_dtype == 1 && !w->kv_scale) {
@@ -131,23 +136,27 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(kn, (size_t)g.L);
   BK(cudaMemcpy(kn, knorm.data(), sizeof(void *) * g.L, cudaMemcpyHostToDevice));
   W->k_norm_dev = kn;
-  // FP8 lm_head ([P1] field lm_head_shared_fp8): the E4M3 codes are widened
-  // once to bf16 (exact: every E4M3 value is a bf16 value) for the
-  // tensor-core GEMM; the per-row scale is applied to the logits in its
-  // epilogue, so the logits are s_v * <z, codes_v>.
-  const void *lm_operand = W->lm_head;
-  if (W->lm_is_fp8) {
-    bf16 *wide = nullptr;
-    BA(wide, (size_t)g.V * H);
-    BK(widen_fp8(W->lm_fp8, (int64_t)g.V * H, wide, 0));
-    lm_operand = wide;
+  // Low-precision lm_head ([P1] fields lm_head_shared_fp8, lm_head_nvfp4):
+  // the codes stream as they are (lm_lowp.cu), dequantised on chip. FP8:
+  // logits s_v * <z, codes_v>; NVFP4: g * <z, e2m1 * scale>.
+  bool ok_lm = true;
+  if (c.lm_head_dtype == 1) {
+    W->lm_lowp = tc::LM_LOWP_FP8;
+    ok_lm = tc::make_map_u8(&W->map_lm_codes, W->lm_fp8, g.V, H, 128, 128, true);
+  } else if (c.lm_head_dtype == 2) {
+    W->lm_lowp = tc::LM_LOWP_NVFP4;
+    W->lm_gscale = w->lm_head_nvfp4_global;
+    ok_lm = tc::make_map_u8(&W->map_lm_codes, w->lm_head_nvfp4, g.V, H / 2, 128, 128, true) &&
+            tc::make_map_u8(&W->map_lm_scales, w->lm_head_nvfp4_scale, g.V, H / 16, 16, 128,
+                            false);
   }
   // TMA maps of every weight operand.
   {
-    bool ok = tc::make_map_2d(&W->map_fc, W->fc, false, H, g.S, 128) &&
+    bool ok = ok_lm && tc::make_map_2d(&W->map_fc, W->fc, false, H, g.S, 128) &&
               tc::make_map_2d(&W->map_wkv, W->w_kv, false, (int64_t)g.L * 2 * kv, H, 128) &&
-              tc::make_map_2d(&W->map_lm, lm_operand, false, g.V, H, 128) &&
-              tc::make_map_2d(&W->map_lm256, lm_operand, false, g.V, H, 256);
+              (W->lm_lowp ||
+               (tc::make_map_2d(&W->map_lm, W->lm_head, false, g.V, H, 128) &&
+                tc::make_map_2d(&W->map_lm256, W->lm_head, false, g.V, H, 256)));
     W->map_qkv.resize(g.L);
     W->map_o.resize(g.L);
     W->map_gu.resize(g.L);
@@ -164,12 +173,13 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
       return DFLASH_ECUDA;
     }
   }
-  // The chained few-row path reads norm gains 16 bytes at a time.
+  // The chained few-row path reads norm gains 16 bytes at a time, and runs
+  // the bf16 lm_head in its last phase.
   {
     auto al = [](const void *q) { return ((uintptr_t)q & 15) == 0; };
     bool ok = al(W->hidden_norm) && al(W->norm);
     for (const LayerW &L : W->layers) ok = ok && al(L.in_norm) && al(L.post_norm);
-    B->use_chain = ok;
+    B->use_chain = ok && c.lm_head_dtype == 0;
   }
   // RoPE table for every position a block row can reach.
   const int max_pos = c.max_seq_len + g.gamma;
@@ -199,6 +209,7 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
   BA(B->qkv_dense, (size_t)R_max * g.qkv_w);
   BA(B->u, (size_t)R_max * I);
   BA(B->z, (size_t)D_max * H);
+  BA(B->z16, (size_t)D_max * H);
   BA(B->row_id, (size_t)D_max);
   BA(B->row_p1, (size_t)D_max);
   BA(B->ctx_pack, (size_t)M_ctx * g.S);
@@ -267,7 +278,8 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     struct A { int id; const void *p; int64_t rows, cols; } acts[ACT_COUNT] = {
         {ACT_H, B->h, R_max, (int64_t)H}, {ACT_O, B->o, R_max, (int64_t)qd},
         {ACT_U, B->u, R_max, (int64_t)I}, {ACT_Z, B->z, D_max, (int64_t)H},
-        {ACT_PACK, B->ctx_pack, M_ctx, (int64_t)g.S}, {ACT_C, B->ctx_c, M_ctx, (int64_t)H}};
+        {ACT_PACK, B->ctx_pack, M_ctx, (int64_t)g.S}, {ACT_C, B->ctx_c, M_ctx, (int64_t)H},
+        {ACT_Z16, B->z16, D_max, (int64_t)H}};   // 16-bit elements: TMA moves f16 as bf16
     const int bns[BN_COUNT] = {16, 32, 64, 128, 256};
     for (auto &a : acts)
       for (int j = 0; j < BN_COUNT; ++j)
@@ -845,10 +857,32 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     an.nd = nd;
     an.gamma = g.gamma;
     an.first = g.draft0;
+    an.z16 = W.lm_lowp ? B.z16 : nullptr;
     LK(add_norm(an, R, s));
   }
   if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));
-  if (D <= 64) {
+  const int vt = (g.V + 127) / 128;
+  if (W.lm_lowp) {
+    // codes streamed and dequantised on chip, every draft row in chunks of
+    // up to 128, per-row partials over 128-row vocab tiles
+    GemmParams p{};
+    p.m_act = D;
+    p.n_w = g.V;
+    p.k = g.H;
+    p.tiles_m = vt;
+    p.epi = EPI_TC_LMHEAD;
+    p.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+    p.gscale = W.lm_gscale;
+    p.status = B.status;
+    p.bitmask = bitmask;
+    p.mask_words = (g.V + 31) / 32;
+    p.nd = nd;
+    p.lm_part = B.lm_part;
+    const int bn = tc::lm_lowp_bn(D, g.H);
+    LK(tc::lm_lowp(W.lm_lowp, W.map_lm_codes, W.map_lm_scales, B.act_map[ACT_Z16][bn_index(bn)],
+                   bn, p, s));
+    LK(lm_reduce(B.lm_part, D, vt, B.row_id, B.row_p1, s));
+  } else if (D <= 64) {
     // Few draft rows: the vocab rows are the MMA's M (the weight stream
     // bounds the kernel), fused per-row reductions over 128-row vocab tiles.
     GemmParams p{};
@@ -898,8 +932,16 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     p.counters = B.counters;
     p.status = B.status;
     p.fault_ns = B.fault_ns;
-    const int bn = tc::pick_bn(D);
-    LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
+    if (W.lm_lowp) {
+      p.tiles_m = vt;
+      p.gscale = W.lm_gscale;
+      const int bn = tc::lm_lowp_bn(D, g.H);
+      LK(tc::lm_lowp(W.lm_lowp, W.map_lm_codes, W.map_lm_scales,
+                     B.act_map[ACT_Z16][bn_index(bn)], bn, p, s));
+    } else {
+      const int bn = tc::pick_bn(D);
+      LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));
+    }
   }
   LK(finalize(B.row_id, B.row_p1, n, nd, B.status, (uint32_t *)(B.out_dev + B.off_drafts),
               (int32_t *)(B.out_dev + B.off_nout), (float *)(B.out_dev + B.off_conf),

@@ -21,6 +21,11 @@ struct Weights {
   const uint8_t *lm_fp8 = nullptr;
   const float *lm_scale = nullptr, *inv_freq = nullptr, *kv_scale = nullptr;
   bool lm_is_fp8 = false;
+  // lm_head streamed as codes (tc::LM_LOWP_FP8 / LM_LOWP_NVFP4; 0 = bf16):
+  // code and block-scale maps, and the factor every logit takes (NVFP4)
+  int lm_lowp = 0;
+  CUtensorMap map_lm_codes, map_lm_scales;
+  float lm_gscale = 0.f;
   std::vector<LayerW> layers;
   const bf16 *const *k_norm_dev = nullptr;  // device array of L k_norm gains
   bf16 *w_kv = nullptr;                     // [L*2*kv, H], rows [K0; V0; K1; V1; ...]
@@ -32,7 +37,7 @@ struct Weights {
 };
 
 // Activation operands of the tensor-core GEMMs, one TMA map per tile width.
-enum ActBuf { ACT_H = 0, ACT_O, ACT_U, ACT_Z, ACT_PACK, ACT_C, ACT_COUNT };
+enum ActBuf { ACT_H = 0, ACT_O, ACT_U, ACT_Z, ACT_PACK, ACT_C, ACT_Z16, ACT_COUNT };
 constexpr int BN_COUNT = 5;   // 16, 32, 64, 128, 256
 inline int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : bn == 128 ? 3 : 4; }
 
@@ -43,6 +48,7 @@ struct Buffers {
   bf16 *u = nullptr;           // [R, I]
   float *qkv_dense = nullptr;  // [R, qkv_w] f32 QKV of a many-row call
   bf16 *z = nullptr;           // [D, H] final-normed draft rows
+  uint16_t *z16 = nullptr;     // [D, H] the same rows as f16 bits (streamed lm_head operand)
   int32_t *row_id = nullptr;
   float *row_p1 = nullptr;
   bf16 *ctx_pack = nullptr;    // [M, S]

@@ -60,6 +60,7 @@ __device__ __forceinline__ void finish16(const GemmParams &p, EpiScratch *sm, co
       }
       float x = v[c];
       if (p.wscale && f_ok) x *= p.wscale[f];
+      if (p.gscale != 0.f) x *= p.gscale;
       val[c] = ok ? x : -INFINITY;
     }
 #pragma unroll

@@ -446,6 +446,23 @@ bool make_map_2d(CUtensorMap *map, const void *base, bool fp8, int64_t rows, int
   return r == CUDA_SUCCESS;
 }
 
+bool make_map_u8(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_bytes,
+                 int box_rows, bool swizzle128) {
+  std::call_once(g_once, init_driver);
+  if (!g_encode || cols % 4 || box_bytes % 4) return false;
+  // moved as 4-byte elements (the same bytes and layout; the copy engine
+  // walks a box by elements, so wider elements move a byte table faster)
+  cuuint64_t dims[2] = {(cuuint64_t)(cols / 4), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 4), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_map_3d(CUtensorMap *map, const void *base, const int64_t dims[3],
                  const int64_t strides_bytes[2], const int box[3]) {
   std::call_once(g_once, init_driver);

@@ -91,6 +91,7 @@ struct GemmParams {
   void *out;          // [m_act, ldo] f32 or bf16 (not LMHEAD)
   int ldo;
   const float *wscale;  // per weight row scale or NULL
+  float gscale;         // lm_head: every logit times this (0: none)
   // stream-K
   float *ws;          // partial slots: 2 * grid * BN * 128 floats
   int *counters;      // per tile, zero between launches
@@ -142,6 +143,24 @@ cudaError_t lmhead(const CUtensorMap &map_x, const CUtensorMap &map_w, const LmA
                    cudaStream_t s);
 int lmhead_vocab_tiles(int vocab);
 int pick_bn(int m_act);
+// Weight-only low-precision lm_head (lm_lowp.cu): FP8 E4M3 codes with the
+// per-row scale in GemmParams::wscale, or NVFP4 codes with block scales and
+// the global factor in GemmParams::gscale. map_codes: [V, k] or [V, k/2] u8
+// (128-byte swizzled boxes of 128 rows x 128 bytes); map_scales: [V, k/16]
+// u8 (boxes of 128 rows x 16 bytes, NVFP4 only); map_z: the draft rows
+// [m_act, k] as f16 in boxes of bn rows x 64. p.epi is EPI_TC_LMHEAD (per-row
+// partials in lm_part, tiles_m = ceil(V/128)) or EPI_TC_STORE_F32 (logits to
+// out). k must be a multiple of lm_lowp_k_step(fmt).
+enum { LM_LOWP_FP8 = 1, LM_LOWP_NVFP4 = 2 };
+int lm_lowp_bn(int m_act, int k);
+int lm_lowp_k_step(int fmt);
+cudaError_t lm_lowp(int fmt, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
+                    const CUtensorMap &map_z, int bn, const GemmParams &p, cudaStream_t s);
+// A 2D map of a byte table [rows, cols] (cols a multiple of 4) with boxes of
+// box_rows x box_bytes, 128-byte swizzled or not. Its x coordinate counts
+// 4-byte words: byte column c is x = c / 4.
+bool make_map_u8(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_bytes,
+                 int box_rows, bool swizzle128);
 // Tile width for a data-parallel (whole-tile) launch of this shape.
 int pick_bn_dp(int m_act, int n_w, int k);
 // 2-D row-major map [rows, cols], box = 128 bytes of a row x box_rows rows, 128B swizzle.

@@ -228,21 +228,6 @@ cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int 
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------- FP8 widening --
-// E4M3 codes to bf16, exactly (E4M3 values are a subset of bf16 values).
-__global__ void k_widen_fp8(const uint8_t *__restrict__ src, int64_t n, bf16 *__restrict__ dst) {
-  pdl_trigger();
-  pdl_wait();
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = __float2bfloat16_rn(fp8_to_float(src[i]));
-}
-
-cudaError_t widen_fp8(const uint8_t *src, int64_t n, bf16 *dst, cudaStream_t s) {
-  launch_pdl(k_widen_fp8, dim3(4096), dim3(256), 0, s, src, n, dst);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------ RoPE table --
 // cos/sin of pos * inv_freq[i] for every position the head can reach, times
 // the attention temperature scale (1 without YaRN), evaluated in double and

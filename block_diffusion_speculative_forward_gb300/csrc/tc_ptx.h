@@ -55,6 +55,25 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     }
   }
 }
+// The same bounded wait with a sleep of sleep_ns between polls, for waits
+// that are long and not latency-critical: a parked warp then leaves its
+// scheduler's issue slots to the warps doing the work.
+static __device__ __noinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity,
+                                                   volatile int *abort_flag, uint32_t sleep_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(sleep_ns);
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 7) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > TIMEOUT_NS) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
 // The same wait by every lane of a warp, with one answer for the whole warp:
 // a lane that gives up (abort or timeout) makes every lane give up, so the
 // warp-collective tcgen05 loads after a wait stay convergent even when a
@@ -62,6 +81,11 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
                                                volatile int *abort_flag) {
   const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+__device__ __forceinline__ bool mbar_wait_warp_idle(uint32_t bar, uint32_t parity,
+                                                    volatile int *abort_flag, uint32_t sleep_ns) {
+  const bool ok = mbar_wait_idle(bar, parity, abort_flag, sleep_ns);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 // Agreement of the four epilogue warps (named barrier 1, 128 threads): true
@@ -131,6 +155,43 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same MMA with A read from tensor memory: a_tmem addresses a 128-lane
+// x 8-column block holding 128 rows x 16 K elements, two bf16 per column
+// (element 2c in the low half), row i in lane i.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same, always accumulating into D (no predicate to set up).
+__device__ __forceinline__ void umma_bf16_tmem_a_acc(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+               "r"(a_tmem), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+// 32 TMEM lanes (this warp's quarter) x 32 consecutive 32-bit columns, from
+// registers; complete (visible to later tensor-core reads after a thread
+// sync with the tcgen05 fences) once tmem_wait_st() returns.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -186,6 +247,11 @@ template <int M, int N>
 __device__ __forceinline__ uint32_t idesc_bf16_mn() {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+// The same with f16 A and B (formats 0).
+template <int M, int N>
+__device__ __forceinline__ uint32_t idesc_f16_mn() {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 }  // namespace tc

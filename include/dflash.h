@@ -101,7 +101,10 @@ typedef struct {
     int32_t max_seq_len;         /* per-state position ceiling ([P1] field max_seq_len) */
     int32_t kv_pool_blocks;      /* pages in the pool; 0 = max_batch * (min(ctx_window, max_seq_len)/kv_block + 2) */
     int32_t kv_dtype;            /* 0 = bf16 cache ([P2] kv_cache), 1 = FP8 E4M3 with kv_scale ([P1] kv_cache) */
-    int32_t lm_head_dtype;       /* 0 = bf16 lm_head, 1 = FP8 E4M3 codes + per-row scales */
+    int32_t lm_head_dtype;       /* 0 = bf16 lm_head; 1 = FP8 E4M3 codes + per-row scales; 2 =
+                                    NVFP4: E2M1 codes + E4M3 scales per 16 elements + a global
+                                    scale. 1 and 2 stream the codes (no 16-bit copy of the table
+                                    is made) and need hidden a multiple of 256 */
     float rope_attn_factor;      /* YaRN attention temperature: the rotated q and k (ctx keys
                                     included) are scaled by it; 0 = none (1). For rope_scaling
                                     factor s, dflash_yarn_inv_freq returns 0.1 ln(s) + 1 */
@@ -112,12 +115,19 @@ typedef struct {
 } dflash_config;
 
 typedef struct {
-    const void *embed, *lm_head;                       /* dev, borrowed */
+    const void *embed, *lm_head;                       /* dev, borrowed; lm_head may be NULL when
+                                                          lm_head_dtype != 0 */
     const void *lm_head_fp8; const float *lm_head_scale;/* dev, used when lm_head_dtype == 1 */
     const void *fc, *hidden_norm, *norm;               /* dev */
     const float *inv_freq;                             /* dev [head_dim/2] */
     const float *kv_scale;                             /* dev, used when kv_dtype == 1 */
     const void *const *layers;                         /* HOST array of num_layers*11 dev pointers */
+    /* used when lm_head_dtype == 2 ([P1]/[P2] field lm_head_nvfp4, "packed + scales"):
+     * codes [vocab, hidden/2] u8, element 2j in the low nibble; scales
+     * [vocab, hidden/16] E4M3 bytes, one per 16 consecutive elements of a row;
+     * value = e2m1 * e4m3(scale) * global */
+    const void *lm_head_nvfp4; const void *lm_head_nvfp4_scale;
+    float lm_head_nvfp4_global;
 } dflash_weights;
 
 /* Build a head ([P1] from_weights). Validates the geometry, stitches the fused

@@ -55,11 +55,12 @@ class Pair:
     """Oracle and library heads over the same weights."""
 
     def __init__(self, geom, seed, cfg_kw=None, lm_fp8=False, kv_fp8=False, taps=True,
-                 max_rows=None):
+                 max_rows=None, lm_nvfp4=False):
         self.geom = geom
-        self.cfg = cfg_for(geom, **(cfg_kw or {}),
-                           kv_dtype=int(kv_fp8), lm_head_dtype=int(lm_fp8))
-        self.w = syn.make_weights(geom, seed, lm_head_fp8=lm_fp8, kv_fp8=kv_fp8)
+        self.cfg = cfg_for(geom, **(cfg_kw or {}), kv_dtype=int(kv_fp8),
+                           lm_head_dtype=2 if lm_nvfp4 else int(lm_fp8))
+        self.w = syn.make_weights(geom, seed, lm_head_fp8=lm_fp8, kv_fp8=kv_fp8,
+                                  lm_head_nvfp4=lm_nvfp4)
         self.ora = oracle.DraftHeadOracle(self.cfg, self.w)
         self.wd = B.weights_to_device(self.w)
         self.lib = B.DraftHead(self.cfg, self.wd)

@@ -15,7 +15,8 @@ from block_diffusion_speculative_forward_gb300 import binding as B
 from tests.test_oracle_pins import MICRO
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SMALL = replace(MICRO, gamma=16, ctx_window=4096, kv_block=16, vocab=4096, mask_token_id=4095)
+SMALL = replace(MICRO, hidden=256, gamma=16, ctx_window=4096, kv_block=16, vocab=4096,
+                mask_token_id=4095)
 
 
 class _Event:
@@ -68,7 +69,8 @@ def bench(monkeypatch):
 def test_batch1_leg(bench):
     args = bench.argparse.Namespace(gpus=1, steps=12, warmup=3, impl="ours", cpu_steps=1,
                                     no_cpu=True, no_batch=True, batch_only=False,
-                                    no_window=True, no_fp8=True, kernel=None, lm_traffic=1.0)
+                                    no_window=True, no_fp8=True, no_lowp=True, kernel=None,
+                                    lm_traffic=1.0)
     out = {}
     bench.print = lambda s, **k: out.setdefault("line", s)
     bench.run_ours(args)

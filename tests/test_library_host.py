@@ -44,7 +44,8 @@ def test_geometry_validation():
         B.DraftHead(cfg, None)
     assert e.value.code == "EINVAL" and "validate_against_target" in str(e.value)
     for bad in (dict(head_dim=48), dict(num_q_heads=3), dict(gamma=1), dict(mask_token_id=256),
-                dict(kv_dtype=2), dict(hidden=100)):
+                dict(kv_dtype=2), dict(hidden=100), dict(lm_head_dtype=3),
+                dict(lm_head_dtype=2)):   # MICRO's hidden 128: NVFP4 stages take 256
         c = cfg_of(MICRO)
         c.update(bad)
         with pytest.raises(B.DFlashError):
