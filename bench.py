@@ -209,12 +209,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     launches0 = lib.dflash_debug_launch_count()
     with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("propose_rounds")   # (selects the steps in a profiler)
         ev0.record(stream)
         for _ in range(K):
             step(rows_dev[used:used + 1])
             used += 1
         ev1.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     launches = lib.dflash_debug_launch_count() - launches0
     t_ms = ev0.elapsed_time(ev1)
     # then the probes (events around the lm_head stage and the whole forward,
@@ -498,11 +500,13 @@ def run_batched(geom, seed, n, ctx_lo, ctx_hi, nd, fp8, use_mask, K, W):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.nvtx.range_push("propose_rounds")   # (selects the rounds in a profiler)
         e0.record(s)
         for t in range(W, W + K):
             step(t)
         e1.record(s)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     ms = e0.elapsed_time(e1) / K
     phases = {name: (sum(w[name][0] for w in work) / K, sum(w[name][1] for w in work) / K)
               for name in work[0]}
@@ -844,6 +848,9 @@ def main():
                     help="skip the batch-1 legs with the lm_head streamed as FP8 / NVFP4 codes")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the 128-sequence FP8 leg (32 rounds)")
+    ap.add_argument("--leg", default=None,
+                    choices=["batch32", "window", "fp8_b128", "b1_lm_fp8", "b1_lm_nvfp4"],
+                    help="run one secondary leg alone and print its JSON (for profiling it)")
     ap.add_argument("--path", default="auto", choices=["auto", "per-step", "chained"],
                     help="batch-1 leg: the library's default path, the kernel-per-step path, or "
                          "the chained single launch")
@@ -863,6 +870,19 @@ def main():
         from block_diffusion_speculative_forward_gb300 import build
         build.build()
         run_kernel_case(args)
+    elif args.leg:
+        from block_diffusion_speculative_forward_gb300 import build
+        build.build()
+        if args.leg == "batch32":
+            r = run_batched(syn.FULL, 1004, 32, 256, 4096, 15, False, True, args.steps, args.warmup)
+        elif args.leg == "window":
+            r = run_window(args.steps, args.warmup)
+        elif args.leg == "fp8_b128":
+            r = run_batched(syn.FULL_G8, 1005, 128, 512, 4096, 7, True, False, args.steps,
+                            args.warmup)
+        else:
+            r = run_b1_lowp(args.leg[6:], args.steps, args.warmup)
+        print(json.dumps({args.leg: r}), flush=True)
     elif args.batch_only:
         from block_diffusion_speculative_forward_gb300 import build
         build.build()

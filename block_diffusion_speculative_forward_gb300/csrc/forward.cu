@@ -150,13 +150,27 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
             tc::make_map_u8(&W->map_lm_scales, w->lm_head_nvfp4_scale, g.V, H / 16, 16, 128,
                             false);
   }
+  // A propose with more than 16 draft rows is no longer bound by the table's
+  // bytes but by tensor-core work, where converting the codes once per row
+  // chunk costs more than it saves: those calls multiply by the table widened
+  // to bf16 (exactly) once here, made only when such a call is possible.
+  const void *lm_operand = W->lm_head;
+  if (W->lm_lowp && (D_max > 16 || !tc::lm_lowp_fits(1, g.H))) {
+    bf16 *wide = nullptr;
+    BA(wide, (size_t)g.V * H);
+    BK(widen_lm_table(c.lm_head_dtype, W->lm_lowp == tc::LM_LOWP_FP8
+                                           ? W->lm_fp8 : (const uint8_t *)w->lm_head_nvfp4,
+                      (const uint8_t *)w->lm_head_nvfp4_scale, g.V, H, wide, 0));
+    BK(cudaDeviceSynchronize());
+    lm_operand = wide;
+  }
   // TMA maps of every weight operand.
   {
     bool ok = ok_lm && tc::make_map_2d(&W->map_fc, W->fc, false, H, g.S, 128) &&
               tc::make_map_2d(&W->map_wkv, W->w_kv, false, (int64_t)g.L * 2 * kv, H, 128) &&
-              (W->lm_lowp ||
-               (tc::make_map_2d(&W->map_lm, W->lm_head, false, g.V, H, 128) &&
-                tc::make_map_2d(&W->map_lm256, W->lm_head, false, g.V, H, 256)));
+              (!lm_operand ||
+               (tc::make_map_2d(&W->map_lm, lm_operand, false, g.V, H, 128) &&
+                tc::make_map_2d(&W->map_lm256, lm_operand, false, g.V, H, 256)));
     W->map_qkv.resize(g.L);
     W->map_o.resize(g.L);
     W->map_gu.resize(g.L);
@@ -862,9 +876,9 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   }
   if (B.probe_begin && B.probe_end) FK(cudaEventRecordWithFlags(B.probe_begin, s, cudaEventRecordExternal));
   const int vt = (g.V + 127) / 128;
-  if (W.lm_lowp) {
-    // codes streamed and dequantised on chip, every draft row in chunks of
-    // up to 128, per-row partials over 128-row vocab tiles
+  if (W.lm_lowp && tc::lm_lowp_fits(D, g.H)) {
+    // codes streamed and dequantised on chip (the draft rows resident),
+    // per-row partials over 128-row vocab tiles
     GemmParams p{};
     p.m_act = D;
     p.n_w = g.V;
@@ -878,9 +892,8 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     p.mask_words = (g.V + 31) / 32;
     p.nd = nd;
     p.lm_part = B.lm_part;
-    const int bn = tc::lm_lowp_bn(D, g.H);
-    LK(tc::lm_lowp(W.lm_lowp, W.map_lm_codes, W.map_lm_scales, B.act_map[ACT_Z16][bn_index(bn)],
-                   bn, p, s));
+    LK(tc::lm_lowp(W.lm_lowp, W.map_lm_codes, W.map_lm_scales, B.act_map[ACT_Z16][bn_index(16)],
+                   p, s));
     LK(lm_reduce(B.lm_part, D, vt, B.row_id, B.row_p1, s));
   } else if (D <= 64) {
     // Few draft rows: the vocab rows are the MMA's M (the weight stream
@@ -891,6 +904,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     p.k = g.H;
     p.epi = EPI_TC_LMHEAD;
     p.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+    p.gscale = W.lm_gscale;
     p.ws = B.ws;
     p.counters = B.counters;
     p.status = B.status;
@@ -913,6 +927,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     p.mask_words = (g.V + 31) / 32;
     p.nd = nd;
     p.wscale = W.lm_is_fp8 ? W.lm_scale : nullptr;
+    p.gscale = W.lm_gscale;
     p.out = B.lm_part;
     p.status = B.status;
     LK(tc::lmhead(B.act_map[ACT_Z][bn_index(128)], W.map_lm256, p, s));
@@ -932,12 +947,11 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
     p.counters = B.counters;
     p.status = B.status;
     p.fault_ns = B.fault_ns;
-    if (W.lm_lowp) {
+    p.gscale = W.lm_gscale;
+    if (W.lm_lowp && tc::lm_lowp_fits(D, g.H)) {
       p.tiles_m = vt;
-      p.gscale = W.lm_gscale;
-      const int bn = tc::lm_lowp_bn(D, g.H);
       LK(tc::lm_lowp(W.lm_lowp, W.map_lm_codes, W.map_lm_scales,
-                     B.act_map[ACT_Z16][bn_index(bn)], bn, p, s));
+                     B.act_map[ACT_Z16][bn_index(16)], p, s));
     } else {
       const int bn = tc::pick_bn(D);
       LK(tc::gemm(W.map_lm, B.act_map[ACT_Z][bn_index(bn)], bn, p, s));

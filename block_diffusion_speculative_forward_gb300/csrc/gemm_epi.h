@@ -210,7 +210,7 @@ __device__ __forceinline__ void finish16(const GemmParams &p, EpiScratch *sm, co
     return;
   }
   if (!f_ok) return;
-  const float sc = p.wscale ? p.wscale[f] : 1.f;
+  const float sc = (p.wscale ? p.wscale[f] : 1.f) * (p.gscale != 0.f ? p.gscale : 1.f);
   const int nrows = p.m_act - a0 < 16 ? p.m_act - a0 : 16;
   if (EPI == EPI_TC_ADD_F32) {
     // all loads first, then the stores

@@ -132,6 +132,7 @@ struct LmArgs {
   int mask_words;
   int nd;                  // draft rows per sequence
   const float *wscale;     // per vocab row scale (FP8 head) or NULL
+  float gscale;            // every logit times this (NVFP4 head's global scale; 0: none)
   LmPartial *out;          // [m_act][vocab tiles of 256]
   int *status;
 };
@@ -143,19 +144,19 @@ cudaError_t lmhead(const CUtensorMap &map_x, const CUtensorMap &map_w, const LmA
                    cudaStream_t s);
 int lmhead_vocab_tiles(int vocab);
 int pick_bn(int m_act);
-// Weight-only low-precision lm_head (lm_lowp.cu): FP8 E4M3 codes with the
-// per-row scale in GemmParams::wscale, or NVFP4 codes with block scales and
-// the global factor in GemmParams::gscale. map_codes: [V, k] or [V, k/2] u8
-// (128-byte swizzled boxes of 128 rows x 128 bytes); map_scales: [V, k/16]
-// u8 (boxes of 128 rows x 16 bytes, NVFP4 only); map_z: the draft rows
-// [m_act, k] as f16 in boxes of bn rows x 64. p.epi is EPI_TC_LMHEAD (per-row
-// partials in lm_part, tiles_m = ceil(V/128)) or EPI_TC_STORE_F32 (logits to
-// out). k must be a multiple of lm_lowp_k_step(fmt).
+// Weight-only low-precision lm_head (lm_lowp.cu) over at most 16 draft
+// rows: FP8 E4M3 codes with the per-row scale in GemmParams::wscale, or
+// NVFP4 codes with block scales and the global factor in GemmParams::gscale.
+// map_codes: [V, k] or [V, k/2] bytes (128-byte swizzled boxes of 128 rows x
+// 128 bytes); map_scales: [V, k/16] bytes (boxes of 128 rows x 16 bytes,
+// NVFP4 only); map_z: the draft rows [m_act, k] as f16 in boxes of 16 rows x
+// 64. p.epi is EPI_TC_LMHEAD (per-row partials in lm_part, tiles_m =
+// ceil(V/128)) or EPI_TC_STORE_F32 (logits to out). lm_lowp_fits says which
+// shapes it takes (m_act <= 16, k a multiple of 256, at most 2048).
 enum { LM_LOWP_FP8 = 1, LM_LOWP_NVFP4 = 2 };
-int lm_lowp_bn(int m_act, int k);
-int lm_lowp_k_step(int fmt);
+bool lm_lowp_fits(int m_act, int k);
 cudaError_t lm_lowp(int fmt, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
-                    const CUtensorMap &map_z, int bn, const GemmParams &p, cudaStream_t s);
+                    const CUtensorMap &map_z, const GemmParams &p, cudaStream_t s);
 // A 2D map of a byte table [rows, cols] (cols a multiple of 4) with boxes of
 // box_rows x box_bytes, 128-byte swizzled or not. Its x coordinate counts
 // 4-byte words: byte column c is x = c / 4.

@@ -130,6 +130,9 @@ cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int 
                      const int *status, uint32_t *drafts, int32_t *n_out, float *conf,
                      int32_t *status_out, cudaStream_t s);
 
+cudaError_t widen_lm_table(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t rows,
+                           int64_t k, bf16 *dst, cudaStream_t s);
+
 cudaError_t rope_table(const float *inv_freq, int max_pos, int half, float scale, float *cos_t,
                        float *sin_t, cudaStream_t s);
 

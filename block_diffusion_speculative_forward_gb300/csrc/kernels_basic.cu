@@ -9,6 +9,9 @@
 #include "gemm_tc.h"
 #include "internal.h"
 
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
+
 #include <cfloat>
 #include <cmath>
 
@@ -225,6 +228,38 @@ cudaError_t finalize(const int32_t *row_id, const float *row_p1, int n_seq, int 
                      int32_t *status_out, cudaStream_t s) {
   launch_pdl(k_finalize, dim3((n_seq + 127) / 128), dim3(128), 0, s, row_id, row_p1, n_seq, nd, status, drafts, n_out,
                                                   conf, status_out);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------- lm_head table widening --
+// A low-precision lm_head table as bf16 values, exactly (every E4M3 value and
+// every E2M1 x E4M3 product is a bf16 value), for the many-row tensor-core
+// kernels; the row scale (FP8) or global scale (NVFP4) stays in their
+// epilogues. fmt 1: codes [rows, k] E4M3; fmt 2: codes [rows, k/2] E2M1
+// pairs (element 2j in the low nibble) and scales [rows, k/16] E4M3.
+__global__ void k_widen_lm(int fmt, const uint8_t *__restrict__ codes,
+                           const uint8_t *__restrict__ scales, int64_t rows, int64_t k,
+                           bf16 *__restrict__ dst) {
+  const int64_t n = rows * k;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v;
+    if (fmt == 1) {
+      v = fp8_to_float(codes[i]);
+    } else {
+      const int64_t r = i / k, c = i % k;
+      const uint8_t b = codes[r * (k / 2) + c / 2];
+      const __half_raw e = __nv_cvt_fp4_to_halfraw((__nv_fp4_storage_t)((c & 1) ? b >> 4 : b & 15),
+                                                   __NV_E2M1);
+      v = __half2float(*reinterpret_cast<const __half *>(&e)) * fp8_to_float(scales[r * (k / 16) + c / 16]);
+    }
+    dst[i] = __float2bfloat16_rn(v);
+  }
+}
+
+cudaError_t widen_lm_table(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t rows,
+                           int64_t k, bf16 *dst, cudaStream_t s) {
+  k_widen_lm<<<4096, 256, 0, s>>>(fmt, codes, scales, rows, k, dst);
   return cudaGetLastError();
 }
 

@@ -6,12 +6,16 @@
 //   FP8:   logit[a, v] = s_v * sum_k z[a, k] * e4m3(c[v, k])
 //   NVFP4: logit[a, v] = g * sum_k z[a, k] * e2m1(c[v, k]) * e4m3(s[v, k / 16])
 //
+// It serves proposes of at most 16 draft rows (batch 1), where the table's
+// bytes bound the step; wider proposes are bound by tensor-core work and
+// multiply by the table widened to bf16 once (see build_device_side).
+//
 // z (the final-normed draft rows) is not quantised: the weight is
 // dequantised, the activations are not. The product runs on the tensor cores
 // as kind::f16 with f16 operands: the vocab rows as A (M = 128 rows per tile)
-// and up to BN draft rows as B, read from an f16 copy of the rows (every bf16
-// value down to 2^-17 in magnitude is an f16 value, so that copy changes no
-// product a logit of any weight here can feel).
+// and the 16 draft rows as B (N = 16), read from an f16 copy of the rows
+// (every bf16 value down to 2^-17 in magnitude is an f16 value, so that copy
+// changes no product a logit of any weight here can feel).
 //
 // Why A comes from tensor memory: at the HBM rate an SM receives about 22
 // code bytes per cycle; dequantising into shared memory would add a 16-bit
@@ -34,17 +38,16 @@
 // multiply produce; the per-row scale (FP8) or global scale (NVFP4)
 // multiplies the fp32 logit in the epilogue.
 //
-// Work: items (vocab tile of 128 rows, chunk of BN draft rows), item-major
-// over vocab tiles, one persistent CTA per SM walking items c, c + G, ...;
-// each item runs the whole reduction (K = hidden) into a double-buffered
-// TMEM accumulator, and the epilogue writes the tile's per-row (max, lowest
-// argmax, sum exp) partial, as the bf16 lm_head does. Sixteen draft rows
-// (batch 1) stay resident in shared memory for the whole launch; chunks of 32
-// or 64 rows stream their z rows in 256-K stages of their own.
+// Work: vocab tiles of 128 rows, one persistent CTA per SM walking tiles
+// c, c + G, ...; each tile runs the whole reduction (K = hidden) into a
+// double-buffered TMEM accumulator, and the epilogue writes the tile's
+// per-row (max, lowest argmax, sum exp) partial, as the bf16 lm_head does.
+// The draft rows stay resident in shared memory for the whole launch: loaded
+// once, so no load of them ever queues behind the code stream.
 //
 // Warp roles (352 threads): warp 0 issues the code (and scale) TMA loads into
 // their ring, which the converters release as soon as the codes are in
-// registers; warp 10 issues the z loads; warp 1 owns TMEM and issues MMAs;
+// registers; warp 10 loads the draft rows; warp 1 owns TMEM and issues MMAs;
 // warps 2-5 run the epilogue; warps 6-9 convert (converting a slot takes less
 // time than its 16 MMAs, so one warpgroup keeps the issuer fed). Every wait
 // is bounded; on a timeout the CTA raises the status word, drains its own
@@ -76,31 +79,26 @@ constexpr int LP_SMEM_MAX = 232448;     // dynamic shared memory per CTA
 constexpr int LP_K_RES = 2048;          // widest reduction with resident draft rows
 
 struct LpSmem {
-  uint64_t cfull[8], cempty[8], zfull[8], zempty[8];
+  uint64_t cfull[8], cempty[8], zfull;
   uint64_t a_full[4], a_empty[4], acc_full[2], acc_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
-  uint32_t c_issued, c_parity, z_issued, z_parity;
+  uint32_t c_issued, c_parity, z_issued;
   int abort_flag;
   EpiScratch epi;
 };
 
-template <int BN, int FMT>
+constexpr int LP_BN = 16;               // draft rows (the MMA's N)
+
+template <int FMT>
 struct LpCfg {
   // one stage = 256 K of 128 vocab rows: FP8 two 128-byte boxes per row,
   // NVFP4 one (two codes a byte) plus 16 block-scale bytes
   static constexpr int CODE_BYTES = FMT == LM_LOWP_FP8 ? 2 * 128 * 128 : 128 * 128;
   static constexpr int SCALE_BYTES = FMT == LM_LOWP_NVFP4 ? 128 * 16 : 0;
   static constexpr int CSTAGE = CODE_BYTES + SCALE_BYTES;
-  static constexpr int Z_TILE = BN * 128;                      // BN rows x 64 f16
-  // 16 draft rows stay resident for the whole launch (every item uses the
-  // same rows): loaded once, so no z load ever queues behind the code
-  // stream. Wider row chunks stream their z tiles through a ring.
-  static constexpr bool ZRES = BN == 16;
-  // streamed: stages of 256 K (LP_SUB tiles behind one barrier, one hand-off)
-  static constexpr int ZSTAGE = LP_SUB * Z_TILE;
-  static constexpr int ZSTAGES = 2;
-  static constexpr int Z_BYTES = ZRES ? (LP_K_RES / 64) * Z_TILE : ZSTAGES * ZSTAGE;
+  static constexpr int Z_TILE = LP_BN * 128;                   // 16 rows x 64 f16
+  static constexpr int Z_BYTES = (LP_K_RES / 64) * Z_TILE;     // the resident draft rows
   static constexpr int CFIT = (LP_SMEM_MAX - 1024 - (int)sizeof(LpSmem) - Z_BYTES) / CSTAGE;
   static constexpr int CSTAGES = CFIT > 8 ? 8 : CFIT;
   static constexpr int SMEM = 1024 + Z_BYTES + CSTAGES * CSTAGE + (int)sizeof(LpSmem);
@@ -108,11 +106,10 @@ struct LpCfg {
   static_assert(SMEM <= LP_SMEM_MAX, "shared memory");
   static_assert(CSTAGE % 1024 == 0 && Z_TILE % 1024 == 0,
                 "swizzled tiles stay 1024-byte aligned");
-  // TMEM: the two accumulators (2 BN columns, rounded to 32), then the A slots
-  static constexpr int A_COL0 = (2 * BN + 31) / 32 * 32;
-  static constexpr int A_FIT = (LP_TMEM_COLS - A_COL0) / LP_SLOT_COLS;
-  static constexpr int A_SLOTS = A_FIT > 4 ? 4 : A_FIT;
-  static_assert(A_SLOTS >= 2, "two A slots at least");
+  // TMEM: the two accumulators (32 columns), then the A slots
+  static constexpr int A_COL0 = 2 * LP_BN;
+  static constexpr int A_SLOTS = (LP_TMEM_COLS - A_COL0) / LP_SLOT_COLS;   // 3
+  static_assert(A_SLOTS >= 2 && A_SLOTS <= 4, "A slots");
 };
 
 __device__ __forceinline__ uint32_t halfraw2_bits(__half2_raw r) {
@@ -158,11 +155,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-template <int BN, int FMT>
+template <int FMT>
 __global__ void __launch_bounds__(LP_THREADS, 1)
     k_lm_lowp(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_s,
               const __grid_constant__ CUtensorMap map_z, GemmParams p) {
-  using C = LpCfg<BN, FMT>;
+  using C = LpCfg<FMT>;
+  constexpr int BN = LP_BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;          // z tiles, then the code ring
@@ -170,17 +168,14 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
   LpSmem *sm = (LpSmem *)(smem_raw + (base - raw) + C::Z_BYTES + C::CSTAGES * C::CSTAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int n_rc = (p.m_act + BN - 1) / BN;
-  const int n_items = p.tiles_m * n_rc;
+  const int n_items = p.tiles_m;
   const int G = (int)gridDim.x;
   const int my_items = (int)blockIdx.x < n_items ? (n_items - (int)blockIdx.x + G - 1) / G : 0;
   const int n_st = p.k / LP_KS;
   const int64_t total = (int64_t)my_items * n_st;      // stages (= A slots filled) of this CTA
-  // (item, stage) of the CTA's j-th stage
-  auto item_of = [&](int64_t j, int *tm, int *rc, int *s) {
-    const int it = (int)blockIdx.x + (int)(j / n_st) * G;
-    *tm = it / n_rc;
-    *rc = it % n_rc;
+  // (vocab tile, stage) of the CTA's j-th stage
+  auto item_of = [&](int64_t j, int *tm, int *s) {
+    *tm = (int)blockIdx.x + (int)(j / n_st) * G;
     *s = (int)(j % n_st);
   };
 
@@ -189,10 +184,7 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
       mbar_init(smem_u32(&sm->cfull[s]), 1);
       mbar_init(smem_u32(&sm->cempty[s]), 4);   // the converter warps
     }
-    for (int s = 0; s < (C::ZRES ? 1 : C::ZSTAGES); ++s) {
-      mbar_init(smem_u32(&sm->zfull[s]), 1);
-      mbar_init(smem_u32(&sm->zempty[s]), 1);   // the MMA commit
-    }
+    mbar_init(smem_u32(&sm->zfull), 1);
     for (int s = 0; s < C::A_SLOTS; ++s) {
       mbar_init(smem_u32(&sm->a_full[s]), 4);   // the converter warps
       mbar_init(smem_u32(&sm->a_empty[s]), 1);
@@ -203,7 +195,7 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
     }
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort_flag = 0;
-    sm->c_issued = sm->c_parity = sm->z_issued = sm->z_parity = 0;
+    sm->c_issued = sm->c_parity = sm->z_issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -238,8 +230,8 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
         if (j >= C::CSTAGES &&
             !mbar_wait_idle(smem_u32(&sm->cempty[stage]), phase ^ 1, abort_flag, 64))
           break;
-        int tm, rc, s;
-        item_of(j, &tm, &rc, &s);
+        int tm, s;
+        item_of(j, &tm, &s);
         const uint32_t sb = cbase + stage * C::CSTAGE;
         const uint32_t fb = smem_u32(&sm->cfull[stage]);
         mbar_expect_tx(fb, C::CSTAGE);
@@ -259,56 +251,30 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
       sm->c_parity = parity;
     }
   } else if (warp == 10) {
-    // ---------------------------------------------- z producer ----------
+    // ------------------------------------------- draft rows ---------------
     pdl_wait();
-    if (lane == 0 && C::ZRES && total > 0) {
-      // every z tile of the reduction, once, behind one barrier
-      const uint32_t fb = smem_u32(&sm->zfull[0]);
+    if (lane == 0 && total > 0) {
+      // every 64-K tile of the rows, once, behind one barrier
+      const uint32_t fb = smem_u32(&sm->zfull);
       mbar_expect_tx(fb, (uint32_t)(p.k / 64) * C::Z_TILE);
       for (int t = 0; t < p.k / 64; ++t)
         tma_load_2d(base + t * C::Z_TILE, &map_z, fb, 64 * t, 0, policy_evict_last());
       sm->z_issued = 1;
-      sm->z_parity = 0;
-    } else if (lane == 0 && !C::ZRES) {
-      // the z rows of each stage (256 K of the item's row chunk)
-      const uint64_t pol_z = policy_evict_last();
-      uint32_t issued = 0, parity = 0;
-      int slot = 0;
-      uint32_t phase = 0;
-      for (int64_t j = 0; j < total && !*abort_flag; ++j) {
-        if (j >= C::ZSTAGES &&
-            !mbar_wait_idle(smem_u32(&sm->zempty[slot]), phase ^ 1, abort_flag, 64))
-          break;
-        int tm, rc, s;
-        item_of(j, &tm, &rc, &s);
-        const uint32_t fb = smem_u32(&sm->zfull[slot]);
-        mbar_expect_tx(fb, C::ZSTAGE);
-        for (int u = 0; u < LP_SUB; ++u)
-          tma_load_2d(base + slot * C::ZSTAGE + u * C::Z_TILE, &map_z, fb, s * LP_KS + 64 * u,
-                      rc * BN, pol_z);
-        issued |= 1u << slot;
-        parity = (parity & ~(1u << slot)) | (phase << slot);
-        if (++slot == C::ZSTAGES) { slot = 0; phase ^= 1; }
-      }
-      sm->z_issued = issued;
-      sm->z_parity = parity;
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer --------
     pdl_wait();
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_mn<BM, BN>();
-      int slot = 0, zs = 0, acc = 0;
-      uint32_t a_phase = 0, z_phase = 0, acc_phase = 0;
-      bool ok = !(C::ZRES && my_items > 0) ||
-                mbar_wait(smem_u32(&sm->zfull[0]), 0, abort_flag);   // the resident rows
+      int slot = 0, acc = 0;
+      uint32_t a_phase = 0, acc_phase = 0;
+      bool ok = my_items == 0 || mbar_wait(smem_u32(&sm->zfull), 0, abort_flag);   // the rows
       for (int i = 0; i < my_items && ok; ++i) {
         if (!mbar_wait_idle(smem_u32(&sm->acc_empty[acc]), acc_phase ^ 1, abort_flag, 64)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
         for (int s = 0; s < n_st && ok; ++s) {
-          if (!mbar_wait(smem_u32(&sm->a_full[slot]), a_phase, abort_flag) ||
-              (!C::ZRES && !mbar_wait(smem_u32(&sm->zfull[zs]), z_phase, abort_flag))) {
+          if (!mbar_wait(smem_u32(&sm->a_full[slot]), a_phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -317,8 +283,7 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
           for (int u = 0; u < LP_SUB; ++u) {
             const int g = s * LP_SUB + u;   // 64-K sub-block of the item
             // the descriptor's start address counts 16-byte units: +2 per 16 K
-            const uint64_t bd = sw128_desc(
-                base + (C::ZRES ? g * C::Z_TILE : zs * C::ZSTAGE + u * C::Z_TILE));
+            const uint64_t bd = sw128_desc(base + g * C::Z_TILE);
             const uint32_t au = a + u * 32;
             if (g == 0)
               umma_bf16_tmem_a(d, au, bd, idesc, 0u);
@@ -328,10 +293,6 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
             for (int kk = 1; kk < 4; ++kk) umma_bf16_tmem_a_acc(d, au + kk * 8, bd + 2 * kk, idesc);
           }
           umma_commit(smem_u32(&sm->a_empty[slot]));
-          if (!C::ZRES) {
-            umma_commit(smem_u32(&sm->zempty[zs]));
-            if (++zs == C::ZSTAGES) { zs = 0; z_phase ^= 1; }
-          }
           if (++slot == C::A_SLOTS) { slot = 0; a_phase ^= 1; }
         }
         if (!ok) break;
@@ -348,8 +309,7 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int i = 0; i < my_items; ++i) {
-      const int it = (int)blockIdx.x + i * G;
-      const int tm = it / n_rc, rc = it % n_rc;
+      const int tm = (int)blockIdx.x + i * G;
       const int f = tm * BM + q * 32 + lane;
       if (!epi_all(mbar_wait_idle(smem_u32(&sm->acc_full[acc]), acc_phase, abort_flag, 256)))
         break;
@@ -364,12 +324,12 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
           if (p.wscale && f < p.n_w) sc *= p.wscale[f];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int a = rc * BN + cb + e;
+            const int a = cb + e;
             if (a < p.m_act && f < p.n_w)
               static_cast<float *>(p.out)[(int64_t)a * p.ldo + f] = v[e] * sc;
           }
         } else {
-          finish16<EPI_TC_LMHEAD>(p, &sm->epi, v, f, tm, rc * BN + cb, q, lane, et);
+          finish16<EPI_TC_LMHEAD>(p, &sm->epi, v, f, tm, cb, q, lane, et);
         }
       }
       tc_fence_before();
@@ -450,12 +410,11 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
     // let this CTA's own copies land before its shared memory goes away
     if (threadIdx.x == 0) {
       atomicOr(p.status, ST_TIMEOUT);
-      for (int s = 0; s < C::CSTAGES + (C::ZRES ? 1 : C::ZSTAGES); ++s) {
+      for (int s = 0; s <= C::CSTAGES; ++s) {
         const bool code = s < C::CSTAGES;
-        const int k = code ? s : s - C::CSTAGES;
-        if (!(((code ? sm->c_issued : sm->z_issued) >> k) & 1u)) continue;
-        const uint32_t par = ((code ? sm->c_parity : sm->z_parity) >> k) & 1u;
-        const uint32_t bar = smem_u32(code ? &sm->cfull[k] : &sm->zfull[k]);
+        if (!(code ? (sm->c_issued >> s) & 1u : sm->z_issued)) continue;
+        const uint32_t par = code ? (sm->c_parity >> s) & 1u : 0u;
+        const uint32_t bar = smem_u32(code ? &sm->cfull[s] : &sm->zfull);
         const uint64_t t0 = global_ns();
         while (!mbar_test(bar, par) && global_ns() - t0 < 100000000ull) {
         }
@@ -477,51 +436,33 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
   }
 }
 
-template <int BN, int FMT>
+template <int FMT>
 cudaError_t launch_lp(const CUtensorMap &mc, const CUtensorMap &ms, const CUtensorMap &mz,
                       const GemmParams &p, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_lm_lowp<BN, FMT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         LpCfg<BN, FMT>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_lm_lowp<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         LpCfg<FMT>::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int n_items = p.tiles_m * ((p.m_act + BN - 1) / BN);
-  const int grid = n_items < num_sms() ? n_items : num_sms();
-  cudaError_t e = launch_pdl(k_lm_lowp<BN, FMT>, dim3(grid), dim3(LP_THREADS),
-                             LpCfg<BN, FMT>::SMEM, s, mc, ms, mz, p);
+  const int grid = p.tiles_m < num_sms() ? p.tiles_m : num_sms();
+  cudaError_t e = launch_pdl(k_lm_lowp<FMT>, dim3(grid), dim3(LP_THREADS), LpCfg<FMT>::SMEM, s,
+                             mc, ms, mz, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int FMT>
-cudaError_t launch_fmt(int bn, const CUtensorMap &mc, const CUtensorMap &ms,
-                       const CUtensorMap &mz, const GemmParams &p, cudaStream_t s) {
-  switch (bn) {
-    case 16: return launch_lp<16, FMT>(mc, ms, mz, p, s);
-    case 32: return launch_lp<32, FMT>(mc, ms, mz, p, s);
-    case 64: return launch_lp<64, FMT>(mc, ms, mz, p, s);
-  }
-  return cudaErrorInvalidValue;
-}
-
 }  // namespace
 
-int lm_lowp_bn(int m_act, int k) {
-  if (m_act <= 16 && k <= LP_K_RES) return 16;
-  return m_act <= 32 ? 32 : 64;
-}
-
-int lm_lowp_k_step(int) { return LP_KS; }
+bool lm_lowp_fits(int m_act, int k) { return m_act <= LP_BN && k <= LP_K_RES && k % LP_KS == 0; }
 
 cudaError_t lm_lowp(int fmt, const CUtensorMap &map_codes, const CUtensorMap &map_scales,
-                    const CUtensorMap &map_z, int bn, const GemmParams &p, cudaStream_t s) {
+                    const CUtensorMap &map_z, const GemmParams &p, cudaStream_t s) {
   if (p.m_act <= 0) return cudaSuccess;
-  if (p.k <= 0 || p.k % LP_KS != 0 || (bn == 16 && p.k > LP_K_RES)) return cudaErrorInvalidValue;
-  if (fmt == LM_LOWP_FP8) return launch_fmt<LM_LOWP_FP8>(bn, map_codes, map_scales, map_z, p, s);
-  if (fmt == LM_LOWP_NVFP4) return launch_fmt<LM_LOWP_NVFP4>(bn, map_codes, map_scales, map_z, p, s);
+  if (!lm_lowp_fits(p.m_act, p.k)) return cudaErrorInvalidValue;
+  if (fmt == LM_LOWP_FP8) return launch_lp<LM_LOWP_FP8>(map_codes, map_scales, map_z, p, s);
+  if (fmt == LM_LOWP_NVFP4) return launch_lp<LM_LOWP_NVFP4>(map_codes, map_scales, map_z, p, s);
   return cudaErrorInvalidValue;
 }
 

@@ -257,6 +257,10 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
               for (int c = 0; c < 16; ++c) x[c] *= (v0 + c < p.n_w) ? __ldg(p.wscale + v0 + c) : 0.f;
             }
           }
+          if (p.gscale != 0.f) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) x[c] *= p.gscale;
+          }
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             x[c] = (v0 + c < p.n_w && ((bits >> c) & 1u)) ? x[c] : -INFINITY;

@@ -1,16 +1,18 @@
-"""GPU parity of the lm_head streamed as codes ([P1] fields
-lm_head_shared_fp8 and lm_head_nvfp4): FP8 E4M3 codes with per-row scales
-and NVFP4 (E2M1 codes, E4M3 scales per 16 elements, a global scale),
-dequantised on chip into tensor memory; the oracle multiplies by the
+"""GPU parity of the low-precision lm_heads ([P1] fields lm_head_shared_fp8
+and lm_head_nvfp4): FP8 E4M3 codes with per-row scales and NVFP4 (E2M1
+codes, E4M3 scales per 16 elements, a global scale). Up to 16 draft rows the
+codes stream and are dequantised on chip into tensor memory; wider proposes
+multiply by the table widened to bf16 once. The oracle multiplies by the
 dequantised table in float64.
 
-The dequantisation is exact (every E4M3 value and every E2M1 x E4M3 product
-is a bf16 value), so the logits match the oracle's to the fp32 accumulation
-of a bf16 GEMM: the bf16 tolerance applies, not the FP8 one. Covered: a few
-draft rows (one 16-row chunk), many rows in one 128-row chunk and in two, the
-debug logit tap, the grammar bitmask, and the shipped geometry with
-sharpened logits (top-1 probabilities across 1e-3 .. 1), teacher-forced from
-the GPU's own final-normed rows."""
+Both dequantisations are exact (every E4M3 value and every E2M1 x E4M3
+product is a bf16 and an f16 value), so the logits match the oracle's to the
+fp32 accumulation of a 16-bit GEMM: the bf16 tolerance applies, not the FP8
+one. Covered: one sequence (the streamed kernel), 24 / 72 / 144 draft rows
+(the widened table on the few-row GEMM and on the many-row kernel, with
+bitmasks), the debug logit tap, and the shipped geometry with sharpened
+logits (top-1 probabilities across 1e-3 .. 1), teacher-forced from the GPU's
+own final-normed rows."""
 import pytest
 import torch
 
@@ -50,10 +52,10 @@ def test_tiny_single_sequence(fmt):
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
-@pytest.mark.parametrize("n", [24, 48])
+@pytest.mark.parametrize("n", [8, 24, 48])
 def test_tiny_many_rows(fmt, n):
-    """n sequences x 3 drafts: 72 draft rows (one 128-row chunk) or 144 (two
-    chunks, the second ragged), with a bitmask per sequence."""
+    """n sequences x 3 drafts: 24, 72 or 144 draft rows over the widened
+    table, with a bitmask per sequence."""
     pair = _pair(fmt, 1303 + n, cfg_kw=dict(max_batch=n))
     ctx = syn.uniform_ints(5, 30, n, 1303, 1)
     so, sl = [], []
