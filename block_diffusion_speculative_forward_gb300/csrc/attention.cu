@@ -6,7 +6,7 @@
 //
 // Split-KV: the host cuts every (sequence, kv head) key range into chunks;
 // each CTA takes one chunk and holds the whole group's gamma x (nq/nkv) query
-// vectors (<= 128) as one Q tile. QK^T and PV run on tensor cores
+// vectors (<= 128) as one Q tile of 64 or 128 rows. QK^T and PV run on tensor cores
 // (mma.sync m16n8k16, bf16 in, f32 accumulate) with an online softmax in
 // registers; K/V tiles of 32 keys stream through a double-buffered cp.async
 // ring. A pair cut into several chunks writes unnormalised partials
@@ -20,7 +20,7 @@ namespace dfl {
 
 namespace {
 
-constexpr int QT = 128;     // query vectors per CTA (rows of the Q tile)
+constexpr int QT = 128;     // query vectors per CTA at most (rows of the Q tile)
 constexpr int KT = 32;      // keys per K/V tile
 constexpr int THREADS = 128;
 
@@ -66,22 +66,85 @@ __device__ __forceinline__ float fp8_to_float(uint8_t c) {
   return __half2float(__half(hr));
 }
 
-template <int D>
+template <int D, int QR = QT>
 struct Smem {
   static constexpr int LD = D + 8;   // padded row (bf16): conflict-free ldmatrix
-  bf16 q[QT * LD];
+  bf16 q[QR * LD];
   bf16 k[2][KT * LD];
   bf16 v[2][KT * LD];
 };
+// FP8 ctx keys: the raw E4M3 codes of both stages land here asynchronously
+// (16 codes per copy) and are widened into the bf16 stages after their wait.
+template <int D>
+struct SmemRaw {
+  uint8_t k[2][KT * D];
+  uint8_t v[2][KT * D];
+};
+template <int D, bool FP8, int MT>
+constexpr int attn_smem_bytes() {
+  return (int)sizeof(Smem<D, 64 * MT>) + (FP8 ? (int)sizeof(SmemRaw<D>) : 0);
+}
 
 // Loads keys [kt, kt+KT) of the item (key index space: [0, n_ctx) ctx rows at
 // positions ws.., then the gamma block rows) into one K/V stage. Keys past
 // k1 are zero-filled (and masked by the caller).
-template <int D, bool FP8>
+template <int D>
+__device__ __forceinline__ void load_kv_tile_fp8(const AttnArgs &a, const AttnItem &it,
+                                                 const SeqMeta &sm, SmemRaw<D> *raw, int stage,
+                                                 int kt, int *status) {
+  constexpr int CH = D / 16;   // 16-byte chunks per row (E4M3 codes)
+  const Geo &g = a.g;
+  for (int idx = threadIdx.x; idx < KT * CH; idx += THREADS) {
+    const int r = idx / CH, c = idx % CH;
+    const int kk = kt + r;
+    const bool valid = kk < it.k1;   // (a window item: every valid key is a ctx key)
+    int64_t ko = 0, vo = 0;
+    if (valid) {
+      const int pos = sm.ws + kk;
+      int page = a.page_ids[sm.page_base + (pos / g.B - sm.ws / g.B)];
+      if (page < 0 || page >= g.pages) {
+        atomicOr(status, ST_PAGE);
+        page = 0;
+      }
+      ko = kv_offset(g, page, a.layer, 0, it.g, pos % g.B) + c * 16;
+      vo = kv_offset(g, page, a.layer, 1, it.g, pos % g.B) + c * 16;
+    }
+    // a padding key past k1 lands as zero codes (masked out by the caller)
+    cp_async16(smem_u32(raw->k[stage] + r * D + c * 16), (const uint8_t *)a.pool + ko, valid);
+    cp_async16(smem_u32(raw->v[stage] + r * D + c * 16), (const uint8_t *)a.pool + vo, valid);
+  }
+}
+
+// The raw codes of one stage (every thread's copies complete and visible)
+// widened exactly into the bf16 K/V stage.
+template <int D, int QR>
+__device__ __forceinline__ void widen_kv_stage(const SmemRaw<D> *raw, Smem<D, QR> *sh, int stage) {
+  constexpr int LD = Smem<D, QR>::LD;
+  constexpr int CH = D / 16;
+  for (int idx = threadIdx.x; idx < 2 * KT * CH; idx += THREADS) {
+    const bool is_v = idx >= KT * CH;
+    const int i = is_v ? idx - KT * CH : idx;
+    const int r = i / CH, c = i % CH;
+    const uint4 src = *reinterpret_cast<const uint4 *>((is_v ? raw->v[stage] : raw->k[stage]) +
+                                                       r * D + c * 16);
+    const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      o[2 * e] = pack_bf16(fp8_to_float(w[e] & 0xFF), fp8_to_float((w[e] >> 8) & 0xFF));
+      o[2 * e + 1] = pack_bf16(fp8_to_float((w[e] >> 16) & 0xFF), fp8_to_float(w[e] >> 24));
+    }
+    bf16 *dst = (is_v ? sh->v[stage] : sh->k[stage]) + r * LD + c * 16;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <int D, bool FP8, int QR>
 __device__ __forceinline__ void load_kv_tile(const AttnArgs &a, const AttnItem &it,
-                                             const SeqMeta &sm, Smem<D> *sh, int stage, int kt,
-                                             int *status) {
-  constexpr int LD = Smem<D>::LD;
+                                             const SeqMeta &sm, Smem<D, QR> *sh, int stage,
+                                             int kt, int *status) {
+  constexpr int LD = Smem<D, QR>::LD;
   constexpr int CH = D / 8;   // 16-byte chunks per row (bf16)
   const Geo &g = a.g;
   const int n_ctx = sm.pos - sm.ws;
@@ -137,15 +200,17 @@ __device__ __forceinline__ void load_kv_tile(const AttnArgs &a, const AttnItem &
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int MT>
 __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
   if ((int)blockIdx.x >= a.counts[0]) return;   // grid sized for the capacity
   pdl_trigger();
   pdl_wait();
-  constexpr int LD = Smem<D>::LD;
+  using SM = Smem<D, 64 * MT>;
+  constexpr int LD = SM::LD;
   constexpr int NT = D / 8;          // n8 tiles across the head dim (output)
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  Smem<D> *sh = reinterpret_cast<Smem<D> *>(smem_raw);
+  SM *sh = reinterpret_cast<SM *>(smem_raw);
+  SmemRaw<D> *raw = reinterpret_cast<SmemRaw<D> *>(smem_raw + sizeof(SM));
   const AttnItem it = a.items[blockIdx.x];
   const SeqMeta sm = a.seq[it.s];
   const Geo &g = a.g;
@@ -156,7 +221,7 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
   const int gid = lane >> 2, tig = lane & 3;
 
   // Q tile: query vector qv = i * grp + hh is row i of the block, head g*grp+hh.
-  for (int idx = threadIdx.x; idx < QT * (D / 8); idx += THREADS) {
+  for (int idx = threadIdx.x; idx < 64 * MT * (D / 8); idx += THREADS) {
     const int r = idx / (D / 8), c = idx % (D / 8);
     bf16 *dst = sh->q + r * LD + c * 8;
     const bool valid = r < n_q;
@@ -171,48 +236,58 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
   }
   const float qk_scale = a.scale * sk;
   const int n_tiles = (it.k1 - it.k0 + KT - 1) / KT;
-  load_kv_tile<D, FP8>(a, it, sm, sh, 0, it.k0, a.status);
+  // FP8 ctx keys stream as raw codes (widened per stage below)
+  const bool raw_kv = FP8 && is_ctx;
+  auto load = [&](int stage, int kt) {
+    if (raw_kv) load_kv_tile_fp8<D>(a, it, sm, raw, stage, kt, a.status);
+    else load_kv_tile<D, FP8, 64 * MT>(a, it, sm, sh, stage, kt, a.status);
+  };
+  load(0, it.k0);
   cp_commit();
 
-  float acc[2][NT][4];
+  float acc[MT][NT][4];
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-  float row_m[2][2], row_l[2][2];   // [m-tile][row gid / gid+8]
+  float row_m[MT][2], row_l[MT][2];   // [m-tile][row gid / gid+8]
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt) {
+  for (int mt = 0; mt < MT; ++mt) {
     row_m[mt][0] = row_m[mt][1] = -INFINITY;
     row_l[mt][0] = row_l[mt][1] = 0.f;
   }
-  const int qrow0 = warp * 32;   // this warp's 32 query rows
+  const int qrow0 = warp * 16 * MT;   // this warp's 16 MT query rows
 
   for (int t = 0; t < n_tiles; ++t) {
     const int stage = t & 1;
     if (t + 1 < n_tiles) {
-      load_kv_tile<D, FP8>(a, it, sm, sh, stage ^ 1, it.k0 + (t + 1) * KT, a.status);
+      load(stage ^ 1, it.k0 + (t + 1) * KT);
       cp_commit();
       cp_wait<1>();
     } else {
       cp_wait<0>();
     }
     __syncthreads();
+    if (raw_kv) {
+      widen_kv_stage<D, 64 * MT>(raw, sh, stage);
+      __syncthreads();
+    }
     const int kt = it.k0 + t * KT;
     // S = Q K^T for this warp's 32 rows x 32 keys
-    float s[2][4][4];
+    float s[MT][4][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[mt][j][e] = 0.f;
 #pragma unroll
     for (int k0 = 0; k0 < D; k0 += 16) {
-      uint32_t af[2][4];
+      uint32_t af[MT][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < MT; ++mt) {
         const int row = qrow0 + mt * 16 + (lane & 15);
         const int col = k0 + (lane >> 4) * 8;
         ldsm_x4(smem_u32(sh->q + row * LD + col), af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
@@ -224,7 +299,7 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
         const int col = k0 + ((lane >> 3) & 1) * 8;
         ldsm_x4(smem_u32(sh->k[stage] + key * LD + col), b0, b1, b2, b3);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
           mma16816(s[mt][2 * jp], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
           mma16816(s[mt][2 * jp + 1], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b2, b3);
         }
@@ -232,7 +307,7 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
     }
     // online softmax over the tile's keys (masking keys >= k1)
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {   // row gid (h=0) or gid+8 (h=1)
         float mx = -INFINITY;
@@ -274,9 +349,9 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
     // O += P V  (P from the S registers, values scaled by sv for FP8 ctx)
 #pragma unroll
     for (int kc = 0; kc < 2; ++kc) {   // 16-key slices of the tile
-      uint32_t pa[2][4];
+      uint32_t pa[MT][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < MT; ++mt) {
         pa[mt][0] = pack_bf16(s[mt][2 * kc][0] * sv, s[mt][2 * kc][1] * sv);
         pa[mt][1] = pack_bf16(s[mt][2 * kc][2] * sv, s[mt][2 * kc][3] * sv);
         pa[mt][2] = pack_bf16(s[mt][2 * kc + 1][0] * sv, s[mt][2 * kc + 1][1] * sv);
@@ -289,7 +364,7 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
         const int col = np * 16 + (lane >> 4) * 8;
         ldsm_x4_t(smem_u32(sh->v[stage] + key * LD + col), b0, b1, b2, b3);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < MT; ++mt) {
           mma16816(acc[mt][2 * np], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b0, b1);
           mma16816(acc[mt][2 * np + 1], pa[mt][0], pa[mt][1], pa[mt][2], pa[mt][3], b2, b3);
         }
@@ -300,7 +375,7 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
 
   // epilogue: direct output, or partials for the merge
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt) {
+  for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int qv = qrow0 + mt * 16 + gid + 8 * h;
@@ -407,17 +482,17 @@ __global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
         __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int MT>
 cudaError_t launch(const AttnArgs &a, cudaStream_t s) {
-  const int smem = (int)sizeof(Smem<D>);
+  const int smem = attn_smem_bytes<D, FP8, MT>();
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_split<D, FP8>,
+    cudaError_t e = cudaFuncSetAttribute(k_attn_split<D, FP8, MT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  launch_pdl(k_attn_split<D, FP8>, dim3(a.n_items), dim3(THREADS), smem, s, a);
+  launch_pdl(k_attn_split<D, FP8, MT>, dim3(a.n_items), dim3(THREADS), smem, s, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return attention_merge(a, s);
@@ -439,9 +514,16 @@ cudaError_t attention_merge(const AttnArgs &a, cudaStream_t s) {
 
 cudaError_t attention_split(const AttnArgs &a, cudaStream_t s) {
   if (a.n_items <= 0) return cudaSuccess;
-  if (attn_query_rows(a.g) > QT) return cudaErrorInvalidValue;
-  if (a.g.d == 128) return a.g.kv_fp8 ? launch<128, true>(a, s) : launch<128, false>(a, s);
-  if (a.g.d == 64) return a.g.kv_fp8 ? launch<64, true>(a, s) : launch<64, false>(a, s);
+  const int rows = attn_query_rows(a.g);
+  if (rows > QT) return cudaErrorInvalidValue;
+  // a Q tile of 64 rows when the group's queries fit (half the MMA work)
+  if (rows <= 64) {
+    if (a.g.d == 128) return a.g.kv_fp8 ? launch<128, true, 1>(a, s) : launch<128, false, 1>(a, s);
+    if (a.g.d == 64) return a.g.kv_fp8 ? launch<64, true, 1>(a, s) : launch<64, false, 1>(a, s);
+  } else {
+    if (a.g.d == 128) return a.g.kv_fp8 ? launch<128, true, 2>(a, s) : launch<128, false, 2>(a, s);
+    if (a.g.d == 64) return a.g.kv_fp8 ? launch<64, true, 2>(a, s) : launch<64, false, 2>(a, s);
+  }
   return cudaErrorInvalidValue;
 }
 
