@@ -710,6 +710,8 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       an.x_tap = B.tap_x ? B.tap_x + (size_t)l * R * g.H : nullptr;
       LK(add_norm(an, R, s));
     }
+    // (at batch 1 the partials and a separate norm + RoPE pass measured
+    // faster than the fused stream-K epilogue: 757 vs 791 us per step)
     const bool part = !dp && tc::partial_ok(R, g.qkv_w, g.H);
     if (dp) {
       // whole-tile QKV into a dense f32 buffer, then per-head q/k RMSNorm + RoPE
