@@ -73,25 +73,30 @@ struct Smem {
   bf16 k[2][KT * LD];
   bf16 v[2][KT * LD];
 };
-// FP8 ctx keys: the raw E4M3 codes of both stages land here asynchronously
-// (16 codes per copy) and are widened into the bf16 stages after their wait.
-template <int D>
+// FP8 ctx keys: the raw E4M3 codes land here asynchronously (16 codes per
+// copy), RS - 1 tiles ahead of the one being computed, and each tile is
+// widened into a bf16 stage after its wait.
+template <int MT>
+constexpr int raw_stages() {
+  return 2;   // (deeper rings measured slower: they cost a resident CTA per SM)
+}
+template <int D, int RS>
 struct SmemRaw {
-  uint8_t k[2][KT * D];
-  uint8_t v[2][KT * D];
+  uint8_t k[RS][KT * D];
+  uint8_t v[RS][KT * D];
 };
 template <int D, bool FP8, int MT>
 constexpr int attn_smem_bytes() {
-  return (int)sizeof(Smem<D, 64 * MT>) + (FP8 ? (int)sizeof(SmemRaw<D>) : 0);
+  return (int)sizeof(Smem<D, 64 * MT>) + (FP8 ? (int)sizeof(SmemRaw<D, raw_stages<MT>()>) : 0);
 }
 
 // Loads keys [kt, kt+KT) of the item (key index space: [0, n_ctx) ctx rows at
 // positions ws.., then the gamma block rows) into one K/V stage. Keys past
 // k1 are zero-filled (and masked by the caller).
-template <int D>
+template <int D, int RS>
 __device__ __forceinline__ void load_kv_tile_fp8(const AttnArgs &a, const AttnItem &it,
-                                                 const SeqMeta &sm, SmemRaw<D> *raw, int stage,
-                                                 int kt, int *status) {
+                                                 const SeqMeta &sm, SmemRaw<D, RS> *raw,
+                                                 int stage, int kt, int *status) {
   constexpr int CH = D / 16;   // 16-byte chunks per row (E4M3 codes)
   const Geo &g = a.g;
   for (int idx = threadIdx.x; idx < KT * CH; idx += THREADS) {
@@ -115,17 +120,18 @@ __device__ __forceinline__ void load_kv_tile_fp8(const AttnArgs &a, const AttnIt
   }
 }
 
-// The raw codes of one stage (every thread's copies complete and visible)
-// widened exactly into the bf16 K/V stage.
-template <int D, int QR>
-__device__ __forceinline__ void widen_kv_stage(const SmemRaw<D> *raw, Smem<D, QR> *sh, int stage) {
+// The raw codes of raw stage rs (every thread's copies complete and
+// visible) widened exactly into the bf16 K/V stage.
+template <int D, int RS, int QR>
+__device__ __forceinline__ void widen_kv_stage(const SmemRaw<D, RS> *raw, int rs,
+                                               Smem<D, QR> *sh, int stage) {
   constexpr int LD = Smem<D, QR>::LD;
   constexpr int CH = D / 16;
   for (int idx = threadIdx.x; idx < 2 * KT * CH; idx += THREADS) {
     const bool is_v = idx >= KT * CH;
     const int i = is_v ? idx - KT * CH : idx;
     const int r = i / CH, c = i % CH;
-    const uint4 src = *reinterpret_cast<const uint4 *>((is_v ? raw->v[stage] : raw->k[stage]) +
+    const uint4 src = *reinterpret_cast<const uint4 *>((is_v ? raw->v[rs] : raw->k[rs]) +
                                                        r * D + c * 16);
     const uint32_t w[4] = {src.x, src.y, src.z, src.w};
     uint32_t o[8];
@@ -210,7 +216,8 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
   constexpr int NT = D / 8;          // n8 tiles across the head dim (output)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SM *sh = reinterpret_cast<SM *>(smem_raw);
-  SmemRaw<D> *raw = reinterpret_cast<SmemRaw<D> *>(smem_raw + sizeof(SM));
+  constexpr int RS = raw_stages<MT>();
+  SmemRaw<D, RS> *raw = reinterpret_cast<SmemRaw<D, RS> *>(smem_raw + sizeof(SM));
   const AttnItem it = a.items[blockIdx.x];
   const SeqMeta sm = a.seq[it.s];
   const Geo &g = a.g;
@@ -238,12 +245,16 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
   const int n_tiles = (it.k1 - it.k0 + KT - 1) / KT;
   // FP8 ctx keys stream as raw codes (widened per stage below)
   const bool raw_kv = FP8 && is_ctx;
-  auto load = [&](int stage, int kt) {
-    if (raw_kv) load_kv_tile_fp8<D>(a, it, sm, raw, stage, kt, a.status);
-    else load_kv_tile<D, FP8, 64 * MT>(a, it, sm, sh, stage, kt, a.status);
-  };
-  load(0, it.k0);
-  cp_commit();
+  if (raw_kv) {
+    // one copy group per tile, RS - 1 tiles ahead (empty groups past the end)
+    for (int i = 0; i < RS - 1; ++i) {
+      if (i < n_tiles) load_kv_tile_fp8<D, RS>(a, it, sm, raw, i, it.k0 + i * KT, a.status);
+      cp_commit();
+    }
+  } else {
+    load_kv_tile<D, FP8, 64 * MT>(a, it, sm, sh, 0, it.k0, a.status);
+    cp_commit();
+  }
 
   float acc[MT][NT][4];
 #pragma unroll
@@ -262,16 +273,23 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
 
   for (int t = 0; t < n_tiles; ++t) {
     const int stage = t & 1;
-    if (t + 1 < n_tiles) {
-      load(stage ^ 1, it.k0 + (t + 1) * KT);
-      cp_commit();
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
-    __syncthreads();
     if (raw_kv) {
-      widen_kv_stage<D, 64 * MT>(raw, sh, stage);
+      const int ahead = t + RS - 1;
+      if (ahead < n_tiles)
+        load_kv_tile_fp8<D, RS>(a, it, sm, raw, ahead % RS, it.k0 + ahead * KT, a.status);
+      cp_commit();
+      cp_wait<RS - 1>();   // tile t's group has landed
+      __syncthreads();
+      widen_kv_stage<D, RS, 64 * MT>(raw, t % RS, sh, stage);
+      __syncthreads();
+    } else {
+      if (t + 1 < n_tiles) {
+        load_kv_tile<D, FP8, 64 * MT>(a, it, sm, sh, stage ^ 1, it.k0 + (t + 1) * KT, a.status);
+        cp_commit();
+        cp_wait<1>();
+      } else {
+        cp_wait<0>();
+      }
       __syncthreads();
     }
     const int kt = it.k0 + t * KT;

@@ -275,8 +275,6 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
     }
     // slots start on 16 bytes (vector stores and loads of partial rows)
     B->attn_slot_floats = ((int64_t)n_q * g.d + 2 * n_q + 3) & ~(int64_t)3;
-    B->attn_slots = 3 * sms + 3 * c.max_batch * g.nkv + 64;
-    BA(B->attn_ws, (size_t)B->attn_slots * B->attn_slot_floats);
     // The tensor-core kernel reads whole 16-row blocks of the block K/V
     // rows (masked past gamma): keep never-written rows finite.
     BK(cudaMemset(B->kb, 0, sizeof(bf16) * (size_t)R_max * kv));
@@ -286,6 +284,8 @@ int build_device_side(const dflash_config &c, const Geo &g, const dflash_weights
       return DFLASH_ECUDA;
     }
     B->attn_grid_tc = B->attn_maps.ok ? sms : 0;
+    B->attn_slots = attn_ctx_waves(B->attn_grid_tc) * sms + 3 * c.max_batch * g.nkv + 64;
+    BA(B->attn_ws, (size_t)B->attn_slots * B->attn_slot_floats);
   }
   // TMA maps of the activation operands, one per tile width.
   {
@@ -976,6 +976,13 @@ cudaError_t gather_kv_rows(const Geo &g, const Weights &W, const Buffers &B, con
 
 namespace dfl {
 
+// Ctx items per SM the work split aims at: the persistent tensor-core kernel
+// balances its items over its CTAs itself (three per SM keep the merge
+// small); the split kernel launches one CTA per item, several resident per
+// SM, where whole windows as items leave a tail wave that doubles the layer
+// (measured at 128 sequences), so it gets finer items.
+int attn_ctx_waves(int grid_tc) { return grid_tc > 0 ? 3 : 8; }
+
 bool build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
                      std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
                      std::vector<int32_t> *cta_off) {
@@ -990,10 +997,11 @@ bool build_attn_work_sms(const Geo &g, const std::vector<SeqMeta> &seq, int slot
     total += (int64_t)(m.pos - m.ws) * g.nkv;
     longest = std::max<int64_t>(longest, (int64_t)(m.pos - m.ws) + m.ws % 64);
   }
-  // About three SM waves of ctx items, at least 64 keys each so the partial
-  // merge stays cheap. Chunk boundaries fall on positions that are multiples
-  // of 64, so every tile but a window's first starts on a page.
-  int64_t chunk = (total + 3 * sms - 1) / (3 * sms);
+  // About attn_ctx_waves SM waves of ctx items, at least 64 keys each so the
+  // partial merge stays cheap. Chunk boundaries fall on positions that are
+  // multiples of 64, so every tile but a window's first starts on a page.
+  const int64_t parts = (int64_t)attn_ctx_waves(grid_tc) * sms;
+  int64_t chunk = (total + parts - 1) / parts;
   chunk = std::max<int64_t>(64, (chunk + 63) / 64 * 64);
   for (;;) {
     items->clear();

@@ -96,6 +96,7 @@ struct Buffers {
 // of the tensor-core kernel: CTA b runs items [cta_off[b], cta_off[b + 1]).
 // Returns false (and no items) when even one chunk per window needs more
 // slots than slot_cap; a handle's capacity always holds its widest call.
+int attn_ctx_waves(int grid_tc);
 bool build_attn_work(const Geo &g, const std::vector<SeqMeta> &seq, int slot_cap, int grid_tc,
                      std::vector<AttnItem> *items, std::vector<AttnPair> *pairs,
                      std::vector<int32_t> *cta_off);
