@@ -40,16 +40,24 @@ namespace dfl {
 namespace tc {
 
 constexpr int NUM_THREADS = 192;
+// K elements per pipeline stage (iteration): two 64-element TMA boxes per
+// operand and 8 MMAs behind one commit. Every commit hand-off costs the MMA
+// issuer a fixed few hundred cycles (measured), which at one commit per 4
+// MMAs held the tensor pipe to about half its rate at N = 256 and left the
+// batch-1 weight stream little slack. A K that is not a multiple of 128 reads
+// an all-zero second box at its end (the copy's out-of-bounds fill).
+constexpr int KS = 2 * BK;
 
 template <int BN, int EPI>
 struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // Up to 64 rows: 8 stages (8 x 16 KB of weight tiles in flight per SM,
-  // which the batch-1 weight stream needs; deeper rings measured no faster).
-  // Partial mode reserves no exchange buffer.
+  static constexpr int HALF_BYTES = A_BYTES + B_BYTES;   // one 64-K box of each operand
+  static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
+  // Up to 64 rows: 4 stages (8 x 16 KB of weight tiles in flight per SM,
+  // which the batch-1 weight stream needs). Partial mode reserves no
+  // exchange buffer.
   static constexpr bool kPartial = (EPI == EPI_TC_PARTIAL);
-  static constexpr int STAGES = (BN <= 64) ? 8 : (BN <= 128 ? 6 : 4);
+  static constexpr int STAGES = (BN <= 64) ? 4 : (BN <= 128 ? 3 : 2);
   static_assert(STAGES <= 8, "the barrier arrays in Smem hold 8 stages");
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int EXTRA = kPartial ? 1536 : 10240;   // Smem (without / with xch)
@@ -96,7 +104,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   Smem *sm = (Smem *)(gbase + C::STAGES * C::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int kb = p.k / BK;
+  const int kb = (p.k + KS - 1) / KS;   // iterations (K steps) per tile
   const int tiles = p.tiles_m * p.tiles_n;
   const Part part{(int64_t)tiles * kb, (int)gridDim.x};
   // Iteration range of this CTA. Stream-K: a contiguous range of (tile,
@@ -160,7 +168,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int j = 0; j < n_pre; ++j) {
           const uint32_t fb = smem_u32(&sm->full[j]);
           mbar_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(base + j * C::STAGE_BYTES, &map_w, fb, k * BK, (t % p.tiles_m) * BM, pol_w);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(base + j * C::STAGE_BYTES + h * C::HALF_BYTES, &map_w, fb,
+                        k * KS + h * BK, (t % p.tiles_m) * BM, pol_w);
           issued |= 1u << j;
           if (++k == kb) { k = 0; t += t_step; }
         }
@@ -168,8 +179,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       pdl_wait();
       int t = t0, k = k0;
       for (int j = 0; j < n_pre; ++j) {
-        tma_load_2d(base + j * C::STAGE_BYTES + A_BYTES, &map_x, smem_u32(&sm->full[j]), k * BK,
-                    (t / p.tiles_m) * BN, pol_x);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_2d(base + j * C::STAGE_BYTES + h * C::HALF_BYTES + A_BYTES, &map_x,
+                      smem_u32(&sm->full[j]), k * KS + h * BK, (t / p.tiles_m) * BN, pol_x);
         if (++k == kb) { k = 0; t += t_step; }
       }
       int stage = n_pre % C::STAGES;
@@ -179,8 +192,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t sa = base + stage * C::STAGE_BYTES;
         const uint32_t fb = smem_u32(&sm->full[stage]);
         mbar_expect_tx(fb, C::STAGE_BYTES);
-        tma_load_2d(sa, &map_w, fb, k * BK, (t % p.tiles_m) * BM, pol_w);
-        tma_load_2d(sa + A_BYTES, &map_x, fb, k * BK, (t / p.tiles_m) * BN, pol_x);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tma_load_2d(sa + h * C::HALF_BYTES, &map_w, fb, k * KS + h * BK, (t % p.tiles_m) * BM,
+                      pol_w);
+          tma_load_2d(sa + h * C::HALF_BYTES + A_BYTES, &map_x, fb, k * KS + h * BK,
+                      (t / p.tiles_m) * BN, pol_x);
+        }
         issued |= 1u << stage;
         parity = (parity & ~(1u << stage)) | (phase << stage);
         if (++k == kb) { k = 0; t += t_step; }
@@ -212,11 +230,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t sa = base + stage * C::STAGE_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sw128_desc(sa + kk * 32);
-            const uint64_t bd = sw128_desc(sa + A_BYTES + kk * 32);
-            umma_bf16(d, ad, bd, idesc, (k > k0 || kk > 0) ? 1u : 0u);
-          }
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = sw128_desc(sa + h * C::HALF_BYTES + kk * 32);
+              const uint64_t bd = sw128_desc(sa + h * C::HALF_BYTES + A_BYTES + kk * 32);
+              umma_bf16(d, ad, bd, idesc, (k > k0 || h > 0 || kk > 0) ? 1u : 0u);
+            }
           umma_commit(smem_u32(&sm->empty[stage]));
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -487,10 +507,11 @@ int pick_bn(int m_act) {
 
 bool partial_ok(int m_act, int n_w, int k) {
   const int bn = pick_bn(m_act);
-  const int64_t total = (int64_t)((n_w + BM - 1) / BM) * ((m_act + bn - 1) / bn) * (k / BK);
+  const int ks = (k + KS - 1) / KS;
+  const int64_t total = (int64_t)((n_w + BM - 1) / BM) * ((m_act + bn - 1) / bn) * ks;
   int grid = num_sms();
   if (total < grid) grid = (int)total;
-  return grid > 0 && (total + grid - 1) / grid <= k / BK && total * grid < (1ll << 31);
+  return grid > 0 && (total + grid - 1) / grid <= ks && total * grid < (1ll << 31);
 }
 
 int pick_bn_dp(int m_act, int n_w, int k) {
@@ -522,7 +543,8 @@ cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, Gem
   if (p.k % BK) return cudaErrorInvalidValue;
   p.tiles_m = (p.n_w + BM - 1) / BM;
   p.tiles_n = (p.m_act + bn - 1) / bn;
-  const int64_t total = (int64_t)p.tiles_m * p.tiles_n * (p.k / BK);
+  const int ks = (p.k + KS - 1) / KS;
+  const int64_t total = (int64_t)p.tiles_m * p.tiles_n * ks;
   int grid = num_sms();
   if (p.grid_cap > 0 && p.grid_cap < grid) grid = p.grid_cap;
   if (p.dp) {
@@ -534,12 +556,12 @@ cudaError_t gemm(const CUtensorMap &map_w, const CUtensorMap &map_x, int bn, Gem
   if (total < grid) grid = (int)total;
   if (grid < 1) grid = 1;
   if (p.epi == EPI_TC_PARTIAL) {
-    if ((total + grid - 1) / grid > p.k / BK || !view) return cudaErrorInvalidValue;
+    if ((total + grid - 1) / grid > ks || !view) return cudaErrorInvalidValue;
     view->ws = p.ws;
     view->dense = nullptr;
     view->ld = 0;
     view->tiles_m = p.tiles_m;
-    view->kb = p.k / BK;
+    view->kb = ks;
     view->G = grid;
     view->bn = bn;
     view->total = (int)total;
