@@ -423,15 +423,17 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
 
 // One warp per (pair, query vector), 4 per block: combine the pair's chunks.
 // Lane c holds chunk c's (m, l) (32 chunks per round); the weights reach the
-// other lanes by shuffle, and every chunk's partial row is loaded before any
-// is used.
+// other lanes by shuffle. The partial rows do not depend on the maximum, so
+// the first MERGE_ROWS of them are loaded together with the (m, l) pairs: a
+// pair of up to MERGE_ROWS chunks takes one L2 round trip.
+constexpr int MERGE_ROWS = 24;
 template <int D>
 __global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
   if ((int)blockIdx.x >= a.counts[1]) return;   // grid sized for the capacity
   pdl_trigger();
+  const AttnPair pr = a.pairs[blockIdx.x];   // host-written: read before the wait
   pdl_wait();
   constexpr int VPL = D / 32;   // floats per lane
-  const AttnPair pr = a.pairs[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qv = blockIdx.y * 4 + warp;
   const Geo &g = a.g;
@@ -439,52 +441,50 @@ __global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
   const int n_q = g.gamma * grp;
   if (qv >= n_q) return;
   const int64_t off_m = (int64_t)n_q * D + qv, off_l = (int64_t)n_q * D + n_q + qv;
+  const float *ws0 = a.ws + (int64_t)pr.slot0 * a.slot_floats;
+  auto row4 = [&](int c) -> float4 {
+    const float *row = ws0 + (int64_t)c * a.slot_floats + (int64_t)qv * D + lane * VPL;
+    if constexpr (VPL == 4) return __ldcg(reinterpret_cast<const float4 *>(row));
+    else return make_float4(__ldcg(row), __ldcg(row + 1), 0.f, 0.f);
+  };
+  float4 r[MERGE_ROWS];
+#pragma unroll
+  for (int u = 0; u < MERGE_ROWS; ++u) r[u] = u < pr.nc ? row4(u) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float m0 = lane < pr.nc ? __ldcg(ws0 + (int64_t)lane * a.slot_floats + off_m) : -INFINITY;
+  const float l0 = lane < pr.nc ? __ldcg(ws0 + (int64_t)lane * a.slot_floats + off_l) : 0.f;
   // max over all chunks
-  float M = -INFINITY;
-  for (int c0 = 0; c0 < pr.nc; c0 += 32) {
-    const int c = c0 + lane;
-    if (c < pr.nc) M = fmaxf(M, __ldcg(a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats + off_m));
-  }
+  float M = m0;
+  for (int c = lane + 32; c < pr.nc; c += 32)
+    M = fmaxf(M, __ldcg(ws0 + (int64_t)c * a.slot_floats + off_m));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float l = 0.f;
-  float acc[VPL];
-#pragma unroll
-  for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int c0 = 0; c0 < pr.nc; c0 += 32) {
     const int c = c0 + lane;
     float w = 0.f;
     if (c < pr.nc) {
-      const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
-      const float m = __ldcg(ws + off_m);
+      const float *ws = ws0 + (int64_t)c * a.slot_floats;
+      const float m = c0 == 0 ? m0 : __ldcg(ws + off_m);
       w = (m == -INFINITY) ? 0.f : __expf(m - M);
-      l += w * __ldcg(ws + off_l);
+      l += w * (c0 == 0 ? l0 : __ldcg(ws + off_l));
     }
     const int nc = pr.nc - c0 < 32 ? pr.nc - c0 : 32;
-    // rows of up to 8 chunks in flight, added in chunk order
-    for (int b = 0; b < nc; b += 8) {
-      float4 r[8];
+    // chunk rows added in chunk order; the first batch is already loaded
+    for (int b = 0; b < nc; b += MERGE_ROWS) {
+      if (c0 > 0 || b > 0) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (b + u < nc) {
-          const float *row = a.ws + (int64_t)(pr.slot0 + c0 + b + u) * a.slot_floats +
-                             (int64_t)qv * D + lane * VPL;
-          if constexpr (VPL == 4) r[u] = __ldcg(reinterpret_cast<const float4 *>(row));
-          else r[u] = make_float4(__ldcg(row), __ldcg(row + 1), 0.f, 0.f);
-        } else {
-          r[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int u = 0; u < MERGE_ROWS; ++u)
+          r[u] = b + u < nc ? row4(c0 + b + u) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < MERGE_ROWS; ++u) {
         const float wu = __shfl_sync(0xffffffffu, w, (b + u) & 31);
         if (b + u < nc) {
           acc[0] += wu * r[u].x;
           acc[1] += wu * r[u].y;
-          if constexpr (VPL == 4) {
-            acc[2] += wu * r[u].z;
-            acc[3] += wu * r[u].w;
-          }
+          acc[2] += wu * r[u].z;
+          acc[3] += wu * r[u].w;
         }
       }
     }

@@ -104,6 +104,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint3
       : "memory");
 }
 
+// Pulls a 2D box of a tensor map into L2 (a hint: no shared memory, no
+// barrier, and later loads still see every write).
+__device__ __forceinline__ void tma_prefetch_l2(const void *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(x),
+               "r"(y)
+               : "memory");
+}
+
 // Descriptor of an MN-major operand in the 128-byte swizzle: rows of 64
 // consecutive N elements (128 B), 8 K-rows per 1024-byte atom; lbo = bytes
 // between 64-wide N blocks, sbo = bytes between 8-row K groups.
@@ -186,11 +194,35 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The work list, sequence table and page ids are written by the host before
+  // the launch, so they are read before waiting for the previous kernel: warp
+  // 0 reads its first item's and pulls that item's first KV_STAGES tiles of
+  // K/V pages into L2 (lane 4j + q: group q of tile j); the reads after the
+  // wait then hit L1 and L2.
+  const int c_begin = a.cta_off[blockIdx.x], c_end = a.cta_off[blockIdx.x + 1];
+  if (warp == 0 && c_begin < c_end) {
+    const AttnItem it = a.items[c_begin];
+    const SeqMeta sm = a.seq[it.s];
+    const ItemGeo ig = item_geo(it, sm, g.gamma);
+    const int j = lane >> 2, q = lane & 3;
+    if (!ig.block && j < KV_STAGES && j < ig.ntiles && ((group_mask(ig, j) >> q) & 1u)) {
+      const int pos = ig.p0 + j * AK + 16 * q;
+      const int page = a.page_ids[sm.page_base + pos / 16 - sm.ws / 16];
+      if (page >= 0 && page < g.pages) {
+        const int row_k = (((page * g.L + a.layer) * 2) * g.nkv + it.g) * 16;
+        const int row_v = row_k + g.nkv * 16;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tma_prefetch_l2(&map_pool, h * 64, row_k);
+          tma_prefetch_l2(&map_pool, h * 64, row_v);
+        }
+      }
+    }
+  }
   pdl_trigger();
   pdl_wait();
   const uint32_t tmem = bar->tmem_base;
   volatile int *abort_flag = &bar->abort_flag;
-  const int c_begin = a.cta_off[blockIdx.x], c_end = a.cta_off[blockIdx.x + 1];
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ------

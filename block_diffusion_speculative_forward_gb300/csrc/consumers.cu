@@ -23,15 +23,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 // One block of 1024 threads per row: x[a] (+)= y[a]; out = bf16(g * x / rms(x)).
 __global__ void __launch_bounds__(1024) k_add_norm(AddNormArgs p) {
   pdl_trigger();
-  pdl_wait();
   __shared__ float sh[32];
   __shared__ TileRange tr[32];
   const int a = blockIdx.x;
   const int n = p.n;
   constexpr int MAXE = 4;    // up to 4096 features per row
+  // contributor ranges depend on no earlier kernel: before the wait
   if (p.has_y && p.y.ws && threadIdx.x < (n + 127) / 128)
     tr[threadIdx.x] = part_range(p.y, part_tile(p.y, a, threadIdx.x * 128));
   __syncthreads();
+  pdl_wait();
   float xv[MAXE];
   float ss = 0.f;
 #pragma unroll
@@ -82,7 +83,6 @@ constexpr int NORM_CL = 8;
 __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
   namespace cg = cooperative_groups;
   pdl_trigger();
-  pdl_wait();
   __shared__ float red[8];
   __shared__ float cta_ss;
   cg::cluster_group cl = cg::this_cluster();
@@ -91,6 +91,21 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
   const int n = p.n, per = n / NORM_CL;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int MAXE = 2;   // up to 512 features per CTA
+  // contributor ranges and gains depend on no earlier kernel: before the wait
+  TileRange tr[MAXE];
+  float gv[MAXE];
+#pragma unroll
+  for (int t = 0; t < MAXE; ++t) {
+    const int fl = threadIdx.x + t * 256;
+    const int f = part * per + fl;
+    tr[t] = TileRange{};
+    gv[t] = 0.f;
+    if (fl < per) {
+      if (p.has_y && p.y.ws) tr[t] = part_range(p.y, part_tile(p.y, a, f & ~31));
+      gv[t] = __bfloat162float(p.g[f]);
+    }
+  }
+  pdl_wait();
   float xv[MAXE];
   float ss = 0.f;
 #pragma unroll
@@ -102,8 +117,7 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
       float v = p.x ? p.x[(int64_t)a * n + f] : 0.f;
       if (p.has_y) {
         if (p.y.ws) {
-          const TileRange tr = part_range(p.y, part_tile(p.y, a, f & ~31));
-          v += part_sum(p.y, tr, a, f);
+          v += part_sum(p.y, tr[t], a, f);
         } else {
           v += p.y.dense[(int64_t)a * p.y.ld + f];
         }
@@ -125,6 +139,9 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
   float tot = 0.f;
 #pragma unroll
   for (int r = 0; r < NORM_CL; ++r) tot += *cl.map_shared_rank(&cta_ss, r);
+  // the peers' sums are read (the release orders those loads): arrive now,
+  // wait before exiting, the stores in between
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   const float inv = rsqrtf(tot / (float)n + p.eps);
   int drow = -1;
   if (p.z) {
@@ -139,7 +156,7 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
       const float v = xv[t];
       if (p.x && p.has_y) p.x[(int64_t)a * n + f] = v;
       if (p.x_tap) p.x_tap[(int64_t)a * n + f] = v;
-      const bf16 h = __float2bfloat16_rn(__bfloat162float(p.g[f]) * (v * inv));
+      const bf16 h = __float2bfloat16_rn(gv[t] * (v * inv));
       if (p.out) p.out[(int64_t)a * n + f] = h;
       if (p.z_tap) p.z_tap[(int64_t)a * n + f] = h;
       if (drow >= 0) {
@@ -148,17 +165,47 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
       }
     }
   }
-  cl.sync();   // peers have read cta_ss
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // peers have read cta_ss
 }
 
 // Warp per (row, head): q and k heads take RMSNorm with their gain and RoPE at
-// the row's position; v is rounded to bf16.
+// the row's position. The last y-block of each row rounds its v features to
+// bf16 (its own CTA, so no head's CTA does two passes).
 template <int NP>
 __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
   pdl_trigger();
-  pdl_wait();
   const Geo &g = p.g;
   const int r = blockIdx.x;
+  if ((int)blockIdx.y == (g.nq + g.nkv + 7) / 8) {
+    // v rows: a warp's 32 consecutive features share one tile; the ranges
+    // depend on no earlier kernel (before the wait)
+    constexpr int MAXV = 4;
+    const int vbase = g.nq * g.d + g.kv;
+    for (int e0 = 0; e0 < g.kv; e0 += 256 * MAXV) {
+      TileRange tv[MAXV];
+#pragma unroll
+      for (int u = 0; u < MAXV; ++u) {
+        const int e = e0 + threadIdx.x + 256 * u;
+        tv[u] = TileRange{};
+        if (e < g.kv && p.y.ws) tv[u] = part_range(p.y, part_tile(p.y, r, (vbase + e) & ~31));
+      }
+      pdl_wait();
+      float y[MAXV];
+#pragma unroll
+      for (int u = 0; u < MAXV; ++u) {
+        const int e = e0 + threadIdx.x + 256 * u;
+        y[u] = 0.f;
+        if (e < g.kv)
+          y[u] = p.y.ws ? part_sum(p.y, tv[u], r, vbase + e) : p.y.dense[(int64_t)r * p.y.ld + vbase + e];
+      }
+#pragma unroll
+      for (int u = 0; u < MAXV; ++u) {
+        const int e = e0 + threadIdx.x + 256 * u;
+        if (e < g.kv) p.vb[(int64_t)r * g.kv + e] = __float2bfloat16_rn(y[u]);
+      }
+    }
+    return;
+  }
   const int head = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int d = g.d, half = d / 2;
@@ -170,7 +217,7 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
     // equals it): one contributor range for the warp
     TileRange tr{};
     if (p.y.ws) tr = part_range(p.y, part_tile(p.y, r, base));
-    // gains and the rotation, loaded while the partials are in flight
+    // the range, gains and rotation depend on no earlier kernel: before the wait
     const bf16 *gain = is_q ? p.q_norm : p.k_norm;
     float gn[2 * NP], cs[NP], sn[NP];
 #pragma unroll
@@ -181,6 +228,7 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
       cs[t] = p.cos_t[(int64_t)pos * half + i];
       sn[t] = p.sin_t[(int64_t)pos * half + i];
     }
+    pdl_wait();
     float v[2 * NP];
     float ss = 0.f;
 #pragma unroll
@@ -203,17 +251,6 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
       dst[i + half] = __float2bfloat16_rn(x2 * cs[t] + x1 * sn[t]);
     }
   }
-  if (blockIdx.y == 0) {
-    // v rows: a warp's 32 consecutive features share one tile
-    const int vbase = g.nq * d + g.kv;
-    for (int e = threadIdx.x; e < g.kv; e += blockDim.x) {
-      const int f = vbase + e;
-      float y;
-      if (p.y.ws) y = part_sum(p.y, part_range(p.y, part_tile(p.y, r, f & ~31)), r, f);
-      else y = p.y.dense[(int64_t)r * p.y.ld + f];
-      p.vb[(int64_t)r * g.kv + e] = __float2bfloat16_rn(y);
-    }
-  }
 }
 
 }  // namespace
@@ -229,7 +266,7 @@ cudaError_t add_norm(const AddNormArgs &p, int rows, cudaStream_t s) {
 }
 
 cudaError_t qkv_post(const QkvPostArgs &p, int R, cudaStream_t s) {
-  dim3 grid(R, (p.g.nq + p.g.nkv + 7) / 8);
+  dim3 grid(R, (p.g.nq + p.g.nkv + 7) / 8 + 1);   // + the v block
   if (p.g.d == 128) return launch_pdl(k_qkv_post<2>, grid, dim3(256), 0, s, p);
   if (p.g.d == 64) return launch_pdl(k_qkv_post<1>, grid, dim3(256), 0, s, p);
   return cudaErrorInvalidValue;
