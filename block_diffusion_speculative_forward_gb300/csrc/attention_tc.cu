@@ -496,14 +496,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float inv = 1.f / l;
       bf16 *orow = a.o + ((int64_t)(it.s * g.gamma + r / grp) * g.nq + it.g * grp + r % grp) * AD;
       float *ws = a.ws + (int64_t)(it.slot < 0 ? 0 : it.slot) * a.slot_floats;
-#pragma unroll
+      // Partial rows leave through this warp's 8 KB slice of the two P
+      // buffers (free once the item's last PV is done), 64 columns at a time:
+      // a thread stages its row (16-byte chunk c at c ^ (row % 8)), then each
+      // warp store covers two whole 256-byte row halves instead of 32
+      // scattered 16-byte pieces.
+      const uint32_t stg = base + OFF_P + (uint32_t)q4 * (32 * 256);
+#pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         float v[64];
 #pragma unroll
         for (int i = 0; i < 4; ++i) tmem_ld16_nowait(o_col + hh * 64 + 16 * i, v + 16 * i);
         tmem_wait_ld();
-        if (!write) continue;
         if (it.slot < 0) {
+          if (!write) continue;
 #pragma unroll
           for (int e = 0; e < 64; e += 8) {
             uint4 w;
@@ -514,10 +520,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             *reinterpret_cast<uint4 *>(orow + hh * 64 + e) = w;
           }
         } else {
-          float *arow = ws + (int64_t)r * AD + hh * 64;
 #pragma unroll
-          for (int e = 0; e < 64; e += 4)
-            *reinterpret_cast<float4 *>(arow + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          for (int c = 0; c < 16; ++c)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             stg + lane * 256 + ((uint32_t)(c ^ (lane & 7)) << 4)),
+                         "f"(v[4 * c]), "f"(v[4 * c + 1]), "f"(v[4 * c + 2]), "f"(v[4 * c + 3])
+                         : "memory");
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i = lane + 32 * k, rr = i >> 4, c = i & 15;
+            float4 x;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                         : "r"(stg + rr * 256 + ((uint32_t)(c ^ (rr & 7)) << 4))
+                         : "memory");
+            const int row = q4 * 32 + rr;
+            if (row < n_q)
+              *reinterpret_cast<float4 *>(ws + (int64_t)row * AD + hh * 64 + 4 * c) = x;
+          }
+          __syncwarp();
         }
       }
       if (write && it.slot >= 0) {
