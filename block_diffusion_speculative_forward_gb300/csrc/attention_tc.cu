@@ -226,77 +226,72 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ------
-    if (lane == 0) {
-      const uint64_t pol_kv = policy_evict_first();
-      const uint64_t pol_q = policy_evict_normal();
-      uint32_t q_issued = 0, q_par = 0, kv_issued = 0, kv_par = 0;
-      int stage = 0;
-      uint32_t kv_phase = 0;
-      int qi = 0;
-      for (int c = c_begin; c < c_end && !*abort_flag; ++c, ++qi) {
-        const AttnItem it = a.items[c];
-        const SeqMeta sm = a.seq[it.s];
-        const ItemGeo ig = item_geo(it, sm, g.gamma);
-        const int qb = qi & 1;
-        const uint32_t qph = (qi >> 1) & 1;
-        if (!mbar_wait(smem_u32(&bar->q_empty[qb]), qph ^ 1, abort_flag)) break;
+    // The whole warp runs the loop (each wait gives one answer per warp);
+    // lane 0 arms the barriers and issues Q, and the 16 boxes of a K/V tile
+    // (group q, half h, K or V) are issued in parallel by lanes 4q + 2h + kv:
+    // one thread issuing them back to back took ~2 us per tile.
+    const uint64_t pol_kv = policy_evict_first();
+    const uint64_t pol_q = policy_evict_normal();
+    uint32_t q_issued = 0, q_par = 0, kv_issued = 0, kv_par = 0;
+    int stage = 0;
+    uint32_t kv_phase = 0;
+    int qi = 0;
+    const int lq = lane >> 2, lh = (lane >> 1) & 1, lkv = lane & 1;   // this lane's box (lanes < 16)
+    for (int c = c_begin; c < c_end; ++c, ++qi) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const AttnItem it = a.items[c];
+      const SeqMeta sm = a.seq[it.s];
+      const ItemGeo ig = item_geo(it, sm, g.gamma);
+      const int qb = qi & 1;
+      const uint32_t qph = (qi >> 1) & 1;
+      if (!mbar_wait_warp(smem_u32(&bar->q_empty[qb]), qph ^ 1, abort_flag)) break;
+      if (lane == 0) {
         const uint32_t qf = smem_u32(&bar->q_full[qb]);
         mbar_expect_tx(qf, 2 * 64 * n_q * 2);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           tma_load_3d(base + qb * Q_BYTES + h * Q_HALF, &map_q, qf, h * 64, it.g * grp,
                       it.s * g.gamma, pol_q);
-        q_issued |= 1u << qb;
-        q_par = (q_par & ~(1u << qb)) | (qph << qb);
-        bool ok = true;
-        for (int j = 0; j < ig.ntiles; ++j) {
-          if (!mbar_wait(smem_u32(&bar->kv_empty[stage]), kv_phase ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t gm = group_mask(ig, j);
-          const uint32_t sb = base + OFF_KV + stage * STAGE_BYTES;
-          const uint32_t fb = smem_u32(&bar->kv_full[stage]);
-          mbar_expect_tx(fb, __popc(gm) * 4 * GROUP_BYTES);
-#pragma unroll
-          for (int q = 0; q < AK / 16; ++q) {
-            if (!((gm >> q) & 1u)) continue;
-            if (!ig.block) {
-              const int pos = ig.p0 + j * AK + 16 * q;
-              int page = a.page_ids[sm.page_base + pos / 16 - sm.ws / 16];
-              if (page < 0 || page >= g.pages) {
-                atomicOr(a.status, ST_PAGE);
-                page = 0;
-              }
-              const int row_k = (((page * g.L + a.layer) * 2) * g.nkv + it.g) * 16;
-              const int row_v = row_k + g.nkv * 16;
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                tma_load_2d(sb + h * KT_HALF + q * GROUP_BYTES, &map_pool, fb, h * 64, row_k,
-                            pol_kv);
-                tma_load_2d(sb + KT_BYTES + h * KT_HALF + q * GROUP_BYTES, &map_pool, fb, h * 64,
-                            row_v, pol_kv);
-              }
-            } else {
-              const int row = it.s * g.gamma + j * AK + 16 * q;
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                tma_load_2d(sb + h * KT_HALF + q * GROUP_BYTES, &map_kb, fb, it.g * AD + h * 64,
-                            row, pol_q);
-                tma_load_2d(sb + KT_BYTES + h * KT_HALF + q * GROUP_BYTES, &map_vb, fb,
-                            it.g * AD + h * 64, row, pol_q);
-              }
+      }
+      q_issued |= 1u << qb;
+      q_par = (q_par & ~(1u << qb)) | (qph << qb);
+      bool ok = true;
+      for (int j = 0; j < ig.ntiles; ++j) {
+        if (!mbar_wait_warp(smem_u32(&bar->kv_empty[stage]), kv_phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t gm = group_mask(ig, j);
+        const uint32_t sb = base + OFF_KV + stage * STAGE_BYTES;
+        const uint32_t fb = smem_u32(&bar->kv_full[stage]);
+        if (lane == 0) mbar_expect_tx(fb, __popc(gm) * 4 * GROUP_BYTES);
+        __syncwarp();
+        if (lane < 16 && ((gm >> lq) & 1u)) {
+          const uint32_t dst = sb + lkv * KT_BYTES + lh * KT_HALF + lq * GROUP_BYTES;
+          if (!ig.block) {
+            const int pos = ig.p0 + j * AK + 16 * lq;
+            int page = a.page_ids[sm.page_base + pos / 16 - sm.ws / 16];
+            if (page < 0 || page >= g.pages) {
+              atomicOr(a.status, ST_PAGE);
+              page = 0;
             }
-          }
-          kv_issued |= 1u << stage;
-          kv_par = (kv_par & ~(1u << stage)) | (kv_phase << stage);
-          if (++stage == KV_STAGES) {
-            stage = 0;
-            kv_phase ^= 1;
+            const int row = ((((page * g.L + a.layer) * 2) + lkv) * g.nkv + it.g) * 16;
+            tma_load_2d(dst, &map_pool, fb, lh * 64, row, pol_kv);
+          } else {
+            const int row = it.s * g.gamma + j * AK + 16 * lq;
+            tma_load_2d(dst, lkv ? &map_vb : &map_kb, fb, it.g * AD + lh * 64, row, pol_q);
           }
         }
-        if (!ok) break;
+        kv_issued |= 1u << stage;
+        kv_par = (kv_par & ~(1u << stage)) | (kv_phase << stage);
+        if (++stage == KV_STAGES) {
+          stage = 0;
+          kv_phase ^= 1;
+        }
       }
+      if (!ok) break;
+    }
+    if (lane == 0) {
       bar->q_issued = q_issued;
       bar->q_parity = q_par;
       bar->kv_issued = kv_issued;
