@@ -16,6 +16,8 @@
 
 #include <cmath>
 
+#include "gemm_tc.h"
+
 namespace dfl {
 
 namespace {
@@ -423,12 +425,92 @@ __global__ void __launch_bounds__(THREADS) k_attn_split(AttnArgs a) {
 
 // One warp per (pair, query vector), 4 per block: combine the pair's chunks.
 // Lane c holds chunk c's (m, l) (32 chunks per round); the weights reach the
-// other lanes by shuffle. The partial rows do not depend on the maximum, so
-// the first MERGE_ROWS of them are loaded together with the (m, l) pairs: a
-// pair of up to MERGE_ROWS chunks takes one L2 round trip.
-constexpr int MERGE_ROWS = 24;
+// other lanes by shuffle, and every chunk's partial row is loaded before any
+// is used.
 template <int D>
 __global__ void __launch_bounds__(128) k_attn_merge(AttnArgs a) {
+  if ((int)blockIdx.x >= a.counts[1]) return;   // grid sized for the capacity
+  pdl_trigger();
+  const AttnPair pr = a.pairs[blockIdx.x];   // host-written: read before the wait
+  pdl_wait();
+  constexpr int VPL = D / 32;   // floats per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qv = blockIdx.y * 4 + warp;
+  const Geo &g = a.g;
+  const int grp = g.nq / g.nkv;
+  const int n_q = g.gamma * grp;
+  if (qv >= n_q) return;
+  const int64_t off_m = (int64_t)n_q * D + qv, off_l = (int64_t)n_q * D + n_q + qv;
+  // max over all chunks
+  float M = -INFINITY;
+  for (int c0 = 0; c0 < pr.nc; c0 += 32) {
+    const int c = c0 + lane;
+    if (c < pr.nc) M = fmaxf(M, __ldcg(a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats + off_m));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float l = 0.f;
+  float acc[VPL];
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+  for (int c0 = 0; c0 < pr.nc; c0 += 32) {
+    const int c = c0 + lane;
+    float w = 0.f;
+    if (c < pr.nc) {
+      const float *ws = a.ws + (int64_t)(pr.slot0 + c) * a.slot_floats;
+      const float m = __ldcg(ws + off_m);
+      w = (m == -INFINITY) ? 0.f : __expf(m - M);
+      l += w * __ldcg(ws + off_l);
+    }
+    const int nc = pr.nc - c0 < 32 ? pr.nc - c0 : 32;
+    // rows of up to 8 chunks in flight, added in chunk order
+    for (int b = 0; b < nc; b += 8) {
+      float4 r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (b + u < nc) {
+          const float *row = a.ws + (int64_t)(pr.slot0 + c0 + b + u) * a.slot_floats +
+                             (int64_t)qv * D + lane * VPL;
+          if constexpr (VPL == 4) r[u] = __ldcg(reinterpret_cast<const float4 *>(row));
+          else r[u] = make_float4(__ldcg(row), __ldcg(row + 1), 0.f, 0.f);
+        } else {
+          r[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, w, (b + u) & 31);
+        if (b + u < nc) {
+          acc[0] += wu * r[u].x;
+          acc[1] += wu * r[u].y;
+          if constexpr (VPL == 4) {
+            acc[2] += wu * r[u].z;
+            acc[3] += wu * r[u].w;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  const float inv = 1.f / l;
+  bf16 *orow = a.o + ((int64_t)(pr.s * g.gamma + qv / grp) * g.nq + pr.g * grp + qv % grp) * D +
+               lane * VPL;
+#pragma unroll
+  for (int e = 0; e < VPL; e += 2)
+    *reinterpret_cast<__nv_bfloat162 *>(orow + e) =
+        __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+}
+
+
+// The same merge for a grid of a few blocks per SM (batch 1: one pair per kv
+// head, many chunks). The partial rows do not depend on the maximum, so the
+// first MERGE_ROWS of them are loaded together with the (m, l) pairs: a pair
+// of up to MERGE_ROWS chunks takes one L2 round trip (at ~128 registers, which
+// would cost the many-pair grids their resident blocks).
+constexpr int MERGE_ROWS = 24;
+template <int D>
+__global__ void __launch_bounds__(128) k_attn_merge_wide(AttnArgs a) {
   if ((int)blockIdx.x >= a.counts[1]) return;   // grid sized for the capacity
   pdl_trigger();
   const AttnPair pr = a.pairs[blockIdx.x];   // host-written: read before the wait
@@ -524,9 +606,16 @@ cudaError_t attention_merge(const AttnArgs &a, cudaStream_t s) {
   if (a.n_pairs == 0) return cudaSuccess;   // capacity 0: no ctx window at all
   const int grp = a.g.nq / a.g.nkv;
   const dim3 grid(a.n_pairs, (a.g.gamma * grp + 3) / 4);
-  if (a.g.d == 128) launch_pdl(k_attn_merge<128>, grid, dim3(128), 0, s, a);
-  else if (a.g.d == 64) launch_pdl(k_attn_merge<64>, grid, dim3(128), 0, s, a);
-  else return cudaErrorInvalidValue;
+  const bool wide = (int64_t)grid.x * grid.y <= 2 * (int64_t)tc::num_sms();
+  if (a.g.d == 128) {
+    if (wide) launch_pdl(k_attn_merge_wide<128>, grid, dim3(128), 0, s, a);
+    else launch_pdl(k_attn_merge<128>, grid, dim3(128), 0, s, a);
+  } else if (a.g.d == 64) {
+    if (wide) launch_pdl(k_attn_merge_wide<64>, grid, dim3(128), 0, s, a);
+    else launch_pdl(k_attn_merge<64>, grid, dim3(128), 0, s, a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

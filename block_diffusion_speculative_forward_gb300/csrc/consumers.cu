@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
       float v = p.x ? p.x[(int64_t)a * n + f] : 0.f;
       if (p.has_y) {
         if (p.y.ws) {
-          v += part_sum(p.y, tr[t], a, f);
+          v += part_sum_wide(p.y, tr[t], a, f);
         } else {
           v += p.y.dense[(int64_t)a * p.y.ld + f];
         }
@@ -169,14 +169,16 @@ __global__ void __launch_bounds__(256) k_add_norm_cl(AddNormArgs p) {
 }
 
 // Warp per (row, head): q and k heads take RMSNorm with their gain and RoPE at
-// the row's position. The last y-block of each row rounds its v features to
-// bf16 (its own CTA, so no head's CTA does two passes).
+// the row's position; v is rounded to bf16. From partials (few rows) the v
+// features take a y-block of their own, so that no head's CTA runs two
+// passes of partial sums; from a dense matrix the first head block copies
+// them after its heads.
 template <int NP>
 __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
   pdl_trigger();
   const Geo &g = p.g;
   const int r = blockIdx.x;
-  if ((int)blockIdx.y == (g.nq + g.nkv + 7) / 8) {
+  if (p.y.ws && (int)blockIdx.y == (g.nq + g.nkv + 7) / 8) {
     // v rows: a warp's 32 consecutive features share one tile; the ranges
     // depend on no earlier kernel (before the wait)
     constexpr int MAXV = 4;
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
       for (int u = 0; u < MAXV; ++u) {
         const int e = e0 + threadIdx.x + 256 * u;
         tv[u] = TileRange{};
-        if (e < g.kv && p.y.ws) tv[u] = part_range(p.y, part_tile(p.y, r, (vbase + e) & ~31));
+        if (e < g.kv) tv[u] = part_range(p.y, part_tile(p.y, r, (vbase + e) & ~31));
       }
       pdl_wait();
       float y[MAXV];
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
         const int e = e0 + threadIdx.x + 256 * u;
         y[u] = 0.f;
         if (e < g.kv)
-          y[u] = p.y.ws ? part_sum(p.y, tv[u], r, vbase + e) : p.y.dense[(int64_t)r * p.y.ld + vbase + e];
+          y[u] = part_sum_wide(p.y, tv[u], r, vbase + e);
       }
 #pragma unroll
       for (int u = 0; u < MAXV; ++u) {
@@ -234,8 +236,8 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
       const int f0 = base + lane + 32 * t, f1 = f0 + half;
-      v[2 * t] = p.y.ws ? part_sum(p.y, tr, r, f0) : p.y.dense[(int64_t)r * p.y.ld + f0];
-      v[2 * t + 1] = p.y.ws ? part_sum(p.y, tr, r, f1) : p.y.dense[(int64_t)r * p.y.ld + f1];
+      v[2 * t] = p.y.ws ? part_sum_wide(p.y, tr, r, f0) : p.y.dense[(int64_t)r * p.y.ld + f0];
+      v[2 * t + 1] = p.y.ws ? part_sum_wide(p.y, tr, r, f1) : p.y.dense[(int64_t)r * p.y.ld + f1];
       ss += v[2 * t] * v[2 * t] + v[2 * t + 1] * v[2 * t + 1];
     }
     ss = warp_sum(ss);
@@ -250,6 +252,12 @@ __global__ void __launch_bounds__(256) k_qkv_post(QkvPostArgs p) {
       dst[i] = __float2bfloat16_rn(x1 * cs[t] - x2 * sn[t]);
       dst[i + half] = __float2bfloat16_rn(x2 * cs[t] + x1 * sn[t]);
     }
+  }
+  if (!p.y.ws && blockIdx.y == 0) {
+    pdl_wait();
+    const int vbase = g.nq * d + g.kv;
+    for (int e = threadIdx.x; e < g.kv; e += blockDim.x)
+      p.vb[(int64_t)r * g.kv + e] = __float2bfloat16_rn(p.y.dense[(int64_t)r * p.y.ld + vbase + e]);
   }
 }
 
@@ -266,7 +274,7 @@ cudaError_t add_norm(const AddNormArgs &p, int rows, cudaStream_t s) {
 }
 
 cudaError_t qkv_post(const QkvPostArgs &p, int R, cudaStream_t s) {
-  dim3 grid(R, (p.g.nq + p.g.nkv + 7) / 8 + 1);   // + the v block
+  dim3 grid(R, (p.g.nq + p.g.nkv + 7) / 8 + (p.y.ws ? 1 : 0));   // (+ the v block)
   if (p.g.d == 128) return launch_pdl(k_qkv_post<2>, grid, dim3(256), 0, s, p);
   if (p.g.d == 64) return launch_pdl(k_qkv_post<1>, grid, dim3(256), 0, s, p);
   return cudaErrorInvalidValue;

@@ -53,11 +53,26 @@ __device__ __forceinline__ TileRange part_range(const Partials &P, int t) {
   return r;
 }
 // Partial slots are laid out [slot][bn rows][128 features]; contributors are
-// added in ascending CTA order. The first PART_BATCH contributors' loads are
-// issued together (one L2 round trip covers every tile of the batch-1
-// projections, which have at most 11), the rest four at a time.
-constexpr int PART_BATCH = 12;
+// added in ascending CTA order. part_sum keeps four loads in flight (for the
+// many-row consumers, whose threads each sum several features);
+// part_sum_wide issues the first PART_BATCH contributors' loads together, so
+// one L2 round trip covers every tile of the few-row projections (at most 11
+// contributors at batch 1). Both give the same sum.
 __device__ __forceinline__ float part_sum(const Partials &P, const TileRange &r, int a, int f) {
+  const float *base = P.ws + (a % P.bn) * 128 + (f & 127);
+  const long long stride = (long long)P.bn * 128;
+  float s = __ldcg(base + (2 * r.c_lo + r.lo_second) * stride);
+  for (int c = r.c_lo + 1; c <= r.c_hi; c += 4) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = (c + u <= r.c_hi) ? __ldcg(base + 2 * (c + u) * stride) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) s += v[u];
+  }
+  return s;
+}
+constexpr int PART_BATCH = 12;
+__device__ __forceinline__ float part_sum_wide(const Partials &P, const TileRange &r, int a, int f) {
   const float *base = P.ws + (a % P.bn) * 128 + (f & 127);
   const long long stride = (long long)P.bn * 128;
   float b[PART_BATCH];
