@@ -688,6 +688,14 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
   // GEMM is split-K over all SMs (one SM streams only ~35 GB/s from HBM, so
   // the weight stream needs them all) and the consumers read the partials.
   const bool dp = R > 64;
+  // Few rows, but gate/up has 128-row tiles for at least half the SMs: whole
+  // tiles per CTA there too. Its stream-K fixup tail (partial write, fence,
+  // atomic, the other contributors' partials) cost ~4 us per layer at batch
+  // 1; whole tiles on 96 of the 152 SMs take the weight stream at ~45 GB/s
+  // per SM, and the down projection's CTAs start on the idle SMs and load
+  // their first weight stages meanwhile (measured 13.5 -> 10.3 us per
+  // gate/up, 676 -> 652 us per propose).
+  const bool gu_dp_few = !dp && 2 * ((2 * g.I + 127) / 128) >= tc::num_sms();
   const int bn_qkv = dp ? tc::pick_bn_dp(R, g.qkv_w, g.H) : bnR;
   const int bn_gu = dp ? tc::pick_bn_dp(R, 2 * g.I, g.H) : bnR;
   LK(embed_block(W.embed, cm.seq, n, g, c.mask_token_id, B.x, B.status, s));
@@ -833,9 +841,9 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       LK(add_norm(an, R, s));
     }
     {
-      // gate/up with SwiGLU in the GEMM's epilogue: whole tiles for many rows,
-      // the split-K fixup for few (one kernel instead of partials plus a
-      // separate SwiGLU pass)
+      // gate/up with SwiGLU in the GEMM's epilogue: whole tiles for many rows
+      // (and for few when the tiles cover half the SMs), otherwise the split-K
+      // fixup (one kernel instead of partials plus a separate SwiGLU pass)
       GemmParams p{};
       p.m_act = R;
       p.n_w = 2 * g.I;
@@ -846,7 +854,7 @@ int forward(const Geo &g, const dflash_config &c, const Weights &W, const Buffer
       p.status = B.status;
       p.fault_ns = B.fault_ns;
       p.u_out = B.u;
-      p.dp = dp;
+      p.dp = dp || gu_dp_few;
       LK(tc::gemm(W.map_gu[l], B.act_map[ACT_H][bn_index(bn_gu)], bn_gu, p, s));
     }
     has_pending = tc::partial_ok(R, g.H, g.I);
