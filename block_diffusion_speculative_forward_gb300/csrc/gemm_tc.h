@@ -93,6 +93,34 @@ __device__ __forceinline__ float part_sum_wide(const Partials &P, const TileRang
   }
   return s;
 }
+// N features f[n] of one row and one tile (one contributor range) at once:
+// the first PART_BATCH contributors' loads of every feature are issued
+// together. Each sum has part_sum_wide's order.
+template <int N>
+__device__ __forceinline__ void part_sum_multi(const Partials &P, const TileRange &r, int a,
+                                               const int (&f)[N], float (&out)[N]) {
+  const float *base = P.ws + (a % P.bn) * 128;
+  const long long stride = (long long)P.bn * 128;
+  float b[PART_BATCH][N];
+#pragma unroll
+  for (int u = 0; u < PART_BATCH; ++u) {
+    const int c = r.c_lo + u;
+    const float *slot = base + (2 * c + (u == 0 ? r.lo_second : 0)) * stride;
+#pragma unroll
+    for (int n = 0; n < N; ++n) b[u][n] = c <= r.c_hi ? __ldcg(slot + (f[n] & 127)) : 0.f;
+  }
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    float s = b[0][n];
+#pragma unroll
+    for (int u = 1; u < PART_BATCH; ++u) s += b[u][n];
+    out[n] = s;
+  }
+  for (int c = r.c_lo + PART_BATCH; c <= r.c_hi; ++c) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) out[n] += __ldcg(base + 2 * c * stride + (f[n] & 127));
+  }
+}
 __device__ __forceinline__ int part_tile(const Partials &P, int a, int f) {
   return (a / P.bn) * P.tiles_m + (f >> 7);
 }

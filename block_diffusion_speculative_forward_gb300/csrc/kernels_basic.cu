@@ -35,11 +35,14 @@ __device__ __forceinline__ uint8_t float_to_fp8(float v) {
 // ----------------------------------------------------------- block embed --
 // [P1] fields gamma, mask_token_id, embed_tokens_shared: row 0 of each
 // sequence's block embeds the last verified token, rows 1..gamma-1 the mask.
+// Nothing earlier in the step touches x (the new ctx rows' kernels read and
+// write their own buffers) and the previous step has completed, so the rows
+// are written while the kernel before runs; the wait at the end keeps the
+// next kernel behind both.
 __global__ void k_embed_block(const bf16 *__restrict__ E, const SeqMeta *__restrict__ seq,
                               int gamma, int H, int V, uint32_t mask_token, float *__restrict__ x,
                               int *status) {
   pdl_trigger();
-  pdl_wait();
   int r = blockIdx.x;
   int i = r % gamma;
   uint32_t tok = i == 0 ? (uint32_t)seq[r / gamma].token : mask_token;
@@ -49,6 +52,7 @@ __global__ void k_embed_block(const bf16 *__restrict__ E, const SeqMeta *__restr
   }
   const bf16 *er = E + (int64_t)tok * H;
   for (int e = threadIdx.x; e < H; e += blockDim.x) x[(int64_t)r * H + e] = __bfloat162float(er[e]);
+  pdl_wait();
 }
 
 cudaError_t embed_block(const bf16 *E, const SeqMeta *seq, int n_seq, const Geo &g,
@@ -87,11 +91,12 @@ cudaError_t pack_rows(const RowMeta *rows, int m, int S, bf16 *out, cudaStream_t
 // 32t, i < d/2, elements i and i + d/2), applies gain g, then rotates each
 // pair by the position's angle (rotate-half pairing over the full head,
 // [P1] field rotary_dim). v[2*t] is element i, v[2*t+1] element i + d/2.
+// gk[2t], gk[2t+1]: the gains of elements i and i + d/2; cs[t], sn[t] the
+// rotation of pair i.
 template <int NP>
-__device__ __forceinline__ void norm_rope_warp(float (&v)[2 * NP], const bf16 *g, float eps,
-                                               int d, const float *cos_row,
-                                               const float *sin_row) {
-  const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void norm_rope_warp(float (&v)[2 * NP], const float (&gk)[2 * NP],
+                                               float eps, int d, const float (&cs)[NP],
+                                               const float (&sn)[NP]) {
   float ss = 0.f;
 #pragma unroll
   for (int t = 0; t < 2 * NP; ++t) ss += v[t] * v[t];
@@ -99,12 +104,10 @@ __device__ __forceinline__ void norm_rope_warp(float (&v)[2 * NP], const bf16 *g
   float inv = rsqrtf(ss / (float)d + eps);
 #pragma unroll
   for (int t = 0; t < NP; ++t) {
-    int i = lane + 32 * t;
-    float a = __bfloat162float(g[i]) * (v[2 * t] * inv);
-    float b = __bfloat162float(g[i + d / 2]) * (v[2 * t + 1] * inv);
-    float c = cos_row[i], s = sin_row[i];
-    v[2 * t] = a * c - b * s;
-    v[2 * t + 1] = b * c + a * s;
+    float a = gk[2 * t] * (v[2 * t] * inv);
+    float b = gk[2 * t + 1] * (v[2 * t + 1] * inv);
+    v[2 * t] = a * cs[t] - b * sn[t];
+    v[2 * t + 1] = b * cs[t] + a * sn[t];
   }
 }
 
@@ -118,37 +121,60 @@ __global__ void k_ctx_kv_write(const Partials kv, const RowMeta *__restrict__ ro
                                const float *__restrict__ cos_t, const float *__restrict__ sin_t,
                                void *pool, const float *__restrict__ kv_scale, int *status) {
   pdl_trigger();
-  pdl_wait();
   const int r = blockIdx.x, l = blockIdx.y;
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = g.d, half = d / 2;
+  // the row record, contributor ranges, gains and rotation depend on no
+  // earlier kernel: read before the wait
   const RowMeta rm = rows[r];
-  if (rm.seq < 0) return;   // padding row: computed, never stored
+  if (rm.seq < 0) {   // padding row: computed, never stored
+    pdl_wait();
+    return;
+  }
   if (rm.page < 0 || rm.page >= g.pages) {
     if (threadIdx.x == 0) atomicOr(status, ST_PAGE);
+    pdl_wait();
     return;
   }
   const int kcol = l * 2 * g.kv + h * d, vcol = kcol + g.kv;
   // a head's K (and V) columns lie in one 128-column tile: one contributor
-  // range each for the warp; every load is issued before the first use
-  auto val = [&](const TileRange &tr, int f) -> float {
-    return kv.ws ? part_sum(kv, tr, r, f) : kv.dense[(int64_t)r * kv.ld + f];
-  };
+  // range each for the warp, all of its features' loads issued together
   TileRange trk{}, trv{};
   if (kv.ws) {
     trk = part_range(kv, part_tile(kv, r, kcol));
     trv = part_range(kv, part_tile(kv, r, vcol));
   }
-  float v[2 * NP], vv[2 * NP];
+  const bf16 *kg = k_norm[l];
+  float gk[2 * NP], cs[NP], sn[NP];
 #pragma unroll
   for (int t = 0; t < NP; ++t) {
-    v[2 * t] = val(trk, kcol + lane + 32 * t);
-    v[2 * t + 1] = val(trk, kcol + lane + 32 * t + half);
-    vv[2 * t] = val(trv, vcol + lane + 32 * t);
-    vv[2 * t + 1] = val(trv, vcol + lane + 32 * t + half);
+    const int i = lane + 32 * t;
+    gk[2 * t] = __bfloat162float(kg[i]);
+    gk[2 * t + 1] = __bfloat162float(kg[i + half]);
+    cs[t] = cos_t[(int64_t)rm.pos * half + i];
+    sn[t] = sin_t[(int64_t)rm.pos * half + i];
   }
-  norm_rope_warp<NP>(v, k_norm[l], g.eps, d, cos_t + (int64_t)rm.pos * half,
-                     sin_t + (int64_t)rm.pos * half);
+  int fk[2 * NP], fv[2 * NP];
+#pragma unroll
+  for (int t = 0; t < NP; ++t) {
+    fk[2 * t] = kcol + lane + 32 * t;
+    fk[2 * t + 1] = kcol + lane + 32 * t + half;
+    fv[2 * t] = vcol + lane + 32 * t;
+    fv[2 * t + 1] = vcol + lane + 32 * t + half;
+  }
+  pdl_wait();
+  float v[2 * NP], vv[2 * NP];
+  if (kv.ws) {
+    part_sum_multi<2 * NP>(kv, trk, r, fk, v);
+    part_sum_multi<2 * NP>(kv, trv, r, fv, vv);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 2 * NP; ++t) {
+      v[t] = kv.dense[(int64_t)r * kv.ld + fk[t]];
+      vv[t] = kv.dense[(int64_t)r * kv.ld + fv[t]];
+    }
+  }
+  norm_rope_warp<NP>(v, gk, g.eps, d, cs, sn);
   int64_t ko = kv_offset(g, rm.page, l, 0, h, rm.slot);
   int64_t vo = kv_offset(g, rm.page, l, 1, h, rm.slot);
   if (g.kv_fp8) {
